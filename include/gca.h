@@ -1,0 +1,161 @@
+/*
+ * gca.h -- C ABI of the Grouped Cross Attention (GCA) hot path on GB300.
+ *
+ * GCA is defined in "Efficient Length-Generalizable Attention via Causal
+ * Retrieval for Long-Context Language Modeling" (Hu, Teng, Zhao, Wu, Tu;
+ * ICML 2025, arXiv 2410.01651).  Each chunk of S tokens has one landmark
+ * vector; the landmark of chunk c-1 scores earlier chunks, the top-k are
+ * retrieved for chunk c, every token of chunk c attends separately to each
+ * retrieved chunk (stage 1) and the per-chunk outputs are summed with the
+ * softmaxed relevance scores as weights (stage 2).
+ *
+ * Conventions shared by every entry point
+ *  - Tensor arguments are DEVICE pointers owned by the caller, except where
+ *    an argument says "host".  The library allocates no memory and keeps no
+ *    state except a per-device status word (see gca_get_status) and, for
+ *    the decode entry point, the per-device TMA descriptors it encodes.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *    work is enqueued asynchronously on it.
+ *  - The return value reports argument validation and launch errors.
+ *    Errors detected on the device (a bounded wait that ran out, an index
+ *    out of range) are recorded in the status word and returned by
+ *    gca_get_status().  No call ever traps or aborts the GPU context.
+ *  - Layouts are row-major, innermost dimension last.  Token tensors are
+ *    [B, tokens, H, d]; the chunk c of a token tensor is tokens cS .. cS+S-1.
+ *  - Pointers must be 16-byte aligned.
+ *
+ * Supported shapes (anything else returns GCA_ERR_UNSUPPORTED):
+ *  - dtype GCA_BF16: d = 64, S in {64, 128}            (tensor-core path)
+ *  - dtype GCA_F32 : d in {16, 32, 64}, S in {16, 32, 64} (fp32 FFMA path)
+ *  - 1 <= topk <= 32, landmark dimension <= 8192, chunks per row <= 16384.
+ */
+#ifndef GCA_H_
+#define GCA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GCA_OK = 0,
+    GCA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    GCA_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shapes     */
+    GCA_ERR_WORKSPACE = 3,     /* workspace missing or too small             */
+    GCA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed          */
+    GCA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out         */
+    GCA_ERR_DEVICE_INDEX = 6   /* the device saw an index outside its range  */
+} gca_status_t;
+
+typedef enum { GCA_BF16 = 0, GCA_F32 = 1 } gca_dtype_t;
+
+typedef struct {
+    int B;                  /* batch rows                                         */
+    int Lq;                 /* query tokens per row; a multiple of S (nQ = Lq/S)  */
+    int S;                  /* tokens per chunk                                   */
+    int H;                  /* heads                                              */
+    int d;                  /* head dimension                                     */
+    int topk;               /* retrieved chunks per query chunk                   */
+    int n_pool_chunks;      /* K/V chunks per row (nP); nQ in training            */
+    int landmark_dim;       /* D of the landmark vectors; 0 means H*d             */
+    gca_dtype_t dtype;      /* element type of landmarks and all token tensors    */
+    int softmax_off_by_one; /* 0: vanilla softmax; 1: denominator 1 + sum         */
+    int include_self;       /* 0: candidates kappa < c-1; 1: kappa <= c-1         */
+    float score_scale;      /* r = score_scale * l_{c-1}.l_kappa; 0 => 1/sqrt(D)  */
+    float attn_scale;       /* logits scale inside a chunk; 0 => 1/sqrt(d)        */
+} gca_params_t;
+
+/*
+ * gca_score_topk -- causal relevance scoring, top-k and weight softmax.
+ * Defines: the rebuttal comment "Cmt 1" (Eq. 1 with one group:
+ * r = l_t^T l_k / sqrt(d)); README "Model Architecture" (the landmark of the
+ * previous chunk selects the chunks for the next one); rebuttal Q4 (Eq. 3,
+ * softmax off by one).
+ *   landmarks [B, nC, D] (nC = Lq / S), dtype = params->dtype.
+ *   For query chunk c >= 1 with landmark chunk t = c-1, the candidates are
+ *   kappa < t (or kappa <= t with include_self).  s = l_t . l_kappa is
+ *   accumulated in fp32 (exact for integer landmarks with |s| < 2^24).
+ *   Slots are ordered by s descending, then kappa ascending.
+ *   idx    [B, nC, topk] int32: retrieved chunk, -1 for an empty slot.
+ *   score  [B, nC, topk] fp32: r = score_scale * s (0 for an empty slot).
+ *   weight [B, nC, topk] fp32: softmax or off-by-one softmax of the valid r
+ *                              (0 for an empty slot).
+ */
+gca_status_t gca_score_topk(const gca_params_t* params, const void* landmarks,
+                            int32_t* idx, float* score, float* weight, void* stream);
+
+/*
+ * gca_fwd -- GCA forward: per-chunk attention (stage 1) and weighted fusion
+ * (stage 2).  Defines: README "Model Architecture" (two stages), Figure 1/2,
+ * Eq. 2 (the batch form of Figure 2, rebuttal W2); App. B (the forward
+ * returns O and the log-sum-exp).
+ *   q [B, Lq, H, d]; k, v [B, n_pool_chunks * S, H, d].
+ *   idx, weight [B, nQ, topk] as written by gca_score_topk (or by the caller;
+ *   entries must be -1 or in [0, n_pool_chunks)).
+ *   o   [B, Lq, H, d]: O_t = sum_j weight_j * softmax(attn_scale q_t K_j^T) V_j,
+ *       0 for a chunk without a valid slot.  fp32 accumulation.
+ *   lse [B, Lq, H, topk] fp32 or NULL: ln sum_s exp(attn_scale q_t.k_s) per
+ *       slot, -inf for an empty slot.  Required later by gca_bwd.
+ */
+gca_status_t gca_fwd(const gca_params_t* params, const void* q, const void* k, const void* v,
+                     const int32_t* idx, const float* weight, void* o, float* lse, void* stream);
+
+/* Bytes of device workspace gca_bwd needs for these parameters. */
+size_t gca_bwd_workspace_size(const gca_params_t* params);
+
+/*
+ * gca_bwd -- gradients of GCA into Q, K, V and the relevance scores.
+ * Defines: App. B backward (gradients for Q, K, V and the weights);
+ * section 3 and README "Model Architecture" (the retrieval scores receive
+ * gradients from the next-token loss through the fusion weights).
+ *   Inputs as gca_fwd, plus lse from gca_fwd and dout [B, Lq, H, d].
+ *   dq [B, Lq, H, d]; dk, dv [B, n_pool_chunks * S, H, d] are fully
+ *   overwritten (chunks that no query retrieved get 0).
+ *   dscore [B, nQ, topk] fp32: dLoss/dr for valid slots, 0 for empty ones.
+ *   The reduction over the queries that share a retrieved chunk is done in a
+ *   fixed order without atomics, so results are bitwise reproducible.
+ *   workspace: device buffer of at least gca_bwd_workspace_size() bytes,
+ *   256-byte aligned, owned by the caller, contents need not be initialised.
+ */
+gca_status_t gca_bwd(const gca_params_t* params, const void* q, const void* k, const void* v,
+                     const int32_t* idx, const float* weight, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, float* dscore, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace gca_decode_retrieve needs. */
+size_t gca_decode_workspace_size(int n_landmarks, int D, int topk);
+
+/*
+ * gca_decode_retrieve -- decode-time retrieval: one query landmark against
+ * every stored landmark, top-k, softmax.  Defines: section 3.2 and 4.3 /
+ * Table 3 (retrieval runs once per chunk of generated tokens).
+ *   landmarks [N, D], query_landmark [D], element type `dtype`.
+ *   idx/score/weight [topk] as in gca_score_topk (score desc, index asc).
+ *   workspace: >= gca_decode_workspace_size() bytes, 256-byte aligned.
+ */
+gca_status_t gca_decode_retrieve(const void* landmarks, const void* query_landmark, int N, int D,
+                                 int topk, gca_dtype_t dtype, int softmax_off_by_one,
+                                 float score_scale, int32_t* idx, float* score, float* weight,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gca_get_status -- synchronise `stream`, then return and clear the device
+ * status word of the current device (GCA_OK if no device-side error was
+ * recorded since the last call).
+ */
+gca_status_t gca_get_status(void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* gca_status_string(gca_status_t status);
+
+/* Number of kernel launches the most recent successful call on this host
+ * thread enqueued (for launch accounting in benchmarks). */
+int gca_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCA_H_ */

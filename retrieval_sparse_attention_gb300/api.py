@@ -1,0 +1,165 @@
+"""Thin PyTorch binding of the GCA C ABI (argument marshalling only).
+
+Each ``gca_*`` function has the name and argument order of its C entry point
+and passes ``data_ptr()`` of CUDA tensors plus the current CUDA stream; every
+step of the computation runs in libgca.so.  The convenience functions
+``score_topk``, ``fwd``, ``bwd`` and ``decode_retrieve`` only allocate the
+outputs (and workspace) with PyTorch, then call the same entry points.
+
+GCA itself ("Efficient Length-Generalizable Attention via Causal Retrieval
+for Long-Context Language Modeling", ICML 2025) is documented in
+include/gca.h next to each entry point.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GCA_BF16, GCA_F32, GcaError, GcaParams
+
+_DT = {torch.bfloat16: GCA_BF16, torch.float32: GCA_F32}
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t not in _DT:
+        raise TypeError("GCA supports bfloat16 and float32 tensors, got %s" % t)
+    return _DT[t]
+
+
+def make_params(*, B, Lq, S, H, d, topk, n_pool_chunks=None, landmark_dim=0, dtype=torch.bfloat16,
+                off_by_one=False, include_self=False, score_scale=0.0, attn_scale=0.0) -> GcaParams:
+    return GcaParams(B=B, Lq=Lq, S=S, H=H, d=d, topk=topk,
+                     n_pool_chunks=(Lq // S if n_pool_chunks is None else n_pool_chunks),
+                     landmark_dim=landmark_dim, dtype=dtype_code(dtype),
+                     softmax_off_by_one=int(bool(off_by_one)), include_self=int(bool(include_self)),
+                     score_scale=float(score_scale), attn_scale=float(attn_scale))
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("GCA entry points take CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("GCA entry points take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, code):
+    if code != 0:
+        raise GcaError(fn, code)
+
+
+# --- the C entry points, same names --------------------------------------------------
+def gca_score_topk(params: GcaParams, landmarks, idx, score, weight, stream=None):
+    _check("gca_score_topk", _lib.load().gca_score_topk(ctypes.byref(params), _p(landmarks), _p(idx),
+                                                        _p(score), _p(weight), _stream(stream)))
+
+
+def gca_fwd(params: GcaParams, q, k, v, idx, weight, o, lse=None, stream=None):
+    _check("gca_fwd", _lib.load().gca_fwd(ctypes.byref(params), _p(q), _p(k), _p(v), _p(idx),
+                                          _p(weight), _p(o), _p(lse), _stream(stream)))
+
+
+def gca_bwd_workspace_size(params: GcaParams) -> int:
+    return int(_lib.load().gca_bwd_workspace_size(ctypes.byref(params)))
+
+
+def gca_bwd(params: GcaParams, q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore, workspace,
+            stream=None):
+    _check("gca_bwd", _lib.load().gca_bwd(ctypes.byref(params), _p(q), _p(k), _p(v), _p(idx),
+                                          _p(weight), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv),
+                                          _p(dscore), _p(workspace), workspace.numel(),
+                                          _stream(stream)))
+
+
+def gca_decode_workspace_size(n_landmarks: int, D: int, topk: int) -> int:
+    return int(_lib.load().gca_decode_workspace_size(n_landmarks, D, topk))
+
+
+def gca_decode_retrieve(landmarks, query_landmark, N, D, topk, dtype, off_by_one, score_scale,
+                        idx, score, weight, workspace, stream=None):
+    _check("gca_decode_retrieve", _lib.load().gca_decode_retrieve(
+        _p(landmarks), _p(query_landmark), N, D, topk, dtype_code(dtype), int(bool(off_by_one)),
+        float(score_scale), _p(idx), _p(score), _p(weight), _p(workspace), workspace.numel(),
+        _stream(stream)))
+
+
+def gca_get_status(stream=None) -> int:
+    return int(_lib.load().gca_get_status(_stream(stream)))
+
+
+def gca_last_launch_count() -> int:
+    return int(_lib.load().gca_last_launch_count())
+
+
+def gca_synth_fill_hash(dst, seed: int, tensor_id: int, first_elem: int = 0, stream=None):
+    _check("gca_synth_fill_hash", _lib.load().gca_synth_fill_hash(
+        _p(dst), dst.numel(), dtype_code(dst.dtype), seed, tensor_id, first_elem, _stream(stream)))
+
+
+# --- allocating helpers ----------------------------------------------------------------
+def score_topk(landmarks, *, S, H, d, topk, off_by_one=False, include_self=False, score_scale=0.0):
+    """landmarks [B, nC, D] -> idx int32, score fp32, weight fp32, each [B, nC, topk]."""
+    B, nC, D = landmarks.shape
+    p = make_params(B=B, Lq=nC * S, S=S, H=H, d=d, topk=topk, landmark_dim=D,
+                    dtype=landmarks.dtype, off_by_one=off_by_one, include_self=include_self,
+                    score_scale=score_scale)
+    dev = landmarks.device
+    idx = torch.empty(B, nC, topk, dtype=torch.int32, device=dev)
+    score = torch.empty(B, nC, topk, dtype=torch.float32, device=dev)
+    weight = torch.empty(B, nC, topk, dtype=torch.float32, device=dev)
+    gca_score_topk(p, landmarks, idx, score, weight)
+    return idx, score, weight
+
+
+def fwd(q, k, v, idx, weight, *, S, attn_scale=0.0, with_lse=True):
+    """q [B, Lq, H, d]; k, v [B, nP*S, H, d]; idx, weight [B, Lq/S, topk] -> (o, lse)."""
+    B, Lq, H, d = q.shape
+    topk = idx.shape[-1]
+    p = make_params(B=B, Lq=Lq, S=S, H=H, d=d, topk=topk, n_pool_chunks=k.shape[1] // S,
+                    dtype=q.dtype, attn_scale=attn_scale)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Lq, H, topk, dtype=torch.float32, device=q.device) if with_lse else None
+    gca_fwd(p, q, k, v, idx, weight, o, lse)
+    return o, lse
+
+
+def bwd(q, k, v, idx, weight, lse, dout, *, S, attn_scale=0.0, workspace=None):
+    """Returns (dq, dk, dv, dscore)."""
+    B, Lq, H, d = q.shape
+    topk = idx.shape[-1]
+    p = make_params(B=B, Lq=Lq, S=S, H=H, d=d, topk=topk, n_pool_chunks=k.shape[1] // S,
+                    dtype=q.dtype, attn_scale=attn_scale)
+    need = gca_bwd_workspace_size(p)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dscore = torch.empty(B, Lq // S, topk, dtype=torch.float32, device=q.device)
+    gca_bwd(p, q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore, workspace)
+    return dq, dk, dv, dscore
+
+
+def decode_retrieve(landmarks, query_landmark, *, topk, off_by_one=False, score_scale=0.0,
+                    workspace=None):
+    """landmarks [N, D], query_landmark [D] -> idx, score, weight [topk]."""
+    N, D = landmarks.shape
+    need = gca_decode_workspace_size(N, D, topk)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=landmarks.device)
+    dev = landmarks.device
+    idx = torch.empty(topk, dtype=torch.int32, device=dev)
+    score = torch.empty(topk, dtype=torch.float32, device=dev)
+    weight = torch.empty(topk, dtype=torch.float32, device=dev)
+    gca_decode_retrieve(landmarks, query_landmark, N, D, topk, landmarks.dtype, off_by_one,
+                        score_scale, idx, score, weight, workspace)
+    return idx, score, weight

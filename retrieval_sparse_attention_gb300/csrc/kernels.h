@@ -1,0 +1,67 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gca.h"
+
+namespace gca {
+
+// Validated, defaulted parameters of one call.
+struct Shape {
+    int B, Lq, S, H, d, topk;
+    int nQ;               // query chunks per row = Lq / S
+    int nP;               // pool chunks per row
+    int D;                // landmark dimension
+    gca_dtype_t dtype;
+    int off_by_one;
+    int include_self;
+    float score_scale;
+    float attn_scale;
+};
+
+// Byte offsets of the pieces of the backward workspace.
+struct BwdWorkspace {
+    size_t delta_off;     // fp32 [B, Lq, H, topk]: delta_t^j = dO_t . O_t^j
+    size_t dwpart_off;    // fp32 [B, nQ, H, topk]: sum over the chunk's tokens of delta
+    size_t count_off;     // int32 [B, nP]: how many (c, j) retrieved each pool chunk
+    size_t offset_off;    // int32 [B, nP + 1]: CSR offsets of the inverse index
+    size_t entry_off;     // int32 [B, nQ * topk]: entries c * topk + j, ascending
+    size_t total;
+};
+BwdWorkspace bwd_workspace_layout(const Shape& s);
+
+// Decode workspace: ticket counter + per-block candidate lists.
+int decode_max_blocks(int N);
+size_t decode_workspace_bytes(int N, int topk);
+
+cudaError_t launch_score_topk(const Shape& s, const void* lm, int32_t* idx, float* score,
+                              float* weight, int* status, cudaStream_t st, int* launches);
+
+cudaError_t launch_decode_retrieve(const void* lm, const void* ql, int N, int D, int topk,
+                                   gca_dtype_t dt, int off_by_one, float score_scale,
+                                   int32_t* idx, float* score, float* weight, void* ws,
+                                   int* status, cudaStream_t st, int* launches);
+
+cudaError_t launch_fwd_simt(const Shape& s, const void* q, const void* k, const void* v,
+                            const int32_t* idx, const float* w, void* o, float* lse,
+                            int* status, cudaStream_t st, int* launches);
+
+cudaError_t launch_bwd_simt(const Shape& s, const void* q, const void* k, const void* v,
+                            const int32_t* idx, const float* w, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, float* dscore,
+                            void* ws, int* status, cudaStream_t st, int* launches);
+
+// Shared backward pieces (inverse index, score gradient).
+cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, cudaStream_t st,
+                                 int* launches);
+cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, void* ws,
+                          float* dscore, cudaStream_t st, int* launches);
+
+cudaError_t launch_synth_fill(void* dst, size_t n, gca_dtype_t dt, uint64_t seed, uint64_t tid,
+                              uint64_t first, cudaStream_t st);
+
+}  // namespace gca
