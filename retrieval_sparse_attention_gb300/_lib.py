@@ -19,10 +19,11 @@ STATUS_NAMES = {0: "GCA_OK", 1: "GCA_ERR_INVALID_ARG", 2: "GCA_ERR_UNSUPPORTED",
                 3: "GCA_ERR_WORKSPACE", 4: "GCA_ERR_CUDA", 5: "GCA_ERR_TIMEOUT",
                 6: "GCA_ERR_DEVICE_INDEX"}
 
-#: every symbol include/gca.h and include/gca_synth.h declare
+#: every symbol the headers under include/ declare
 EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_decode_workspace_size", "gca_decode_retrieve", "gca_get_status",
-            "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash")
+            "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
+            "gca_prof_enable", "gca_prof_read")
 
 
 class GcaParams(ctypes.Structure):
@@ -66,6 +67,8 @@ def load() -> ctypes.CDLL:
             "gca_last_launch_count": ([], i32),
             "gca_synth_fill_hash": ([vp, sz, i32, ctypes.c_uint64, ctypes.c_uint64,
                                      ctypes.c_uint64, vp], i32),
+            "gca_prof_enable": ([i32], None),
+            "gca_prof_read": ([i32, vp, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)

@@ -234,8 +234,8 @@ cudaError_t fwd_dh(const Shape& sp, const void* q, const void* k, const void* v,
     auto kern = fwd_simt_kernel<T, DH>;
     const size_t smem = sizeof(float) * 2 * sp.S * DH;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<dim3(sp.nQ, sp.H, sp.B), sp.S, smem, st>>>(sp, (const T*)q, (const T*)k, (const T*)v,
-                                                     idx, w, (T*)o, lse, status);
+    GCA_LAUNCH("fwd_simt", st, kern<<<dim3(sp.nQ, sp.H, sp.B), sp.S, smem, st>>>(sp, (const T*)q, (const T*)k, (const T*)v,
+                                                     idx, w, (T*)o, lse, status));
     return cudaGetLastError();
 }
 
@@ -252,15 +252,15 @@ cudaError_t bwd_dh(const Shape& sp, const void* q, const void* k, const void* v,
     auto kq = bwd_q_simt_kernel<T, DH>;
     const size_t smq = sizeof(float) * (2 * sp.S * DH + sp.S);
     cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
-    kq<<<dim3(sp.nQ, sp.H, sp.B), sp.S, smq, st>>>(sp, (const T*)q, (const T*)k, (const T*)v, idx,
+    GCA_LAUNCH("bwd_q_simt", st, kq<<<dim3(sp.nQ, sp.H, sp.B), sp.S, smq, st>>>(sp, (const T*)q, (const T*)k, (const T*)v, idx,
                                                   w, lse, (const T*)dout, (T*)dq, delta, dwpart,
-                                                  status);
+                                                  status));
     auto kkv = bwd_kv_simt_kernel<T, DH>;
     const size_t smk = sizeof(float) * (2 * sp.S * DH + 2 * sp.S);
     cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
-    kkv<<<dim3(sp.nP, sp.H, sp.B), sp.S, smk, st>>>(sp, (const T*)q, (const T*)k, (const T*)v, w,
+    GCA_LAUNCH("bwd_kv_simt", st, kkv<<<dim3(sp.nP, sp.H, sp.B), sp.S, smk, st>>>(sp, (const T*)q, (const T*)k, (const T*)v, w,
                                                    lse, (const T*)dout, delta, offset, entry,
-                                                   (T*)dk, (T*)dv);
+                                                   (T*)dk, (T*)dv));
     return cudaGetLastError();
 }
 

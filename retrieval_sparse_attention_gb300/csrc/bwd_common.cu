@@ -123,9 +123,9 @@ cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, c
     const int nE = s.nQ * s.topk;
     const int warps = s.B * s.nP;
     const int blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    inv_count_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, count);
-    inv_scan_kernel<<<s.B, 1024, 0, st>>>(count, s.nP, offset);
-    inv_fill_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, offset, entry);
+    GCA_LAUNCH("inv_count", st, inv_count_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, count));
+    GCA_LAUNCH("inv_scan", st, inv_scan_kernel<<<s.B, 1024, 0, st>>>(count, s.nP, offset));
+    GCA_LAUNCH("inv_fill", st, inv_fill_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, offset, entry));
     *launches += 3;
     return cudaGetLastError();
 }
@@ -135,7 +135,7 @@ cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, vo
     const BwdWorkspace L = bwd_workspace_layout(s);
     const float* dwpart = reinterpret_cast<const float*>(static_cast<char*>(ws) + L.dwpart_off);
     const int rows = s.B * s.nQ;
-    dscore_kernel<<<(rows + 127) / 128, 128, 0, st>>>(idx, w, dwpart, rows, s.H, s.topk, dscore);
+    GCA_LAUNCH("dscore", st, dscore_kernel<<<(rows + 127) / 128, 128, 0, st>>>(idx, w, dwpart, rows, s.H, s.topk, dscore));
     *launches += 1;
     return cudaGetLastError();
 }

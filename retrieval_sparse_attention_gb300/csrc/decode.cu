@@ -195,8 +195,8 @@ cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, i
     int* blk_i = reinterpret_cast<int*>(blk_s + (size_t)nb * topk);
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return e;
-    kern<<<nb, kThreads, smem, st>>>((const T*)lm, (const T*)ql, N, D, topk, off_by_one,
-                                     score_scale, idx, score, weight, ticket, blk_s, blk_i);
+    GCA_LAUNCH("decode_retrieve", st, kern<<<nb, kThreads, smem, st>>>((const T*)lm, (const T*)ql, N, D, topk, off_by_one,
+                                     score_scale, idx, score, weight, ticket, blk_s, blk_i));
     return cudaGetLastError();
 }
 

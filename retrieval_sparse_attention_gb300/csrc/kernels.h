@@ -10,6 +10,16 @@
 
 namespace gca {
 
+// Optional per-kernel CUDA-event bracketing (include/gca_prof.h).
+void prof_begin(cudaStream_t st, const char* name);
+void prof_end(cudaStream_t st);
+#define GCA_LAUNCH(name, st, ...)          \
+    do {                                   \
+        ::gca::prof_begin((st), (name));   \
+        __VA_ARGS__;                       \
+        ::gca::prof_end((st));             \
+    } while (0)
+
 // Validated, defaulted parameters of one call.
 struct Shape {
     int B, Lq, S, H, d, topk;

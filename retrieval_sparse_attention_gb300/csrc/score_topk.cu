@@ -107,15 +107,15 @@ cudaError_t launch_score_topk(const Shape& sp, const void* lm, int32_t* idx, flo
     if (sp.dtype == GCA_BF16) {
         auto kern = score_topk_kernel<__nv_bfloat16>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, kThreads, smem, st>>>((const __nv_bfloat16*)lm, sp.nQ, sp.D, sp.topk,
+        GCA_LAUNCH("score_topk", st, kern<<<grid, kThreads, smem, st>>>((const __nv_bfloat16*)lm, sp.nQ, sp.D, sp.topk,
                                            sp.include_self, sp.off_by_one, sp.score_scale, idx,
-                                           score, weight);
+                                           score, weight));
     } else {
         auto kern = score_topk_kernel<float>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, kThreads, smem, st>>>((const float*)lm, sp.nQ, sp.D, sp.topk,
+        GCA_LAUNCH("score_topk", st, kern<<<grid, kThreads, smem, st>>>((const float*)lm, sp.nQ, sp.D, sp.topk,
                                            sp.include_self, sp.off_by_one, sp.score_scale, idx,
-                                           score, weight);
+                                           score, weight));
     }
     *launches += 1;
     return cudaGetLastError();

@@ -36,9 +36,9 @@ cudaError_t launch_synth_fill(void* dst, size_t n, gca_dtype_t dt, uint64_t seed
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int blocks = sms > 0 ? sms * 8 : 1024;
     if (dt == GCA_BF16)
-        synth_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((__nv_bfloat16*)dst, n, key, first);
+        GCA_LAUNCH("synth_fill", st, synth_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((__nv_bfloat16*)dst, n, key, first));
     else
-        synth_fill_kernel<float><<<blocks, 256, 0, st>>>((float*)dst, n, key, first);
+        GCA_LAUNCH("synth_fill", st, synth_fill_kernel<float><<<blocks, 256, 0, st>>>((float*)dst, n, key, first));
     return cudaGetLastError();
 }
 
