@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the GCA hot path on GB300.
+
+One step = the whole hot path on one batch of the GPT-2-small-shaped 16K
+workload (B=8, L=16384, S=64, H=12, d=64, top-k=8, bf16, vanilla softmax):
+gca_score_topk -> gca_fwd -> gca_bwd.  The metric is query tokens per second
+(B*L per step, summed over ranks).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 it is launched under torch.distributed.run, one rank per GPU; the
+batch rows of different ranks are independent (weak scaling, no collective
+on the data path).  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gpt2s_fwdbwd_b8"
+METRIC = "GCA fwd+bwd query-tokens/s at 16K ctx; % of HBM/tensor roofline (1 GB300)"
+UNIT = "query-tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and decode lines")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def read_prof(lib):
+    import ctypes
+    n = 32
+    names = ctypes.create_string_buffer(64 * n)
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    k = lib.gca_prof_read(n, names, ms, cnt)
+    out = {}
+    for i in range(max(k, 0)):
+        nm = names.raw[64 * i:64 * (i + 1)].split(b"\0")[0].decode()
+        out[nm] = (float(ms[i]), int(cnt[i]))
+    return out
+
+
+def traffic_table():
+    """Per-launch DRAM bytes from the committed ncu summary (kernel -> bytes)."""
+    p = os.path.join(ROOT, "profiles", "ncu_dram_traffic.txt")
+    t = {}
+    if os.path.exists(p):
+        for ln in open(p):
+            f = ln.split()
+            if len(f) >= 3 and not ln.startswith("#"):
+                t[(f[0], f[1])] = float(f[2])
+    return t
+
+
+def alg_bytes(wl, U, H, D, k):
+    """Algorithmic bytes per launch of each kernel (bf16 tensors, fp32 lse/delta).
+
+    U = valid (batch row, query chunk, slot) units.  Each unit gathers one
+    retrieved chunk: 2 tiles of S x D (K and V, or Q and dO) of 2 bytes."""
+    B, L, S = wl.B, wl.L, wl.S
+    tok = B * L * D * 2                       # one [B, L, H, d] bf16 tensor
+    lse = B * L * H * k * 4
+    gather = U * 2 * S * D * 2
+    return {
+        "fwd": gather + 2 * tok + lse,                              # K/V gather, Q in, O out, lse out
+        "bwd_q": gather + 3 * tok + 2 * lse,                        # K/V gather, Q, dO in, dQ out; lse in, delta out
+        "bwd_kv": gather + U * 2 * S * H * 4 + 4 * tok,             # Q/dO gather + lse/delta rows; K, V in; dK, dV out
+    }
+
+
+# --------------------------------------------------------------------------- ours
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from retrieval_sparse_attention_gb300 import _lib, api, inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = _lib.load()
+    wl = inputs.WORKLOADS[WORKLOAD]
+    B, L, S, H, d, k = wl.B, wl.L, wl.S, wl.H, wl.d, wl.topk
+    D = H * d
+    x = inputs.make(wl)
+    host = {n: t.pin_memory() for n, t in x.items()}
+    g = {n: t.to(dev) for n, t in x.items()}
+    p = api.make_params(B=B, Lq=L, S=S, H=H, d=d, topk=k, dtype=torch.bfloat16,
+                        off_by_one=wl.off_by_one)
+    idx = torch.empty(B, wl.nC, k, dtype=torch.int32, device=dev)
+    r = torch.empty(B, wl.nC, k, dtype=torch.float32, device=dev)
+    w = torch.empty_like(r)
+    o = torch.empty_like(g["q"])
+    lse = torch.empty(B, L, H, k, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
+    ds = torch.empty_like(r)
+    wsb = torch.empty(api.gca_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    launches = [0]
+
+    def step(t):
+        api.gca_score_topk(p, t["lm"], idx, r, w)
+        n = api.gca_last_launch_count()
+        api.gca_fwd(p, t["q"], t["k"], t["v"], idx, w, o, lse)
+        n += api.gca_last_launch_count()
+        api.gca_bwd(p, t["q"], t["k"], t["v"], idx, w, lse, t["dout"], dq, dk, dv, ds, wsb)
+        n += api.gca_last_launch_count()
+        launches[0] += n
+
+    for _ in range(args.warmup):
+        step(g)
+    torch.cuda.synchronize()
+    assert api.gca_get_status() == 0, "device-side error during warm-up"
+    U = int((idx >= 0).sum().item())
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device events on the launching stream
+    launches[0] = 0
+    lib.gca_prof_read(0, None, None, None)
+    lib.gca_prof_enable(1)
+    barrier()
+    with ClockSampler(local) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step(g)
+        e1.record()
+        barrier()
+    lib.gca_prof_enable(0)
+    ms = e0.elapsed_time(e1)
+    prof = read_prof(lib)
+    n_launch = launches[0]
+    assert api.gca_get_status() == 0, "device-side error in the timed region"
+    ms_max = ms
+    if ws > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    value = ws * B * L * args.steps / (ms_max / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("ds", ds))}
+    dbuf = {n: torch.empty_like(t) for n, t in g.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    def e2e_step():
+        for n in dbuf:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        step(dbuf)
+        for n, src in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("ds", ds)):
+            out_host[n].copy_(src, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    t1.record()
+    barrier()
+    e2e_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = ws * B * L * args.e2e_steps / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant kernel
+    hbm, tflops, src = peaks()
+    ab = alg_bytes(wl, U, H, D, k)
+    total = sum(v[0] for v in prof.values()) or 1.0
+    dom = max(prof.items(), key=lambda kv: kv[1][0])
+    dom_name, (dom_ms, dom_n) = dom
+    fam = "bwd_kv" if "kv" in dom_name else ("bwd_q" if "bwd_q" in dom_name else
+                                             ("fwd" if "fwd" in dom_name else None))
+    avg_s = dom_ms / dom_n / 1e3
+    roof = None
+    if fam is not None:
+        achieved = ab[fam] / avg_s / 1e9
+        tr = traffic_table().get((dom_name, WORKLOAD))
+        roof = {"kernel": dom_name, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % src if src == "measured" else src,
+                "traffic": tr, "alg_bytes_per_launch": ab[fam],
+                "avg_launch_ms": round(dom_ms / dom_n, 4)}
+    kernels = {n: {"ms_total": round(v[0], 3), "launches": v[1], "share": round(v[0] / total, 4),
+                   "ms_per_launch": round(v[0] / v[1], 4)} for n, v in sorted(prof.items())}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; integer landmarks in [-4,4], Q/K/V ~ N(0,1/64), dO ~ N(0,1))",
+        "config": {"workload": WORKLOAD, "B": B, "L": L, "S": S, "H": H, "d": d, "topk": k,
+                   "softmax": "vanilla", "step": "gca_score_topk + gca_fwd + gca_bwd",
+                   "valid_units": U, "parallelism": "replicas" if ws == 1 else "dp%d" % ws,
+                   "l2": "inputs %.2f GB > 129 MB L2; no flush" % (
+                       sum(t.numel() * t.element_size() for t in g.values()) / 1e9)},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": n_launch,
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_extra:
+        line["extra"] = extra_workloads(lib, api, inputs, dev, hbm, tflops)
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def extra_workloads(lib, api, inputs, dev, hbm, tflops):
+    """gca_fwd alone on the B=4 off-by-one workload, and decode retrieval over
+    262144 landmarks followed by gca_fwd on the 51.5 GB K/V cache."""
+    import torch
+    out = {}
+    wl = inputs.WORKLOADS["gpt2s_fwd_b4"]
+    x = {n: t.to(dev) for n, t in inputs.make(wl, with_dout=False).items()}
+    idx, r, w = api.score_topk(x["lm"], S=wl.S, H=wl.H, d=wl.d, topk=wl.topk, off_by_one=True)
+    o, lse = api.fwd(x["q"], x["k"], x["v"], idx, w, S=wl.S)
+    torch.cuda.synchronize()
+    U = int((idx >= 0).sum().item())
+    n = 20
+    for _ in range(3):
+        api.fwd(x["q"], x["k"], x["v"], idx, w, S=wl.S)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        api.fwd(x["q"], x["k"], x["v"], idx, w, S=wl.S)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    D = wl.H * wl.d
+    ab = alg_bytes(wl, U, wl.H, D, wl.topk)["fwd"]
+    out["gpt2s_fwd_b4"] = {"kernel": "gca_fwd", "query_tokens_per_s": round(wl.B * wl.L / (ms / 1e3), 1),
+                           "ms": round(ms, 4), "valid_units": U,
+                           "roofline": {"bound": "hbm", "achieved": round(ab / ms / 1e6, 1), "peak": hbm,
+                                        "unit": "GB/s", "frac": round(ab / ms / 1e6 / hbm, 4)}}
+    del x, o, lse
+    # decode: 16M-token context
+    p = inputs.DECODE
+    hx = inputs.decode_inputs()
+    lm, ql, q = hx["lm"].to(dev), hx["ql"].to(dev), hx["q"].to(dev)
+    N, Dd, kk = p["N"], p["D"], p["topk"]
+    wsb = torch.empty(api.gca_decode_workspace_size(N, Dd, kk), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        api.decode_retrieve(lm, ql, topk=kk, workspace=wsb)
+    e0.record()
+    for _ in range(n):
+        api.decode_retrieve(lm, ql, topk=kk, workspace=wsb)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    byts = N * Dd * 2 + Dd * 2
+    dec = {"kernel": "gca_decode_retrieve", "N": N, "D": Dd, "topk": kk, "us": round(ms * 1e3, 2),
+           "roofline": {"bound": "hbm", "achieved": round(byts / ms / 1e6, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(byts / ms / 1e6 / hbm, 4)}}
+    # decode + forward over the HBM-resident cache
+    try:
+        cache_k = torch.empty(N * p["S"], p["H"], p["d"], dtype=torch.bfloat16, device=dev)
+        cache_v = torch.empty_like(cache_k)
+        api.gca_synth_fill_hash(cache_k, p["seed"], 0)
+        api.gca_synth_fill_hash(cache_v, p["seed"], 1)
+        qq = q.view(1, p["S"], p["H"], p["d"])
+        kc, vc = cache_k.view(1, N * p["S"], p["H"], p["d"]), cache_v.view(1, N * p["S"], p["H"], p["d"])
+
+        def dstep():
+            di, dr, dw = api.decode_retrieve(lm, ql, topk=kk, workspace=wsb)
+            api.fwd(qq, kc, vc, di.view(1, 1, kk), dw.view(1, 1, kk), S=p["S"])
+        for _ in range(3):
+            dstep()
+        e0.record()
+        for _ in range(n):
+            dstep()
+        e1.record()
+        torch.cuda.synchronize()
+        dec["retrieve_plus_fwd_us"] = round(e0.elapsed_time(e1) / n * 1e3, 2)
+        dec["cache_gb"] = round(2 * cache_k.numel() * 2 / 1e9, 2)
+        del cache_k, cache_v
+    except RuntimeError as exc:           # out of device memory on a smaller part
+        dec["retrieve_plus_fwd_us"] = None
+        dec["cache_error"] = str(exc)[:120]
+    out["decode_16m"] = dec
+    return out
+
+
+# --------------------------------------------------------------------------- oracle
+def oracle_step(L_sample):
+    """One oracle pass (score + fwd + bwd) on the first batch row of the
+    workload truncated to L_sample tokens.  Returns seconds."""
+    import numpy as np
+
+    import oracle
+    from retrieval_sparse_attention_gb300 import inputs
+    wl = inputs.WORKLOADS[WORKLOAD]
+    x = inputs.make(wl, B=1, L=L_sample)
+    f = {n: t.double().numpy() for n, t in x.items()}
+    t0 = time.perf_counter()
+    idx, r, w = oracle.score_topk(f["lm"], wl.topk, False, wl.off_by_one)
+    oracle.fwd(f["q"], f["k"], f["v"], idx, w, wl.S)
+    oracle.bwd(f["q"], f["k"], f["v"], idx, w, f["dout"], wl.S)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(L_sample=8192):
+    import oracle
+    oracle.build()
+    t = oracle_step(L_sample)
+    return {"value": round(L_sample / t, 2), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "fp64 oracle score+fwd+bwd on batch row 0, first %d tokens "
+            "(%d chunks) of the workload; %.2f s" % (L_sample, L_sample // 64, t)}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    # size the per-step sample so that warm-up + steps end within about two minutes
+    t1 = oracle_step(1024)
+    L = 1024
+    while L < 16384 and (t1 * (2 * L / 1024)) * (args.steps + args.warmup) < 120.0:
+        L *= 2
+    for _ in range(args.warmup):
+        oracle_step(L)
+    ts = [oracle_step(L) for _ in range(args.steps)]
+    tot = sum(ts)
+    value = L * args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_tokens": L, "B": 1},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "score+fwd+bwd on batch row 0, first %d tokens per step" % L},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
