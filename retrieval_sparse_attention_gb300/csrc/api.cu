@@ -145,7 +145,9 @@ gca_status_t gca_fwd(const gca_params_t* params, const void* q, const void* k, c
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    r = from_cuda(launch_fwd_simt(s, q, k, v, idx, weight, o, lse, st, cs, &n));
+    r = from_cuda(s.dtype == GCA_BF16
+                      ? launch_fwd_tc(s, q, k, v, idx, weight, o, lse, st, cs, &n)
+                      : launch_fwd_simt(s, q, k, v, idx, weight, o, lse, st, cs, &n));
     if (r == GCA_OK) t_launches = n;
     return r;
 }

@@ -60,6 +60,10 @@ cudaError_t launch_fwd_simt(const Shape& s, const void* q, const void* k, const 
                             const int32_t* idx, const float* w, void* o, float* lse,
                             int* status, cudaStream_t st, int* launches);
 
+cudaError_t launch_fwd_tc(const Shape& s, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const float* w, void* o, float* lse, int* status,
+                          cudaStream_t st, int* launches);
+
 cudaError_t launch_bwd_simt(const Shape& s, const void* q, const void* k, const void* v,
                             const int32_t* idx, const float* w, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, float* dscore,

@@ -1,0 +1,16 @@
+// tma_host.h -- host-side TMA tensor-map encoding used by the tensor-core kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace gca {
+
+// Tensor map over a row-major bf16 matrix [rows, row_elems] (row stride
+// row_elems * 2 bytes, a multiple of 16), box of 64 columns x box_rows rows,
+// 128-byte swizzle.  Returns false if the driver entry point is missing or
+// rejects the arguments.
+bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                      uint32_t box_rows);
+
+}  // namespace gca
