@@ -1,0 +1,410 @@
+// attn_bwd_tc.cu -- GCA backward on the Blackwell tensor cores (bf16, d = 64).
+//
+// App. B backward (gradients for Q, K, V and the weights) of the forward
+// O_t = sum_j w_j softmax(s q_t K_j^T) V_j.  With p = exp(s q.k - lse_j),
+// G_ts = dO_t . v_s and delta_t^j = sum_s p_ts G_ts (= dO_t . O_t^j):
+//   dA_ts = w_j p_ts (G_ts - delta_t^j) s,   dQ_t = sum_j sum_s dA_ts k_s,
+//   dK_s  = sum over (query chunk, slot) retrieving the chunk of sum_t dA_ts q_t,
+//   dV_s  = same of sum_t w_j p_ts dO_t,     dw_j = sum_{t, h} delta_t^j.
+//
+// Two passes, neither with atomics (every output element is written by
+// exactly one CTA, reductions run in a fixed order):
+//   pass A, query-major, item = (batch row, query chunk, head): gathers the
+//     retrieved chunks' K/V tiles like the forward, recomputes S = Q K^T and
+//     G = dO V^T on the tensor cores, forms dA in shared memory and
+//     accumulates dQ += dA K in TMEM; it also stores delta and lse per
+//     (query chunk, slot, head) as contiguous rows for pass B, and the per-head
+//     partial dw.
+//   pass B, key-major, item = (batch row, pool chunk, head): walks the inverse
+//     index of (query chunk, slot) entries that retrieved the chunk, gathers
+//     their Q/dO tiles and delta/lse rows, recomputes S^T = K Q^T and
+//     G^T = V dO^T, and accumulates dK += dA^T Q and dV += (w P)^T dO in TMEM.
+// Both use the warp roles of the forward kernel: warp 0 TMA producer, warp 1
+// MMA issuer and TMEM owner, warps 2-5 element-wise math and epilogue.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace gca {
+namespace {
+
+using namespace tc;
+using tcx::fast_exp2;
+using tcx::kLog2e;
+using tcx::pack8;
+using tcx::pack8u;
+using tcx::Ring;
+using tcx::sw128_off;
+
+constexpr int kThreads = 192;
+
+struct __align__(8) BarsA {
+    uint64_t it_full[2], it_empty[2];
+    uint64_t kv_full[4], kv_empty[4];
+    uint64_t s_full, s_empty;
+    uint64_t p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2];
+    uint64_t done;
+    uint32_t tmem;
+    int abort;
+};
+
+struct BwdArgs {
+    const int32_t* idx;
+    const float* w;
+    const float* lse;          // [B, Lq, H, topk]
+    float* lse2_rows;          // [B, nQ, topk, H, S]: lse * log2(e)
+    float* delta_rows;         // [B, nQ, topk, H, S]
+    float* dwpart;             // [B, nQ, H, 4, topk]: per TMEM lane quadrant
+    const int* offset;         // [B, nP + 1]
+    const int* entry;          // [B, nQ * topk]
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    int* status;
+    int B, nQ, nP, H, topk, Lq;
+    float scale_log2;          // attn_scale * log2(e)
+    float attn_scale;
+    int n_items;
+};
+
+__device__ __forceinline__ int valid_slots(const BwdArgs& a, int b, int c, int* js, int* kaps) {
+    const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
+    int n = 0;
+    for (int j = 0; j < a.topk; ++j) {
+        const int kap = row[j];
+        if (kap >= 0 && kap < a.nP) { js[n] = j; kaps[n] = kap; ++n; }
+    }
+    return n;
+}
+
+// ============================================================================ pass A
+template <int S>
+struct CfgA {
+    static constexpr int M = S;
+    static constexpr int GS = 128 / S;
+    static constexpr int NG = 128;
+    static constexpr int STAGES = (S == 64) ? 4 : 2;
+    static constexpr int TILE = S * 128;
+    static constexpr int ITEM_BYTES = 2 * TILE;            // Q then dO
+    static constexpr int STAGE_BYTES = 2 * NG * 128;       // K half then V half
+    static constexpr int P_BLOCK = M * 128;
+    static constexpr int P_BYTES = M * NG * 2;
+    static constexpr int OFF_IT = 0;
+    static constexpr int OFF_KV = 2 * ITEM_BYTES;
+    static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
+    static constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = 0, COL_G = 128, COL_DQ = 256;
+};
+
+template <int S>
+__global__ void __launch_bounds__(kThreads, 1)
+gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                    const BwdArgs a) {
+    using C = CfgA<S>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ BarsA sb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sb.it_full[i], 1);
+            mbar_init(&sb.it_empty[i], 1);
+            mbar_init(&sb.p_full[i], 128);
+            mbar_init(&sb.p_empty[i], 1);
+            mbar_init(&sb.o_full[i], 1);
+            mbar_init(&sb.o_empty[i], 128);
+        }
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&sb.kv_full[i], 1);
+            mbar_init(&sb.kv_empty[i], 1);
+        }
+        mbar_init(&sb.s_full, 1);
+        mbar_init(&sb.s_empty, 128);
+        mbar_init(&sb.done, 1);
+        sb.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tdo);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sb.tmem, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sb.tmem;
+    int js[kMaxTopk], kaps[kMaxTopk];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            Ring kv{0, 0}, it{0, 0};
+            bool kv_out[4] = {false, false, false, false}, it_out[2] = {false, false};
+            uint32_t kv_ph[4] = {0, 0, 0, 0}, it_ph[2] = {0, 0};
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
+                const int n = valid_slots(a, b, c, js, kaps);
+                if (n == 0) continue;
+                if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+                uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
+                mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
+                tma_load_2d(ib, &tq, &sb.it_full[it.i], h * 64, b * a.Lq + c * S);
+                tma_load_2d(ib + C::TILE, &tdo, &sb.it_full[it.i], h * 64, b * a.Lq + c * S);
+                it_out[it.i] = true;
+                it_ph[it.i] = it.ph;
+                it.next(2);
+                bool ok = true;
+                for (int g = 0; g * C::GS < n; ++g) {
+                    const int ns = min(C::GS, n - g * C::GS);
+                    if (!wait(&sb.kv_empty[kv.i], kv.ph ^ 1u)) { ok = false; break; }
+                    uint8_t* stg = sm + C::OFF_KV + kv.i * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&sb.kv_full[kv.i], ns * 2 * C::TILE);
+                    for (int u = 0; u < ns; ++u) {
+                        const int y = (b * a.nP + kaps[g * C::GS + u]) * S;
+                        tma_load_2d(stg + u * C::TILE, &tk, &sb.kv_full[kv.i], h * 64, y);
+                        tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tv, &sb.kv_full[kv.i], h * 64, y);
+                    }
+                    kv_out[kv.i] = true;
+                    kv_ph[kv.i] = kv.ph;
+                    kv.next(C::STAGES);
+                }
+                if (!ok) break;
+            }
+            for (int i = 0; i < C::STAGES; ++i)
+                if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < 2; ++i)
+                if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            Ring kv{0, 0}, it{0, 0}, p{0, 0}, o{0, 0};
+            uint32_t s_ph = 0;
+            bool issued = false;
+            const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
+            const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
+            const uint32_t id_dq = idesc_bf16(C::M, 64, false, true);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                const int bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
+                const int n = valid_slots(a, b, c, js, kaps);
+                if (n == 0) continue;
+                const int G = (n + C::GS - 1) / C::GS;
+                if (!wait(&sb.it_full[it.i], it.ph)) break;
+                if (!wait(&sb.o_empty[o.i], o.ph ^ 1u)) break;
+                tc_fence_after();
+                const uint32_t qaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
+                const uint32_t doaddr = qaddr + C::TILE;
+                const uint32_t d_dq = tmem + C::COL_DQ + o.i * 64;
+                bool ok = true;
+                for (int g = 0; g < G; ++g) {
+                    const int ns = min(C::GS, n - g * C::GS);
+                    if (!wait(&sb.kv_full[kv.i], kv.ph) || !wait(&sb.s_empty, s_ph ^ 1u)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
+                    const uint32_t vaddr = kaddr + C::NG * 128;
+                    const uint32_t id = (ns * S == 128) ? id_n128 : id_n64;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16(tmem + C::COL_S, desc_kmajor_sw128(qaddr + 32 * ks),
+                                 desc_kmajor_sw128(kaddr + 32 * ks), id, ks > 0);
+                        mma_bf16(tmem + C::COL_G, desc_kmajor_sw128(doaddr + 32 * ks),
+                                 desc_kmajor_sw128(vaddr + 32 * ks), id, ks > 0);
+                    }
+                    mma_commit(&sb.s_full);
+                    s_ph ^= 1u;
+                    issued = true;
+                    if (!wait(&sb.p_full[p.i], p.ph)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + p.i * C::P_BYTES);
+                    const int ksteps = ns * S / 16;
+                    for (int ks = 0; ks < ksteps; ++ks)
+                        mma_bf16(d_dq, desc_kmajor_sw128(paddr + (ks >> 2) * C::P_BLOCK + (ks & 3) * 32),
+                                 desc_mnmajor_sw128(kaddr + ks * 2048), id_dq, (g > 0 || ks > 0));
+                    mma_commit(&sb.kv_empty[kv.i]);
+                    mma_commit(&sb.p_empty[p.i]);
+                    kv.next(C::STAGES);
+                    p.next(2);
+                }
+                if (!ok) break;
+                mma_commit(&sb.o_full[o.i]);
+                mma_commit(&sb.it_empty[it.i]);
+                o.next(2);
+                it.next(2);
+            }
+            if (issued) {
+                mma_commit(&sb.done);
+                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+            }
+        }
+    } else {
+        const int qd = warp & 3;
+        const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
+        const int u = (S == 64) ? (lane >> 4) : 0;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+        Ring p{0, 0}, o{0, 0};
+        uint32_t s_ph = 0;
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+            const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
+            const int n = valid_slots(a, b, c, js, kaps);
+            const size_t tok = (size_t)b * a.Lq + (size_t)c * S + row;
+            __nv_bfloat16* dqrow = a.dq + (tok * a.H + h) * 64;
+            if (threadIdx.x == 64) {
+                const int32_t* irow = a.idx + ((size_t)b * a.nQ + c) * a.topk;
+                for (int j = 0; j < a.topk; ++j)
+                    if (!(irow[j] >= 0 && irow[j] < a.nP))
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            a.dwpart[((((size_t)b * a.nQ + c) * a.H + h) * 4 + q4) * a.topk + j] = 0.f;
+            }
+            if (n == 0) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                if (S == 64) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dqrow + u * 32)[q4] = z;
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) reinterpret_cast<uint4*>(dqrow)[q4] = z;
+                }
+                continue;
+            }
+            bool ok = true;
+            for (int g = 0; g * C::GS < n; ++g) {
+                const int ns = min(C::GS, n - g * C::GS);
+                const bool active = u < ns;
+                const int j = active ? js[g * C::GS + u] : 0;
+                const float L2 = active ? a.lse[(tok * a.H + h) * a.topk + j] * kLog2e : 0.f;
+                const float wsc = active ? a.w[((size_t)b * a.nQ + c) * a.topk + j] * a.attn_scale : 0.f;
+                if (!wait(&sb.s_full, s_ph)) { ok = false; break; }
+                s_ph ^= 1u;
+                tc_fence_after();
+                float dl = 0.f;
+                // 64 keys per chunk; S = 64 has one chunk per thread, S = 128 two.
+                constexpr int NCH = (S == 64) ? 1 : 2;
+                float xs[64], xg[64];
+                auto load_chunk = [&](int ch) {
+                    const uint32_t ts = tmem + lane_base + C::COL_S + ch * 64;
+                    const uint32_t tg = tmem + lane_base + C::COL_G + ch * 64;
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        uint32_t r1[16], r2[16];
+                        if (S == 64) {
+                            tmem_ld_16x32bx2_x16<64>(ts + 16 * ci, r1);
+                            tmem_ld_16x32bx2_x16<64>(tg + 16 * ci, r2);
+                        } else {
+                            tmem_ld_32x32b_x16(ts + 16 * ci, r1);
+                            tmem_ld_32x32b_x16(tg + 16 * ci, r2);
+                        }
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            xs[16 * ci + t] = __uint_as_float(r1[t]);
+                            xg[16 * ci + t] = __uint_as_float(r2[t]);
+                        }
+                    }
+                    tmem_wait_ld();
+                };
+                if (NCH == 2) {            // first sweep: delta only
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        load_chunk(ch);
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            dl = fmaf(fast_exp2(fmaf(xs[i], a.scale_log2, -L2)), xg[i], dl);
+                    }
+                }
+                if (!wait(&sb.p_empty[p.i], p.ph ^ 1u)) { ok = false; break; }
+                uint8_t* pb = sm + C::OFF_P + p.i * C::P_BYTES;
+                for (int ch = 0; ch < NCH; ++ch) {
+                    load_chunk(ch);
+                    if (ch == NCH - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) xs[i] = fast_exp2(fmaf(xs[i], a.scale_log2, -L2));
+                    if (NCH == 1) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) dl = fmaf(xs[i], xg[i], dl);
+                    }
+                    if (active) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) xs[i] = xs[i] * (xg[i] - dl);
+                        const int blk = (S == 64) ? u : ch;
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8)
+                            *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, c8)) =
+                                pack8(xs + 8 * c8, wsc);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sb.p_full[p.i]);
+                p.next(2);
+                // rows for pass B and the per-head partial of dw
+                if (active) {
+                    const size_t rr = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S + row;
+                    a.delta_rows[rr] = dl;
+                    a.lse2_rows[rr] = L2;
+                }
+                // per-quadrant partial of dw (summed over this warp's rows; the
+                // score-gradient kernel adds the quadrants and heads in order)
+                float part = active ? dl : 0.f;
+#pragma unroll
+                for (int o2 = (S == 64 ? 8 : 16); o2 > 0; o2 >>= 1)
+                    part += __shfl_xor_sync(0xffffffffu, part, o2);
+                if (active && (lane & (S == 64 ? 15 : 31)) == 0)
+                    a.dwpart[((((size_t)b * a.nQ + c) * a.H + h) * 4 + qd) * a.topk + j] = part;
+            }
+            if (!ok) break;
+            if (!wait(&sb.o_full[o.i], o.ph)) break;
+            tc_fence_after();
+            const uint32_t oaddr = tmem + lane_base + C::COL_DQ + o.i * 64;
+            if (S == 64) {
+                uint32_t r0[16], r1[16];
+                tmem_ld_16x32bx2_x16<32>(oaddr, r0);
+                tmem_ld_16x32bx2_x16<32>(oaddr + 16, r1);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sb.o_empty[o.i]);
+                uint4* dst = reinterpret_cast<uint4*>(dqrow + u * 32);
+                dst[0] = pack8u(r0);
+                dst[1] = pack8u(r0 + 8);
+                dst[2] = pack8u(r1);
+                dst[3] = pack8u(r1 + 8);
+            } else {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(oaddr + 16 * ci, r[ci]);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sb.o_empty[o.i]);
+                uint4* dst = reinterpret_cast<uint4*>(dqrow);
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) {
+                    dst[2 * ci] = pack8u(r[ci]);
+                    dst[2 * ci + 1] = pack8u(r[ci] + 8);
+                }
+            }
+            o.next(2);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, CfgA<S>::TMEM_COLS);
+    }
+}
+
+}  // namespace
+}  // namespace gca

@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -38,10 +39,12 @@ namespace {
 
 using namespace tc;
 
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr int kThreads = 192;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
+using tcx::Ring;
+using tcx::fast_exp2;
+using tcx::pack_bf16;
+using tcx::kLog2e;
+using tcx::kLn2;
 
 template <int S>
 struct Cfg {
@@ -87,14 +90,6 @@ struct __align__(8) Bars {
     int abort;
 };
 
-struct Ring {
-    int i;
-    uint32_t ph;
-    __device__ void next(int n) {
-        if (++i == n) { i = 0; ph ^= 1u; }
-    }
-};
-
 // Valid slots of one item: slot numbers and their chunks, in slot order.
 __device__ __forceinline__ int item_slots(const FwdArgs& a, int b, int c, int* js, int* kaps,
                                           bool report) {
@@ -108,32 +103,9 @@ __device__ __forceinline__ int item_slots(const FwdArgs& a, int b, int c, int* j
     return n;
 }
 
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Bounded wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool wait_bar(Bars& sb, uint64_t* bar, uint32_t parity, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*((volatile int*)&sb.abort)) return false;
-        if (global_timer_ns() - t0 > kWaitNs) {
-            set_status(status, GCA_ERR_TIMEOUT);
-            *((volatile int*)&sb.abort) = 1;
-            return false;
-        }
-    }
+    return tcx::wait_bar(&sb.abort, bar, parity, status);
 }
-
 
 template <int S>
 __global__ void __launch_bounds__(kThreads, 1)

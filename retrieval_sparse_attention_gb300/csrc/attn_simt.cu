@@ -109,11 +109,11 @@ __global__ void bwd_q_simt_kernel(Shape sp, const T* __restrict__ q, const T* __
         const size_t so = ((size_t)b * sp.nQ + c) * sp.topk + j;
         const int kap = idx[so];
         const size_t di = (tok * sp.H + h) * sp.topk + j;
-        const size_t pi = (((size_t)b * sp.nQ + c) * sp.H + h) * sp.topk + j;
+        const size_t pi = (((size_t)b * sp.nQ + c) * sp.H + h) * 4 * sp.topk + j;   // quadrant 0
         if (kap < 0 || kap >= sp.nP) {
             if (kap >= sp.nP && t == 0) set_status(status, GCA_ERR_DEVICE_INDEX);
             delta[di] = 0.f;
-            if (t == 0) dwpart[pi] = 0.f;
+            if (t < 4) dwpart[pi + t * sp.topk] = 0.f;
             continue;
         }
         const float wj = w[so];
@@ -156,6 +156,7 @@ __global__ void bwd_q_simt_kernel(Shape sp, const T* __restrict__ q, const T* __
             __syncthreads();
         }
         if (t == 0) dwpart[pi] = red[0];
+        if (t > 0 && t < 4) dwpart[pi + t * sp.topk] = 0.f;
     }
 #pragma unroll
     for (int e = 0; e < DH; ++e) dq[tok * ld + (size_t)h * DH + e] = from_f<T>(dqa[e]);

@@ -17,7 +17,8 @@ BwdWorkspace bwd_workspace_layout(const Shape& s) {
     BwdWorkspace w{};
     size_t off = 0;
     w.delta_off = off;  off += align256(sizeof(float) * (size_t)s.B * s.Lq * s.H * s.topk);
-    w.dwpart_off = off; off += align256(sizeof(float) * (size_t)s.B * s.nQ * s.H * s.topk);
+    w.dwpart_off = off; off += align256(sizeof(float) * (size_t)s.B * s.nQ * s.H * 4 * s.topk);
+    w.lse2_off = off;   off += align256(sizeof(float) * (size_t)s.B * s.Lq * s.H * s.topk);
     w.count_off = off;  off += align256(sizeof(int) * (size_t)s.B * s.nP);
     w.offset_off = off; off += align256(sizeof(int) * (size_t)s.B * (s.nP + 1));
     w.entry_off = off;  off += align256(sizeof(int) * (size_t)s.B * s.nQ * s.topk);
@@ -89,25 +90,28 @@ __global__ void inv_fill_kernel(const int32_t* __restrict__ idx, int B, int nE, 
     }
 }
 
-// One thread per (b, c): reduce the per-head partial dw in head order, then
+// One thread per (b, c): reduce the partial dw (per head and per quarter of
+// the chunk's tokens) in a fixed order, then
 // apply the softmax Jacobian (same form for the vanilla and off-by-one
 // softmax, whose Jacobians are both diag(w) - w w^T).
 __global__ void dscore_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w,
                               const float* __restrict__ dwpart, int n_rows, int H, int topk,
-                              float* __restrict__ dscore) {
+                              int nP, float* __restrict__ dscore) {
     const int row = blockIdx.x * blockDim.x + threadIdx.x;
     if (row >= n_rows) return;
     float dw[kMaxTopk];
     float wdw = 0.f;
     for (int j = 0; j < topk; ++j) {
         float acc = 0.f;
-        for (int h = 0; h < H; ++h) acc += dwpart[((size_t)row * H + h) * topk + j];
+        for (int hq = 0; hq < 4 * H; ++hq) acc += dwpart[((size_t)row * 4 * H + hq) * topk + j];
         dw[j] = acc;
-        if (idx[(size_t)row * topk + j] >= 0) wdw += w[(size_t)row * topk + j] * acc;
+        const int kap = idx[(size_t)row * topk + j];
+        if (kap >= 0 && kap < nP) wdw += w[(size_t)row * topk + j] * acc;
     }
     for (int j = 0; j < topk; ++j) {
         const size_t o = (size_t)row * topk + j;
-        dscore[o] = idx[o] >= 0 ? w[o] * (dw[j] - wdw) : 0.f;
+        const int kap = idx[o];
+        dscore[o] = (kap >= 0 && kap < nP) ? w[o] * (dw[j] - wdw) : 0.f;
     }
 }
 
@@ -135,7 +139,7 @@ cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, vo
     const BwdWorkspace L = bwd_workspace_layout(s);
     const float* dwpart = reinterpret_cast<const float*>(static_cast<char*>(ws) + L.dwpart_off);
     const int rows = s.B * s.nQ;
-    GCA_LAUNCH("dscore", st, dscore_kernel<<<(rows + 127) / 128, 128, 0, st>>>(idx, w, dwpart, rows, s.H, s.topk, dscore));
+    GCA_LAUNCH("dscore", st, dscore_kernel<<<(rows + 127) / 128, 128, 0, st>>>(idx, w, dwpart, rows, s.H, s.topk, s.nP, dscore));
     *launches += 1;
     return cudaGetLastError();
 }

@@ -35,8 +35,11 @@ struct Shape {
 
 // Byte offsets of the pieces of the backward workspace.
 struct BwdWorkspace {
-    size_t delta_off;     // fp32 [B, Lq, H, topk]: delta_t^j = dO_t . O_t^j
-    size_t dwpart_off;    // fp32 [B, nQ, H, topk]: sum over the chunk's tokens of delta
+    size_t delta_off;     // fp32 delta_t^j = dO_t . O_t^j: [B, Lq, H, topk] (FFMA path) or
+                          // [B, nQ, topk, H, S] rows (tensor-core path)
+    size_t dwpart_off;    // fp32 [B, nQ, H, 4, topk]: partial sums of delta over a quarter
+                          // of the chunk's tokens (each quarter one TMEM lane quadrant)
+    size_t lse2_off;      // fp32 [B, nQ, topk, H, S]: lse * log2(e) rows for the key pass
     size_t count_off;     // int32 [B, nP]: how many (c, j) retrieved each pool chunk
     size_t offset_off;    // int32 [B, nP + 1]: CSR offsets of the inverse index
     size_t entry_off;     // int32 [B, nQ * topk]: entries c * topk + j, ascending

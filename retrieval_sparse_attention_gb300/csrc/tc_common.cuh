@@ -1,0 +1,87 @@
+// tc_common.cuh -- helpers shared by the warp-specialised tensor-core kernels
+// (forward, backward query-major pass, backward key-major pass).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace gca {
+namespace tcx {
+
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far above any legitimate wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Stage index + phase bit of a ring of mbarrier-guarded buffers.
+struct Ring {
+    int i;
+    uint32_t ph;
+    __device__ __forceinline__ void next(int n) {
+        if (++i == n) { i = 0; ph ^= 1u; }
+    }
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* x, float s) {
+    return make_uint4(pack_bf16(x[0] * s, x[1] * s), pack_bf16(x[2] * s, x[3] * s),
+                      pack_bf16(x[4] * s, x[5] * s), pack_bf16(x[6] * s, x[7] * s));
+}
+
+__device__ __forceinline__ uint4 pack8u(const uint32_t* r) {
+    return make_uint4(pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                      pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                      pack_bf16(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                      pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
+}
+
+// Bounded wait that also gives up once another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_bar(int* abort_flag, uint64_t* bar, uint32_t parity,
+                                         int* status) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::global_timer_ns();
+    while (true) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if (*((volatile int*)abort_flag)) return false;
+        if (tc::global_timer_ns() - t0 > kWaitNs) {
+            set_status(status, GCA_ERR_TIMEOUT);
+            *((volatile int*)abort_flag) = 1;
+            return false;
+        }
+    }
+}
+
+// Address of the 16-byte chunk `ch` (0..7 within a 64-element row block) of
+// row `row` in a K-major tile with the 128-byte swizzle (1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
+    return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
+}
+
+// Named barrier over the 128 softmax/epilogue threads (warps 2-5).
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Untiled bulk copy global -> shared, completing on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+
+}  // namespace tcx
+}  // namespace gca
