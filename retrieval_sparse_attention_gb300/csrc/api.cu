@@ -173,8 +173,11 @@ gca_status_t gca_bwd(const gca_params_t* params, const void* q, const void* k, c
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    r = from_cuda(launch_bwd_simt(s, q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore,
-                                  workspace, st, cs, &n));
+    r = from_cuda(s.dtype == GCA_BF16
+                      ? launch_bwd_tc(s, q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore,
+                                      workspace, st, cs, &n)
+                      : launch_bwd_simt(s, q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore,
+                                        workspace, st, cs, &n));
     if (r == GCA_OK) t_launches = n;
     return r;
 }

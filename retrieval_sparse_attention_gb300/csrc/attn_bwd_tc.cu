@@ -406,5 +406,399 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     }
 }
 
+
+// ============================================================================ pass B
+template <int S>
+struct CfgB {
+    static constexpr int M = S;                           // keys of the item
+    static constexpr int GS = 128 / S;                    // entries per group
+    static constexpr int NG = 128;                        // tokens per full group
+    static constexpr int STAGES = (S == 64) ? 3 : 2;
+    static constexpr int TILE = S * 128;
+    static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
+    static constexpr int VEC_OFF = 2 * NG * 128;          // after the Q and dO tiles
+    static constexpr int STAGE_BYTES = VEC_OFF + 1024;    // + lse2/delta rows of the entries
+    static constexpr int P_BLOCK = M * 128;
+    static constexpr int P_BYTES = M * NG * 2;            // one operand (dA^T or wP^T)
+    static constexpr int PB = (S == 64) ? 2 : 1;          // operand-pair buffers
+    static constexpr int OFF_IT = 0;
+    static constexpr int OFF_ST = 2 * ITEM_BYTES;
+    static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
+    static constexpr int SMEM = OFF_P + PB * 2 * P_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = 0, COL_G = 128, COL_ACC = 256;   // dK, dV: 2 x (64 + 64)
+};
+
+struct __align__(8) BarsB {
+    uint64_t it_full[2], it_empty[2];
+    uint64_t st_full[3], st_empty[3];
+    uint64_t s_full, s_empty;
+    uint64_t p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2];
+    uint64_t done;
+    uint32_t tmem;
+    int abort;
+};
+
+template <int S>
+__global__ void __launch_bounds__(kThreads, 1)
+gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                     const BwdArgs a) {
+    using C = CfgB<S>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ BarsB sb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
+    const int nE = a.nQ * a.topk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sb.it_full[i], 1);
+            mbar_init(&sb.it_empty[i], 1);
+            mbar_init(&sb.p_full[i], 128);
+            mbar_init(&sb.p_empty[i], 1);
+            mbar_init(&sb.o_full[i], 1);
+            mbar_init(&sb.o_empty[i], 128);
+        }
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&sb.st_full[i], 1);
+            mbar_init(&sb.st_empty[i], 1);
+        }
+        mbar_init(&sb.s_full, 1);
+        mbar_init(&sb.s_empty, 128);
+        mbar_init(&sb.done, 1);
+        sb.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tdo);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sb.tmem, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sb.tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            Ring st{0, 0}, it{0, 0};
+            bool st_out[3] = {false, false, false}, it_out[2] = {false, false};
+            uint32_t st_ph[3] = {0, 0, 0}, it_ph[2] = {0, 0};
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
+                const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
+                const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
+                if (ne <= 0) continue;
+                const int* ent = a.entry + (size_t)b * nE + e0;
+                if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+                uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
+                mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
+                tma_load_2d(ib, &tk, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
+                tma_load_2d(ib + C::TILE, &tv, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
+                it_out[it.i] = true;
+                it_ph[it.i] = it.ph;
+                it.next(2);
+                bool ok = true;
+                for (int g = 0; g * C::GS < ne; ++g) {
+                    const int ns = min(C::GS, ne - g * C::GS);
+                    if (!wait(&sb.st_empty[st.i], st.ph ^ 1u)) { ok = false; break; }
+                    uint8_t* stg = sm + C::OFF_ST + st.i * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&sb.st_full[st.i], ns * (2 * C::TILE + 2 * S * 4));
+                    for (int u = 0; u < ns; ++u) {
+                        const int e = ent[g * C::GS + u];
+                        const int c = e / a.topk, j = e % a.topk;
+                        tma_load_2d(stg + u * C::TILE, &tq, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
+                        tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tdo, &sb.st_full[st.i], h * 64,
+                                    b * a.Lq + c * S);
+                        const size_t rb = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S;
+                        tcx::bulk_load(stg + C::VEC_OFF + u * 2 * S * 4, a.lse2_rows + rb, S * 4,
+                                       &sb.st_full[st.i]);
+                        tcx::bulk_load(stg + C::VEC_OFF + u * 2 * S * 4 + S * 4, a.delta_rows + rb,
+                                       S * 4, &sb.st_full[st.i]);
+                    }
+                    st_out[st.i] = true;
+                    st_ph[st.i] = st.ph;
+                    st.next(C::STAGES);
+                }
+                if (!ok) break;
+            }
+            for (int i = 0; i < C::STAGES; ++i)
+                if (st_out[i]) mbar_wait(&sb.st_full[i], st_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < 2; ++i)
+                if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            Ring st{0, 0}, it{0, 0}, p{0, 0}, o{0, 0};
+            uint32_t s_ph = 0;
+            bool issued = false;
+            const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
+            const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
+            const uint32_t id_acc = idesc_bf16(C::M, 64, false, true);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                const int bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
+                const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
+                const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
+                if (ne <= 0) continue;
+                if (!wait(&sb.it_full[it.i], it.ph)) break;
+                if (!wait(&sb.o_empty[o.i], o.ph ^ 1u)) break;
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
+                const uint32_t vaddr = kaddr + C::TILE;
+                const uint32_t d_dk = tmem + C::COL_ACC + o.i * 128;
+                const uint32_t d_dv = d_dk + 64;
+                bool ok = true;
+                for (int g = 0; g * C::GS < ne; ++g) {
+                    const int ns = min(C::GS, ne - g * C::GS);
+                    if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_empty, s_ph ^ 1u)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
+                    const uint32_t doaddr = qaddr + C::NG * 128;
+                    const uint32_t id = (ns * S == 128) ? id_n128 : id_n64;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16(tmem + C::COL_S, desc_kmajor_sw128(kaddr + 32 * ks),
+                                 desc_kmajor_sw128(qaddr + 32 * ks), id, ks > 0);
+                        mma_bf16(tmem + C::COL_G, desc_kmajor_sw128(vaddr + 32 * ks),
+                                 desc_kmajor_sw128(doaddr + 32 * ks), id, ks > 0);
+                    }
+                    mma_commit(&sb.s_full);
+                    s_ph ^= 1u;
+                    issued = true;
+                    if (!wait(&sb.p_full[p.i], p.ph)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + p.i * 2 * C::P_BYTES);
+                    const int ksteps = ns * S / 16;
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const uint32_t aoff = (ks >> 2) * C::P_BLOCK + (ks & 3) * 32;
+                        mma_bf16(d_dk, desc_kmajor_sw128(paddr + aoff), desc_mnmajor_sw128(qaddr + ks * 2048),
+                                 id_acc, (g > 0 || ks > 0));
+                        mma_bf16(d_dv, desc_kmajor_sw128(paddr + C::P_BYTES + aoff),
+                                 desc_mnmajor_sw128(doaddr + ks * 2048), id_acc, (g > 0 || ks > 0));
+                    }
+                    mma_commit(&sb.st_empty[st.i]);
+                    mma_commit(&sb.p_empty[p.i]);
+                    st.next(C::STAGES);
+                    p.next(C::PB);
+                }
+                if (!ok) break;
+                mma_commit(&sb.o_full[o.i]);
+                mma_commit(&sb.it_empty[it.i]);
+                o.next(2);
+                it.next(2);
+            }
+            if (issued) {
+                mma_commit(&sb.done);
+                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+            }
+        }
+    } else {
+        const int qd = warp & 3;
+        const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
+        const int u = (S == 64) ? (lane >> 4) : 0;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+        Ring st{0, 0}, p{0, 0}, o{0, 0};
+        uint32_t s_ph = 0;
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+            const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
+            const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
+            const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
+            const size_t krow = (size_t)(b * a.nP + kap) * S + row;
+            __nv_bfloat16* dkrow = a.dk + (krow * a.H + h) * 64;
+            __nv_bfloat16* dvrow = a.dv + (krow * a.H + h) * 64;
+            if (ne <= 0) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                const int nq = (S == 64) ? 4 : 8;
+                const int off = (S == 64) ? u * 32 : 0;
+                for (int q4 = 0; q4 < nq; ++q4) {
+                    reinterpret_cast<uint4*>(dkrow + off)[q4] = z;
+                    reinterpret_cast<uint4*>(dvrow + off)[q4] = z;
+                }
+                continue;
+            }
+            const int* ent = a.entry + (size_t)b * nE + e0;
+            bool ok = true;
+            for (int g = 0; g * C::GS < ne; ++g) {
+                const int ns = min(C::GS, ne - g * C::GS);
+                const bool active = u < ns;
+                float wv = 0.f;
+                if (active) {
+                    const int e = ent[g * C::GS + u];
+                    wv = a.w[((size_t)b * a.nQ + e / a.topk) * a.topk + e % a.topk];
+                }
+                const float wsc = wv * a.attn_scale;
+                if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_full, s_ph)) { ok = false; break; }
+                s_ph ^= 1u;
+                tc_fence_after();
+                if (!wait(&sb.p_empty[p.i], p.ph ^ 1u)) { ok = false; break; }
+                const float* vec = reinterpret_cast<const float*>(sm + C::OFF_ST + st.i * C::STAGE_BYTES +
+                                                                  C::VEC_OFF + u * 2 * S * 4);
+                uint8_t* pb = sm + C::OFF_P + p.i * 2 * C::P_BYTES;
+                constexpr int NCH = (S == 64) ? 1 : 2;
+                for (int ch = 0; ch < NCH; ++ch) {
+                    float xs[64], xg[64];
+                    const uint32_t ts = tmem + lane_base + C::COL_S + ch * 64;
+                    const uint32_t tg = tmem + lane_base + C::COL_G + ch * 64;
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        uint32_t r1[16], r2[16];
+                        if (S == 64) {
+                            tmem_ld_16x32bx2_x16<64>(ts + 16 * ci, r1);
+                            tmem_ld_16x32bx2_x16<64>(tg + 16 * ci, r2);
+                        } else {
+                            tmem_ld_32x32b_x16(ts + 16 * ci, r1);
+                            tmem_ld_32x32b_x16(tg + 16 * ci, r2);
+                        }
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            xs[16 * ci + t] = __uint_as_float(r1[t]);
+                            xg[16 * ci + t] = __uint_as_float(r2[t]);
+                        }
+                    }
+                    tmem_wait_ld();
+                    if (ch == NCH - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty);
+                    }
+                    if (active) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            const int t = ch * 64 + i;
+                            const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -vec[t]));
+                            xs[i] = pr * (xg[i] - vec[S + t]);      // dA^T / (w s)
+                            xg[i] = pr;                             // P^T / w
+                        }
+                        const int blk = (S == 64) ? u : ch;
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const uint32_t off = blk * C::P_BLOCK + tcx::sw128_off(row, c8);
+                            *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c8, wsc);
+                            *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c8, wv);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sb.p_full[p.i]);
+                p.next(C::PB);
+                st.next(C::STAGES);
+            }
+            if (!ok) break;
+            if (!wait(&sb.o_full[o.i], o.ph)) break;
+            tc_fence_after();
+            const uint32_t acc = tmem + lane_base + C::COL_ACC + o.i * 128;
+            if (S == 64) {
+                uint32_t k0[16], k1[16], v0[16], v1[16];
+                tmem_ld_16x32bx2_x16<32>(acc, k0);
+                tmem_ld_16x32bx2_x16<32>(acc + 16, k1);
+                tmem_ld_16x32bx2_x16<32>(acc + 64, v0);
+                tmem_ld_16x32bx2_x16<32>(acc + 80, v1);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sb.o_empty[o.i]);
+                uint4* dk4 = reinterpret_cast<uint4*>(dkrow + u * 32);
+                uint4* dv4 = reinterpret_cast<uint4*>(dvrow + u * 32);
+                dk4[0] = pack8u(k0); dk4[1] = pack8u(k0 + 8); dk4[2] = pack8u(k1); dk4[3] = pack8u(k1 + 8);
+                dv4[0] = pack8u(v0); dv4[1] = pack8u(v0 + 8); dv4[2] = pack8u(v1); dv4[3] = pack8u(v1 + 8);
+            } else {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(acc + 16 * ci, r[ci]);
+                tmem_wait_ld();
+                uint4* dk4 = reinterpret_cast<uint4*>(dkrow);
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) { dk4[2 * ci] = pack8u(r[ci]); dk4[2 * ci + 1] = pack8u(r[ci] + 8); }
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(acc + 64 + 16 * ci, r[ci]);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sb.o_empty[o.i]);
+                uint4* dv4 = reinterpret_cast<uint4*>(dvrow);
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) { dv4[2 * ci] = pack8u(r[ci]); dv4[2 * ci + 1] = pack8u(r[ci] + 8); }
+            }
+            o.next(2);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, CfgB<S>::TMEM_COLS);
+    }
+}
+
+// ============================================================================ launch
+template <int S>
+cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const void* v,
+                         const int32_t* idx, const float* w, const float* lse, const void* dout,
+                         void* dq, void* dk, void* dv, void* ws, int* status, cudaStream_t st) {
+    CUtensorMap tq, tdo, tk, tv;
+    const uint64_t cols = (uint64_t)sp.H * 64;
+    if (!encode_bf16_rows(&tq, q, (uint64_t)sp.B * sp.Lq, cols, S) ||
+        !encode_bf16_rows(&tdo, dout, (uint64_t)sp.B * sp.Lq, cols, S) ||
+        !encode_bf16_rows(&tk, k, (uint64_t)sp.B * sp.nP * S, cols, S) ||
+        !encode_bf16_rows(&tv, v, (uint64_t)sp.B * sp.nP * S, cols, S))
+        return cudaErrorInvalidValue;
+    const BwdWorkspace L = bwd_workspace_layout(sp);
+    char* base = static_cast<char*>(ws);
+    BwdArgs a;
+    a.idx = idx; a.w = w; a.lse = lse;
+    a.lse2_rows = reinterpret_cast<float*>(base + L.lse2_off);
+    a.delta_rows = reinterpret_cast<float*>(base + L.delta_off);
+    a.dwpart = reinterpret_cast<float*>(base + L.dwpart_off);
+    a.offset = reinterpret_cast<const int*>(base + L.offset_off);
+    a.entry = reinterpret_cast<const int*>(base + L.entry_off);
+    a.dq = static_cast<__nv_bfloat16*>(dq);
+    a.dk = static_cast<__nv_bfloat16*>(dk);
+    a.dv = static_cast<__nv_bfloat16*>(dv);
+    a.status = status;
+    a.B = sp.B; a.nQ = sp.nQ; a.nP = sp.nP; a.H = sp.H; a.topk = sp.topk; a.Lq = sp.Lq;
+    a.scale_log2 = sp.attn_scale * kLog2e;
+    a.attn_scale = sp.attn_scale;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+    a.n_items = sp.B * sp.nQ * sp.H;
+    auto ka = gca_bwd_q_tc_kernel<S>;
+    cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgA<S>::SMEM);
+    if (e != cudaSuccess) return e;
+    int grid = a.n_items < sms ? a.n_items : sms;
+    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreads, CfgA<S>::SMEM, st>>>(tq, tdo, tk, tv, a));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    a.n_items = sp.B * sp.nP * sp.H;
+    auto kb = gca_bwd_kv_tc_kernel<S>;
+    e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S>::SMEM);
+    if (e != cudaSuccess) return e;
+    grid = a.n_items < sms ? a.n_items : sms;
+    GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgB<S>::SMEM, st>>>(tq, tdo, tk, tv, a));
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_tc(const Shape& sp, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const float* w, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, float* dscore, void* ws, int* status,
+                          cudaStream_t st, int* launches) {
+    cudaError_t e = launch_inverse_index(sp, idx, ws, st, launches);
+    if (e != cudaSuccess) return e;
+    e = (sp.S == 64) ? launch_bwd_s<64>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st)
+                     : launch_bwd_s<128>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);
+    if (e != cudaSuccess) return e;
+    *launches += 2;
+    return launch_dscore(sp, idx, w, ws, dscore, st, launches);
+}
+
 }  // namespace gca

@@ -1,7 +1,8 @@
 // attn_simt.cu -- fp32 FFMA kernels of the GCA forward and backward.
 //
-// These carry the fp32 element type, whose tolerance (1e-4) rules out the
-// tensor cores' reduced-precision fp32 modes.  One CTA per (query chunk,
+// These carry the fp32 element type (the bf16 type runs on the tensor cores,
+// attn_fwd_tc.cu / attn_bwd_tc.cu); its 1e-4 tolerance rules out the tensor
+// cores' reduced-precision fp32 modes.  One CTA per (query chunk,
 // head, batch row) in the query-major kernels and per (pool chunk, head,
 // batch row) in the key-major one; one thread per token (or per key) row.
 // Every retrieved chunk's K/V (or every retrieving chunk's Q/dO) tile is
@@ -275,8 +276,6 @@ cudaError_t launch_fwd_simt(const Shape& sp, const void* q, const void* k, const
         if (sp.d == 16) e = fwd_dh<float, 16>(sp, q, k, v, idx, w, o, lse, status, st);
         if (sp.d == 32) e = fwd_dh<float, 32>(sp, q, k, v, idx, w, o, lse, status, st);
         if (sp.d == 64) e = fwd_dh<float, 64>(sp, q, k, v, idx, w, o, lse, status, st);
-    } else if (sp.d == 64) {
-        e = fwd_dh<__nv_bfloat16, 64>(sp, q, k, v, idx, w, o, lse, status, st);
     }
     if (e == cudaSuccess) *launches += 1;
     return e;
@@ -293,8 +292,6 @@ cudaError_t launch_bwd_simt(const Shape& sp, const void* q, const void* k, const
         if (sp.d == 16) e = bwd_dh<float, 16>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);
         if (sp.d == 32) e = bwd_dh<float, 32>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);
         if (sp.d == 64) e = bwd_dh<float, 64>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);
-    } else if (sp.d == 64) {
-        e = bwd_dh<__nv_bfloat16, 64>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);
     }
     if (e != cudaSuccess) return e;
     *launches += 2;

@@ -72,6 +72,11 @@ cudaError_t launch_bwd_simt(const Shape& s, const void* q, const void* k, const 
                             const void* dout, void* dq, void* dk, void* dv, float* dscore,
                             void* ws, int* status, cudaStream_t st, int* launches);
 
+cudaError_t launch_bwd_tc(const Shape& s, const void* q, const void* k, const void* v,
+                          const int32_t* idx, const float* w, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, float* dscore,
+                          void* ws, int* status, cudaStream_t st, int* launches);
+
 // Shared backward pieces (inverse index, score gradient).
 cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, cudaStream_t st,
                                  int* launches);
