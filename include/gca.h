@@ -12,8 +12,8 @@
  * Conventions shared by every entry point
  *  - Tensor arguments are DEVICE pointers owned by the caller, except where
  *    an argument says "host".  The library allocates no memory and keeps no
- *    state except a per-device status word (see gca_get_status) and, for
- *    the decode entry point, the per-device TMA descriptors it encodes.
+ *    state except a per-device status word (see gca_get_status) and the
+ *    fixed scratch array of gca_decode_retrieve_noalloc.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *    work is enqueued asynchronously on it.
  *  - The return value reports argument validation and launch errors.
@@ -139,6 +139,36 @@ gca_status_t gca_decode_retrieve(const void* landmarks, const void* query_landma
                                  int topk, gca_dtype_t dtype, int softmax_off_by_one,
                                  float score_scale, int32_t* idx, float* score, float* weight,
                                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gca_decode_retrieve_noalloc -- gca_decode_retrieve for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this is a usage
+ * variant of the same decode retrieval, not a different operation.
+ *   Some callers are handed only their input and output buffers and may not
+ *   call cudaMalloc (or any allocating routine) themselves: plugin interfaces
+ *   of inference engines, runtimes that plan every device byte at start-up,
+ *   and latency-critical loops where an allocation's implicit device
+ *   synchronisation is not acceptable.  This entry point needs no workspace
+ *   argument: its scratch (a ticket counter and the per-CTA candidate lists)
+ *   lives in a file-scope device array of GCA_DECODE_STATIC_SCRATCH_BYTES
+ *   bytes that every GPU loading the library holds until the process exits.
+ *   Arguments, layouts and results are those of gca_decode_retrieve.
+ *   Limits: the scratch holds 32768 (CTA, rank) candidates, i.e. any N with
+ *   topk <= 16, or N <= 131072 with topk <= 32; larger requests return
+ *   GCA_ERR_WORKSPACE and enqueue nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls on a device share the one array, which keeps the previous
+ *   call's contents (the counter is cleared on the stream before each
+ *   launch): calls whose executions overlap on the GPU (other streams, other
+ *   host threads) race on it and must be serialised by the caller.
+ *   Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define GCA_DECODE_STATIC_SCRATCH_BYTES (256u + 262144u)
+gca_status_t gca_decode_retrieve_noalloc(const void* landmarks, const void* query_landmark, int N,
+                                         int D, int topk, gca_dtype_t dtype,
+                                         int softmax_off_by_one, float score_scale, int32_t* idx,
+                                         float* score, float* weight, void* stream);
 
 /*
  * gca_get_status -- synchronise `stream`, then return and clear the device

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "GCA_OK", 1: "GCA_ERR_INVALID_ARG", 2: "GCA_ERR_UNSUPPORTED",
 EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_decode_workspace_size", "gca_decode_retrieve", "gca_get_status",
             "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
-            "gca_prof_enable", "gca_prof_read")
+            "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc")
 
 
 class GcaParams(ctypes.Structure):
@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
             "gca_decode_workspace_size": ([i32, i32, i32], sz),
             "gca_decode_retrieve": ([vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, sz, vp],
                                     i32),
+            "gca_decode_retrieve_noalloc": ([vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp],
+                                            i32),
             "gca_get_status": ([vp], i32),
             "gca_status_string": ([i32], ctypes.c_char_p),
             "gca_last_launch_count": ([], i32),

@@ -92,6 +92,15 @@ def gca_decode_retrieve(landmarks, query_landmark, N, D, topk, dtype, off_by_one
         _stream(stream)))
 
 
+def gca_decode_retrieve_noalloc(landmarks, query_landmark, N, D, topk, dtype, off_by_one,
+                                score_scale, idx, score, weight, stream=None):
+    """Decode retrieval without a workspace argument, for callers that may not
+    allocate device memory (the library's own fixed device array is used)."""
+    _check("gca_decode_retrieve_noalloc", _lib.load().gca_decode_retrieve_noalloc(
+        _p(landmarks), _p(query_landmark), N, D, topk, dtype_code(dtype), int(bool(off_by_one)),
+        float(score_scale), _p(idx), _p(score), _p(weight), _stream(stream)))
+
+
 def gca_get_status(stream=None) -> int:
     return int(_lib.load().gca_get_status(_stream(stream)))
 

@@ -12,6 +12,8 @@
 // are exact in fp32, so the ranking is the exact (score desc, index asc) one.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -232,3 +234,64 @@ cudaError_t launch_decode_retrieve(const void* lm, const void* ql, int N, int D,
 }
 
 }  // namespace gca
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the scratch lives in a file-scope device array.
+// ---------------------------------------------------------------------------
+namespace gca {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[GCA_DECODE_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDev = 64;
+void* g_scratch_ptr[kMaxDev];
+std::mutex g_scratch_mu;
+
+// Device address of g_decode_scratch on the current device (looked up once
+// per device).  In host code the array's name is only a host-side stand-in.
+cudaError_t static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace gca
+
+extern "C" gca_status_t gca_decode_retrieve_noalloc(const void* landmarks,
+                                                    const void* query_landmark, int N, int D,
+                                                    int topk, gca_dtype_t dtype,
+                                                    int softmax_off_by_one, float score_scale,
+                                                    int32_t* idx, float* score, float* weight,
+                                                    void* stream) {
+    using namespace gca;
+    if (N < 1 || D < 1 || topk < 1) return GCA_ERR_INVALID_ARG;
+    if (dtype != GCA_BF16 && dtype != GCA_F32) return GCA_ERR_INVALID_ARG;
+    if (!(score_scale >= 0.f)) return GCA_ERR_INVALID_ARG;
+    const void* ptrs[5] = {landmarks, query_landmark, idx, score, weight};
+    for (const void* p : ptrs)
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GCA_ERR_INVALID_ARG;
+    if (topk > kMaxTopk) return GCA_ERR_UNSUPPORTED;
+    const int esize = dtype == GCA_BF16 ? 2 : 4;
+    if ((D * esize) % 16 != 0 || D * esize > 16 * 256) return GCA_ERR_UNSUPPORTED;
+    if (decode_workspace_bytes(N, topk) > GCA_DECODE_STATIC_SCRATCH_BYTES) return GCA_ERR_WORKSPACE;
+    void* ws = nullptr;
+    if (static_scratch(&ws) != cudaSuccess) return GCA_ERR_CUDA;
+    const float sc = score_scale > 0.f ? score_scale : 1.0f / sqrtf((float)D);
+    int n = 0;
+    const cudaError_t e = launch_decode_retrieve(landmarks, query_landmark, N, D, topk, dtype,
+                                                 softmax_off_by_one ? 1 : 0, sc, idx, score,
+                                                 weight, ws, nullptr,
+                                                 static_cast<cudaStream_t>(stream), &n);
+    return e == cudaSuccess ? GCA_OK : GCA_ERR_CUDA;
+}
