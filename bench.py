@@ -41,7 +41,15 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the forward-only and decode lines")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--case", default=None, choices=sorted(CASES),
+                    help="profiling mode: run only this path (warm-up + steps), print timings")
     return ap.parse_args()
+
+
+#: small cases for profiler captures: (workload, batch rows, with backward)
+CASES = {"fwd_b4": ("gpt2s_fwd_b4", 4, False), "fwdbwd_b4": ("gpt2s_fwdbwd_b8", 4, True),
+         "fwdbwd_b8": ("gpt2s_fwdbwd_b8", 8, True), "long_s64_k16": ("long64k_S64_k16", 1, True),
+         "long_s128_k8": ("long64k_S128_k8", 1, True), "decode": (None, 1, False)}
 
 
 def peaks():
@@ -444,9 +452,48 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Profiling mode: only the named path, W warm-up + K timed steps."""
+    import torch
+
+    from retrieval_sparse_attention_gb300 import api, inputs
+    name, B, backward = CASES[args.case]
+    dev = torch.device("cuda", 0)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if name is None:
+        hx = inputs.decode_inputs()
+        lm, ql = hx["lm"].to(dev), hx["ql"].to(dev)
+        p = inputs.DECODE
+        ws = torch.empty(api.gca_decode_workspace_size(p["N"], p["D"], p["topk"]), dtype=torch.uint8,
+                         device=dev)
+        step = lambda: api.decode_retrieve(lm, ql, topk=p["topk"], workspace=ws)
+    else:
+        wl = inputs.WORKLOADS[name]
+        x = {n: t.to(dev) for n, t in inputs.make(wl, B=B, with_dout=backward).items()}
+        ob = wl.off_by_one
+
+        def step():
+            idx, r, w = api.score_topk(x["lm"], S=wl.S, H=wl.H, d=wl.d, topk=wl.topk, off_by_one=ob)
+            o, lse = api.fwd(x["q"], x["k"], x["v"], idx, w, S=wl.S)
+            if backward:
+                api.bwd(x["q"], x["k"], x["v"], idx, w, lse, x["dout"], S=wl.S)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    assert api.gca_get_status() == 0
+    print(json.dumps({"case": args.case, "ms_per_step": ev0.elapsed_time(ev1) / args.steps}))
+
+
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.case is not None:
+        run_case(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)
