@@ -3,19 +3,25 @@
 // Long-Context Language Modeling": once per chunk of generated tokens the new
 // landmark scores every stored landmark and the top-k chunks are reloaded).
 //
-// The landmark table is streamed once from HBM: each warp walks rows with
-// 16-byte vector loads (several rows in flight), scores them against the
-// query landmark held in shared memory as fp32, and keeps a running top-k in
-// registers, one rank per lane.  Warps merge into a per-CTA list; the CTA
-// that finishes last (ticket counter, no waiting) merges every CTA's list,
-// applies the softmax and writes the result.  Scores of integer landmarks
-// are exact in fp32, so the ranking is the exact (score desc, index asc) one.
+// The landmark table is streamed once from HBM.  Each CTA owns a contiguous
+// range of rows and pulls it through a 4-stage shared-memory ring with bulk
+// asynchronous copies (cp.async.bulk, one thread issues, an mbarrier counts
+// the bytes), so the copy engine keeps HBM busy independently of the math.
+// Warps score the staged rows against the query landmark held in registers
+// as fp32 (exact for integer landmarks) and keep a running top-k in
+// registers, one rank per lane, with the admission threshold replicated in
+// every lane so that the common case (row not in the top-k) costs one
+// compare.  Warps merge into a per-CTA list; the CTA that finishes last
+// (ticket counter, no waiting) merges every CTA's list, filtering 32
+// candidates per ballot, applies the softmax and resets the counter.
 #include <math.h>
 
 #include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace gca {
 namespace {
@@ -23,21 +29,39 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxBlocks = 2048;
-constexpr int kRowsInFlight = 4;
+constexpr int kStages = 4;
+constexpr int kStageBytes = 24576;
 
-// Insert (s, i) into the warp's sorted top-k list (lane j holds rank j).
-__device__ __forceinline__ void warp_insert(float& ts, int& ti, int topk, float s, int i) {
-    const int lane = threadIdx.x & 31;
-    const float ws = __shfl_sync(0xffffffffu, ts, topk - 1);
-    const int wi = __shfl_sync(0xffffffffu, ti, topk - 1);
-    if (!ranks_before(s, i, ws, wi)) return;            // uniform across the warp
-    const unsigned ahead = __ballot_sync(0xffffffffu, lane < topk && ranks_before(ts, ti, s, i));
-    const int pos = __popc(ahead);
-    const float us = __shfl_up_sync(0xffffffffu, ts, 1);
-    const int ui = __shfl_up_sync(0xffffffffu, ti, 1);
-    if (lane == pos) { ts = s; ti = i; }
-    else if (lane > pos && lane < topk) { ts = us; ti = ui; }
-}
+// Running top-k of a warp: lane j holds rank j (score desc, index asc); every
+// lane also holds the current admission threshold (rank topk-1).
+struct WarpTopk {
+    float ts, thr_s;
+    int ti, thr_i;
+    __device__ void init() { ts = thr_s = -INFINITY; ti = thr_i = 0x7fffffff; }
+    // (s, i) is uniform across the warp.
+    __device__ __forceinline__ void offer(int topk, float s, int i) {
+        if (!ranks_before(s, i, thr_s, thr_i)) return;
+        const int lane = threadIdx.x & 31;
+        const unsigned ahead = __ballot_sync(0xffffffffu, lane < topk && ranks_before(ts, ti, s, i));
+        const int pos = __popc(ahead);
+        const float us = __shfl_up_sync(0xffffffffu, ts, 1);
+        const int ui = __shfl_up_sync(0xffffffffu, ti, 1);
+        if (lane == pos) { ts = s; ti = i; }
+        else if (lane > pos && lane < topk) { ts = us; ti = ui; }
+        thr_s = __shfl_sync(0xffffffffu, ts, topk - 1);
+        thr_i = __shfl_sync(0xffffffffu, ti, topk - 1);
+    }
+    // Offer 32 candidates at once (lane l holds one); only those that beat the
+    // threshold are inserted, in lane order.
+    __device__ __forceinline__ void offer32(int topk, float cs, int ci) {
+        unsigned m = __ballot_sync(0xffffffffu, ranks_before(cs, ci, thr_s, thr_i));
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            offer(topk, __shfl_sync(0xffffffffu, cs, src), __shfl_sync(0xffffffffu, ci, src));
+        }
+    }
+};
 
 template <typename T>
 __device__ __forceinline__ float dot16(const uint4& raw, const float* qv);
@@ -61,23 +85,62 @@ __device__ __forceinline__ float dot16<float>(const uint4& raw, const float* qv)
     return f[0] * qv[0] + f[1] * qv[1] + f[2] * qv[2] + f[3] * qv[3];
 }
 
+struct __align__(8) DecodeBars {
+    uint64_t full[kStages], empty[kStages];
+    int abort;
+    bool is_last;
+};
+
 template <typename T, int VPL>
 __global__ void __launch_bounds__(kThreads)
 decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N, int D,
                        int topk, int off_by_one, float sscale, int32_t* __restrict__ out_idx,
                        float* __restrict__ out_score, float* __restrict__ out_weight,
-                       unsigned* ticket, float* blk_s, int* blk_i) {
+                       unsigned* ticket, float* blk_s, int* blk_i, int* status) {
     constexpr int kEPV = 16 / sizeof(T);                 // elements per 16-byte vector
-    extern __shared__ float qsh[];                       // [D] query landmark
+    extern __shared__ uint8_t dsm_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 127) &
+                                               ~static_cast<uintptr_t>(127));
+    float* qsh = reinterpret_cast<float*>(ring + kStages * kStageBytes);   // [D]
+    __shared__ DecodeBars bars;
     __shared__ float ws_s[kWarps][kMaxTopk];
     __shared__ int ws_i[kWarps][kMaxTopk];
-    __shared__ bool is_last;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nvec = D / kEPV;                           // vectors per row (<= 32 * VPL)
+    const int row_bytes = nvec * 16;
+    const int rows_per_stage = kStageBytes / row_bytes;
+    const int per_blk = (N + gridDim.x - 1) / gridDim.x;
+    const int r0 = min(N, blockIdx.x * per_blk);
+    const int r1 = min(N, r0 + per_blk);
+    const int n_stages_total = (r1 - r0 + rows_per_stage - 1) / rows_per_stage;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(&bars.full[i], 1);
+            tc::mbar_init(&bars.empty[i], kWarps);
+        }
+        bars.abort = 0;
+        tc::fence_barrier_init();
+    }
     for (int e = threadIdx.x; e < D; e += kThreads) qsh[e] = to_f(ql[e]);
     __syncthreads();
 
-    const int nvec = D / kEPV;                           // vectors per row (<= 32 * VPL)
+    // Copies of stage g cover rows r0 + g*rows_per_stage ...
+    auto issue = [&](int g) {
+        const int slot = g % kStages;
+        const int ra = r0 + g * rows_per_stage;
+        const int nr = min(rows_per_stage, r1 - ra);
+        const uint32_t bytes = static_cast<uint32_t>(nr) * row_bytes;
+        tc::mbar_arrive_expect_tx(&bars.full[slot], bytes);
+        tcx::bulk_load(ring + slot * kStageBytes,
+                       reinterpret_cast<const uint8_t*>(lm) + (size_t)ra * row_bytes, bytes,
+                       &bars.full[slot]);
+    };
+    int n_issued = 0;                                    // meaningful in thread 0 only
+    if (threadIdx.x == 0)
+        for (; n_issued < kStages && n_issued < n_stages_total; ++n_issued) issue(n_issued);
+
     float qv[VPL][kEPV];
 #pragma unroll
     for (int u = 0; u < VPL; ++u) {
@@ -86,75 +149,87 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
         for (int x = 0; x < kEPV; ++x) qv[u][x] = (vi < nvec) ? qsh[vi * kEPV + x] : 0.f;
     }
 
-    float ts = -INFINITY;
-    int ti = 0x7fffffff;
-    // Contiguous block of rows per CTA, rows interleaved across its warps.
-    const int per_blk = (N + gridDim.x - 1) / gridDim.x;
-    const int r0 = blockIdx.x * per_blk;
-    const int r1 = min(N, r0 + per_blk);
-    const uint4* base = reinterpret_cast<const uint4*>(lm);
-    for (int r = r0 + warp * kRowsInFlight; r < r1; r += kWarps * kRowsInFlight) {
-        uint4 raw[kRowsInFlight][VPL];
-#pragma unroll
-        for (int a = 0; a < kRowsInFlight; ++a)
+    WarpTopk tk;
+    tk.init();
+    bool ok = true;
+    for (int g = 0; g < n_stages_total; ++g) {
+        const int slot = g % kStages;
+        const uint32_t par = static_cast<uint32_t>(g / kStages) & 1u;
+        if (!tcx::wait_bar(&bars.abort, &bars.full[slot], par, status)) { ok = false; break; }
+        const int ra = r0 + g * rows_per_stage;
+        const int nr = min(rows_per_stage, r1 - ra);
+        const uint4* st = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
+        for (int rr = warp; rr < nr; rr += kWarps) {
+            float acc = 0.f;
 #pragma unroll
             for (int u = 0; u < VPL; ++u) {
                 const int vi = lane + 32 * u;
-                if (r + a < r1 && vi < nvec)
-                    raw[a][u] = __ldcs(base + (size_t)(r + a) * nvec + vi);
-                else
-                    raw[a][u] = make_uint4(0, 0, 0, 0);
+                if (vi < nvec) acc += dot16<T>(st[rr * nvec + vi], qv[u]);
             }
-#pragma unroll
-        for (int a = 0; a < kRowsInFlight; ++a) {
-            float acc = 0.f;
-#pragma unroll
-            for (int u = 0; u < VPL; ++u) acc += dot16<T>(raw[a][u], qv[u]);
             acc = warp_sum(acc);
-            if (r + a < r1) warp_insert(ts, ti, topk, acc, r + a);
+            tk.offer(topk, acc, ra + rr);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars.empty[slot]);
+        if (threadIdx.x == 0 && g + kStages < n_stages_total) {
+            // refill this slot once every warp has released it
+            if (!tcx::wait_bar(&bars.abort, &bars.empty[slot], par, status)) { ok = false; break; }
+            issue(g + kStages);
+            ++n_issued;
         }
     }
-    if (lane < kMaxTopk) { ws_s[warp][lane] = ts; ws_i[warp][lane] = ti; }
+    // Never leave a copy in flight behind an early exit: wait (bounded) for the
+    // last copy issued into each slot.
+    if (threadIdx.x == 0 && !ok)
+        for (int g = max(0, n_issued - kStages); g < n_issued; ++g)
+            tc::mbar_wait(&bars.full[g % kStages], static_cast<uint32_t>(g / kStages) & 1u, nullptr,
+                          100000000ull);
+
+    if (lane < kMaxTopk) { ws_s[warp][lane] = tk.ts; ws_i[warp][lane] = tk.ti; }
     __syncthreads();
     if (warp == 0) {
         for (int w = 1; w < kWarps; ++w)
-            for (int j = 0; j < topk; ++j) warp_insert(ts, ti, topk, ws_s[w][j], ws_i[w][j]);
+            tk.offer32(topk, lane < topk ? ws_s[w][lane] : -INFINITY,
+                       lane < topk ? ws_i[w][lane] : 0x7fffffff);
         if (lane < topk) {
-            blk_s[(size_t)blockIdx.x * topk + lane] = ts;
-            blk_i[(size_t)blockIdx.x * topk + lane] = ti;
+            blk_s[(size_t)blockIdx.x * topk + lane] = tk.ts;
+            blk_i[(size_t)blockIdx.x * topk + lane] = tk.ti;
         }
         __threadfence();
-        if (lane == 0) is_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
+        if (lane == 0) bars.is_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
     }
     __syncthreads();
-    if (!is_last) return;
+    if (!bars.is_last) return;
 
-    // Last CTA: merge every CTA's list (warps split the CTAs, then warp 0).
+    // Last CTA: merge every CTA's list, 32 candidates per ballot.
     __threadfence();
-    ts = -INFINITY;
-    ti = 0x7fffffff;
-    for (int bk = warp; bk < (int)gridDim.x; bk += kWarps)
-        for (int j = 0; j < topk; ++j)
-            warp_insert(ts, ti, topk, __ldcg(blk_s + (size_t)bk * topk + j),
-                        __ldcg(blk_i + (size_t)bk * topk + j));
-    if (lane < kMaxTopk) { ws_s[warp][lane] = ts; ws_i[warp][lane] = ti; }
+    tk.init();
+    const int total = gridDim.x * topk;
+    for (int base = warp * 32; base < total; base += kWarps * 32) {
+        const int e = base + lane;
+        const float cs = e < total ? __ldcg(blk_s + e) : -INFINITY;
+        const int ci = e < total ? __ldcg(blk_i + e) : 0x7fffffff;
+        tk.offer32(topk, cs, ci);
+    }
+    if (lane < kMaxTopk) { ws_s[warp][lane] = tk.ts; ws_i[warp][lane] = tk.ti; }
     __syncthreads();
     if (warp == 0) {
         for (int w = 1; w < kWarps; ++w)
-            for (int j = 0; j < topk; ++j) warp_insert(ts, ti, topk, ws_s[w][j], ws_i[w][j]);
+            tk.offer32(topk, lane < topk ? ws_s[w][lane] : -INFINITY,
+                       lane < topk ? ws_i[w][lane] : 0x7fffffff);
         const int m = N < topk ? N : topk;
-        const bool ok = lane < m;
-        const float r = ok ? ts * sscale : -INFINITY;
+        const bool okl = lane < m;
+        const float r = okl ? tk.ts * sscale : -INFINITY;
         float mx = r;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (off_by_one) mx = fmaxf(mx, 0.f);
-        const float e = ok ? expf(r - mx) : 0.f;
+        const float e = okl ? expf(r - mx) : 0.f;
         float den = warp_sum(e) + (off_by_one ? expf(-mx) : 0.f);
         if (lane < topk) {
-            out_idx[lane] = ok ? ti : -1;
-            out_score[lane] = ok ? r : 0.f;
-            out_weight[lane] = ok ? e / den : 0.f;
+            out_idx[lane] = okl ? tk.ti : -1;
+            out_score[lane] = okl ? r : 0.f;
+            out_weight[lane] = okl ? e / den : 0.f;
         }
         if (lane == 0) *ticket = 0u;     // leave the counter reset for the next call
     }
@@ -180,9 +255,9 @@ namespace {
 template <typename T, int VPL>
 cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, int off_by_one,
                        float score_scale, int32_t* idx, float* score, float* weight, void* ws,
-                       cudaStream_t st) {
+                       int* status, cudaStream_t st) {
     auto kern = decode_retrieve_kernel<T, VPL>;
-    const size_t smem = sizeof(float) * (size_t)D;
+    const size_t smem = (size_t)kStages * kStageBytes + 128 + sizeof(float) * (size_t)D;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, per_sm = 0;
@@ -197,24 +272,28 @@ cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, i
     int* blk_i = reinterpret_cast<int*>(blk_s + (size_t)nb * topk);
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return e;
-    GCA_LAUNCH("decode_retrieve", st, kern<<<nb, kThreads, smem, st>>>((const T*)lm, (const T*)ql, N, D, topk, off_by_one,
-                                     score_scale, idx, score, weight, ticket, blk_s, blk_i));
+    GCA_LAUNCH("decode_retrieve", st,
+               kern<<<nb, kThreads, smem, st>>>((const T*)lm, (const T*)ql, N, D, topk, off_by_one,
+                                                score_scale, idx, score, weight, ticket, blk_s,
+                                                blk_i, status));
     return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_t(const void* lm, const void* ql, int N, int D, int topk, int off_by_one,
-                     float sc, int32_t* idx, float* score, float* weight, void* ws, cudaStream_t st) {
+                     float sc, int32_t* idx, float* score, float* weight, void* ws, int* status,
+                     cudaStream_t st) {
     const int nvec = D * (int)sizeof(T) / 16;
     const int vpl = (nvec + 31) / 32;
     switch (vpl) {
-        case 1: return launch_vpl<T, 1>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, st);
-        case 2: return launch_vpl<T, 2>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, st);
-        case 3: return launch_vpl<T, 3>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, st);
-        case 4: return launch_vpl<T, 4>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, st);
-        case 6: return launch_vpl<T, 6>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, st);
-        case 5: case 7: case 8:
-            return launch_vpl<T, 8>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, st);
+        case 1: return launch_vpl<T, 1>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, status, st);
+        case 2: return launch_vpl<T, 2>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, status, st);
+        case 3: return launch_vpl<T, 3>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, status, st);
+        case 4: return launch_vpl<T, 4>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, status, st);
+        case 5: case 6:
+            return launch_vpl<T, 6>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, status, st);
+        case 7: case 8:
+            return launch_vpl<T, 8>(lm, ql, N, D, topk, off_by_one, sc, idx, score, weight, ws, status, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -225,10 +304,9 @@ cudaError_t launch_decode_retrieve(const void* lm, const void* ql, int N, int D,
                                    gca_dtype_t dt, int off_by_one, float score_scale,
                                    int32_t* idx, float* score, float* weight, void* ws,
                                    int* status, cudaStream_t st, int* launches) {
-    (void)status;
     cudaError_t e = (dt == GCA_BF16)
-        ? launch_t<__nv_bfloat16>(lm, ql, N, D, topk, off_by_one, score_scale, idx, score, weight, ws, st)
-        : launch_t<float>(lm, ql, N, D, topk, off_by_one, score_scale, idx, score, weight, ws, st);
+        ? launch_t<__nv_bfloat16>(lm, ql, N, D, topk, off_by_one, score_scale, idx, score, weight, ws, status, st)
+        : launch_t<float>(lm, ql, N, D, topk, off_by_one, score_scale, idx, score, weight, ws, status, st);
     if (e == cudaSuccess) *launches += 1;
     return e;
 }
