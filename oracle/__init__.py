@@ -53,6 +53,9 @@ def _load():
         lib.oracle_fwd.argtypes = [i32] * 7 + [f64] + [vp] * 8
         lib.oracle_bwd.argtypes = [i32] * 7 + [f64] + [vp] * 12
         lib.oracle_num_threads.restype = i32
+        lib.oracle_landmark_bwd.argtypes = [i32, i32, i32, i32, f64, vp, vp, vp, vp]
+        lib.oracle_score_topk_noisy.argtypes = [i32, i32, i32, i32, i32, i32, f64, vp, vp, vp, vp, vp]
+        lib.oracle_score_topk_noisy.restype = i32
         _lib = lib
     return _lib
 
@@ -158,3 +161,39 @@ def bwd(q, k, v, idx, w, dout, S: int, attn_scale: float | None = None, qmask=No
                        _ptr(idx), _ptr(w), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ds),
                        _ptr(qm), _ptr(km))
     return dq, dk, dv, ds
+
+
+def landmark_bwd(lm, idx, dscore, score_scale: float | None = None):
+    """Gradient of the loss w.r.t. the landmarks given dLoss/dr.  lm [B, nC, D]."""
+    lm = _f64(lm)
+    dscore = _f64(dscore)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    B, nC, D = lm.shape
+    topk = idx.shape[-1]
+    if score_scale is None:
+        score_scale = 1.0 / np.sqrt(D)
+    dl = np.zeros_like(lm)
+    _load().oracle_landmark_bwd(B, nC, D, topk, float(score_scale), _ptr(lm), _ptr(idx),
+                                _ptr(dscore), _ptr(dl))
+    return dl
+
+
+def score_topk_noisy(lm, noise, topk: int, include_self: bool = False, off_by_one: bool = False,
+                     score_scale: float | None = None):
+    """Top-k selected by r + noise (fp32 key), softmax over the clean r.
+    noise [B, nC, nC] float32."""
+    lm = _f64(lm)
+    noise = np.ascontiguousarray(noise, dtype=np.float32)
+    B, nC, D = lm.shape
+    assert noise.shape == (B, nC, nC)
+    if score_scale is None:
+        score_scale = 1.0 / np.sqrt(D)
+    idx = np.empty((B, nC, topk), dtype=np.int32)
+    r = np.empty((B, nC, topk))
+    w = np.empty((B, nC, topk))
+    rc = _load().oracle_score_topk_noisy(B, nC, D, topk, int(include_self), int(off_by_one),
+                                         float(score_scale), _ptr(lm), _ptr(noise), _ptr(idx),
+                                         _ptr(r), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_score_topk_noisy: topk must be in [1, 64]")
+    return idx, r, w

@@ -358,3 +358,98 @@ int oracle_num_threads(void) { return omp_get_max_threads(); }
 #else
 int oracle_num_threads(void) { return 1; }
 #endif
+
+/* ---------------------------------------------------------------------- */
+/* Landmark gradients ([P1] sections 1 and 3: the relevance scores take    */
+/* part in next-token prediction, so the retriever that produces the       */
+/* landmarks learns from the loss; [P2] Cmt 1: r = sigma * l_{c-1} . l_k). */
+/* For every valid slot (b, c, j) with chunk kappa:                        */
+/*   dl[b][c-1]   += sigma * dr[b][c][j] * l[b][kappa]                     */
+/*   dl[b][kappa] += sigma * dr[b][c][j] * l[b][c-1]                       */
+/*   lm, dl [B, nC, D]; idx, dr [B, nC, topk]; dl is overwritten.          */
+/* ---------------------------------------------------------------------- */
+void oracle_landmark_bwd(int B, int nC, int D, int topk, double score_scale, const double* lm,
+                         const int32_t* idx, const double* dr, double* dl)
+{
+    memset(dl, 0, sizeof(double) * (size_t)B * nC * D);
+    for (int b = 0; b < B; ++b) {
+        for (int c = 1; c < nC; ++c) {
+            const double* lt = lm + ((size_t)b * nC + (c - 1)) * D;
+            double* dlt = dl + ((size_t)b * nC + (c - 1)) * D;
+            for (int j = 0; j < topk; ++j) {
+                int kappa = idx[((size_t)b * nC + c) * topk + j];
+                if (kappa < 0 || kappa >= nC) continue;
+                double g = score_scale * dr[((size_t)b * nC + c) * topk + j];
+                const double* lk = lm + ((size_t)b * nC + kappa) * D;
+                double* dlk = dl + ((size_t)b * nC + kappa) * D;
+                for (int e = 0; e < D; ++e) {
+                    dlt[e] += g * lk[e];
+                    dlk[e] += g * lt[e];
+                }
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Top-k under Gumbel noise ([P1] section 3.2: during training, noise is    */
+/* added to the relevance scores before the top-k selection; the pages do  */
+/* not say which scores the softmax then uses: here the clean ones).       */
+/* The selection key is  fl32(fl32(fl32(s) * fl32(sigma)) + fl32(g))        */
+/* evaluated in single precision exactly as written (no fused multiply-    */
+/* add), so that the integer decision is taken in the same precision as on */
+/* the GPU; ties go to the lower chunk index.  noise [B, nC, nC]: the noise */
+/* for query chunk c and candidate kappa is noise[b][c][kappa].             */
+/* ---------------------------------------------------------------------- */
+typedef struct { float key; int kappa; double s; } ncand_t;
+
+static int ncand_cmp(const void* a, const void* b)
+{
+    const ncand_t* x = (const ncand_t*)a;
+    const ncand_t* y = (const ncand_t*)b;
+    if (x->key > y->key) return -1;
+    if (x->key < y->key) return 1;
+    return (x->kappa > y->kappa) - (x->kappa < y->kappa);
+}
+
+int oracle_score_topk_noisy(int B, int nC, int D, int topk, int include_self, int off_by_one,
+                            double score_scale, const double* lm, const float* noise,
+                            int32_t* idx, double* score, double* weight)
+{
+    if (topk < 1 || topk > 64) return -1;
+    volatile float sigma32 = (float)score_scale;
+    for (int b = 0; b < B; ++b) {
+        for (int c = 0; c < nC; ++c) {
+            int32_t* ir = idx + ((size_t)b * nC + c) * topk;
+            double* sr = score + ((size_t)b * nC + c) * topk;
+            double* wr = weight + ((size_t)b * nC + c) * topk;
+            int t = c - 1;
+            int n = (t < 0) ? 0 : (include_self ? t + 1 : t);
+            ncand_t* cand = (ncand_t*)malloc(sizeof(ncand_t) * (size_t)(n > 0 ? n : 1));
+            const double* lt = lm + ((size_t)b * nC + (t < 0 ? 0 : t)) * D;
+            for (int kappa = 0; kappa < n; ++kappa) {
+                const double* lk = lm + ((size_t)b * nC + kappa) * D;
+                double s = 0.0;
+                for (int e = 0; e < D; ++e) s += lt[e] * lk[e];
+                volatile float s32 = (float)s;
+                volatile float r32 = s32 * sigma32;
+                volatile float key = r32 + noise[((size_t)b * nC + c) * nC + kappa];
+                cand[kappa].key = key;
+                cand[kappa].kappa = kappa;
+                cand[kappa].s = s;
+            }
+            qsort(cand, (size_t)n, sizeof(ncand_t), ncand_cmp);
+            int m = n < topk ? n : topk;
+            double r[64];
+            for (int j = 0; j < topk; ++j) { ir[j] = -1; sr[j] = 0.0; wr[j] = 0.0; }
+            for (int j = 0; j < m; ++j) {
+                ir[j] = cand[j].kappa;
+                r[j] = cand[j].s * score_scale;
+                sr[j] = r[j];
+            }
+            oracle_weights_from_scores(m, r, off_by_one, wr);
+            free(cand);
+        }
+    }
+    return 0;
+}
