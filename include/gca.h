@@ -87,6 +87,21 @@ gca_status_t gca_score_topk(const gca_params_t* params, const void* landmarks,
                             int32_t* idx, float* score, float* weight, void* stream);
 
 /*
+ * gca_score_topk_noisy -- gca_score_topk with the training-time exploration
+ * of section 3.2 (Gumbel noise is added to the relevance scores before the
+ * top-k selection).  The noise is drawn by the caller.
+ *   noise [B, nC, nC] fp32: noise[b][c][kappa] perturbs candidate kappa of
+ *   query chunk c (entries for kappa outside the candidate set are unused).
+ *   The selection key is fl32(fl32(s * score_scale) + noise), rounded step
+ *   by step (no fused multiply-add); ties go to the lower chunk index.
+ *   score and weight are computed from the clean scores of the selected
+ *   chunks, exactly as in gca_score_topk.  Other arguments as gca_score_topk.
+ */
+gca_status_t gca_score_topk_noisy(const gca_params_t* params, const void* landmarks,
+                                  const float* noise, int32_t* idx, float* score, float* weight,
+                                  void* stream);
+
+/*
  * gca_fwd -- GCA forward: per-chunk attention (stage 1) and weighted fusion
  * (stage 2).  Defines: README "Model Architecture" (two stages), Figure 1/2,
  * Eq. 2 (the batch form of Figure 2, rebuttal W2); App. B (the forward
@@ -123,6 +138,24 @@ gca_status_t gca_bwd(const gca_params_t* params, const void* q, const void* k, c
                      const int32_t* idx, const float* weight, const float* lse, const void* dout,
                      void* dq, void* dk, void* dv, float* dscore, void* workspace,
                      size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace gca_landmark_bwd needs. */
+size_t gca_landmark_bwd_workspace_size(const gca_params_t* params);
+
+/*
+ * gca_landmark_bwd -- gradient into the landmark vectors, closing the loop
+ * from the relevance-score gradient (gca_bwd's dscore) to the retriever.
+ * Defines: sections 1 and 3 (the retriever learns from the next-token loss
+ * through the relevance scores) with r = score_scale * l_{c-1} . l_kappa.
+ *   landmarks [B, nC, D], idx [B, nC, topk] (as used in the forward),
+ *   dscore [B, nC, topk] fp32 -> dlandmarks [B, nC, D] (params->dtype),
+ *   fully overwritten; fp32 accumulation in a fixed order, no atomics.
+ *   The selection itself is not differentiated.
+ *   workspace: >= gca_landmark_bwd_workspace_size() bytes, 256-byte aligned.
+ */
+gca_status_t gca_landmark_bwd(const gca_params_t* params, const void* landmarks,
+                              const int32_t* idx, const float* dscore, void* dlandmarks,
+                              void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of device workspace gca_decode_retrieve needs. */
 size_t gca_decode_workspace_size(int n_landmarks, int D, int topk);

@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "GCA_OK", 1: "GCA_ERR_INVALID_ARG", 2: "GCA_ERR_UNSUPPORTED",
 EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_decode_workspace_size", "gca_decode_retrieve", "gca_get_status",
             "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
-            "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc")
+            "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc",
+            "gca_score_topk_noisy", "gca_landmark_bwd_workspace_size", "gca_landmark_bwd")
 
 
 class GcaParams(ctypes.Structure):
@@ -57,6 +58,9 @@ def load() -> ctypes.CDLL:
         sig = {
             "gca_score_topk": ([P, vp, vp, vp, vp, vp], i32),
             "gca_fwd": ([P, vp, vp, vp, vp, vp, vp, vp, vp], i32),
+            "gca_score_topk_noisy": ([P, vp, vp, vp, vp, vp, vp], i32),
+            "gca_landmark_bwd_workspace_size": ([P], sz),
+            "gca_landmark_bwd": ([P, vp, vp, vp, vp, vp, sz, vp], i32),
             "gca_bwd_workspace_size": ([P], sz),
             "gca_bwd": ([P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "gca_decode_workspace_size": ([i32, i32, i32], sz),

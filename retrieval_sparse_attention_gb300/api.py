@@ -63,6 +63,22 @@ def gca_score_topk(params: GcaParams, landmarks, idx, score, weight, stream=None
                                                         _p(score), _p(weight), _stream(stream)))
 
 
+def gca_score_topk_noisy(params: GcaParams, landmarks, noise, idx, score, weight, stream=None):
+    _check("gca_score_topk_noisy", _lib.load().gca_score_topk_noisy(
+        ctypes.byref(params), _p(landmarks), _p(noise), _p(idx), _p(score), _p(weight),
+        _stream(stream)))
+
+
+def gca_landmark_bwd_workspace_size(params: GcaParams) -> int:
+    return int(_lib.load().gca_landmark_bwd_workspace_size(ctypes.byref(params)))
+
+
+def gca_landmark_bwd(params: GcaParams, landmarks, idx, dscore, dlandmarks, workspace, stream=None):
+    _check("gca_landmark_bwd", _lib.load().gca_landmark_bwd(
+        ctypes.byref(params), _p(landmarks), _p(idx), _p(dscore), _p(dlandmarks), _p(workspace),
+        workspace.numel(), _stream(stream)))
+
+
 def gca_fwd(params: GcaParams, q, k, v, idx, weight, o, lse=None, stream=None):
     _check("gca_fwd", _lib.load().gca_fwd(ctypes.byref(params), _p(q), _p(k), _p(v), _p(idx),
                                           _p(weight), _p(o), _p(lse), _stream(stream)))
@@ -127,6 +143,32 @@ def score_topk(landmarks, *, S, H, d, topk, off_by_one=False, include_self=False
     weight = torch.empty(B, nC, topk, dtype=torch.float32, device=dev)
     gca_score_topk(p, landmarks, idx, score, weight)
     return idx, score, weight
+
+
+def score_topk_noisy(landmarks, noise, *, S, H, d, topk, off_by_one=False, include_self=False,
+                     score_scale=0.0):
+    """Like score_topk, selecting by score + noise (noise [B, nC, nC] fp32)."""
+    B, nC, D = landmarks.shape
+    p = make_params(B=B, Lq=nC * S, S=S, H=H, d=d, topk=topk, landmark_dim=D,
+                    dtype=landmarks.dtype, off_by_one=off_by_one, include_self=include_self,
+                    score_scale=score_scale)
+    dev = landmarks.device
+    idx = torch.empty(B, nC, topk, dtype=torch.int32, device=dev)
+    score = torch.empty(B, nC, topk, dtype=torch.float32, device=dev)
+    weight = torch.empty(B, nC, topk, dtype=torch.float32, device=dev)
+    gca_score_topk_noisy(p, landmarks, noise, idx, score, weight)
+    return idx, score, weight
+
+
+def landmark_bwd(landmarks, idx, dscore, *, S, H, d, score_scale=0.0):
+    """dLoss/dlandmarks [B, nC, D] from dLoss/dr."""
+    B, nC, D = landmarks.shape
+    p = make_params(B=B, Lq=nC * S, S=S, H=H, d=d, topk=idx.shape[-1], landmark_dim=D,
+                    dtype=landmarks.dtype, score_scale=score_scale)
+    ws = torch.empty(gca_landmark_bwd_workspace_size(p), dtype=torch.uint8, device=landmarks.device)
+    dl = torch.empty_like(landmarks)
+    gca_landmark_bwd(p, landmarks, idx, dscore, dl, ws)
+    return dl
 
 
 def fwd(q, k, v, idx, weight, *, S, attn_scale=0.0, with_lse=True):

@@ -127,8 +127,47 @@ gca_status_t gca_score_topk(const gca_params_t* params, const void* landmarks, i
     int* st = status_ptr();
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
-    r = from_cuda(launch_score_topk(s, landmarks, idx, score, weight, st,
+    r = from_cuda(launch_score_topk(s, landmarks, nullptr, idx, score, weight, st,
                                     static_cast<cudaStream_t>(stream), &n));
+    if (r == GCA_OK) t_launches = n;
+    return r;
+}
+
+gca_status_t gca_score_topk_noisy(const gca_params_t* params, const void* landmarks,
+                                  const float* noise, int32_t* idx, float* score, float* weight,
+                                  void* stream) {
+    Shape s;
+    gca_status_t r = make_shape(params, false, &s);
+    if (r != GCA_OK) return r;
+    if ((r = check_ptrs({landmarks, noise, idx, score, weight})) != GCA_OK) return r;
+    if (sizeof(float) * ((size_t)s.D + 2 * (size_t)s.nQ) > 200 * 1024) return GCA_ERR_UNSUPPORTED;
+    int* st = status_ptr();
+    if (!st) return GCA_ERR_CUDA;
+    int n = 0;
+    r = from_cuda(launch_score_topk(s, landmarks, noise, idx, score, weight, st,
+                                    static_cast<cudaStream_t>(stream), &n));
+    if (r == GCA_OK) t_launches = n;
+    return r;
+}
+
+size_t gca_landmark_bwd_workspace_size(const gca_params_t* params) {
+    Shape s;
+    if (make_shape(params, false, &s) != GCA_OK) return 0;
+    return inverse_index_bytes(s.B, s.nQ, s.nQ, s.topk);
+}
+
+gca_status_t gca_landmark_bwd(const gca_params_t* params, const void* landmarks,
+                              const int32_t* idx, const float* dscore, void* dlandmarks,
+                              void* workspace, size_t ws_bytes, void* stream) {
+    Shape s;
+    gca_status_t r = make_shape(params, false, &s);
+    if (r != GCA_OK) return r;
+    if ((r = check_ptrs({landmarks, idx, dscore, dlandmarks})) != GCA_OK) return r;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GCA_ERR_WORKSPACE;
+    if (ws_bytes < inverse_index_bytes(s.B, s.nQ, s.nQ, s.topk)) return GCA_ERR_WORKSPACE;
+    int n = 0;
+    r = from_cuda(launch_landmark_bwd(s, landmarks, idx, dscore, dlandmarks, workspace,
+                                      static_cast<cudaStream_t>(stream), &n));
     if (r == GCA_OK) t_launches = n;
     return r;
 }

@@ -13,14 +13,16 @@
 //     retrieved chunks' K/V tiles like the forward, recomputes S = Q K^T and
 //     G = dO V^T on the tensor cores, forms dA in shared memory and
 //     accumulates dQ += dA K in TMEM; it also stores delta and lse per
-//     (query chunk, slot, head) as contiguous rows for pass B, and the per-head
-//     partial dw.
+//     (query chunk, slot, head) as contiguous rows for pass B, and partial dw
+//     sums per quarter of the chunk's tokens.
 //   pass B, key-major, item = (batch row, pool chunk, head): walks the inverse
 //     index of (query chunk, slot) entries that retrieved the chunk, gathers
 //     their Q/dO tiles and delta/lse rows, recomputes S^T = K Q^T and
 //     G^T = V dO^T, and accumulates dK += dA^T Q and dV += (w P)^T dO in TMEM.
-// Both use the warp roles of the forward kernel: warp 0 TMA producer, warp 1
-// MMA issuer and TMEM owner, warps 2-5 element-wise math and epilogue.
+// Both use the warp roles of the forward kernel: warp 0 producer (decodes the
+// item metadata into shared memory, issues the TMA / bulk copies), warp 1 MMA
+// issuer and TMEM owner, warps 2-9 two math warpgroups taking alternate
+// groups and alternate item epilogues.
 #include <math.h>
 
 #include "common.cuh"
@@ -40,18 +42,8 @@ using tcx::pack8u;
 using tcx::Ring;
 using tcx::sw128_off;
 
-constexpr int kThreads = 192;
-
-struct __align__(8) BarsA {
-    uint64_t it_full[2], it_empty[2];
-    uint64_t kv_full[4], kv_empty[4];
-    uint64_t s_full, s_empty;
-    uint64_t p_full[2], p_empty[2];
-    uint64_t o_full[2], o_empty[2];
-    uint64_t done;
-    uint32_t tmem;
-    int abort;
-};
+constexpr int kThreads = 320;
+constexpr int kInfo = 4;
 
 struct BwdArgs {
     const int32_t* idx;
@@ -72,17 +64,100 @@ struct BwdArgs {
     int n_items;
 };
 
-__device__ __forceinline__ int valid_slots(const BwdArgs& a, int b, int c, int* js, int* kaps) {
-    const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
-    int n = 0;
-    for (int j = 0; j < a.topk; ++j) {
-        const int kap = row[j];
-        if (kap >= 0 && kap < a.nP) { js[n] = j; kaps[n] = kap; ++n; }
+__device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
+__device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
+
+// 16 consecutive fp32 TMEM columns of this thread's row (S = 64: the 16x32bx2
+// shape, whose second half starts 64 columns on; S = 128: 32x32b).
+template <int S>
+__device__ __forceinline__ void load_cols16(uint32_t taddr, float* x) {
+    uint32_t r[16];
+    if (S == 64) tmem_ld_16x32bx2_x16<64>(taddr, r);
+    else tmem_ld_32x32b_x16(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int t = 0; t < 16; ++t) x[t] = __uint_as_float(r[t]);
+}
+
+template <int S>
+__device__ __forceinline__ void load_cols64(uint32_t taddr, float* x) {
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+        uint32_t r[16];
+        if (S == 64) tmem_ld_16x32bx2_x16<64>(taddr + 16 * ci, r);
+        else tmem_ld_32x32b_x16(taddr + 16 * ci, r);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) x[16 * ci + t] = __uint_as_float(r[t]);
     }
-    return n;
+    tmem_wait_ld();
+}
+
+// TMEM loads of one 64-column chunk of S and of G for this thread's row.
+template <int S>
+__device__ __forceinline__ void load_sg(uint32_t ts, uint32_t tg, float* xs, float* xg) {
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+        uint32_t r1[16], r2[16];
+        if (S == 64) {
+            tmem_ld_16x32bx2_x16<64>(ts + 16 * ci, r1);
+            tmem_ld_16x32bx2_x16<64>(tg + 16 * ci, r2);
+        } else {
+            tmem_ld_32x32b_x16(ts + 16 * ci, r1);
+            tmem_ld_32x32b_x16(tg + 16 * ci, r2);
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            xs[16 * ci + t] = __uint_as_float(r1[t]);
+            xg[16 * ci + t] = __uint_as_float(r2[t]);
+        }
+    }
+    tmem_wait_ld();
+}
+
+// Store 64 (S = 64: this thread's half) or 64 (S = 128: the full row) fp32
+// TMEM columns as bf16 into a [.., 64] row.
+template <int S>
+__device__ __forceinline__ void store_row64(uint32_t taddr, __nv_bfloat16* dst_row, int u) {
+    if (S == 64) {
+        uint32_t r0[16], r1[16];
+        tmem_ld_16x32bx2_x16<32>(taddr, r0);
+        tmem_ld_16x32bx2_x16<32>(taddr + 16, r1);
+        tmem_wait_ld();
+        uint4* dst = reinterpret_cast<uint4*>(dst_row + u * 32);
+        dst[0] = pack8u(r0);
+        dst[1] = pack8u(r0 + 8);
+        dst[2] = pack8u(r1);
+        dst[3] = pack8u(r1 + 8);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+        for (int ci = 0; ci < 4; ++ci) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(taddr + 16 * ci, r);
+            tmem_wait_ld();
+            dst[2 * ci] = pack8u(r);
+            dst[2 * ci + 1] = pack8u(r + 8);
+        }
+    }
+}
+
+template <int S>
+__device__ __forceinline__ void zero_row64(__nv_bfloat16* dst_row, int u) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const int nq = (S == 64) ? 4 : 8;
+    uint4* dst = reinterpret_cast<uint4*>(dst_row + ((S == 64) ? u * 32 : 0));
+    for (int q4 = 0; q4 < nq; ++q4) dst[q4] = z;
 }
 
 // ============================================================================ pass A
+struct ItemInfoA {
+    int b, c, h, n;
+    int js[kMaxTopk];
+    int kaps[kMaxTopk];
+    float w[kMaxTopk];
+    int8_t code[kMaxTopk];     // 0 valid, otherwise an empty or out-of-range slot
+};
+
 template <int S>
 struct CfgA {
     static constexpr int M = S;
@@ -102,6 +177,19 @@ struct CfgA {
     static constexpr uint32_t COL_S = 0, COL_G = 128, COL_DQ = 256;
 };
 
+struct __align__(8) BarsA {
+    uint64_t info_full[kInfo], info_empty[kInfo];
+    uint64_t it_full[2], it_empty[2];
+    uint64_t kv_full[4], kv_empty[4];
+    uint64_t s_full[2], s_empty;       // s_full per math warpgroup, s_empty shared
+    uint64_t p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2];
+    uint64_t done;
+    uint32_t tmem;
+    int abort;
+    ItemInfoA info[kInfo];
+};
+
 template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
 gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
@@ -116,6 +204,10 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < kInfo; ++i) {
+            mbar_init(&sb.info_full[i], 1);
+            mbar_init(&sb.info_empty[i], 1 + 256);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
             mbar_init(&sb.it_empty[i], 1);
@@ -128,7 +220,8 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             mbar_init(&sb.kv_full[i], 1);
             mbar_init(&sb.kv_empty[i], 1);
         }
-        mbar_init(&sb.s_full, 1);
+        mbar_init(&sb.s_full[0], 1);
+        mbar_init(&sb.s_full[1], 1);
         mbar_init(&sb.s_empty, 128);
         mbar_init(&sb.done, 1);
         sb.abort = 0;
@@ -148,16 +241,28 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sb.tmem;
-    int js[kMaxTopk], kaps[kMaxTopk];
 
     if (warp == 0) {
         if (lane == 0) {
-            Ring kv{0, 0}, it{0, 0};
+            Ring kv{0, 0}, it{0, 0}, inf{0, 0};
             bool kv_out[4] = {false, false, false, false}, it_out[2] = {false, false};
             uint32_t kv_ph[4] = {0, 0, 0, 0}, it_ph[2] = {0, 0};
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-                const int n = valid_slots(a, b, c, js, kaps);
+                if (!wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
+                ItemInfoA& I = sb.info[inf.i];
+                const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
+                const float* wrow = a.w + ((size_t)b * a.nQ + c) * a.topk;
+                int n = 0;
+                for (int j = 0; j < a.topk; ++j) {
+                    const int kap = row[j];
+                    const bool ok = kap >= 0 && kap < a.nP;
+                    I.code[j] = ok ? 0 : 1;
+                    if (ok) { I.js[n] = j; I.kaps[n] = kap; I.w[n] = wrow[j]; ++n; }
+                }
+                I.b = b; I.c = c; I.h = h; I.n = n;
+                mbar_arrive(&sb.info_full[inf.i]);
+                inf.next(kInfo);
                 if (n == 0) continue;
                 if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
@@ -174,7 +279,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     uint8_t* stg = sm + C::OFF_KV + kv.i * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&sb.kv_full[kv.i], ns * 2 * C::TILE);
                     for (int u = 0; u < ns; ++u) {
-                        const int y = (b * a.nP + kaps[g * C::GS + u]) * S;
+                        const int y = (b * a.nP + I.kaps[g * C::GS + u]) * S;
                         tma_load_2d(stg + u * C::TILE, &tk, &sb.kv_full[kv.i], h * 64, y);
                         tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tv, &sb.kv_full[kv.i], h * 64, y);
                     }
@@ -191,27 +296,46 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            Ring kv{0, 0}, it{0, 0}, p{0, 0}, o{0, 0};
-            uint32_t s_ph = 0;
+            Ring kv{0, 0}, it{0, 0}, inf{0, 0};
+            int q = 0, e = 0;
             bool issued = false;
             const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
             const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
             const uint32_t id_dq = idesc_bf16(C::M, 64, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-                const int bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-                const int n = valid_slots(a, b, c, js, kaps);
+                if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+                const int n = sb.info[inf.i].n;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
                 if (n == 0) continue;
                 const int G = (n + C::GS - 1) / C::GS;
+                const int ob = e & 1;
                 if (!wait(&sb.it_full[it.i], it.ph)) break;
-                if (!wait(&sb.o_empty[o.i], o.ph ^ 1u)) break;
+                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
                 const uint32_t qaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t doaddr = qaddr + C::TILE;
-                const uint32_t d_dq = tmem + C::COL_DQ + o.i * 64;
+                const uint32_t d_dq = tmem + C::COL_DQ + ob * 64;
+                int stg_of[2] = {0, 0}, ns_of[2] = {0, 0};
+                auto issue_dq = [&](int g) -> bool {
+                    const int qq = q + g, pb = qq & 1;
+                    if (!wait(&sb.p_full[pb], full_par(qq >> 1))) return false;
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
+                    const uint32_t kaddr = smem_u32(sm + C::OFF_KV + stg_of[g & 1] * C::STAGE_BYTES);
+                    const int ksteps = ns_of[g & 1] * S / 16;
+                    for (int ks = 0; ks < ksteps; ++ks)
+                        mma_bf16(d_dq, desc_kmajor_sw128(paddr + (ks >> 2) * C::P_BLOCK + (ks & 3) * 32),
+                                 desc_mnmajor_sw128(kaddr + ks * 2048), id_dq, (g > 0 || ks > 0));
+                    mma_commit(&sb.kv_empty[stg_of[g & 1]]);
+                    mma_commit(&sb.p_empty[pb]);
+                    return true;
+                };
                 bool ok = true;
                 for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
-                    if (!wait(&sb.kv_full[kv.i], kv.ph) || !wait(&sb.s_empty, s_ph ^ 1u)) { ok = false; break; }
+                    const int qq = q + g;
+                    if (!wait(&sb.kv_full[kv.i], kv.ph) || !wait(&sb.s_empty, empty_par(qq))) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
                     const uint32_t vaddr = kaddr + C::NG * 128;
@@ -223,26 +347,19 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                         mma_bf16(tmem + C::COL_G, desc_kmajor_sw128(doaddr + 32 * ks),
                                  desc_kmajor_sw128(vaddr + 32 * ks), id, ks > 0);
                     }
-                    mma_commit(&sb.s_full);
-                    s_ph ^= 1u;
+                    mma_commit(&sb.s_full[qq & 1]);
                     issued = true;
-                    if (!wait(&sb.p_full[p.i], p.ph)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + p.i * C::P_BYTES);
-                    const int ksteps = ns * S / 16;
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        mma_bf16(d_dq, desc_kmajor_sw128(paddr + (ks >> 2) * C::P_BLOCK + (ks & 3) * 32),
-                                 desc_mnmajor_sw128(kaddr + ks * 2048), id_dq, (g > 0 || ks > 0));
-                    mma_commit(&sb.kv_empty[kv.i]);
-                    mma_commit(&sb.p_empty[p.i]);
+                    stg_of[g & 1] = kv.i;
+                    ns_of[g & 1] = ns;
                     kv.next(C::STAGES);
-                    p.next(2);
+                    if (g > 0 && !issue_dq(g - 1)) { ok = false; break; }
                 }
-                if (!ok) break;
-                mma_commit(&sb.o_full[o.i]);
+                if (!ok || !issue_dq(G - 1)) break;
+                mma_commit(&sb.o_full[ob]);
                 mma_commit(&sb.it_empty[it.i]);
-                o.next(2);
                 it.next(2);
+                q += G;
+                ++e;
             }
             if (issued) {
                 mma_commit(&sb.done);
@@ -250,151 +367,117 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             }
         }
     } else {
+        const int wg = (warp - 2) >> 2;
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
         const int u = (S == 64) ? (lane >> 4) : 0;
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-        Ring p{0, 0}, o{0, 0};
-        uint32_t s_ph = 0;
-        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-            const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-            const int n = valid_slots(a, b, c, js, kaps);
+        Ring inf{0, 0};
+        int q = 0, e = 0, n_all = 0, kg = 0, ko = 0;
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_all) {
+            if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+            const ItemInfoA& I = sb.info[inf.i];
+            const int b = I.b, c = I.c, h = I.h, n = I.n;
             const size_t tok = (size_t)b * a.Lq + (size_t)c * S + row;
             __nv_bfloat16* dqrow = a.dq + (tok * a.H + h) * 64;
-            if (threadIdx.x == 64) {
-                const int32_t* irow = a.idx + ((size_t)b * a.nQ + c) * a.topk;
+            const bool my_epi = (n == 0) ? ((n_all & 1) == wg) : ((e & 1) == wg);
+            float* dwp = a.dwpart + (((size_t)b * a.nQ + c) * a.H + h) * 4 * a.topk;
+            if (my_epi && threadIdx.x == 64 + wg * 128)
                 for (int j = 0; j < a.topk; ++j)
-                    if (!(irow[j] >= 0 && irow[j] < a.nP))
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            a.dwpart[((((size_t)b * a.nQ + c) * a.H + h) * 4 + q4) * a.topk + j] = 0.f;
-            }
+                    if (I.code[j] != 0)
+                        for (int q4 = 0; q4 < 4; ++q4) dwp[q4 * a.topk + j] = 0.f;
             if (n == 0) {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                if (S == 64) {
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(dqrow + u * 32)[q4] = z;
-                } else {
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) reinterpret_cast<uint4*>(dqrow)[q4] = z;
-                }
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (my_epi) zero_row64<S>(dqrow, u);
                 continue;
             }
+            const int G = (n + C::GS - 1) / C::GS;
             bool ok = true;
-            for (int g = 0; g * C::GS < n; ++g) {
+            for (int g = 0; g < G; ++g) {
+                const int qq = q + g;
+                if ((qq & 1) != wg) continue;
                 const int ns = min(C::GS, n - g * C::GS);
                 const bool active = u < ns;
-                const int j = active ? js[g * C::GS + u] : 0;
-                const float L2 = active ? a.lse[(tok * a.H + h) * a.topk + j] * kLog2e : 0.f;
-                const float wsc = active ? a.w[((size_t)b * a.nQ + c) * a.topk + j] * a.attn_scale : 0.f;
-                if (!wait(&sb.s_full, s_ph)) { ok = false; break; }
-                s_ph ^= 1u;
+                const int j = active ? I.js[g * C::GS + u] : 0;
+                const float L2 = active ? __ldg(a.lse + (tok * a.H + h) * a.topk + j) * kLog2e : 0.f;
+                const float wsc = active ? I.w[g * C::GS + u] * a.attn_scale : 0.f;
+                if (!wait(&sb.s_full[wg], full_par(kg))) { ok = false; break; }
                 tc_fence_after();
+                constexpr int NCH = (S == 64) ? 1 : 2;      // 64-key chunks per row
+                const uint32_t ts0 = tmem + lane_base + C::COL_S;
+                const uint32_t tg0 = tmem + lane_base + C::COL_G;
+                float x[64];
                 float dl = 0.f;
-                // 64 keys per chunk; S = 64 has one chunk per thread, S = 128 two.
-                constexpr int NCH = (S == 64) ? 1 : 2;
-                float xs[64], xg[64];
-                auto load_chunk = [&](int ch) {
-                    const uint32_t ts = tmem + lane_base + C::COL_S + ch * 64;
-                    const uint32_t tg = tmem + lane_base + C::COL_G + ch * 64;
+                // sweep 1: p (kept for the last chunk) and delta = sum_s p G
+                for (int ch = 0; ch < NCH; ++ch) {
+                    load_cols64<S>(ts0 + ch * 64, x);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
 #pragma unroll
                     for (int ci = 0; ci < 4; ++ci) {
-                        uint32_t r1[16], r2[16];
-                        if (S == 64) {
-                            tmem_ld_16x32bx2_x16<64>(ts + 16 * ci, r1);
-                            tmem_ld_16x32bx2_x16<64>(tg + 16 * ci, r2);
-                        } else {
-                            tmem_ld_32x32b_x16(ts + 16 * ci, r1);
-                            tmem_ld_32x32b_x16(tg + 16 * ci, r2);
-                        }
+                        float g[16];
+                        load_cols16<S>(tg0 + ch * 64 + 16 * ci, g);
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            xs[16 * ci + t] = __uint_as_float(r1[t]);
-                            xg[16 * ci + t] = __uint_as_float(r2[t]);
-                        }
-                    }
-                    tmem_wait_ld();
-                };
-                if (NCH == 2) {            // first sweep: delta only
-                    for (int ch = 0; ch < NCH; ++ch) {
-                        load_chunk(ch);
-#pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            dl = fmaf(fast_exp2(fmaf(xs[i], a.scale_log2, -L2)), xg[i], dl);
+                        for (int t = 0; t < 16; ++t) dl = fmaf(x[16 * ci + t], g[t], dl);
                     }
                 }
-                if (!wait(&sb.p_empty[p.i], p.ph ^ 1u)) { ok = false; break; }
-                uint8_t* pb = sm + C::OFF_P + p.i * C::P_BYTES;
+                if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                uint8_t* pb = sm + C::OFF_P + wg * C::P_BYTES;
+                // sweep 2: dA = w s p (G - delta) into the A operand of dQ += dA K
                 for (int ch = 0; ch < NCH; ++ch) {
-                    load_chunk(ch);
-                    if (ch == NCH - 1) {
-                        tc_fence_before();
-                        mbar_arrive(&sb.s_empty);
+                    if (NCH == 2) {
+                        load_cols64<S>(ts0 + ch * 64, x);
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
                     }
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) xs[i] = fast_exp2(fmaf(xs[i], a.scale_log2, -L2));
-                    if (NCH == 1) {
+                    for (int ci = 0; ci < 4; ++ci) {
+                        float g[16];
+                        load_cols16<S>(tg0 + ch * 64 + 16 * ci, g);
+                        if (ch == NCH - 1 && ci == 3) {
+                            tc_fence_before();
+                            mbar_arrive(&sb.s_empty);
+                        }
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) dl = fmaf(xs[i], xg[i], dl);
-                    }
-                    if (active) {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) xs[i] = xs[i] * (xg[i] - dl);
-                        const int blk = (S == 64) ? u : ch;
-#pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8)
-                            *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, c8)) =
-                                pack8(xs + 8 * c8, wsc);
+                        for (int t = 0; t < 16; ++t) g[t] = x[16 * ci + t] * (g[t] - dl);
+                        if (active) {
+                            const int blk = (S == 64) ? u : ch;
+                            *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, 2 * ci)) =
+                                pack8(g, wsc);
+                            *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, 2 * ci + 1)) =
+                                pack8(g + 8, wsc);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&sb.p_full[p.i]);
-                p.next(2);
-                // rows for pass B and the per-head partial of dw
+                mbar_arrive(&sb.p_full[wg]);
+                ++kg;
                 if (active) {
                     const size_t rr = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S + row;
                     a.delta_rows[rr] = dl;
                     a.lse2_rows[rr] = L2;
                 }
-                // per-quadrant partial of dw (summed over this warp's rows; the
-                // score-gradient kernel adds the quadrants and heads in order)
+                // per-quadrant partial of dw over this warp's rows
                 float part = active ? dl : 0.f;
 #pragma unroll
                 for (int o2 = (S == 64 ? 8 : 16); o2 > 0; o2 >>= 1)
                     part += __shfl_xor_sync(0xffffffffu, part, o2);
-                if (active && (lane & (S == 64 ? 15 : 31)) == 0)
-                    a.dwpart[((((size_t)b * a.nQ + c) * a.H + h) * 4 + qd) * a.topk + j] = part;
+                if (active && (lane & (S == 64 ? 15 : 31)) == 0) dwp[qd * a.topk + j] = part;
             }
+            mbar_arrive(&sb.info_empty[inf.i]);
+            inf.next(kInfo);
             if (!ok) break;
-            if (!wait(&sb.o_full[o.i], o.ph)) break;
+            q += G;
+            const bool mine = (e & 1) == wg;
+            ++e;
+            if (!mine) continue;
+            if (!wait(&sb.o_full[wg], full_par(ko))) break;
+            ++ko;
             tc_fence_after();
-            const uint32_t oaddr = tmem + lane_base + C::COL_DQ + o.i * 64;
-            if (S == 64) {
-                uint32_t r0[16], r1[16];
-                tmem_ld_16x32bx2_x16<32>(oaddr, r0);
-                tmem_ld_16x32bx2_x16<32>(oaddr + 16, r1);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.o_empty[o.i]);
-                uint4* dst = reinterpret_cast<uint4*>(dqrow + u * 32);
-                dst[0] = pack8u(r0);
-                dst[1] = pack8u(r0 + 8);
-                dst[2] = pack8u(r1);
-                dst[3] = pack8u(r1 + 8);
-            } else {
-                uint32_t r[4][16];
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(oaddr + 16 * ci, r[ci]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.o_empty[o.i]);
-                uint4* dst = reinterpret_cast<uint4*>(dqrow);
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) {
-                    dst[2 * ci] = pack8u(r[ci]);
-                    dst[2 * ci + 1] = pack8u(r[ci] + 8);
-                }
-            }
-            o.next(2);
+            store_row64<S>(tmem + lane_base + C::COL_DQ + wg * 64, dqrow, u);
+            tc_fence_before();
+            mbar_arrive(&sb.o_empty[wg]);
         }
     }
 
@@ -406,38 +489,50 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     }
 }
 
-
 // ============================================================================ pass B
+struct ItemInfoB {
+    int b, kap, h, ne;
+};
+
+struct EntryInfo {
+    int c, j;
+    float w;
+    int pad;
+};
+
 template <int S>
 struct CfgB {
     static constexpr int M = S;                           // keys of the item
     static constexpr int GS = 128 / S;                    // entries per group
     static constexpr int NG = 128;                        // tokens per full group
+    static constexpr int NWG = (S == 64) ? 2 : 1;         // math warpgroups in use
     static constexpr int STAGES = (S == 64) ? 3 : 2;
     static constexpr int TILE = S * 128;
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
     static constexpr int VEC_OFF = 2 * NG * 128;          // after the Q and dO tiles
-    static constexpr int STAGE_BYTES = VEC_OFF + 1024;    // + lse2/delta rows of the entries
+    static constexpr int ENT_OFF = VEC_OFF + 1024;        // lse2/delta rows, then entry info
+    static constexpr int STAGE_BYTES = VEC_OFF + 2048;
     static constexpr int P_BLOCK = M * 128;
     static constexpr int P_BYTES = M * NG * 2;            // one operand (dA^T or wP^T)
-    static constexpr int PB = (S == 64) ? 2 : 1;          // operand-pair buffers
     static constexpr int OFF_IT = 0;
     static constexpr int OFF_ST = 2 * ITEM_BYTES;
     static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
-    static constexpr int SMEM = OFF_P + PB * 2 * P_BYTES + 1024;
+    static constexpr int SMEM = OFF_P + NWG * 2 * P_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0, COL_G = 128, COL_ACC = 256;   // dK, dV: 2 x (64 + 64)
 };
 
 struct __align__(8) BarsB {
+    uint64_t info_full[kInfo], info_empty[kInfo];
     uint64_t it_full[2], it_empty[2];
     uint64_t st_full[3], st_empty[3];
-    uint64_t s_full, s_empty;
+    uint64_t s_full[2], s_empty;       // s_full per math warpgroup, s_empty shared
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
     uint64_t done;
     uint32_t tmem;
     int abort;
+    ItemInfoB info[kInfo];
 };
 
 template <int S>
@@ -455,6 +550,10 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     const int nE = a.nQ * a.topk;
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < kInfo; ++i) {
+            mbar_init(&sb.info_full[i], 1);
+            mbar_init(&sb.info_empty[i], 1 + 256);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
             mbar_init(&sb.it_empty[i], 1);
@@ -467,7 +566,8 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             mbar_init(&sb.st_full[i], 1);
             mbar_init(&sb.st_empty[i], 1);
         }
-        mbar_init(&sb.s_full, 1);
+        mbar_init(&sb.s_full[0], 1);
+        mbar_init(&sb.s_full[1], 1);
         mbar_init(&sb.s_empty, 128);
         mbar_init(&sb.done, 1);
         sb.abort = 0;
@@ -490,13 +590,18 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {
-            Ring st{0, 0}, it{0, 0};
+            Ring st{0, 0}, it{0, 0}, inf{0, 0};
             bool st_out[3] = {false, false, false}, it_out[2] = {false, false};
             uint32_t st_ph[3] = {0, 0, 0}, it_ph[2] = {0, 0};
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
                 const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
                 const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
+                if (!wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
+                ItemInfoB& I = sb.info[inf.i];
+                I.b = b; I.kap = kap; I.h = h; I.ne = ne;
+                mbar_arrive(&sb.info_full[inf.i]);
+                inf.next(kInfo);
                 if (ne <= 0) continue;
                 const int* ent = a.entry + (size_t)b * nE + e0;
                 if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
@@ -510,12 +615,21 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 bool ok = true;
                 for (int g = 0; g * C::GS < ne; ++g) {
                     const int ns = min(C::GS, ne - g * C::GS);
-                    if (!wait(&sb.st_empty[st.i], st.ph ^ 1u)) { ok = false; break; }
-                    uint8_t* stg = sm + C::OFF_ST + st.i * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&sb.st_full[st.i], ns * (2 * C::TILE + 2 * S * 4));
+                    int cs[C::GS], jj[C::GS];
+                    float ww[C::GS];
                     for (int u = 0; u < ns; ++u) {
                         const int e = ent[g * C::GS + u];
-                        const int c = e / a.topk, j = e % a.topk;
+                        cs[u] = e / a.topk;
+                        jj[u] = e % a.topk;
+                        ww[u] = a.w[((size_t)b * a.nQ + cs[u]) * a.topk + jj[u]];
+                    }
+                    if (!wait(&sb.st_empty[st.i], st.ph ^ 1u)) { ok = false; break; }
+                    uint8_t* stg = sm + C::OFF_ST + st.i * C::STAGE_BYTES;
+                    EntryInfo* ei = reinterpret_cast<EntryInfo*>(stg + C::ENT_OFF);
+                    for (int u = 0; u < ns; ++u) { ei[u].c = cs[u]; ei[u].j = jj[u]; ei[u].w = ww[u]; }
+                    mbar_arrive_expect_tx(&sb.st_full[st.i], ns * (2 * C::TILE + 2 * S * 4));
+                    for (int u = 0; u < ns; ++u) {
+                        const int c = cs[u], j = jj[u];
                         tma_load_2d(stg + u * C::TILE, &tq, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
                         tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tdo, &sb.st_full[st.i], h * 64,
                                     b * a.Lq + c * S);
@@ -538,28 +652,52 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            Ring st{0, 0}, it{0, 0}, p{0, 0}, o{0, 0};
-            uint32_t s_ph = 0;
+            Ring st{0, 0}, it{0, 0}, inf{0, 0};
+            int q = 0, e = 0;
             bool issued = false;
             const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
             const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
             const uint32_t id_acc = idesc_bf16(C::M, 64, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-                const int bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
-                const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
-                const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
+                if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+                const int ne = sb.info[inf.i].ne;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
                 if (ne <= 0) continue;
+                const int G = (ne + C::GS - 1) / C::GS;
+                const int ob = e & 1;
                 if (!wait(&sb.it_full[it.i], it.ph)) break;
-                if (!wait(&sb.o_empty[o.i], o.ph ^ 1u)) break;
+                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
                 const uint32_t kaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t vaddr = kaddr + C::TILE;
-                const uint32_t d_dk = tmem + C::COL_ACC + o.i * 128;
+                const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
                 const uint32_t d_dv = d_dk + 64;
+                int stg_of[2] = {0, 0}, ns_of[2] = {0, 0};
+                auto issue_acc = [&](int g) -> bool {
+                    const int qq = q + g, pbuf = qq % C::NWG;
+                    if (!wait(&sb.p_full[pbuf], full_par(qq / C::NWG))) return false;
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
+                    const uint32_t qaddr = smem_u32(sm + C::OFF_ST + stg_of[g & 1] * C::STAGE_BYTES);
+                    const uint32_t doaddr = qaddr + C::NG * 128;
+                    const int ksteps = ns_of[g & 1] * S / 16;
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const uint32_t aoff = (ks >> 2) * C::P_BLOCK + (ks & 3) * 32;
+                        mma_bf16(d_dk, desc_kmajor_sw128(paddr + aoff), desc_mnmajor_sw128(qaddr + ks * 2048),
+                                 id_acc, (g > 0 || ks > 0));
+                        mma_bf16(d_dv, desc_kmajor_sw128(paddr + C::P_BYTES + aoff),
+                                 desc_mnmajor_sw128(doaddr + ks * 2048), id_acc, (g > 0 || ks > 0));
+                    }
+                    mma_commit(&sb.st_empty[stg_of[g & 1]]);
+                    mma_commit(&sb.p_empty[pbuf]);
+                    return true;
+                };
                 bool ok = true;
-                for (int g = 0; g * C::GS < ne; ++g) {
+                for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, ne - g * C::GS);
-                    if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_empty, s_ph ^ 1u)) { ok = false; break; }
+                    const int qq = q + g;
+                    if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_empty, empty_par(qq))) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
                     const uint32_t doaddr = qaddr + C::NG * 128;
@@ -571,30 +709,19 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                         mma_bf16(tmem + C::COL_G, desc_kmajor_sw128(vaddr + 32 * ks),
                                  desc_kmajor_sw128(doaddr + 32 * ks), id, ks > 0);
                     }
-                    mma_commit(&sb.s_full);
-                    s_ph ^= 1u;
+                    mma_commit(&sb.s_full[qq % C::NWG]);
                     issued = true;
-                    if (!wait(&sb.p_full[p.i], p.ph)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + p.i * 2 * C::P_BYTES);
-                    const int ksteps = ns * S / 16;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint32_t aoff = (ks >> 2) * C::P_BLOCK + (ks & 3) * 32;
-                        mma_bf16(d_dk, desc_kmajor_sw128(paddr + aoff), desc_mnmajor_sw128(qaddr + ks * 2048),
-                                 id_acc, (g > 0 || ks > 0));
-                        mma_bf16(d_dv, desc_kmajor_sw128(paddr + C::P_BYTES + aoff),
-                                 desc_mnmajor_sw128(doaddr + ks * 2048), id_acc, (g > 0 || ks > 0));
-                    }
-                    mma_commit(&sb.st_empty[st.i]);
-                    mma_commit(&sb.p_empty[p.i]);
+                    stg_of[g & 1] = st.i;
+                    ns_of[g & 1] = ns;
                     st.next(C::STAGES);
-                    p.next(C::PB);
+                    if (g > 0 && !issue_acc(g - 1)) { ok = false; break; }
                 }
-                if (!ok) break;
-                mma_commit(&sb.o_full[o.i]);
+                if (!ok || !issue_acc(G - 1)) break;
+                mma_commit(&sb.o_full[ob]);
                 mma_commit(&sb.it_empty[it.i]);
-                o.next(2);
                 it.next(2);
+                q += G;
+                ++e;
             }
             if (issued) {
                 mma_commit(&sb.done);
@@ -602,130 +729,96 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             }
         }
     } else {
+        const int wg = (warp - 2) >> 2;
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
         const int u = (S == 64) ? (lane >> 4) : 0;
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-        Ring st{0, 0}, p{0, 0}, o{0, 0};
-        uint32_t s_ph = 0;
-        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-            const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
-            const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
-            const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
-            const size_t krow = (size_t)(b * a.nP + kap) * S + row;
-            __nv_bfloat16* dkrow = a.dk + (krow * a.H + h) * 64;
-            __nv_bfloat16* dvrow = a.dv + (krow * a.H + h) * 64;
-            if (ne <= 0) {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                const int nq = (S == 64) ? 4 : 8;
-                const int off = (S == 64) ? u * 32 : 0;
-                for (int q4 = 0; q4 < nq; ++q4) {
-                    reinterpret_cast<uint4*>(dkrow + off)[q4] = z;
-                    reinterpret_cast<uint4*>(dvrow + off)[q4] = z;
+        Ring inf{0, 0}, st{0, 0};
+        int q = 0, e = 0, n_all = 0, kg = 0;
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_all) {
+            if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+            const ItemInfoB I = sb.info[inf.i];
+            mbar_arrive(&sb.info_empty[inf.i]);
+            inf.next(kInfo);
+            const size_t krow = (size_t)(I.b * a.nP + I.kap) * S + row;
+            __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * 64;
+            __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * 64;
+            if (I.ne <= 0) {
+                if ((n_all % C::NWG) == wg) {
+                    zero_row64<S>(dkrow, u);
+                    zero_row64<S>(dvrow, u);
                 }
                 continue;
             }
-            const int* ent = a.entry + (size_t)b * nE + e0;
+            const int G = (I.ne + C::GS - 1) / C::GS;
             bool ok = true;
-            for (int g = 0; g * C::GS < ne; ++g) {
-                const int ns = min(C::GS, ne - g * C::GS);
+            for (int g = 0; g < G; ++g) {
+                const int qq = q + g;
+                const int stage = st.i;
+                const uint32_t stph = st.ph;
+                st.next(C::STAGES);
+                if ((qq % C::NWG) != wg) continue;
+                const int ns = min(C::GS, I.ne - g * C::GS);
                 const bool active = u < ns;
-                float wv = 0.f;
-                if (active) {
-                    const int e = ent[g * C::GS + u];
-                    wv = a.w[((size_t)b * a.nQ + e / a.topk) * a.topk + e % a.topk];
-                }
-                const float wsc = wv * a.attn_scale;
-                if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_full, s_ph)) { ok = false; break; }
-                s_ph ^= 1u;
+                // our own s_full first: its completion implies this group's stage copy
+                // has landed, so the stage barrier's phase below is unambiguous
+                if (!wait(&sb.s_full[wg], full_par(kg)) || !wait(&sb.st_full[stage], stph)) { ok = false; break; }
                 tc_fence_after();
-                if (!wait(&sb.p_empty[p.i], p.ph ^ 1u)) { ok = false; break; }
-                const float* vec = reinterpret_cast<const float*>(sm + C::OFF_ST + st.i * C::STAGE_BYTES +
-                                                                  C::VEC_OFF + u * 2 * S * 4);
-                uint8_t* pb = sm + C::OFF_P + p.i * 2 * C::P_BYTES;
-                constexpr int NCH = (S == 64) ? 1 : 2;
-                for (int ch = 0; ch < NCH; ++ch) {
-                    float xs[64], xg[64];
-                    const uint32_t ts = tmem + lane_base + C::COL_S + ch * 64;
-                    const uint32_t tg = tmem + lane_base + C::COL_G + ch * 64;
-#pragma unroll
-                    for (int ci = 0; ci < 4; ++ci) {
-                        uint32_t r1[16], r2[16];
-                        if (S == 64) {
-                            tmem_ld_16x32bx2_x16<64>(ts + 16 * ci, r1);
-                            tmem_ld_16x32bx2_x16<64>(tg + 16 * ci, r2);
-                        } else {
-                            tmem_ld_32x32b_x16(ts + 16 * ci, r1);
-                            tmem_ld_32x32b_x16(tg + 16 * ci, r2);
-                        }
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            xs[16 * ci + t] = __uint_as_float(r1[t]);
-                            xg[16 * ci + t] = __uint_as_float(r2[t]);
-                        }
-                    }
-                    tmem_wait_ld();
-                    if (ch == NCH - 1) {
+                const uint8_t* stg = sm + C::OFF_ST + stage * C::STAGE_BYTES;
+                const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[active ? u : 0];
+                const float wv = active ? ei.w : 0.f;
+                const float wsc = wv * a.attn_scale;
+                const float* vec = reinterpret_cast<const float*>(stg + C::VEC_OFF + u * 2 * S * 4);
+                if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                uint8_t* pb = sm + C::OFF_P + wg * 2 * C::P_BYTES;
+                constexpr int NC32 = (S == 64) ? 2 : 4;      // 32-token pieces per row
+                const uint32_t ts0 = tmem + lane_base + C::COL_S;
+                const uint32_t tg0 = tmem + lane_base + C::COL_G;
+                for (int pc = 0; pc < NC32; ++pc) {
+                    float xs[32], xg[32];
+                    load_cols16<S>(ts0 + 32 * pc, xs);
+                    load_cols16<S>(ts0 + 32 * pc + 16, xs + 16);
+                    load_cols16<S>(tg0 + 32 * pc, xg);
+                    load_cols16<S>(tg0 + 32 * pc + 16, xg + 16);
+                    if (pc == NC32 - 1) {
                         tc_fence_before();
                         mbar_arrive(&sb.s_empty);
                     }
                     if (active) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            const int t = ch * 64 + i;
+                        for (int i = 0; i < 32; ++i) {
+                            const int t = 32 * pc + i;
                             const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -vec[t]));
                             xs[i] = pr * (xg[i] - vec[S + t]);      // dA^T / (w s)
                             xg[i] = pr;                             // P^T / w
                         }
-                        const int blk = (S == 64) ? u : ch;
+                        const int blk = (S == 64) ? u : (pc >> 1);
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
-                            const uint32_t off = blk * C::P_BLOCK + tcx::sw128_off(row, c8);
-                            *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c8, wsc);
-                            *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c8, wv);
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const uint32_t off = blk * C::P_BLOCK + sw128_off(row, (pc & 1) * 4 + c4);
+                            *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c4, wsc);
+                            *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c4, wv);
                         }
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&sb.p_full[p.i]);
-                p.next(C::PB);
-                st.next(C::STAGES);
+                mbar_arrive(&sb.p_full[wg]);
+                ++kg;
             }
             if (!ok) break;
-            if (!wait(&sb.o_full[o.i], o.ph)) break;
+            q += G;
+            const bool mine = (e % C::NWG) == wg;
+            const int ob = e & 1, ko = e >> 1;
+            ++e;
+            if (!mine) continue;
+            if (!wait(&sb.o_full[ob], full_par(ko))) break;
             tc_fence_after();
-            const uint32_t acc = tmem + lane_base + C::COL_ACC + o.i * 128;
-            if (S == 64) {
-                uint32_t k0[16], k1[16], v0[16], v1[16];
-                tmem_ld_16x32bx2_x16<32>(acc, k0);
-                tmem_ld_16x32bx2_x16<32>(acc + 16, k1);
-                tmem_ld_16x32bx2_x16<32>(acc + 64, v0);
-                tmem_ld_16x32bx2_x16<32>(acc + 80, v1);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.o_empty[o.i]);
-                uint4* dk4 = reinterpret_cast<uint4*>(dkrow + u * 32);
-                uint4* dv4 = reinterpret_cast<uint4*>(dvrow + u * 32);
-                dk4[0] = pack8u(k0); dk4[1] = pack8u(k0 + 8); dk4[2] = pack8u(k1); dk4[3] = pack8u(k1 + 8);
-                dv4[0] = pack8u(v0); dv4[1] = pack8u(v0 + 8); dv4[2] = pack8u(v1); dv4[3] = pack8u(v1 + 8);
-            } else {
-                uint32_t r[4][16];
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(acc + 16 * ci, r[ci]);
-                tmem_wait_ld();
-                uint4* dk4 = reinterpret_cast<uint4*>(dkrow);
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) { dk4[2 * ci] = pack8u(r[ci]); dk4[2 * ci + 1] = pack8u(r[ci] + 8); }
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(acc + 64 + 16 * ci, r[ci]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.o_empty[o.i]);
-                uint4* dv4 = reinterpret_cast<uint4*>(dvrow);
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) { dv4[2 * ci] = pack8u(r[ci]); dv4[2 * ci + 1] = pack8u(r[ci] + 8); }
-            }
-            o.next(2);
+            const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 128;
+            store_row64<S>(acc, dkrow, u);
+            store_row64<S>(acc + 64, dvrow, u);
+            tc_fence_before();
+            mbar_arrive(&sb.o_empty[ob]);
         }
     }
 

@@ -6,16 +6,20 @@
 // outputs are fused as O_t = sum_j w_j O_t^j (stage 2).  App. B: the forward
 // also returns the log-sum-exp of every (token, slot).
 //
-// Design (one persistent CTA per SM, 6 warps, warp-specialised):
-//   warp 0     TMA producer: Q tile of the work item, then the K and V tiles of
-//              each retrieved chunk, gathered straight from the [tokens, H*d]
-//              tensors (box 64 x S, 128-byte swizzle) into a ring of stages.
+// Design (one persistent CTA per SM, 10 warps, warp-specialised):
+//   warp 0     producer: decodes each work item's retrieval row (valid slots,
+//              their weights, codes of empty / out-of-range slots) into a
+//              shared-memory info ring, then TMA-loads the Q tile and, for each
+//              group of retrieved chunks, their K and V tiles (box 64 x S,
+//              128-byte swizzle) straight from the [tokens, H*d] tensors into
+//              a ring of stages.
 //   warp 1     MMA issuer (one thread) and TMEM owner: S_g = Q K_g^T for a
 //              group of retrieved chunks (N = 128 keys), then O += P_g V_g.
-//   warps 2-5  softmax + epilogue: read S_g from TMEM, per-slot max / sum /
-//              exp2, write P_g = exp(S - m) * (w_j / l_j) as bf16 into shared
-//              memory (the A operand of the PV MMA), write the lse; at the end
-//              of the item read O from TMEM and store it as bf16.
+//   warps 2-9  two softmax warpgroups taking alternate groups: read S_g from
+//              TMEM, per-slot max / sum / exp2, write P_g = exp(S - m) *
+//              (w_j / l_j) as bf16 into shared memory (the A operand of the
+//              PV MMA), write the lse; each warpgroup also stores O (read
+//              from TMEM) for alternate items.
 // Because each slot's softmax is normalised before PV and carries its fusion
 // weight, the per-slot outputs O_t^j are summed by the tensor core in TMEM
 // and never exist in memory.  A work item is (batch row, query chunk, head).
@@ -39,7 +43,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kInfo = 4;                 // item-info ring depth
 using tcx::Ring;
 using tcx::fast_exp2;
 using tcx::pack_bf16;
@@ -79,7 +84,16 @@ struct FwdArgs {
     int n_items;
 };
 
+struct ItemInfo {
+    int b, c, h, n;          // n = valid slots
+    int js[kMaxTopk];        // slot number of each valid slot, in slot order
+    int kaps[kMaxTopk];      // its retrieved chunk
+    float w[kMaxTopk];       // its fusion weight
+    int8_t code[kMaxTopk];   // per slot j: 0 valid, 1 empty (-1), 2 outside the pool
+};
+
 struct __align__(8) Bars {
+    uint64_t info_full[kInfo], info_empty[kInfo];
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[4], kv_empty[4];
     uint64_t s_full[2], s_empty[2];
@@ -88,24 +102,17 @@ struct __align__(8) Bars {
     uint64_t done;
     uint32_t tmem;
     int abort;
+    ItemInfo info[kInfo];
 };
-
-// Valid slots of one item: slot numbers and their chunks, in slot order.
-__device__ __forceinline__ int item_slots(const FwdArgs& a, int b, int c, int* js, int* kaps,
-                                          bool report) {
-    const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
-    int n = 0;
-    for (int j = 0; j < a.topk; ++j) {
-        const int kap = row[j];
-        if (kap >= 0 && kap < a.nP) { js[n] = j; kaps[n] = kap; ++n; }
-        else if (kap >= a.nP && report) set_status(a.status, GCA_ERR_DEVICE_INDEX);
-    }
-    return n;
-}
 
 __device__ __forceinline__ bool wait_bar(Bars& sb, uint64_t* bar, uint32_t parity, int* status) {
     return tcx::wait_bar(&sb.abort, bar, parity, status);
 }
+
+// Parity to wait for on the k-th use (k = 0, 1, ...) of a buffer: "full"
+// barriers complete once per use, "empty" ones start out released.
+__device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
+__device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
 
 template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -119,6 +126,10 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < kInfo; ++i) {
+            mbar_init(&sb.info_full[i], 1);
+            mbar_init(&sb.info_empty[i], 1 + 256);     // MMA thread + every softmax thread
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.q_full[i], 1);
             mbar_init(&sb.q_empty[i], 1);
@@ -150,17 +161,33 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sb.tmem;
-    int js[kMaxTopk], kaps[kMaxTopk];
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            Ring kv{0, 0}, qr{0, 0};
+            Ring kv{0, 0}, qr{0, 0}, inf{0, 0};
             bool kv_out[4] = {false, false, false, false}, q_out[2] = {false, false};
             uint32_t kv_ph[4] = {0, 0, 0, 0}, q_ph[2] = {0, 0};
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-                const int n = item_slots(a, b, c, js, kaps, true);
+                if (!wait_bar(sb, &sb.info_empty[inf.i], inf.ph ^ 1u, a.status)) break;
+                ItemInfo& I = sb.info[inf.i];
+                const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
+                const float* wrow = a.w + ((size_t)b * a.nQ + c) * a.topk;
+                int n = 0;
+                for (int j = 0; j < a.topk; ++j) {
+                    const int kap = row[j];
+                    if (kap >= 0 && kap < a.nP) {
+                        I.js[n] = j; I.kaps[n] = kap; I.w[n] = wrow[j]; ++n;
+                        I.code[j] = 0;
+                    } else {
+                        I.code[j] = kap < 0 ? 1 : 2;
+                        if (kap >= a.nP) set_status(a.status, GCA_ERR_DEVICE_INDEX);
+                    }
+                }
+                I.b = b; I.c = c; I.h = h; I.n = n;
+                mbar_arrive(&sb.info_full[inf.i]);
+                inf.next(kInfo);
                 if (n == 0) continue;
                 if (!wait_bar(sb, &sb.q_empty[qr.i], qr.ph ^ 1u, a.status)) break;
                 mbar_arrive_expect_tx(&sb.q_full[qr.i], C::Q_BYTES);
@@ -176,7 +203,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     uint8_t* stg = sm + C::OFF_KV + kv.i * C::STAGE_BYTES;
                     mbar_arrive_expect_tx(&sb.kv_full[kv.i], ns * 2 * C::TILE);
                     for (int u = 0; u < ns; ++u) {
-                        const int y = (b * a.nP + kaps[g * C::GS + u]) * S;
+                        const int y = (b * a.nP + I.kaps[g * C::GS + u]) * S;
                         tma_load_2d(stg + u * C::TILE, &tk, &sb.kv_full[kv.i], h * 64, y);
                         tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tv, &sb.kv_full[kv.i],
                                     h * 64, y);
@@ -196,39 +223,43 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            Ring kv{0, 0}, qr{0, 0}, s{0, 0}, p{0, 0}, o{0, 0};
+            Ring kv{0, 0}, qr{0, 0}, inf{0, 0};
+            int q = 0;         // groups issued so far (S and P buffers alternate)
+            int e = 0;         // non-empty items so far (O buffers alternate)
             bool issued = false;
             const uint32_t id_s128 = idesc_bf16(C::M, 128, false, false);
             const uint32_t id_s64 = idesc_bf16(C::M, 64, false, false);
             const uint32_t id_o = idesc_bf16(C::M, 64, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-                const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-                (void)h;
-                const int n = item_slots(a, b, c, js, kaps, false);
+                if (!wait_bar(sb, &sb.info_full[inf.i], inf.ph, a.status)) break;
+                const int n = sb.info[inf.i].n;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
                 if (n == 0) continue;
                 const int G = (n + C::GS - 1) / C::GS;
+                const int ob = e & 1;
                 if (!wait_bar(sb, &sb.q_full[qr.i], qr.ph, a.status)) break;
-                if (!wait_bar(sb, &sb.o_empty[o.i], o.ph ^ 1u, a.status)) break;
+                if (!wait_bar(sb, &sb.o_empty[ob], empty_par(e >> 1), a.status)) break;
                 tc_fence_after();
                 const uint32_t qaddr = smem_u32(sm + C::OFF_Q + qr.i * C::Q_BYTES);
-                const uint32_t d_o = tmem + C::COL_O + o.i * 64;
+                const uint32_t d_o = tmem + C::COL_O + ob * 64;
                 int stg_of[2] = {0, 0};
                 auto issue_s = [&](int g) -> bool {
                     const int ns = min(C::GS, n - g * C::GS);
+                    const int qq = q + g, sbuf = qq & 1;
                     if (!wait_bar(sb, &sb.kv_full[kv.i], kv.ph, a.status)) return false;
-                    if (!wait_bar(sb, &sb.s_empty[s.i], s.ph ^ 1u, a.status)) return false;
+                    if (!wait_bar(sb, &sb.s_empty[sbuf], empty_par(qq >> 1), a.status)) return false;
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    const uint32_t d = tmem + C::COL_S + s.i * 128;
+                    const uint32_t d = tmem + C::COL_S + sbuf * 128;
                     const uint32_t id = (ns * S == 128) ? id_s128 : id_s64;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16(d, desc_kmajor_sw128(qaddr + 32 * ks),
                                  desc_kmajor_sw128(kaddr + 32 * ks), id, ks > 0);
-                    mma_commit(&sb.s_full[s.i]);
+                    mma_commit(&sb.s_full[sbuf]);
                     stg_of[g & 1] = kv.i;
                     kv.next(C::STAGES);
-                    s.next(2);
                     issued = true;
                     return true;
                 };
@@ -236,9 +267,10 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int g = 0; ok && g < G; ++g) {
                     if (g + 1 < G && !issue_s(g + 1)) { ok = false; break; }
                     const int ns = min(C::GS, n - g * C::GS);
-                    if (!wait_bar(sb, &sb.p_full[p.i], p.ph, a.status)) { ok = false; break; }
+                    const int qq = q + g, pbuf = qq & 1;
+                    if (!wait_bar(sb, &sb.p_full[pbuf], full_par(qq >> 1), a.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + p.i * C::P_BYTES);
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * C::P_BYTES);
                     const uint32_t vaddr =
                         smem_u32(sm + C::OFF_KV + stg_of[g & 1] * C::STAGE_BYTES + C::NG * 128);
                     const int ksteps = ns * S / 16;
@@ -246,14 +278,14 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         mma_bf16(d_o, desc_kmajor_sw128(paddr + (ks >> 2) * C::P_BLOCK + (ks & 3) * 32),
                                  desc_mnmajor_sw128(vaddr + ks * 2048), id_o, (g > 0 || ks > 0));
                     mma_commit(&sb.kv_empty[stg_of[g & 1]]);
-                    mma_commit(&sb.p_empty[p.i]);
-                    p.next(2);
+                    mma_commit(&sb.p_empty[pbuf]);
                 }
                 if (!ok) break;
-                mma_commit(&sb.o_full[o.i]);
+                mma_commit(&sb.o_full[ob]);
                 mma_commit(&sb.q_empty[qr.i]);
-                o.next(2);
                 qr.next(2);
+                q += G;
+                ++e;
             }
             if (issued) {
                 // every MMA must have finished before TMEM is released
@@ -263,44 +295,57 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
+        const int wg = (warp - 2) >> 2;                 // warpgroup 0 or 1
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
         const int u = (S == 64) ? (lane >> 4) : 0;
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-        Ring s{0, 0}, p{0, 0}, o{0, 0};
-        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-            const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-            const int n = item_slots(a, b, c, js, kaps, false);
+        Ring inf{0, 0};
+        int q = 0, e = 0, n_all = 0;
+        int kg = 0, ko = 0;          // groups / epilogues handled by this warpgroup
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_all) {
+            if (!wait_bar(sb, &sb.info_full[inf.i], inf.ph, a.status)) break;
+            const ItemInfo& I = sb.info[inf.i];
+            const int b = I.b, c = I.c, h = I.h, n = I.n;
             const size_t tok = (size_t)b * a.Lq + (size_t)c * S + row;
-            const int32_t* irow = a.idx + ((size_t)b * a.nQ + c) * a.topk;
-            const float* wrow = a.w + ((size_t)b * a.nQ + c) * a.topk;
             __nv_bfloat16* orow = a.o + (tok * a.H + h) * 64;
             float* lrow = a.lse ? a.lse + (tok * a.H + h) * a.topk : nullptr;
-            if (lrow && u == 0)
+            // the epilogue of an item is done by one warpgroup, alternating
+            const bool my_epi = (n == 0) ? ((n_all & 1) == wg) : ((e & 1) == wg);
+            if (my_epi && lrow && u == 0)
                 for (int j = 0; j < a.topk; ++j) {
-                    const int kap = irow[j];
-                    if (kap < 0) lrow[j] = -INFINITY;
-                    else if (kap >= a.nP) lrow[j] = NAN;
+                    const int cd = I.code[j];
+                    if (cd == 1) lrow[j] = -INFINITY;
+                    else if (cd == 2) lrow[j] = NAN;
                 }
             if (n == 0) {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                if (S == 64) {
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (my_epi) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    if (S == 64) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + u * 32)[q4] = z;
-                } else {
+                        for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + u * 32)[q4] = z;
+                    } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) reinterpret_cast<uint4*>(orow)[q4] = z;
+                        for (int q4 = 0; q4 < 8; ++q4) reinterpret_cast<uint4*>(orow)[q4] = z;
+                    }
                 }
                 continue;
             }
+            const int G = (n + C::GS - 1) / C::GS;
             bool ok = true;
-            for (int g = 0; g * C::GS < n; ++g) {
+            for (int g = 0; g < G; ++g) {
+                const int qq = q + g;
+                if ((qq & 1) != wg) continue;
                 const int ns = min(C::GS, n - g * C::GS);
                 const bool active = u < ns;
-                if (!wait_bar(sb, &sb.s_full[s.i], s.ph, a.status)) { ok = false; break; }
+                const int j = active ? I.js[g * C::GS + u] : 0;
+                const float wj = active ? I.w[g * C::GS + u] : 0.f;
+                if (!wait_bar(sb, &sb.s_full[wg], full_par(kg), a.status)) { ok = false; break; }
                 tc_fence_after();
                 float x[C::VALS];
-                const uint32_t taddr = tmem + lane_base + C::COL_S + s.i * 128;
+                const uint32_t taddr = tmem + lane_base + C::COL_S + wg * 128;
                 if (S == 64) {
 #pragma unroll
                     for (int ci = 0; ci < C::VALS / 16; ++ci) {
@@ -320,8 +365,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&sb.s_empty[s.i]);
-                s.next(2);
+                mbar_arrive(&sb.s_empty[wg]);
                 float mx = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < C::VALS; ++i) mx = fmaxf(mx, x[i]);
@@ -332,73 +376,60 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -mb));
                     l += x[i];
                 }
-                float coef = 0.f;
+                const float coef = active ? wj / l : 0.f;
+                if (active && lrow) lrow[j] = (mb + log2f(l)) * kLn2;
+                if (!wait_bar(sb, &sb.p_empty[wg], empty_par(kg), a.status)) { ok = false; break; }
                 if (active) {
-                    const int j = js[g * C::GS + u];
-                    coef = wrow[j] / l;
-                    if (lrow) lrow[j] = (mb + log2f(l)) * kLn2;
-                }
-                if (!wait_bar(sb, &sb.p_empty[p.i], p.ph ^ 1u, a.status)) { ok = false; break; }
-                if (active) {
-                    uint8_t* pbase = sm + C::OFF_P + p.i * C::P_BYTES + row * 128;
+                    uint8_t* pbase = sm + C::OFF_P + wg * C::P_BYTES + row * 128;
 #pragma unroll
                     for (int ch = 0; ch < C::VALS / 8; ++ch) {
-                        uint4 v;
-                        v.x = pack_bf16(x[8 * ch + 0] * coef, x[8 * ch + 1] * coef);
-                        v.y = pack_bf16(x[8 * ch + 2] * coef, x[8 * ch + 3] * coef);
-                        v.z = pack_bf16(x[8 * ch + 4] * coef, x[8 * ch + 5] * coef);
-                        v.w = pack_bf16(x[8 * ch + 6] * coef, x[8 * ch + 7] * coef);
                         const int blk = (S == 64) ? u : (ch >> 3);
                         const int cc = ch & 7;
-                        *reinterpret_cast<uint4*>(pbase + blk * C::P_BLOCK + ((cc ^ (row & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4*>(pbase + blk * C::P_BLOCK + ((cc ^ (row & 7)) << 4)) =
+                            tcx::pack8(x + 8 * ch, coef);
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&sb.p_full[p.i]);
-                p.next(2);
+                mbar_arrive(&sb.p_full[wg]);
+                ++kg;
             }
+            mbar_arrive(&sb.info_empty[inf.i]);
+            inf.next(kInfo);
             if (!ok) break;
-            if (!wait_bar(sb, &sb.o_full[o.i], o.ph, a.status)) break;
+            q += G;
+            const bool mine = (e & 1) == wg;
+            ++e;
+            if (!mine) continue;
+            if (!wait_bar(sb, &sb.o_full[wg], full_par(ko), a.status)) break;
+            ++ko;
             tc_fence_after();
-            const uint32_t oaddr = tmem + lane_base + C::COL_O + o.i * 64;
+            const uint32_t oaddr = tmem + lane_base + C::COL_O + wg * 64;
             if (S == 64) {
                 uint32_t r0[16], r1[16];
                 tmem_ld_16x32bx2_x16<32>(oaddr, r0);
                 tmem_ld_16x32bx2_x16<32>(oaddr + 16, r1);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&sb.o_empty[o.i]);
+                mbar_arrive(&sb.o_empty[wg]);
                 uint4* dst = reinterpret_cast<uint4*>(orow + u * 32);
-#pragma unroll
-                for (int q4 = 0; q4 < 2; ++q4) {
-                    dst[q4] = make_uint4(pack_bf16(__uint_as_float(r0[8 * q4 + 0]), __uint_as_float(r0[8 * q4 + 1])),
-                                         pack_bf16(__uint_as_float(r0[8 * q4 + 2]), __uint_as_float(r0[8 * q4 + 3])),
-                                         pack_bf16(__uint_as_float(r0[8 * q4 + 4]), __uint_as_float(r0[8 * q4 + 5])),
-                                         pack_bf16(__uint_as_float(r0[8 * q4 + 6]), __uint_as_float(r0[8 * q4 + 7])));
-                    dst[2 + q4] = make_uint4(pack_bf16(__uint_as_float(r1[8 * q4 + 0]), __uint_as_float(r1[8 * q4 + 1])),
-                                             pack_bf16(__uint_as_float(r1[8 * q4 + 2]), __uint_as_float(r1[8 * q4 + 3])),
-                                             pack_bf16(__uint_as_float(r1[8 * q4 + 4]), __uint_as_float(r1[8 * q4 + 5])),
-                                             pack_bf16(__uint_as_float(r1[8 * q4 + 6]), __uint_as_float(r1[8 * q4 + 7])));
-                }
+                dst[0] = tcx::pack8u(r0);
+                dst[1] = tcx::pack8u(r0 + 8);
+                dst[2] = tcx::pack8u(r1);
+                dst[3] = tcx::pack8u(r1 + 8);
             } else {
                 uint32_t r[4][16];
 #pragma unroll
                 for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(oaddr + 16 * ci, r[ci]);
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&sb.o_empty[o.i]);
+                mbar_arrive(&sb.o_empty[wg]);
                 uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci)
-#pragma unroll
-                    for (int q4 = 0; q4 < 2; ++q4)
-                        dst[2 * ci + q4] = make_uint4(
-                            pack_bf16(__uint_as_float(r[ci][8 * q4 + 0]), __uint_as_float(r[ci][8 * q4 + 1])),
-                            pack_bf16(__uint_as_float(r[ci][8 * q4 + 2]), __uint_as_float(r[ci][8 * q4 + 3])),
-                            pack_bf16(__uint_as_float(r[ci][8 * q4 + 4]), __uint_as_float(r[ci][8 * q4 + 5])),
-                            pack_bf16(__uint_as_float(r[ci][8 * q4 + 6]), __uint_as_float(r[ci][8 * q4 + 7])));
+                for (int ci = 0; ci < 4; ++ci) {
+                    dst[2 * ci] = tcx::pack8u(r[ci]);
+                    dst[2 * ci + 1] = tcx::pack8u(r[ci] + 8);
+                }
             }
-            o.next(2);
         }
     }
 

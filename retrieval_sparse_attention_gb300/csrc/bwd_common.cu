@@ -121,9 +121,18 @@ cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, c
                                  int* launches) {
     const BwdWorkspace L = bwd_workspace_layout(s);
     char* base = static_cast<char*>(ws);
-    int* count = reinterpret_cast<int*>(base + L.count_off);
-    int* offset = reinterpret_cast<int*>(base + L.offset_off);
-    int* entry = reinterpret_cast<int*>(base + L.entry_off);
+    return launch_inverse_index_to(s, idx, reinterpret_cast<int*>(base + L.count_off),
+                                   reinterpret_cast<int*>(base + L.offset_off),
+                                   reinterpret_cast<int*>(base + L.entry_off), st, launches);
+}
+
+size_t inverse_index_bytes(int B, int nQ, int nP, int topk) {
+    return align256(sizeof(int) * (size_t)B * nP) + align256(sizeof(int) * (size_t)B * (nP + 1)) +
+           align256(sizeof(int) * (size_t)B * nQ * topk);
+}
+
+cudaError_t launch_inverse_index_to(const Shape& s, const int32_t* idx, int* count, int* offset,
+                                    int* entry, cudaStream_t st, int* launches) {
     const int nE = s.nQ * s.topk;
     const int warps = s.B * s.nP;
     const int blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;

@@ -51,8 +51,16 @@ BwdWorkspace bwd_workspace_layout(const Shape& s);
 int decode_max_blocks(int N);
 size_t decode_workspace_bytes(int N, int topk);
 
-cudaError_t launch_score_topk(const Shape& s, const void* lm, int32_t* idx, float* score,
-                              float* weight, int* status, cudaStream_t st, int* launches);
+// noise [B, nQ, nQ] fp32 or nullptr (plain top-k)
+cudaError_t launch_score_topk(const Shape& s, const void* lm, const float* noise, int32_t* idx,
+                              float* score, float* weight, int* status, cudaStream_t st,
+                              int* launches);
+
+// Landmark gradients; ws holds an inverse index (inverse_index_bytes()).
+size_t inverse_index_bytes(int B, int nQ, int nP, int topk);
+cudaError_t launch_landmark_bwd(const Shape& s, const void* lm, const int32_t* idx,
+                                const float* dscore, void* dlm, void* ws, cudaStream_t st,
+                                int* launches);
 
 cudaError_t launch_decode_retrieve(const void* lm, const void* ql, int N, int D, int topk,
                                    gca_dtype_t dt, int off_by_one, float score_scale,
@@ -80,6 +88,9 @@ cudaError_t launch_bwd_tc(const Shape& s, const void* q, const void* k, const vo
 // Shared backward pieces (inverse index, score gradient).
 cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, cudaStream_t st,
                                  int* launches);
+// Inverse index into explicit buffers: count [B, nP], offset [B, nP+1], entry [B, nQ*topk].
+cudaError_t launch_inverse_index_to(const Shape& s, const int32_t* idx, int* count, int* offset,
+                                    int* entry, cudaStream_t st, int* launches);
 cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, void* ws,
                           float* dscore, cudaStream_t st, int* launches);
 

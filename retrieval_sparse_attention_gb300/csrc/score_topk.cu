@@ -10,6 +10,11 @@
 // top-k is taken by k rounds of a block-wide arg-max under the order
 // (score descending, chunk ascending).  The whole landmark tensor of a row
 // is small (nC x D) and stays in L2, so the kernel is latency-bound.
+//
+// With a noise tensor (section 3.2: during training Gumbel noise is added to
+// the relevance scores before the top-k selection) the selection key is
+// fl32(fl32(s * sigma) + g), rounded step by step; the weights are still the
+// softmax of the clean scores of the selected chunks.
 #include <float.h>
 #include <math.h>
 
@@ -22,14 +27,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-template <typename T>
+template <typename T, bool NOISY>
 __global__ void __launch_bounds__(kThreads)
-score_topk_kernel(const T* __restrict__ lm, int nC, int D, int topk, int include_self,
-                  int off_by_one, float sscale, int32_t* __restrict__ idx,
-                  float* __restrict__ score, float* __restrict__ weight) {
+score_topk_kernel(const T* __restrict__ lm, const float* __restrict__ noise, int nC, int D,
+                  int topk, int include_self, int off_by_one, float sscale,
+                  int32_t* __restrict__ idx, float* __restrict__ score,
+                  float* __restrict__ weight) {
     extern __shared__ float sh[];
     float* lt = sh;            // [D]   landmark of chunk c-1
     float* s = sh + D;         // [nC]  scores of the candidates
+    float* key = NOISY ? s + nC : s;   // [nC] selection keys
     __shared__ float red_s[kWarps];
     __shared__ int red_i[kWarps];
     __shared__ float sel_s[kMaxTopk];
@@ -50,7 +57,12 @@ score_topk_kernel(const T* __restrict__ lm, int nC, int D, int topk, int include
         float acc = 0.f;
         for (int e = lane; e < D; e += 32) acc = fmaf(lt[e], to_f(lk[e]), acc);
         acc = warp_sum(acc);
-        if (lane == 0) s[kap] = acc;
+        if (lane == 0) {
+            s[kap] = acc;
+            if (NOISY)
+                key[kap] = __fadd_rn(__fmul_rn(acc, sscale),
+                                     noise[((size_t)b * nC + c) * nC + kap]);
+        }
     }
     __syncthreads();
 
@@ -59,7 +71,7 @@ score_topk_kernel(const T* __restrict__ lm, int nC, int D, int topk, int include
         float bs = -INFINITY;
         int bi = 0x7fffffff;
         for (int kap = threadIdx.x; kap < n; kap += kThreads) {
-            float v = s[kap];
+            float v = key[kap];
             if (v != -INFINITY && ranks_before(v, kap, bs, bi)) { bs = v; bi = kap; }
         }
 #pragma unroll
@@ -73,9 +85,9 @@ score_topk_kernel(const T* __restrict__ lm, int nC, int D, int topk, int include
         if (threadIdx.x == 0) {
             for (int w = 1; w < kWarps; ++w)
                 if (ranks_before(red_s[w], red_i[w], bs, bi)) { bs = red_s[w]; bi = red_i[w]; }
-            sel_s[j] = bs;
+            sel_s[j] = s[bi];    // the clean score
             sel_i[j] = bi;
-            s[bi] = -INFINITY;   // taken
+            key[bi] = -INFINITY; // taken
         }
         __syncthreads();
     }
@@ -97,25 +109,31 @@ score_topk_kernel(const T* __restrict__ lm, int nC, int D, int topk, int include
     }
 }
 
+template <typename T, bool NOISY>
+void launch_typed(const Shape& sp, const void* lm, const float* noise, int32_t* idx, float* score,
+                  float* weight, cudaStream_t st) {
+    const size_t smem = sizeof(float) * ((size_t)sp.D + (NOISY ? 2 : 1) * (size_t)sp.nQ);
+    dim3 grid(sp.nQ, sp.B);
+    auto kern = score_topk_kernel<T, NOISY>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    GCA_LAUNCH(NOISY ? "score_topk_noisy" : "score_topk", st,
+               kern<<<grid, kThreads, smem, st>>>((const T*)lm, noise, sp.nQ, sp.D, sp.topk,
+                                                  sp.include_self, sp.off_by_one, sp.score_scale,
+                                                  idx, score, weight));
+}
+
 }  // namespace
 
-cudaError_t launch_score_topk(const Shape& sp, const void* lm, int32_t* idx, float* score,
-                              float* weight, int* status, cudaStream_t st, int* launches) {
+cudaError_t launch_score_topk(const Shape& sp, const void* lm, const float* noise, int32_t* idx,
+                              float* score, float* weight, int* status, cudaStream_t st,
+                              int* launches) {
     (void)status;
-    const size_t smem = sizeof(float) * ((size_t)sp.D + sp.nQ);
-    dim3 grid(sp.nQ, sp.B);
     if (sp.dtype == GCA_BF16) {
-        auto kern = score_topk_kernel<__nv_bfloat16>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        GCA_LAUNCH("score_topk", st, kern<<<grid, kThreads, smem, st>>>((const __nv_bfloat16*)lm, sp.nQ, sp.D, sp.topk,
-                                           sp.include_self, sp.off_by_one, sp.score_scale, idx,
-                                           score, weight));
+        if (noise) launch_typed<__nv_bfloat16, true>(sp, lm, noise, idx, score, weight, st);
+        else launch_typed<__nv_bfloat16, false>(sp, lm, noise, idx, score, weight, st);
     } else {
-        auto kern = score_topk_kernel<float>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        GCA_LAUNCH("score_topk", st, kern<<<grid, kThreads, smem, st>>>((const float*)lm, sp.nQ, sp.D, sp.topk,
-                                           sp.include_self, sp.off_by_one, sp.score_scale, idx,
-                                           score, weight));
+        if (noise) launch_typed<float, true>(sp, lm, noise, idx, score, weight, st);
+        else launch_typed<float, false>(sp, lm, noise, idx, score, weight, st);
     }
     *launches += 1;
     return cudaGetLastError();
