@@ -204,6 +204,26 @@ gca_status_t gca_decode_retrieve_noalloc(const void* landmarks, const void* quer
                                          float* score, float* weight, void* stream);
 
 /*
+ * gca_gather_chunks -- bring the retrieved chunks of an offloaded K/V cache
+ * into a compact device pool.  Defines: section 3.2 (past chunks can be
+ * offloaded to CPU memory and reloaded when retrieved) and the rebuttal's
+ * offload-cost estimate (answer to Q2 of reviewer 3).
+ *   src_k, src_v: caches of n_src chunks of chunk_bytes each, in memory the
+ *     device can address (device memory, or page-locked host memory, whose
+ *     host pointer is device-valid under unified addressing); read-only.
+ *   idx [topk] int32 (device): retrieved chunks, -1 for an empty slot.
+ *   dst_k, dst_v [topk, chunk_bytes] (device): chunk idx[j] is copied to
+ *     slot j; empty slots are zero-filled.
+ *   dst_idx [topk] int32 (device): j for a filled slot, -1 for an empty one,
+ *     i.e. the idx to pass to gca_fwd together with n_pool_chunks = topk.
+ *   chunk_bytes must be a multiple of 16.  An index >= n_src is reported as
+ *   GCA_ERR_DEVICE_INDEX and its slot zero-filled.
+ */
+gca_status_t gca_gather_chunks(const void* src_k, const void* src_v, int n_src,
+                               size_t chunk_bytes, const int32_t* idx, int topk, void* dst_k,
+                               void* dst_v, int32_t* dst_idx, void* stream);
+
+/*
  * gca_get_status -- synchronise `stream`, then return and clear the device
  * status word of the current device (GCA_OK if no device-side error was
  * recorded since the last call).

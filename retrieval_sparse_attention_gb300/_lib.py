@@ -24,7 +24,8 @@ EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_decode_workspace_size", "gca_decode_retrieve", "gca_get_status",
             "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
             "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc",
-            "gca_score_topk_noisy", "gca_landmark_bwd_workspace_size", "gca_landmark_bwd")
+            "gca_score_topk_noisy", "gca_landmark_bwd_workspace_size", "gca_landmark_bwd",
+            "gca_gather_chunks")
 
 
 class GcaParams(ctypes.Structure):
@@ -68,6 +69,7 @@ def load() -> ctypes.CDLL:
                                     i32),
             "gca_decode_retrieve_noalloc": ([vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp],
                                             i32),
+            "gca_gather_chunks": ([vp, vp, i32, sz, vp, i32, vp, vp, vp, vp], i32),
             "gca_get_status": ([vp], i32),
             "gca_status_string": ([i32], ctypes.c_char_p),
             "gca_last_launch_count": ([], i32),

@@ -117,6 +117,38 @@ def gca_decode_retrieve_noalloc(landmarks, query_landmark, N, D, topk, dtype, of
         float(score_scale), _p(idx), _p(score), _p(weight), _stream(stream)))
 
 
+def _pa(t):
+    """Pointer of a CUDA tensor, or of a pinned host tensor (device-addressable)."""
+    if t.is_cuda:
+        return _p(t)
+    if not t.is_pinned():
+        raise ValueError("offloaded caches must be in page-locked (pinned) host memory")
+    if not t.is_contiguous():
+        raise ValueError("GCA entry points take contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gca_gather_chunks(src_k, src_v, n_src, chunk_bytes, idx, topk, dst_k, dst_v, dst_idx,
+                      stream=None):
+    _check("gca_gather_chunks", _lib.load().gca_gather_chunks(
+        _pa(src_k), _pa(src_v), n_src, chunk_bytes, _p(idx), topk, _p(dst_k), _p(dst_v),
+        _p(dst_idx), _stream(stream)))
+
+
+def gather_chunks(cache_k, cache_v, idx):
+    """cache_k/v [n_chunks, S, H, d] (device or pinned host) -> compact
+    pools [1, topk*S, H, d] on the device and the remapped idx [1, 1, topk]."""
+    n, S, H, d = cache_k.shape
+    topk = idx.numel()
+    dev = idx.device
+    dk = torch.empty(topk * S, H, d, dtype=cache_k.dtype, device=dev)
+    dv = torch.empty_like(dk)
+    di = torch.empty(topk, dtype=torch.int32, device=dev)
+    chunk_bytes = S * H * d * cache_k.element_size()
+    gca_gather_chunks(cache_k, cache_v, n, chunk_bytes, idx, topk, dk, dv, di)
+    return dk.view(1, topk * S, H, d), dv.view(1, topk * S, H, d), di.view(1, 1, topk)
+
+
 def gca_get_status(stream=None) -> int:
     return int(_lib.load().gca_get_status(_stream(stream)))
 

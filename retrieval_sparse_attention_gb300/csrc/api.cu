@@ -251,6 +251,22 @@ gca_status_t gca_decode_retrieve(const void* landmarks, const void* query_landma
     return r;
 }
 
+gca_status_t gca_gather_chunks(const void* src_k, const void* src_v, int n_src,
+                               size_t chunk_bytes, const int32_t* idx, int topk, void* dst_k,
+                               void* dst_v, int32_t* dst_idx, void* stream) {
+    if (n_src < 1 || topk < 1 || chunk_bytes == 0 || chunk_bytes % 16 != 0) return GCA_ERR_INVALID_ARG;
+    if (topk > kMaxTopk) return GCA_ERR_UNSUPPORTED;
+    gca_status_t r = check_ptrs({src_k, src_v, idx, dst_k, dst_v, dst_idx});
+    if (r != GCA_OK) return r;
+    int* st = status_ptr();
+    if (!st) return GCA_ERR_CUDA;
+    int n = 0;
+    r = from_cuda(launch_gather_chunks(src_k, src_v, n_src, chunk_bytes, idx, topk, dst_k, dst_v,
+                                       dst_idx, st, static_cast<cudaStream_t>(stream), &n));
+    if (r == GCA_OK) t_launches = n;
+    return r;
+}
+
 gca_status_t gca_synth_fill_hash(void* dst, size_t n_elems, gca_dtype_t dtype, uint64_t seed,
                                  uint64_t tensor_id, uint64_t first_elem, void* stream) {
     if (!dst || (dtype != GCA_BF16 && dtype != GCA_F32)) return GCA_ERR_INVALID_ARG;

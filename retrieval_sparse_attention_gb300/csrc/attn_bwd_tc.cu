@@ -80,6 +80,12 @@ __device__ __forceinline__ void load_cols16(uint32_t taddr, float* x) {
 }
 
 template <int S>
+__device__ __forceinline__ void issue_cols16(uint32_t taddr, uint32_t (&r)[16]) {
+    if (S == 64) tmem_ld_16x32bx2_x16<64>(taddr, r);
+    else tmem_ld_32x32b_x16(taddr, r);
+}
+
+template <int S>
 __device__ __forceinline__ void load_cols64(uint32_t taddr, float* x) {
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
@@ -414,13 +420,22 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     load_cols64<S>(ts0 + ch * 64, x);
 #pragma unroll
                     for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
+                    float d8[8];
 #pragma unroll
-                    for (int ci = 0; ci < 4; ++ci) {
-                        float g[16];
-                        load_cols16<S>(tg0 + ch * 64 + 16 * ci, g);
+                    for (int i = 0; i < 8; ++i) d8[i] = 0.f;
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) dl = fmaf(x[16 * ci + t], g[t], dl);
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t g0[16], g1[16];
+                        issue_cols16<S>(tg0 + ch * 64 + 32 * half, g0);
+                        issue_cols16<S>(tg0 + ch * 64 + 32 * half + 16, g1);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            d8[t & 7] = fmaf(x[32 * half + t], __uint_as_float(g0[t]), d8[t & 7]);
+                            d8[t & 7] = fmaf(x[32 * half + 16 + t], __uint_as_float(g1[t]), d8[t & 7]);
+                        }
                     }
+                    dl += ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
                 }
                 if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
                 uint8_t* pb = sm + C::OFF_P + wg * C::P_BYTES;
@@ -432,21 +447,27 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                         for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
                     }
 #pragma unroll
-                    for (int ci = 0; ci < 4; ++ci) {
-                        float g[16];
-                        load_cols16<S>(tg0 + ch * 64 + 16 * ci, g);
-                        if (ch == NCH - 1 && ci == 3) {
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t g0[16], g1[16];
+                        issue_cols16<S>(tg0 + ch * 64 + 32 * half, g0);
+                        issue_cols16<S>(tg0 + ch * 64 + 32 * half + 16, g1);
+                        tmem_wait_ld();
+                        if (ch == NCH - 1 && half == 1) {
                             tc_fence_before();
                             mbar_arrive(&sb.s_empty);
                         }
+                        float g[32];
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) g[t] = x[16 * ci + t] * (g[t] - dl);
+                        for (int t = 0; t < 16; ++t) {
+                            g[t] = x[32 * half + t] * (__uint_as_float(g0[t]) - dl);
+                            g[16 + t] = x[32 * half + 16 + t] * (__uint_as_float(g1[t]) - dl);
+                        }
                         if (active) {
                             const int blk = (S == 64) ? u : ch;
-                            *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, 2 * ci)) =
-                                pack8(g, wsc);
-                            *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, 2 * ci + 1)) =
-                                pack8(g + 8, wsc);
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4)
+                                *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, 4 * half + c4)) =
+                                    pack8(g + 8 * c4, wsc);
                         }
                     }
                 }
@@ -777,10 +798,21 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 const uint32_t tg0 = tmem + lane_base + C::COL_G;
                 for (int pc = 0; pc < NC32; ++pc) {
                     float xs[32], xg[32];
-                    load_cols16<S>(ts0 + 32 * pc, xs);
-                    load_cols16<S>(ts0 + 32 * pc + 16, xs + 16);
-                    load_cols16<S>(tg0 + 32 * pc, xg);
-                    load_cols16<S>(tg0 + 32 * pc + 16, xg + 16);
+                    {
+                        uint32_t r0[16], r1[16], r2[16], r3[16];
+                        issue_cols16<S>(ts0 + 32 * pc, r0);
+                        issue_cols16<S>(ts0 + 32 * pc + 16, r1);
+                        issue_cols16<S>(tg0 + 32 * pc, r2);
+                        issue_cols16<S>(tg0 + 32 * pc + 16, r3);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            xs[t] = __uint_as_float(r0[t]);
+                            xs[16 + t] = __uint_as_float(r1[t]);
+                            xg[t] = __uint_as_float(r2[t]);
+                            xg[16 + t] = __uint_as_float(r3[t]);
+                        }
+                    }
                     if (pc == NC32 - 1) {
                         tc_fence_before();
                         mbar_arrive(&sb.s_empty);
