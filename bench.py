@@ -514,16 +514,23 @@ def run_case(args):
             o, lse = api.fwd(x["q"], x["k"], x["v"], idx, w, S=wl.S)
             if backward:
                 api.bwd(x["q"], x["k"], x["v"], idx, w, lse, x["dout"], S=wl.S)
+    from retrieval_sparse_attention_gb300 import _lib
+    lib = _lib.load()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    lib.gca_prof_read(0, None, None, None)
+    lib.gca_prof_enable(1)
     ev0.record()
     for _ in range(args.steps):
         step()
     ev1.record()
     torch.cuda.synchronize()
+    lib.gca_prof_enable(0)
+    prof = read_prof(lib)
     assert api.gca_get_status() == 0
-    print(json.dumps({"case": args.case, "ms_per_step": ev0.elapsed_time(ev1) / args.steps}))
+    print(json.dumps({"case": args.case, "ms_per_step": ev0.elapsed_time(ev1) / args.steps,
+                      "kernel_ms": {k: round(v[0] / v[1], 4) for k, v in sorted(prof.items())}}))
 
 
 if __name__ == "__main__":

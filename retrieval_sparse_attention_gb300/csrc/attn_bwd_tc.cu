@@ -19,10 +19,12 @@
 //     index of (query chunk, slot) entries that retrieved the chunk, gathers
 //     their Q/dO tiles and delta/lse rows, recomputes S^T = K Q^T and
 //     G^T = V dO^T, and accumulates dK += dA^T Q and dV += (w P)^T dO in TMEM.
-// Both use the warp roles of the forward kernel: warp 0 producer (decodes the
-// item metadata into shared memory, issues the TMA / bulk copies), warp 1 MMA
-// issuer and TMEM owner, warps 2-9 two math warpgroups taking alternate
-// groups and alternate item epilogues.
+// Warp roles: warp 0 producer (decodes the item metadata into shared memory,
+// issues the TMA / bulk copies); warp 1 issues the score products (S and G,
+// or S^T and G^T) and owns TMEM; warp 2 issues the accumulation products
+// (dQ, or dK and dV), so neither kind of product waits behind the other's
+// issue; warps 3-10 are two math warpgroups taking alternate groups and
+// alternate item epilogues.
 #include <math.h>
 
 #include "common.cuh"
@@ -42,7 +44,7 @@ using tcx::pack8u;
 using tcx::Ring;
 using tcx::sw128_off;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;         // producer, 2 MMA issuers, 2 math warpgroups
 constexpr int kInfo = 4;
 
 struct BwdArgs {
@@ -190,7 +192,7 @@ struct __align__(8) BarsA {
     uint64_t s_full[2], s_empty;       // s_full per math warpgroup, s_empty shared
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
-    uint64_t done;
+    uint64_t done, done2;
     uint32_t tmem;
     int abort;
     ItemInfoA info[kInfo];
@@ -212,7 +214,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInfo; ++i) {
             mbar_init(&sb.info_full[i], 1);
-            mbar_init(&sb.info_empty[i], 1 + 256);
+            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + math threads
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
@@ -230,6 +232,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         mbar_init(&sb.s_full[1], 1);
         mbar_init(&sb.s_empty, 128);
         mbar_init(&sb.done, 1);
+        mbar_init(&sb.done2, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -301,13 +304,13 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
+        // S / G products: S = Q K^T and G = dO V^T of each group
         if (lane == 0) {
             Ring kv{0, 0}, it{0, 0}, inf{0, 0};
-            int q = 0, e = 0;
+            int q = 0;
             bool issued = false;
             const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
             const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
-            const uint32_t id_dq = idesc_bf16(C::M, 64, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int n = sb.info[inf.i].n;
@@ -315,28 +318,10 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 inf.next(kInfo);
                 if (n == 0) continue;
                 const int G = (n + C::GS - 1) / C::GS;
-                const int ob = e & 1;
                 if (!wait(&sb.it_full[it.i], it.ph)) break;
-                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
                 const uint32_t qaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t doaddr = qaddr + C::TILE;
-                const uint32_t d_dq = tmem + C::COL_DQ + ob * 64;
-                int stg_of[2] = {0, 0}, ns_of[2] = {0, 0};
-                auto issue_dq = [&](int g) -> bool {
-                    const int qq = q + g, pb = qq & 1;
-                    if (!wait(&sb.p_full[pb], full_par(qq >> 1))) return false;
-                    tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
-                    const uint32_t kaddr = smem_u32(sm + C::OFF_KV + stg_of[g & 1] * C::STAGE_BYTES);
-                    const int ksteps = ns_of[g & 1] * S / 16;
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        mma_bf16(d_dq, desc_kmajor_sw128(paddr + (ks >> 2) * C::P_BLOCK + (ks & 3) * 32),
-                                 desc_mnmajor_sw128(kaddr + ks * 2048), id_dq, (g > 0 || ks > 0));
-                    mma_commit(&sb.kv_empty[stg_of[g & 1]]);
-                    mma_commit(&sb.p_empty[pb]);
-                    return true;
-                };
                 bool ok = true;
                 for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
@@ -346,34 +331,70 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
                     const uint32_t vaddr = kaddr + C::NG * 128;
                     const uint32_t id = (ns * S == 128) ? id_n128 : id_n64;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16(tmem + C::COL_S, desc_kmajor_sw128(qaddr + 32 * ks),
-                                 desc_kmajor_sw128(kaddr + 32 * ks), id, ks > 0);
-                        mma_bf16(tmem + C::COL_G, desc_kmajor_sw128(doaddr + 32 * ks),
-                                 desc_kmajor_sw128(vaddr + 32 * ks), id, ks > 0);
-                    }
+                    tcx::mma_kmajor_k64(tmem + C::COL_S, qaddr, kaddr, id, 0);
+                    tcx::mma_kmajor_k64(tmem + C::COL_G, doaddr, vaddr, id, 0);
                     mma_commit(&sb.s_full[qq & 1]);
                     issued = true;
-                    stg_of[g & 1] = kv.i;
-                    ns_of[g & 1] = ns;
                     kv.next(C::STAGES);
-                    if (g > 0 && !issue_dq(g - 1)) { ok = false; break; }
                 }
-                if (!ok || !issue_dq(G - 1)) break;
-                mma_commit(&sb.o_full[ob]);
-                mma_commit(&sb.it_empty[it.i]);
+                if (!ok) break;
+                mma_commit(&sb.it_empty[it.i]);     // Q and dO are read only by these products
                 it.next(2);
                 q += G;
-                ++e;
             }
             if (issued) {
                 mma_commit(&sb.done);
                 mbar_wait(&sb.done, 0, nullptr, 100000000ull);
             }
         }
+    } else if (warp == 2) {
+        // accumulation products: dQ += dA K of each group
+        if (lane == 0) {
+            Ring kv{0, 0}, inf{0, 0};
+            int q = 0, e = 0;
+            bool issued = false;
+            const uint32_t id_dq = idesc_bf16(C::M, 64, false, true);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+                const int n = sb.info[inf.i].n;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (n == 0) continue;
+                const int G = (n + C::GS - 1) / C::GS;
+                const int ob = e & 1;
+                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
+                tc_fence_after();
+                const uint32_t d_dq = tmem + C::COL_DQ + ob * 64;
+                bool ok = true;
+                for (int g = 0; g < G; ++g) {
+                    const int ns = min(C::GS, n - g * C::GS);
+                    const int qq = q + g, pb = qq & 1;
+                    if (!wait(&sb.p_full[pb], full_par(qq >> 1))) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
+                    const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
+                    if (ns * S == 128)
+                        tcx::mma_kmajor_mnmajor<8>(d_dq, paddr, C::P_BLOCK, kaddr, id_dq, g > 0);
+                    else
+                        tcx::mma_kmajor_mnmajor<4>(d_dq, paddr, C::P_BLOCK, kaddr, id_dq, g > 0);
+                    // the S / G products of this group are complete (their P exists)
+                    mma_commit(&sb.kv_empty[kv.i]);
+                    mma_commit(&sb.p_empty[pb]);
+                    issued = true;
+                    kv.next(C::STAGES);
+                }
+                if (!ok) break;
+                mma_commit(&sb.o_full[ob]);
+                q += G;
+                ++e;
+            }
+            if (issued) {
+                mma_commit(&sb.done2);
+                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+            }
+        }
     } else {
-        const int wg = (warp - 2) >> 2;
+        const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
         const int u = (S == 64) ? (lane >> 4) : 0;
@@ -388,7 +409,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             __nv_bfloat16* dqrow = a.dq + (tok * a.H + h) * 64;
             const bool my_epi = (n == 0) ? ((n_all & 1) == wg) : ((e & 1) == wg);
             float* dwp = a.dwpart + (((size_t)b * a.nQ + c) * a.H + h) * 4 * a.topk;
-            if (my_epi && threadIdx.x == 64 + wg * 128)
+            if (my_epi && threadIdx.x == 96 + wg * 128)
                 for (int j = 0; j < a.topk; ++j)
                     if (I.code[j] != 0)
                         for (int q4 = 0; q4 < 4; ++q4) dwp[q4 * a.topk + j] = 0.f;
@@ -550,7 +571,7 @@ struct __align__(8) BarsB {
     uint64_t s_full[2], s_empty;       // s_full per math warpgroup, s_empty shared
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
-    uint64_t done;
+    uint64_t done, done2;
     uint32_t tmem;
     int abort;
     ItemInfoB info[kInfo];
@@ -573,7 +594,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInfo; ++i) {
             mbar_init(&sb.info_full[i], 1);
-            mbar_init(&sb.info_empty[i], 1 + 256);
+            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + math threads
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
@@ -591,6 +612,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         mbar_init(&sb.s_full[1], 1);
         mbar_init(&sb.s_empty, 128);
         mbar_init(&sb.done, 1);
+        mbar_init(&sb.done2, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -672,13 +694,13 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
+        // S^T / G^T products: S^T = K Q^T and G^T = V dO^T of each group
         if (lane == 0) {
             Ring st{0, 0}, it{0, 0}, inf{0, 0};
-            int q = 0, e = 0;
+            int q = 0;
             bool issued = false;
             const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
             const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
-            const uint32_t id_acc = idesc_bf16(C::M, 64, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
@@ -686,34 +708,10 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 inf.next(kInfo);
                 if (ne <= 0) continue;
                 const int G = (ne + C::GS - 1) / C::GS;
-                const int ob = e & 1;
                 if (!wait(&sb.it_full[it.i], it.ph)) break;
-                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
                 const uint32_t kaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t vaddr = kaddr + C::TILE;
-                const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
-                const uint32_t d_dv = d_dk + 64;
-                int stg_of[2] = {0, 0}, ns_of[2] = {0, 0};
-                auto issue_acc = [&](int g) -> bool {
-                    const int qq = q + g, pbuf = qq % C::NWG;
-                    if (!wait(&sb.p_full[pbuf], full_par(qq / C::NWG))) return false;
-                    tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
-                    const uint32_t qaddr = smem_u32(sm + C::OFF_ST + stg_of[g & 1] * C::STAGE_BYTES);
-                    const uint32_t doaddr = qaddr + C::NG * 128;
-                    const int ksteps = ns_of[g & 1] * S / 16;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint32_t aoff = (ks >> 2) * C::P_BLOCK + (ks & 3) * 32;
-                        mma_bf16(d_dk, desc_kmajor_sw128(paddr + aoff), desc_mnmajor_sw128(qaddr + ks * 2048),
-                                 id_acc, (g > 0 || ks > 0));
-                        mma_bf16(d_dv, desc_kmajor_sw128(paddr + C::P_BYTES + aoff),
-                                 desc_mnmajor_sw128(doaddr + ks * 2048), id_acc, (g > 0 || ks > 0));
-                    }
-                    mma_commit(&sb.st_empty[stg_of[g & 1]]);
-                    mma_commit(&sb.p_empty[pbuf]);
-                    return true;
-                };
                 bool ok = true;
                 for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, ne - g * C::GS);
@@ -723,34 +721,75 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
                     const uint32_t doaddr = qaddr + C::NG * 128;
                     const uint32_t id = (ns * S == 128) ? id_n128 : id_n64;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16(tmem + C::COL_S, desc_kmajor_sw128(kaddr + 32 * ks),
-                                 desc_kmajor_sw128(qaddr + 32 * ks), id, ks > 0);
-                        mma_bf16(tmem + C::COL_G, desc_kmajor_sw128(vaddr + 32 * ks),
-                                 desc_kmajor_sw128(doaddr + 32 * ks), id, ks > 0);
-                    }
+                    tcx::mma_kmajor_k64(tmem + C::COL_S, kaddr, qaddr, id, 0);
+                    tcx::mma_kmajor_k64(tmem + C::COL_G, vaddr, doaddr, id, 0);
                     mma_commit(&sb.s_full[qq % C::NWG]);
                     issued = true;
-                    stg_of[g & 1] = st.i;
-                    ns_of[g & 1] = ns;
                     st.next(C::STAGES);
-                    if (g > 0 && !issue_acc(g - 1)) { ok = false; break; }
                 }
-                if (!ok || !issue_acc(G - 1)) break;
-                mma_commit(&sb.o_full[ob]);
-                mma_commit(&sb.it_empty[it.i]);
+                if (!ok) break;
+                mma_commit(&sb.it_empty[it.i]);     // K and V are read only by these products
                 it.next(2);
                 q += G;
-                ++e;
             }
             if (issued) {
                 mma_commit(&sb.done);
                 mbar_wait(&sb.done, 0, nullptr, 100000000ull);
             }
         }
+    } else if (warp == 2) {
+        // accumulation products: dK += dA^T Q and dV += (w P)^T dO of each group
+        if (lane == 0) {
+            Ring st{0, 0}, inf{0, 0};
+            int q = 0, e = 0;
+            bool issued = false;
+            const uint32_t id_acc = idesc_bf16(C::M, 64, false, true);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+                const int ne = sb.info[inf.i].ne;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (ne <= 0) continue;
+                const int G = (ne + C::GS - 1) / C::GS;
+                const int ob = e & 1;
+                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
+                tc_fence_after();
+                const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
+                const uint32_t d_dv = d_dk + 64;
+                bool ok = true;
+                for (int g = 0; g < G; ++g) {
+                    const int ns = min(C::GS, ne - g * C::GS);
+                    const int qq = q + g, pbuf = qq % C::NWG;
+                    if (!wait(&sb.p_full[pbuf], full_par(qq / C::NWG))) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
+                    const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
+                    const uint32_t doaddr = qaddr + C::NG * 128;
+                    if (ns * S == 128) {
+                        tcx::mma_kmajor_mnmajor<8>(d_dk, paddr, C::P_BLOCK, qaddr, id_acc, g > 0);
+                        tcx::mma_kmajor_mnmajor<8>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, id_acc, g > 0);
+                    } else {
+                        tcx::mma_kmajor_mnmajor<4>(d_dk, paddr, C::P_BLOCK, qaddr, id_acc, g > 0);
+                        tcx::mma_kmajor_mnmajor<4>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, id_acc, g > 0);
+                    }
+                    // the S^T / G^T products of this group are complete (their P exists)
+                    mma_commit(&sb.st_empty[st.i]);
+                    mma_commit(&sb.p_empty[pbuf]);
+                    issued = true;
+                    st.next(C::STAGES);
+                }
+                if (!ok) break;
+                mma_commit(&sb.o_full[ob]);
+                q += G;
+                ++e;
+            }
+            if (issued) {
+                mma_commit(&sb.done2);
+                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+            }
+        }
     } else {
-        const int wg = (warp - 2) >> 2;
+        const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
         const int u = (S == 64) ? (lane >> 4) : 0;

@@ -69,6 +69,38 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
     return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
 }
 
+// ---------------------------------------------------------------------------
+// MMA sequences with the operand descriptors built once: the start-address
+// field holds (address >> 4) in the low 14 bits, so advancing an operand by
+// B bytes adds B / 16 to the 64-bit descriptor (no carry: shared memory is
+// below 256 KB).
+// ---------------------------------------------------------------------------
+// D (+)= A B^T over 64 elements of K (4 steps of 16), both operands K-major
+// 128-byte-swizzled tiles whose rows are 128 bytes.
+__device__ __forceinline__ void mma_kmajor_k64(uint32_t d, uint32_t a_addr, uint32_t b_addr,
+                                               uint32_t idesc, uint32_t acc_first) {
+    const uint64_t ad = tc::desc_kmajor_sw128(a_addr);
+    const uint64_t bd = tc::desc_kmajor_sw128(b_addr);
+    tc::mma_bf16(d, ad, bd, idesc, acc_first);
+    tc::mma_bf16(d, ad + 2, bd + 2, idesc, 1);
+    tc::mma_bf16(d, ad + 4, bd + 4, idesc, 1);
+    tc::mma_bf16(d, ad + 6, bd + 6, idesc, 1);
+}
+
+// D (+)= P X over KSTEPS*16 elements of K: P K-major in blocks of 64 K
+// elements (p_block bytes apart), X MN-major with 128-byte K rows.
+template <int KSTEPS>
+__device__ __forceinline__ void mma_kmajor_mnmajor(uint32_t d, uint32_t p_addr, uint32_t p_block,
+                                                   uint32_t x_addr, uint32_t idesc,
+                                                   uint32_t acc_first) {
+    const uint64_t pd = tc::desc_kmajor_sw128(p_addr);
+    const uint64_t xd = tc::desc_mnmajor_sw128(x_addr);
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks)
+        tc::mma_bf16(d, pd + (uint64_t)(((ks >> 2) * p_block + (ks & 3) * 32) >> 4),
+                     xd + (uint64_t)(ks * 128), idesc, ks == 0 ? acc_first : 1u);
+}
+
 // Named barrier over the 128 softmax/epilogue threads (warps 2-5).
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
