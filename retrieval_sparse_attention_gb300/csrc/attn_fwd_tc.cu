@@ -6,16 +6,20 @@
 // outputs are fused as O_t = sum_j w_j O_t^j (stage 2).  App. B: the forward
 // also returns the log-sum-exp of every (token, slot).
 //
-// Design (one persistent CTA per SM, 10 warps, warp-specialised):
+// Design (one persistent CTA per SM, 11 warps, warp-specialised):
 //   warp 0     producer: decodes each work item's retrieval row (valid slots,
 //              their weights, codes of empty / out-of-range slots) into a
 //              shared-memory info ring, then TMA-loads the Q tile and, for each
 //              group of retrieved chunks, their K and V tiles (box 64 x S,
 //              128-byte swizzle) straight from the [tokens, H*d] tensors into
 //              a ring of stages.
-//   warp 1     MMA issuer (one thread) and TMEM owner: S_g = Q K_g^T for a
-//              group of retrieved chunks (N = 128 keys), then O += P_g V_g.
-//   warps 2-9  two softmax warpgroups taking alternate groups: read S_g from
+//   warp 1     S issuer (one thread) and TMEM owner: S_g = Q K_g^T for a
+//              group of retrieved chunks (N = 128 keys) into one of two TMEM
+//              buffers.
+//   warp 2     P V issuer (one thread): O += P_g V_g in a TMEM accumulator.
+//              Two issuers keep either kind of product from waiting behind
+//              the other's issue (a tcgen05.mma blocks while the queue drains).
+//   warps 3-10 two softmax warpgroups taking alternate groups: read S_g from
 //              TMEM, per-slot max / sum / exp2, write P_g = exp(S - m) *
 //              (w_j / l_j) as bf16 into shared memory (the A operand of the
 //              PV MMA), write the lse; each warpgroup also stores O (read
@@ -43,7 +47,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;         // producer, 2 MMA issuers, 2 softmax warpgroups
 constexpr int kInfo = 4;                 // item-info ring depth
 using tcx::Ring;
 using tcx::fast_exp2;
@@ -99,7 +103,7 @@ struct __align__(8) Bars {
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
-    uint64_t done;
+    uint64_t done, done2;
     uint32_t tmem;
     int abort;
     ItemInfo info[kInfo];
@@ -128,7 +132,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInfo; ++i) {
             mbar_init(&sb.info_full[i], 1);
-            mbar_init(&sb.info_empty[i], 1 + 256);     // MMA thread + every softmax thread
+            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + every softmax thread
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.q_full[i], 1);
@@ -145,6 +149,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(&sb.kv_empty[i], 1);
         }
         mbar_init(&sb.done, 1);
+        mbar_init(&sb.done2, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -221,14 +226,55 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (q_out[i]) mbar_wait(&sb.q_full[i], q_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S issuer
+        // S_g = Q K_g^T into the S buffer of group g (two, alternating).
         if (lane == 0) {
             Ring kv{0, 0}, qr{0, 0}, inf{0, 0};
-            int q = 0;         // groups issued so far (S and P buffers alternate)
-            int e = 0;         // non-empty items so far (O buffers alternate)
+            int q = 0;
             bool issued = false;
             const uint32_t id_s128 = idesc_bf16(C::M, 128, false, false);
             const uint32_t id_s64 = idesc_bf16(C::M, 64, false, false);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                if (!wait_bar(sb, &sb.info_full[inf.i], inf.ph, a.status)) break;
+                const int n = sb.info[inf.i].n;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (n == 0) continue;
+                const int G = (n + C::GS - 1) / C::GS;
+                if (!wait_bar(sb, &sb.q_full[qr.i], qr.ph, a.status)) break;
+                tc_fence_after();
+                const uint32_t qaddr = smem_u32(sm + C::OFF_Q + qr.i * C::Q_BYTES);
+                bool ok = true;
+                for (int g = 0; g < G; ++g) {
+                    const int ns = min(C::GS, n - g * C::GS);
+                    const int qq = q + g, sbuf = qq & 1;
+                    if (!wait_bar(sb, &sb.kv_full[kv.i], kv.ph, a.status) ||
+                        !wait_bar(sb, &sb.s_empty[sbuf], empty_par(qq >> 1), a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
+                    tcx::mma_kmajor_k64(tmem + C::COL_S + sbuf * 128, qaddr, kaddr,
+                                        (ns * S == 128) ? id_s128 : id_s64, 0);
+                    mma_commit(&sb.s_full[sbuf]);
+                    issued = true;
+                    kv.next(C::STAGES);
+                }
+                if (!ok) break;
+                mma_commit(&sb.q_empty[qr.i]);     // Q is read only by these products
+                qr.next(2);
+                q += G;
+            }
+            if (issued) {
+                mma_commit(&sb.done);
+                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ P V issuer
+        // O += P_g V_g as each softmax warpgroup delivers P_g.
+        if (lane == 0) {
+            Ring kv{0, 0}, inf{0, 0};
+            int q = 0, e = 0;
+            bool issued = false;
             const uint32_t id_o = idesc_bf16(C::M, 64, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait_bar(sb, &sb.info_full[inf.i], inf.ph, a.status)) break;
@@ -238,64 +284,40 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (n == 0) continue;
                 const int G = (n + C::GS - 1) / C::GS;
                 const int ob = e & 1;
-                if (!wait_bar(sb, &sb.q_full[qr.i], qr.ph, a.status)) break;
                 if (!wait_bar(sb, &sb.o_empty[ob], empty_par(e >> 1), a.status)) break;
                 tc_fence_after();
-                const uint32_t qaddr = smem_u32(sm + C::OFF_Q + qr.i * C::Q_BYTES);
                 const uint32_t d_o = tmem + C::COL_O + ob * 64;
-                int stg_of[2] = {0, 0};
-                auto issue_s = [&](int g) -> bool {
-                    const int ns = min(C::GS, n - g * C::GS);
-                    const int qq = q + g, sbuf = qq & 1;
-                    if (!wait_bar(sb, &sb.kv_full[kv.i], kv.ph, a.status)) return false;
-                    if (!wait_bar(sb, &sb.s_empty[sbuf], empty_par(qq >> 1), a.status)) return false;
-                    tc_fence_after();
-                    const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    const uint32_t d = tmem + C::COL_S + sbuf * 128;
-                    const uint32_t id = (ns * S == 128) ? id_s128 : id_s64;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(d, desc_kmajor_sw128(qaddr + 32 * ks),
-                                 desc_kmajor_sw128(kaddr + 32 * ks), id, ks > 0);
-                    mma_commit(&sb.s_full[sbuf]);
-                    stg_of[g & 1] = kv.i;
-                    kv.next(C::STAGES);
-                    issued = true;
-                    return true;
-                };
-                bool ok = issue_s(0);
-                for (int g = 0; ok && g < G; ++g) {
-                    if (g + 1 < G && !issue_s(g + 1)) { ok = false; break; }
+                bool ok = true;
+                for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
                     const int qq = q + g, pbuf = qq & 1;
                     if (!wait_bar(sb, &sb.p_full[pbuf], full_par(qq >> 1), a.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * C::P_BYTES);
-                    const uint32_t vaddr =
-                        smem_u32(sm + C::OFF_KV + stg_of[g & 1] * C::STAGE_BYTES + C::NG * 128);
-                    const int ksteps = ns * S / 16;
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        mma_bf16(d_o, desc_kmajor_sw128(paddr + (ks >> 2) * C::P_BLOCK + (ks & 3) * 32),
-                                 desc_mnmajor_sw128(vaddr + ks * 2048), id_o, (g > 0 || ks > 0));
-                    mma_commit(&sb.kv_empty[stg_of[g & 1]]);
+                    const uint32_t vaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES + C::NG * 128);
+                    if (ns * S == 128)
+                        tcx::mma_kmajor_mnmajor<8>(d_o, paddr, C::P_BLOCK, vaddr, id_o, g > 0);
+                    else
+                        tcx::mma_kmajor_mnmajor<4>(d_o, paddr, C::P_BLOCK, vaddr, id_o, g > 0);
+                    // S_g is complete (its P exists), so the whole stage may be reused
+                    mma_commit(&sb.kv_empty[kv.i]);
                     mma_commit(&sb.p_empty[pbuf]);
+                    issued = true;
+                    kv.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.o_full[ob]);
-                mma_commit(&sb.q_empty[qr.i]);
-                qr.next(2);
                 q += G;
                 ++e;
             }
             if (issued) {
-                // every MMA must have finished before TMEM is released
-                mma_commit(&sb.done);
-                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+                mma_commit(&sb.done2);
+                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
             }
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int wg = (warp - 2) >> 2;                 // warpgroup 0 or 1
+        const int wg = (warp - 3) >> 2;                 // warpgroup 0 or 1
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
         const int u = (S == 64) ? (lane >> 4) : 0;
