@@ -19,12 +19,16 @@
 //     index of (query chunk, slot) entries that retrieved the chunk, gathers
 //     their Q/dO tiles and delta/lse rows, recomputes S^T = K Q^T and
 //     G^T = V dO^T, and accumulates dK += dA^T Q and dV += (w P)^T dO in TMEM.
-// Warp roles: warp 0 producer (decodes the item metadata into shared memory,
-// issues the TMA / bulk copies); warp 1 issues the score products (S and G,
-// or S^T and G^T) and owns TMEM; warp 2 issues the accumulation products
-// (dQ, or dK and dV), so neither kind of product waits behind the other's
-// issue; warps 3-10 are two math warpgroups taking alternate groups and
-// alternate item epilogues.
+// A group is one retrieved chunk of an item (pass A: one slot; pass B: one
+// entry).  Warp roles: warp 0 producer (the whole warp fetches the item
+// metadata -- slot rows, inverse-index entries -- 32 at a time into shared
+// memory; lane 0 issues the TMA / bulk copies; pass A's item lse block rides
+// on the info barrier as a TMA transaction); warp 1 issues the score products
+// (S and G, or S^T and G^T) into a ring of TMEM buffers (S = 64: three in
+// pass A, two in pass B) and owns TMEM; warp 2 issues the accumulation
+// products (dQ, or dK and dV), so neither kind of product waits behind the
+// other's issue; warps 3-10 are two math warpgroups taking alternate groups
+// and alternate item epilogues.
 #include <math.h>
 
 #include "common.cuh"
@@ -64,6 +68,7 @@ struct BwdArgs {
     float scale_log2;          // attn_scale * log2(e)
     float attn_scale;
     int n_items;
+    int lse_smem;              // pass A: lse blocks staged by TMA (else read per slot)
 };
 
 __device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
@@ -169,27 +174,41 @@ struct ItemInfoA {
 template <int S>
 struct CfgA {
     static constexpr int M = S;
-    static constexpr int GS = 128 / S;
-    static constexpr int NG = 128;
-    static constexpr int STAGES = (S == 64) ? 4 : 2;
+    static constexpr int NG = S;                           // keys per group
+    static constexpr int NSB = (S == 64) ? 3 : 1;          // S/G TMEM buffers
+    static constexpr int STAGES = (S == 64) ? 8 : 2;
     static constexpr int TILE = S * 128;
     static constexpr int ITEM_BYTES = 2 * TILE;            // Q then dO
-    static constexpr int STAGE_BYTES = 2 * NG * 128;       // K half then V half
+    static constexpr int STAGE_BYTES = 2 * TILE;           // K then V of one slot
     static constexpr int P_BLOCK = M * 128;
     static constexpr int P_BYTES = M * NG * 2;
     static constexpr int OFF_IT = 0;
     static constexpr int OFF_KV = 2 * ITEM_BYTES;
     static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
-    static constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;
+    // per info-ring entry: the item's lse block, S rows of topk floats
+    static constexpr int LSE_TOPK_MAX = (S == 64) ? 16 : 8;
+    static constexpr int LSE_BYTES = S * LSE_TOPK_MAX * 4;
+    static constexpr int OFF_LSE = OFF_P + 2 * P_BYTES;
+    static constexpr int SMEM = OFF_LSE + kInfo * LSE_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0, COL_G = 128, COL_DQ = 256;
+    static constexpr uint32_t SGW = 2 * S;                 // columns of one S/G buffer
+    static constexpr uint32_t COL_DQ = NSB * SGW;          // two dQ accumulators of 64 columns
+    // S/G-full barrier of group qq and the parity of its phase.  With one
+    // buffer the two warpgroups alternate on it, so each has its own barrier
+    // (kg = the warpgroup's group count).  With several buffers the issuer may
+    // run two groups of one warpgroup ahead, so the barrier is per buffer: its
+    // next commit needs the buffer's s_empty, i.e. the previous consumer saw it.
+    __device__ static int sfull_index(int qq) { return NSB == 1 ? (qq & 1) : qq % NSB; }
+    __device__ static uint32_t sfull_par(int qq, int kg) {
+        return static_cast<uint32_t>(NSB == 1 ? kg : qq / NSB) & 1u;
+    }
 };
 
 struct __align__(8) BarsA {
     uint64_t info_full[kInfo], info_empty[kInfo];
     uint64_t it_full[2], it_empty[2];
-    uint64_t kv_full[4], kv_empty[4];
-    uint64_t s_full[2], s_empty;       // s_full per math warpgroup, s_empty shared
+    uint64_t kv_full[8], kv_empty[8];
+    uint64_t s_full[3], s_empty[3];    // per S/G buffer (per warpgroup when one buffer)
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
     uint64_t done, done2;
@@ -202,7 +221,7 @@ template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
 gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tl, const BwdArgs a) {
     using C = CfgA<S>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -228,9 +247,8 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             mbar_init(&sb.kv_full[i], 1);
             mbar_init(&sb.kv_empty[i], 1);
         }
-        mbar_init(&sb.s_full[0], 1);
-        mbar_init(&sb.s_full[1], 1);
-        mbar_init(&sb.s_empty, 128);
+        for (int i = 0; i < 3; ++i) mbar_init(&sb.s_full[i], 1);
+        for (int i = 0; i < C::NSB; ++i) mbar_init(&sb.s_empty[i], 128);
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
         sb.abort = 0;
@@ -241,6 +259,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         prefetch_tmap(&tdo);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+        if (a.lse_smem) prefetch_tmap(&tl);
     }
     if (warp == 1) {
         tmem_alloc(&sb.tmem, C::TMEM_COLS);
@@ -252,56 +271,93 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     const uint32_t tmem = sb.tmem;
 
     if (warp == 0) {
-        if (lane == 0) {
-            Ring kv{0, 0}, it{0, 0}, inf{0, 0};
-            bool kv_out[4] = {false, false, false, false}, it_out[2] = {false, false};
-            uint32_t kv_ph[4] = {0, 0, 0, 0}, it_ph[2] = {0, 0};
-            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-                const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
-                if (!wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
-                ItemInfoA& I = sb.info[inf.i];
-                const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
-                const float* wrow = a.w + ((size_t)b * a.nQ + c) * a.topk;
-                int n = 0;
-                for (int j = 0; j < a.topk; ++j) {
-                    const int kap = row[j];
-                    const bool ok = kap >= 0 && kap < a.nP;
-                    I.code[j] = ok ? 0 : 1;
-                    if (ok) { I.js[n] = j; I.kaps[n] = kap; I.w[n] = wrow[j]; ++n; }
+        // The whole warp reads an item's retrieval row (one slot per lane) and
+        // compacts its valid slots with a ballot; lane 0 alone waits on
+        // barriers and issues the copies.  The item's lse block [S x topk]
+        // rides on the info barrier as a TMA transaction.
+        constexpr unsigned kAll = 0xffffffffu;
+        Ring kv{0, 0}, it{0, 0}, inf{0, 0};
+        bool kv_out[C::STAGES] = {}, it_out[2] = {false, false}, inf_out[kInfo] = {};
+        uint32_t kv_ph[C::STAGES] = {}, it_ph[2] = {0, 0}, inf_ph[kInfo] = {};
+        auto lane0_wait = [&](uint64_t* bar, uint32_t par) {
+            int r = 0;
+            if (lane == 0) r = wait(bar, par) ? 1 : 0;
+            return __shfl_sync(kAll, r, 0) != 0;
+        };
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+            const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
+            const int32_t* row = a.idx + ((size_t)b * a.nQ + c) * a.topk;
+            const float* wrow = a.w + ((size_t)b * a.nQ + c) * a.topk;
+            int kap0 = -1, kap1 = -1;
+            float w0 = 0.f, w1 = 0.f;
+            if (lane < a.topk) { kap0 = row[lane]; w0 = wrow[lane]; }
+            if (32 + lane < a.topk) { kap1 = row[32 + lane]; w1 = wrow[32 + lane]; }
+            if (!lane0_wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
+            ItemInfoA& I = sb.info[inf.i];
+            int n = 0;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int j = 32 * half + lane;
+                const int kap = half ? kap1 : kap0;
+                const bool okj = j < a.topk && kap >= 0 && kap < a.nP;
+                if (j < a.topk) I.code[j] = okj ? 0 : 1;
+                const unsigned m = __ballot_sync(kAll, okj);
+                if (okj) {
+                    const int pos = n + __popc(m & ((1u << lane) - 1u));
+                    I.js[pos] = j;
+                    I.kaps[pos] = kap;
+                    I.w[pos] = half ? w1 : w0;
                 }
+                n += __popc(m);
+            }
+            __syncwarp();
+            if (lane == 0) {
                 I.b = b; I.c = c; I.h = h; I.n = n;
-                mbar_arrive(&sb.info_full[inf.i]);
-                inf.next(kInfo);
-                if (n == 0) continue;
-                if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+                if (a.lse_smem) {
+                    mbar_arrive_expect_tx(&sb.info_full[inf.i], S * a.topk * 4);
+                    tma_load_2d(sm + C::OFF_LSE + inf.i * C::LSE_BYTES, &tl, &sb.info_full[inf.i],
+                                h * a.topk, b * a.Lq + c * S);
+                    inf_out[inf.i] = true;
+                    inf_ph[inf.i] = inf.ph;
+                } else {
+                    mbar_arrive(&sb.info_full[inf.i]);
+                }
+            }
+            inf.next(kInfo);
+            if (n == 0) continue;
+            if (!lane0_wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+            if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
                 mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
                 tma_load_2d(ib, &tq, &sb.it_full[it.i], h * 64, b * a.Lq + c * S);
                 tma_load_2d(ib + C::TILE, &tdo, &sb.it_full[it.i], h * 64, b * a.Lq + c * S);
-                it_out[it.i] = true;
-                it_ph[it.i] = it.ph;
-                it.next(2);
-                bool ok = true;
-                for (int g = 0; g * C::GS < n; ++g) {
-                    const int ns = min(C::GS, n - g * C::GS);
-                    if (!wait(&sb.kv_empty[kv.i], kv.ph ^ 1u)) { ok = false; break; }
-                    uint8_t* stg = sm + C::OFF_KV + kv.i * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&sb.kv_full[kv.i], ns * 2 * C::TILE);
-                    for (int u = 0; u < ns; ++u) {
-                        const int y = (b * a.nP + I.kaps[g * C::GS + u]) * S;
-                        tma_load_2d(stg + u * C::TILE, &tk, &sb.kv_full[kv.i], h * 64, y);
-                        tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tv, &sb.kv_full[kv.i], h * 64, y);
-                    }
-                    kv_out[kv.i] = true;
-                    kv_ph[kv.i] = kv.ph;
-                    kv.next(C::STAGES);
-                }
-                if (!ok) break;
             }
+            it_out[it.i] = true;
+            it_ph[it.i] = it.ph;
+            it.next(2);
+            bool ok = true;
+            for (int g = 0; g < n; ++g) {
+                if (!lane0_wait(&sb.kv_empty[kv.i], kv.ph ^ 1u)) { ok = false; break; }
+                if (lane == 0) {
+                    uint8_t* stg = sm + C::OFF_KV + kv.i * C::STAGE_BYTES;
+                    const int y = (b * a.nP + I.kaps[g]) * S;
+                    mbar_arrive_expect_tx(&sb.kv_full[kv.i], 2 * C::TILE);
+                    tma_load_2d(stg, &tk, &sb.kv_full[kv.i], h * 64, y);
+                    tma_load_2d(stg + C::TILE, &tv, &sb.kv_full[kv.i], h * 64, y);
+                }
+                kv_out[kv.i] = true;
+                kv_ph[kv.i] = kv.ph;
+                kv.next(C::STAGES);
+            }
+            if (!ok) break;
+        }
+        if (lane == 0) {
             for (int i = 0; i < C::STAGES; ++i)
                 if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
             for (int i = 0; i < 2; ++i)
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < kInfo; ++i)
+                if (inf_out[i]) mbar_wait(&sb.info_full[i], inf_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
         // S / G products: S = Q K^T and G = dO V^T of each group
@@ -309,38 +365,36 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             Ring kv{0, 0}, it{0, 0}, inf{0, 0};
             int q = 0;
             bool issued = false;
-            const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
-            const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
+            const uint32_t id_s = idesc_bf16(C::M, S, false, false);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int n = sb.info[inf.i].n;
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
                 if (n == 0) continue;
-                const int G = (n + C::GS - 1) / C::GS;
                 if (!wait(&sb.it_full[it.i], it.ph)) break;
                 tc_fence_after();
                 const uint32_t qaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t doaddr = qaddr + C::TILE;
                 bool ok = true;
-                for (int g = 0; g < G; ++g) {
-                    const int ns = min(C::GS, n - g * C::GS);
+                for (int g = 0; g < n; ++g) {
                     const int qq = q + g;
-                    if (!wait(&sb.kv_full[kv.i], kv.ph) || !wait(&sb.s_empty, empty_par(qq))) { ok = false; break; }
+                    const int sbuf = qq % C::NSB;
+                    if (!wait(&sb.kv_full[kv.i], kv.ph) ||
+                        !wait(&sb.s_empty[sbuf], empty_par(qq / C::NSB))) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    const uint32_t vaddr = kaddr + C::NG * 128;
-                    const uint32_t id = (ns * S == 128) ? id_n128 : id_n64;
-                    tcx::mma_kmajor_k64(tmem + C::COL_S, qaddr, kaddr, id, 0);
-                    tcx::mma_kmajor_k64(tmem + C::COL_G, doaddr, vaddr, id, 0);
-                    mma_commit(&sb.s_full[qq & 1]);
+                    const uint32_t vaddr = kaddr + C::TILE;
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, qaddr, kaddr, id_s, 0);
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + S, doaddr, vaddr, id_s, 0);
+                    mma_commit(&sb.s_full[C::sfull_index(qq)]);
                     issued = true;
                     kv.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.it_empty[it.i]);     // Q and dO are read only by these products
                 it.next(2);
-                q += G;
+                q += n;
             }
             if (issued) {
                 mma_commit(&sb.done);
@@ -360,23 +414,18 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
                 if (n == 0) continue;
-                const int G = (n + C::GS - 1) / C::GS;
                 const int ob = e & 1;
                 if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
                 const uint32_t d_dq = tmem + C::COL_DQ + ob * 64;
                 bool ok = true;
-                for (int g = 0; g < G; ++g) {
-                    const int ns = min(C::GS, n - g * C::GS);
+                for (int g = 0; g < n; ++g) {
                     const int qq = q + g, pb = qq & 1;
                     if (!wait(&sb.p_full[pb], full_par(qq >> 1))) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    if (ns * S == 128)
-                        tcx::mma_kmajor_mnmajor<8>(d_dq, paddr, C::P_BLOCK, kaddr, id_dq, g > 0);
-                    else
-                        tcx::mma_kmajor_mnmajor<4>(d_dq, paddr, C::P_BLOCK, kaddr, id_dq, g > 0);
+                    tcx::mma_kmajor_mnmajor<S / 16>(d_dq, paddr, C::P_BLOCK, kaddr, id_dq, g > 0);
                     // the S / G products of this group are complete (their P exists)
                     mma_commit(&sb.kv_empty[kv.i]);
                     mma_commit(&sb.p_empty[pb]);
@@ -385,7 +434,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 }
                 if (!ok) break;
                 mma_commit(&sb.o_full[ob]);
-                q += G;
+                q += n;
                 ++e;
             }
             if (issued) {
@@ -419,98 +468,133 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 if (my_epi) zero_row64<S>(dqrow, u);
                 continue;
             }
-            const int G = (n + C::GS - 1) / C::GS;
+            const float* lse_s = reinterpret_cast<const float*>(sm + C::OFF_LSE + inf.i * C::LSE_BYTES);
             bool ok = true;
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < n; ++g) {
                 const int qq = q + g;
                 if ((qq & 1) != wg) continue;
-                const int ns = min(C::GS, n - g * C::GS);
-                const bool active = u < ns;
-                const int j = active ? I.js[g * C::GS + u] : 0;
-                const float L2 = active ? __ldg(a.lse + (tok * a.H + h) * a.topk + j) * kLog2e : 0.f;
-                const float wsc = active ? I.w[g * C::GS + u] * a.attn_scale : 0.f;
-                if (!wait(&sb.s_full[wg], full_par(kg))) { ok = false; break; }
+                const int j = I.js[g];
+                const float L2 = (a.lse_smem ? lse_s[row * a.topk + j]
+                                             : __ldg(a.lse + (tok * a.H + h) * a.topk + j)) * kLog2e;
+                const float wsc = I.w[g] * a.attn_scale;
+                const int sbuf = qq % C::NSB;
+                if (!wait(&sb.s_full[C::sfull_index(qq)], C::sfull_par(qq, kg))) { ok = false; break; }
                 tc_fence_after();
-                constexpr int NCH = (S == 64) ? 1 : 2;      // 64-key chunks per row
-                const uint32_t ts0 = tmem + lane_base + C::COL_S;
-                const uint32_t tg0 = tmem + lane_base + C::COL_G;
-                float x[64];
+                const uint32_t ts0 = tmem + lane_base + sbuf * C::SGW;
+                const uint32_t tg0 = ts0 + S;
+                uint8_t* pb = sm + C::OFF_P + wg * C::P_BYTES;
                 float dl = 0.f;
-                // sweep 1: p (kept for the last chunk) and delta = sum_s p G
-                for (int ch = 0; ch < NCH; ++ch) {
-                    load_cols64<S>(ts0 + ch * 64, x);
+                // the row's delta and lse*log2(e) for the key-major pass, and this
+                // warp's partial of dw (for S = 64 both halves of the warp hold the
+                // same rows' delta: reduce within one); for S = 64 issued before
+                // the P buffer wait so the stores overlap it
+                auto emit_rows = [&](float dlv) {
+                    if (u == 0) {
+                        const size_t rr = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S + row;
+                        a.delta_rows[rr] = dlv;
+                        a.lse2_rows[rr] = L2;
+                    }
+                    float part = dlv;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
+                    for (int o2 = (S == 64 ? 8 : 16); o2 > 0; o2 >>= 1)
+                        part += __shfl_xor_sync(0xffffffffu, part, o2);
+                    if (lane == 0) dwp[qd * a.topk + j] = part;
+                };
+                if constexpr (S == 64) {
+                    // this thread: one token row, keys u*32 .. u*32+31 of the slot
+                    uint32_t r0[16], r1[16], r2[16], r3[16];
+                    tmem_ld_16x32bx2_x16<32>(ts0, r0);
+                    tmem_ld_16x32bx2_x16<32>(ts0 + 16, r1);
+                    tmem_ld_16x32bx2_x16<32>(tg0, r2);
+                    tmem_ld_16x32bx2_x16<32>(tg0 + 16, r3);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&sb.s_empty[sbuf]);
+                    float pr[32], gv[32];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        pr[t] = fast_exp2(fmaf(__uint_as_float(r0[t]), a.scale_log2, -L2));
+                        pr[16 + t] = fast_exp2(fmaf(__uint_as_float(r1[t]), a.scale_log2, -L2));
+                        gv[t] = __uint_as_float(r2[t]);
+                        gv[16 + t] = __uint_as_float(r3[t]);
+                    }
                     float d8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) d8[i] = 0.f;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t g0[16], g1[16];
-                        issue_cols16<S>(tg0 + ch * 64 + 32 * half, g0);
-                        issue_cols16<S>(tg0 + ch * 64 + 32 * half + 16, g1);
-                        tmem_wait_ld();
+                    for (int i = 0; i < 32; ++i) d8[i & 7] = fmaf(pr[i], gv[i], d8[i & 7]);
+                    dl = ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
+                    dl += __shfl_xor_sync(0xffffffffu, dl, 16);     // the row's other 32 keys
+                    emit_rows(dl);
+                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            d8[t & 7] = fmaf(x[32 * half + t], __uint_as_float(g0[t]), d8[t & 7]);
-                            d8[t & 7] = fmaf(x[32 * half + 16 + t], __uint_as_float(g1[t]), d8[t & 7]);
-                        }
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        float v8[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) v8[t] = pr[8 * c4 + t] * (gv[8 * c4 + t] - dl);
+                        *reinterpret_cast<uint4*>(pb + sw128_off(row, 4 * u + c4)) = pack8(v8, wsc);
                     }
-                    dl += ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
-                }
-                if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
-                uint8_t* pb = sm + C::OFF_P + wg * C::P_BYTES;
-                // sweep 2: dA = w s p (G - delta) into the A operand of dQ += dA K
-                for (int ch = 0; ch < NCH; ++ch) {
-                    if (NCH == 2) {
+                } else {
+                    // this thread: one token row, all 128 keys in two 64-key chunks
+                    float x[64];
+                    for (int ch = 0; ch < 2; ++ch) {
                         load_cols64<S>(ts0 + ch * 64, x);
 #pragma unroll
                         for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
+                        float d8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) d8[i] = 0.f;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t g0[16], g1[16];
+                            issue_cols16<S>(tg0 + ch * 64 + 32 * half, g0);
+                            issue_cols16<S>(tg0 + ch * 64 + 32 * half + 16, g1);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) {
+                                d8[t & 7] = fmaf(x[32 * half + t], __uint_as_float(g0[t]), d8[t & 7]);
+                                d8[t & 7] = fmaf(x[32 * half + 16 + t], __uint_as_float(g1[t]), d8[t & 7]);
+                            }
+                        }
+                        dl += ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
                     }
+                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                    for (int ch = 0; ch < 2; ++ch) {
+                        load_cols64<S>(ts0 + ch * 64, x);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t g0[16], g1[16];
-                        issue_cols16<S>(tg0 + ch * 64 + 32 * half, g0);
-                        issue_cols16<S>(tg0 + ch * 64 + 32 * half + 16, g1);
-                        tmem_wait_ld();
-                        if (ch == NCH - 1 && half == 1) {
-                            tc_fence_before();
-                            mbar_arrive(&sb.s_empty);
-                        }
-                        float g[32];
+                        for (int i = 0; i < 64; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -L2));
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            g[t] = x[32 * half + t] * (__uint_as_float(g0[t]) - dl);
-                            g[16 + t] = x[32 * half + 16 + t] * (__uint_as_float(g1[t]) - dl);
-                        }
-                        if (active) {
-                            const int blk = (S == 64) ? u : ch;
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t g0[16], g1[16];
+                            issue_cols16<S>(tg0 + ch * 64 + 32 * half, g0);
+                            issue_cols16<S>(tg0 + ch * 64 + 32 * half + 16, g1);
+                            tmem_wait_ld();
+                            if (ch == 1 && half == 1) {
+                                tc_fence_before();
+                                mbar_arrive(&sb.s_empty[sbuf]);
+                            }
+                            float gg[32];
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) {
+                                gg[t] = x[32 * half + t] * (__uint_as_float(g0[t]) - dl);
+                                gg[16 + t] = x[32 * half + 16 + t] * (__uint_as_float(g1[t]) - dl);
+                            }
 #pragma unroll
                             for (int c4 = 0; c4 < 4; ++c4)
-                                *reinterpret_cast<uint4*>(pb + blk * C::P_BLOCK + sw128_off(row, 4 * half + c4)) =
-                                    pack8(g + 8 * c4, wsc);
+                                *reinterpret_cast<uint4*>(pb + ch * C::P_BLOCK + sw128_off(row, 4 * half + c4)) =
+                                    pack8(gg + 8 * c4, wsc);
                         }
                     }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&sb.p_full[wg]);
                 ++kg;
-                if (active) {
-                    const size_t rr = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S + row;
-                    a.delta_rows[rr] = dl;
-                    a.lse2_rows[rr] = L2;
-                }
-                // per-quadrant partial of dw over this warp's rows
-                float part = active ? dl : 0.f;
-#pragma unroll
-                for (int o2 = (S == 64 ? 8 : 16); o2 > 0; o2 >>= 1)
-                    part += __shfl_xor_sync(0xffffffffu, part, o2);
-                if (active && (lane & (S == 64 ? 15 : 31)) == 0) dwp[qd * a.topk + j] = part;
+                if constexpr (S != 64) emit_rows(dl);     // (S = 64 emitted them before the P wait)
             }
             mbar_arrive(&sb.info_empty[inf.i]);
             inf.next(kInfo);
             if (!ok) break;
-            q += G;
+            q += n;
             const bool mine = (e & 1) == wg;
             ++e;
             if (!mine) continue;
@@ -545,13 +629,13 @@ struct EntryInfo {
 template <int S>
 struct CfgB {
     static constexpr int M = S;                           // keys of the item
-    static constexpr int GS = 128 / S;                    // entries per group
-    static constexpr int NG = 128;                        // tokens per full group
+    static constexpr int NG = S;                          // tokens per group
     static constexpr int NWG = (S == 64) ? 2 : 1;         // math warpgroups in use
-    static constexpr int STAGES = (S == 64) ? 3 : 2;
+    static constexpr int NSB = (S == 64) ? 2 : 1;         // S^T/G^T TMEM buffers
+    static constexpr int STAGES = (S == 64) ? 6 : 2;
     static constexpr int TILE = S * 128;
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
-    static constexpr int VEC_OFF = 2 * NG * 128;          // after the Q and dO tiles
+    static constexpr int VEC_OFF = 2 * TILE;              // after the Q and dO tiles
     static constexpr int ENT_OFF = VEC_OFF + 1024;        // lse2/delta rows, then entry info
     static constexpr int STAGE_BYTES = VEC_OFF + 2048;
     static constexpr int P_BLOCK = M * 128;
@@ -561,14 +645,15 @@ struct CfgB {
     static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
     static constexpr int SMEM = OFF_P + NWG * 2 * P_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0, COL_G = 128, COL_ACC = 256;   // dK, dV: 2 x (64 + 64)
+    static constexpr uint32_t SGW = 2 * S;                // columns of one S^T/G^T buffer
+    static constexpr uint32_t COL_ACC = NSB * SGW;        // dK, dV: 2 x (64 + 64)
 };
 
 struct __align__(8) BarsB {
     uint64_t info_full[kInfo], info_empty[kInfo];
     uint64_t it_full[2], it_empty[2];
-    uint64_t st_full[3], st_empty[3];
-    uint64_t s_full[2], s_empty;       // s_full per math warpgroup, s_empty shared
+    uint64_t st_full[6], st_empty[6];
+    uint64_t s_full[2], s_empty[2];    // s_full per math warpgroup, s_empty per S/G buffer
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
     uint64_t done, done2;
@@ -610,7 +695,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         }
         mbar_init(&sb.s_full[0], 1);
         mbar_init(&sb.s_full[1], 1);
-        mbar_init(&sb.s_empty, 128);
+        for (int i = 0; i < C::NSB; ++i) mbar_init(&sb.s_empty[i], 128);
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
         sb.abort = 0;
@@ -632,62 +717,90 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     const uint32_t tmem = sb.tmem;
 
     if (warp == 0) {
-        if (lane == 0) {
-            Ring st{0, 0}, it{0, 0}, inf{0, 0};
-            bool st_out[3] = {false, false, false}, it_out[2] = {false, false};
-            uint32_t st_ph[3] = {0, 0, 0}, it_ph[2] = {0, 0};
-            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
-                const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
-                const int e0 = a.offset[(size_t)b * (a.nP + 1) + kap];
-                const int ne = a.offset[(size_t)b * (a.nP + 1) + kap + 1] - e0;
-                if (!wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
+        // The whole warp walks the items; lane 0 alone waits on barriers and
+        // issues the copies.  The other lanes fetch the item offsets and the
+        // entry records (query chunk, slot, weight) 32 at a time, so those
+        // dependent global loads are paid once per 32 instead of once each.
+        constexpr unsigned kAll = 0xffffffffu;
+        Ring st{0, 0}, it{0, 0}, inf{0, 0};
+        bool st_out[C::STAGES] = {}, it_out[2] = {false, false};
+        uint32_t st_ph[C::STAGES] = {}, it_ph[2] = {0, 0};
+        auto lane0_wait = [&](uint64_t* bar, uint32_t par) {
+            int r = 0;
+            if (lane == 0) r = wait(bar, par) ? 1 : 0;
+            return __shfl_sync(kAll, r, 0) != 0;
+        };
+        int my_e0 = 0, my_ne = 0;
+        int n_item = 0;
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_item) {
+            if ((n_item & 31) == 0) {
+                const int it_l = item + lane * gridDim.x;
+                my_e0 = my_ne = 0;
+                if (it_l < a.n_items) {
+                    const int bk_l = it_l / a.H, kap_l = bk_l % a.nP, b_l = bk_l / a.nP;
+                    const int* off = a.offset + (size_t)b_l * (a.nP + 1) + kap_l;
+                    my_e0 = off[0];
+                    my_ne = off[1] - my_e0;
+                }
+            }
+            const int e0 = __shfl_sync(kAll, my_e0, n_item & 31);
+            const int ne = __shfl_sync(kAll, my_ne, n_item & 31);
+            const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
+            if (!lane0_wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
+            if (lane == 0) {
                 ItemInfoB& I = sb.info[inf.i];
                 I.b = b; I.kap = kap; I.h = h; I.ne = ne;
                 mbar_arrive(&sb.info_full[inf.i]);
-                inf.next(kInfo);
-                if (ne <= 0) continue;
-                const int* ent = a.entry + (size_t)b * nE + e0;
-                if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+            }
+            inf.next(kInfo);
+            if (ne <= 0) continue;
+            const int* ent = a.entry + (size_t)b * nE + e0;
+            if (!lane0_wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+            if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
                 mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
                 tma_load_2d(ib, &tk, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
                 tma_load_2d(ib + C::TILE, &tv, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
-                it_out[it.i] = true;
-                it_ph[it.i] = it.ph;
-                it.next(2);
-                bool ok = true;
-                for (int g = 0; g * C::GS < ne; ++g) {
-                    const int ns = min(C::GS, ne - g * C::GS);
-                    int cs[C::GS], jj[C::GS];
-                    float ww[C::GS];
-                    for (int u = 0; u < ns; ++u) {
-                        const int e = ent[g * C::GS + u];
-                        cs[u] = e / a.topk;
-                        jj[u] = e % a.topk;
-                        ww[u] = a.w[((size_t)b * a.nQ + cs[u]) * a.topk + jj[u]];
-                    }
-                    if (!wait(&sb.st_empty[st.i], st.ph ^ 1u)) { ok = false; break; }
-                    uint8_t* stg = sm + C::OFF_ST + st.i * C::STAGE_BYTES;
-                    EntryInfo* ei = reinterpret_cast<EntryInfo*>(stg + C::ENT_OFF);
-                    for (int u = 0; u < ns; ++u) { ei[u].c = cs[u]; ei[u].j = jj[u]; ei[u].w = ww[u]; }
-                    mbar_arrive_expect_tx(&sb.st_full[st.i], ns * (2 * C::TILE + 2 * S * 4));
-                    for (int u = 0; u < ns; ++u) {
-                        const int c = cs[u], j = jj[u];
-                        tma_load_2d(stg + u * C::TILE, &tq, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
-                        tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tdo, &sb.st_full[st.i], h * 64,
-                                    b * a.Lq + c * S);
+            }
+            it_out[it.i] = true;
+            it_ph[it.i] = it.ph;
+            it.next(2);
+            bool ok = true;
+            for (int base = 0; base < ne && ok; base += 32) {
+                int my_c = 0, my_j = 0;
+                float my_w = 0.f;
+                if (base + lane < ne) {
+                    const int e = ent[base + lane];
+                    my_c = e / a.topk;
+                    my_j = e % a.topk;
+                    my_w = a.w[((size_t)b * a.nQ + my_c) * a.topk + my_j];
+                }
+                const int cnt = min(32, ne - base);
+                for (int u = 0; u < cnt; ++u) {
+                    const int c = __shfl_sync(kAll, my_c, u);
+                    const int j = __shfl_sync(kAll, my_j, u);
+                    const float wv = __shfl_sync(kAll, my_w, u);
+                    if (!lane0_wait(&sb.st_empty[st.i], st.ph ^ 1u)) { ok = false; break; }
+                    if (lane == 0) {
+                        uint8_t* stg = sm + C::OFF_ST + st.i * C::STAGE_BYTES;
+                        EntryInfo* ei = reinterpret_cast<EntryInfo*>(stg + C::ENT_OFF);
+                        ei->c = c; ei->j = j; ei->w = wv;
+                        mbar_arrive_expect_tx(&sb.st_full[st.i], 2 * C::TILE + 2 * S * 4);
+                        tma_load_2d(stg, &tq, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
+                        tma_load_2d(stg + C::TILE, &tdo, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
                         const size_t rb = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S;
-                        tcx::bulk_load(stg + C::VEC_OFF + u * 2 * S * 4, a.lse2_rows + rb, S * 4,
+                        tcx::bulk_load(stg + C::VEC_OFF, a.lse2_rows + rb, S * 4, &sb.st_full[st.i]);
+                        tcx::bulk_load(stg + C::VEC_OFF + S * 4, a.delta_rows + rb, S * 4,
                                        &sb.st_full[st.i]);
-                        tcx::bulk_load(stg + C::VEC_OFF + u * 2 * S * 4 + S * 4, a.delta_rows + rb,
-                                       S * 4, &sb.st_full[st.i]);
                     }
                     st_out[st.i] = true;
                     st_ph[st.i] = st.ph;
                     st.next(C::STAGES);
                 }
-                if (!ok) break;
             }
+            if (!ok) break;
+        }
+        if (lane == 0) {
             for (int i = 0; i < C::STAGES; ++i)
                 if (st_out[i]) mbar_wait(&sb.st_full[i], st_ph[i], nullptr, 100000000ull);
             for (int i = 0; i < 2; ++i)
@@ -699,30 +812,28 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             Ring st{0, 0}, it{0, 0}, inf{0, 0};
             int q = 0;
             bool issued = false;
-            const uint32_t id_n128 = idesc_bf16(C::M, 128, false, false);
-            const uint32_t id_n64 = idesc_bf16(C::M, 64, false, false);
+            const uint32_t id_s = idesc_bf16(C::M, S, false, false);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
                 if (ne <= 0) continue;
-                const int G = (ne + C::GS - 1) / C::GS;
                 if (!wait(&sb.it_full[it.i], it.ph)) break;
                 tc_fence_after();
                 const uint32_t kaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t vaddr = kaddr + C::TILE;
                 bool ok = true;
-                for (int g = 0; g < G; ++g) {
-                    const int ns = min(C::GS, ne - g * C::GS);
+                for (int g = 0; g < ne; ++g) {
                     const int qq = q + g;
-                    if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_empty, empty_par(qq))) { ok = false; break; }
+                    const int sbuf = qq % C::NSB;
+                    if (!wait(&sb.st_full[st.i], st.ph) ||
+                        !wait(&sb.s_empty[sbuf], empty_par(qq / C::NSB))) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    const uint32_t doaddr = qaddr + C::NG * 128;
-                    const uint32_t id = (ns * S == 128) ? id_n128 : id_n64;
-                    tcx::mma_kmajor_k64(tmem + C::COL_S, kaddr, qaddr, id, 0);
-                    tcx::mma_kmajor_k64(tmem + C::COL_G, vaddr, doaddr, id, 0);
+                    const uint32_t doaddr = qaddr + C::TILE;
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, kaddr, qaddr, id_s, 0);
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + S, vaddr, doaddr, id_s, 0);
                     mma_commit(&sb.s_full[qq % C::NWG]);
                     issued = true;
                     st.next(C::STAGES);
@@ -730,7 +841,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 if (!ok) break;
                 mma_commit(&sb.it_empty[it.i]);     // K and V are read only by these products
                 it.next(2);
-                q += G;
+                q += ne;
             }
             if (issued) {
                 mma_commit(&sb.done);
@@ -750,28 +861,22 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
                 if (ne <= 0) continue;
-                const int G = (ne + C::GS - 1) / C::GS;
                 const int ob = e & 1;
                 if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
                 const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
                 const uint32_t d_dv = d_dk + 64;
                 bool ok = true;
-                for (int g = 0; g < G; ++g) {
-                    const int ns = min(C::GS, ne - g * C::GS);
+                for (int g = 0; g < ne; ++g) {
                     const int qq = q + g, pbuf = qq % C::NWG;
                     if (!wait(&sb.p_full[pbuf], full_par(qq / C::NWG))) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    const uint32_t doaddr = qaddr + C::NG * 128;
-                    if (ns * S == 128) {
-                        tcx::mma_kmajor_mnmajor<8>(d_dk, paddr, C::P_BLOCK, qaddr, id_acc, g > 0);
-                        tcx::mma_kmajor_mnmajor<8>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, id_acc, g > 0);
-                    } else {
-                        tcx::mma_kmajor_mnmajor<4>(d_dk, paddr, C::P_BLOCK, qaddr, id_acc, g > 0);
-                        tcx::mma_kmajor_mnmajor<4>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, id_acc, g > 0);
-                    }
+                    const uint32_t doaddr = qaddr + C::TILE;
+                    tcx::mma_kmajor_mnmajor<S / 16>(d_dk, paddr, C::P_BLOCK, qaddr, id_acc, g > 0);
+                    tcx::mma_kmajor_mnmajor<S / 16>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, id_acc,
+                                                    g > 0);
                     // the S^T / G^T products of this group are complete (their P exists)
                     mma_commit(&sb.st_empty[st.i]);
                     mma_commit(&sb.p_empty[pbuf]);
@@ -780,7 +885,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 }
                 if (!ok) break;
                 mma_commit(&sb.o_full[ob]);
-                q += G;
+                q += ne;
                 ++e;
             }
             if (issued) {
@@ -811,60 +916,97 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 }
                 continue;
             }
-            const int G = (I.ne + C::GS - 1) / C::GS;
             bool ok = true;
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < I.ne; ++g) {
                 const int qq = q + g;
                 const int stage = st.i;
                 const uint32_t stph = st.ph;
                 st.next(C::STAGES);
                 if ((qq % C::NWG) != wg) continue;
-                const int ns = min(C::GS, I.ne - g * C::GS);
-                const bool active = u < ns;
+                const int sbuf = qq % C::NSB;
                 // our own s_full first: its completion implies this group's stage copy
                 // has landed, so the stage barrier's phase below is unambiguous
                 if (!wait(&sb.s_full[wg], full_par(kg)) || !wait(&sb.st_full[stage], stph)) { ok = false; break; }
                 tc_fence_after();
                 const uint8_t* stg = sm + C::OFF_ST + stage * C::STAGE_BYTES;
-                const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[active ? u : 0];
-                const float wv = active ? ei.w : 0.f;
+                const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[0];
+                const float wv = ei.w;
                 const float wsc = wv * a.attn_scale;
-                const float* vec = reinterpret_cast<const float*>(stg + C::VEC_OFF + u * 2 * S * 4);
-                if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                const float* vec = reinterpret_cast<const float*>(stg + C::VEC_OFF);   // lse2[S], delta[S]
                 uint8_t* pb = sm + C::OFF_P + wg * 2 * C::P_BYTES;
-                constexpr int NC32 = (S == 64) ? 2 : 4;      // 32-token pieces per row
-                const uint32_t ts0 = tmem + lane_base + C::COL_S;
-                const uint32_t tg0 = tmem + lane_base + C::COL_G;
-                for (int pc = 0; pc < NC32; ++pc) {
+                const uint32_t ts0 = tmem + lane_base + sbuf * C::SGW;
+                const uint32_t tg0 = ts0 + S;
+                if constexpr (S == 64) {
+                    // this thread: one key row, tokens u*32 .. u*32+31 of the entry
+                    uint32_t r0[16], r1[16], r2[16], r3[16];
+                    tmem_ld_16x32bx2_x16<32>(ts0, r0);
+                    tmem_ld_16x32bx2_x16<32>(ts0 + 16, r1);
+                    tmem_ld_16x32bx2_x16<32>(tg0, r2);
+                    tmem_ld_16x32bx2_x16<32>(tg0 + 16, r3);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&sb.s_empty[sbuf]);
                     float xs[32], xg[32];
-                    {
-                        uint32_t r0[16], r1[16], r2[16], r3[16];
-                        issue_cols16<S>(ts0 + 32 * pc, r0);
-                        issue_cols16<S>(ts0 + 32 * pc + 16, r1);
-                        issue_cols16<S>(tg0 + 32 * pc, r2);
-                        issue_cols16<S>(tg0 + 32 * pc + 16, r3);
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            xs[t] = __uint_as_float(r0[t]);
-                            xs[16 + t] = __uint_as_float(r1[t]);
-                            xg[t] = __uint_as_float(r2[t]);
-                            xg[16 + t] = __uint_as_float(r3[t]);
+                    for (int t = 0; t < 16; ++t) {
+                        xs[t] = __uint_as_float(r0[t]);
+                        xs[16 + t] = __uint_as_float(r1[t]);
+                        xg[t] = __uint_as_float(r2[t]);
+                        xg[16 + t] = __uint_as_float(r3[t]);
+                    }
+                    const float4* l4 = reinterpret_cast<const float4*>(vec + 32 * u);
+                    const float4* d4 = reinterpret_cast<const float4*>(vec + S + 32 * u);
+#pragma unroll
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 lv = l4[i4], dv = d4[i4];
+                        const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int i = 4 * i4 + t;
+                            const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -la[t]));
+                            xs[i] = pr * (xg[i] - da[t]);       // dA^T / (w s)
+                            xg[i] = pr;                         // P^T / w
                         }
                     }
-                    if (pc == NC32 - 1) {
-                        tc_fence_before();
-                        mbar_arrive(&sb.s_empty);
+                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t off = sw128_off(row, 4 * u + c4);
+                        *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c4, wsc);
+                        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c4, wv);
                     }
-                    if (active) {
+                } else {
+                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                    // this thread: one key row, all 128 tokens in four 32-token pieces
+                    for (int pc = 0; pc < 4; ++pc) {
+                        float xs[32], xg[32];
+                        {
+                            uint32_t r0[16], r1[16], r2[16], r3[16];
+                            issue_cols16<S>(ts0 + 32 * pc, r0);
+                            issue_cols16<S>(ts0 + 32 * pc + 16, r1);
+                            issue_cols16<S>(tg0 + 32 * pc, r2);
+                            issue_cols16<S>(tg0 + 32 * pc + 16, r3);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) {
+                                xs[t] = __uint_as_float(r0[t]);
+                                xs[16 + t] = __uint_as_float(r1[t]);
+                                xg[t] = __uint_as_float(r2[t]);
+                                xg[16 + t] = __uint_as_float(r3[t]);
+                            }
+                        }
+                        if (pc == 3) {
+                            tc_fence_before();
+                            mbar_arrive(&sb.s_empty[sbuf]);
+                        }
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int t = 32 * pc + i;
                             const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -vec[t]));
-                            xs[i] = pr * (xg[i] - vec[S + t]);      // dA^T / (w s)
-                            xg[i] = pr;                             // P^T / w
+                            xs[i] = pr * (xg[i] - vec[S + t]);
+                            xg[i] = pr;
                         }
-                        const int blk = (S == 64) ? u : (pc >> 1);
+                        const int blk = pc >> 1;
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4) {
                             const uint32_t off = blk * C::P_BLOCK + sw128_off(row, (pc & 1) * 4 + c4);
@@ -878,7 +1020,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 ++kg;
             }
             if (!ok) break;
-            q += G;
+            q += I.ne;
             const bool mine = (e % C::NWG) == wg;
             const int ob = e & 1, ko = e >> 1;
             ++e;
@@ -929,6 +1071,14 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     a.B = sp.B; a.nQ = sp.nQ; a.nP = sp.nP; a.H = sp.H; a.topk = sp.topk; a.Lq = sp.Lq;
     a.scale_log2 = sp.attn_scale * kLog2e;
     a.attn_scale = sp.attn_scale;
+    // pass A stages each item's lse block [S x topk] by TMA when its rows are
+    // 16-byte granular and the block fits the per-item staging area
+    CUtensorMap tl;
+    a.lse_smem = (sp.topk % 4 == 0 && sp.topk <= CfgA<S>::LSE_TOPK_MAX &&
+                  (reinterpret_cast<uintptr_t>(lse) & 15) == 0 &&
+                  encode_f32_box(&tl, lse, (uint64_t)sp.B * sp.Lq, (uint64_t)sp.H * sp.topk,
+                                 (uint32_t)sp.topk, S)) ? 1 : 0;
+    if (!a.lse_smem) tl = tq;     // unused placeholder
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -938,7 +1088,7 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgA<S>::SMEM);
     if (e != cudaSuccess) return e;
     int grid = a.n_items < sms ? a.n_items : sms;
-    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreads, CfgA<S>::SMEM, st>>>(tq, tdo, tk, tv, a));
+    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreads, CfgA<S>::SMEM, st>>>(tq, tdo, tk, tv, tl, a));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     a.n_items = sp.B * sp.nP * sp.H;

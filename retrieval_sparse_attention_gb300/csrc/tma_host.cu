@@ -46,4 +46,19 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool encode_f32_box(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                    uint32_t box_cols, uint32_t box_rows) {
+    std::call_once(g_once, resolve);
+    if (!g_encode) return false;
+    cuuint64_t dims[2] = {row_elems, rows};
+    cuuint64_t strides[1] = {row_elems * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace gca

@@ -13,4 +13,11 @@ namespace gca {
 bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
                       uint32_t box_rows);
 
+// Tensor map over a row-major fp32 matrix [rows, row_elems] (row stride
+// row_elems * 4 bytes, a multiple of 16), box of box_cols x box_rows (box_cols
+// * 4 a multiple of 16), no swizzle: the box lands in shared memory as
+// box_rows dense rows of box_cols floats.
+bool encode_f32_box(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                    uint32_t box_cols, uint32_t box_rows);
+
 }  // namespace gca
