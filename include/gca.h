@@ -182,7 +182,8 @@ gca_status_t gca_decode_retrieve(const void* landmarks, const void* query_landma
  *   of inference engines, runtimes that plan every device byte at start-up,
  *   and latency-critical loops where an allocation's implicit device
  *   synchronisation is not acceptable.  This entry point needs no workspace
- *   argument: its scratch (a ticket counter and the per-CTA candidate lists)
+ *   argument: its scratch (a ticket counter, a score bound and the per-CTA
+ *   candidate lists)
  *   lives in a file-scope device array of GCA_DECODE_STATIC_SCRATCH_BYTES
  *   bytes that every GPU loading the library holds until the process exits.
  *   Arguments, layouts and results are those of gca_decode_retrieve.
@@ -192,7 +193,7 @@ gca_status_t gca_decode_retrieve(const void* landmarks, const void* query_landma
  *   The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   All calls on a device share the one array, which keeps the previous
- *   call's contents (the counter is cleared on the stream before each
+ *   call's contents (counter and bound are cleared on the stream before each
  *   launch): calls whose executions overlap on the GPU (other streams, other
  *   host threads) race on it and must be serialised by the caller.
  *   Calls no cudaMalloc, cudaFree or other allocating routine.

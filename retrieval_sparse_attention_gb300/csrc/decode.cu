@@ -3,17 +3,23 @@
 // Long-Context Language Modeling": once per chunk of generated tokens the new
 // landmark scores every stored landmark and the top-k chunks are reloaded).
 //
-// The landmark table is streamed once from HBM.  Each CTA owns a contiguous
-// range of rows and pulls it through a 4-stage shared-memory ring with bulk
+// The landmark table is streamed once from HBM in stages of whole rows, dealt
+// round-robin to the CTAs (all CTAs read within one moving front of the table);
+// each CTA pulls its stages through a shared-memory ring with bulk
 // asynchronous copies (cp.async.bulk, one thread issues, an mbarrier counts
 // the bytes), so the copy engine keeps HBM busy independently of the math.
 // Warps score the staged rows against the query landmark held in registers
 // as fp32 (exact for integer landmarks) and keep a running top-k in
 // registers, one rank per lane, with the admission threshold replicated in
 // every lane so that the common case (row not in the top-k) costs one
-// compare.  Warps merge into a per-CTA list; the CTA that finishes last
-// (ticket counter, no waiting) merges every CTA's list, filtering 32
-// candidates per ballot, applies the softmax and resets the counter.
+// compare.  Merges compare 64-bit rank keys (score, then lower index; keys are
+// distinct), so a candidate's place is the number of larger keys among its
+// rivals, counted 32 per ballot.  Warps merge into a per-CTA list that way;
+// the CTA that finishes last (ticket counter, no waiting) loads every list,
+// takes the k-th best list head as a lower bound on the global k-th best (the
+// heads are a subset of all rows), keeps the entries ranking at or before it
+// (they come from at most topk lists: at most topk^2 of them), ranks those,
+// applies the softmax and resets the counter.
 #include <math.h>
 
 #include <mutex>
@@ -29,8 +35,13 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxBlocks = 2048;
-constexpr int kStages = 4;
-constexpr int kStageBytes = 24576;
+constexpr int kStages = 2;
+constexpr int kStageBytes = 49152;
+// 64-bit rank keys the last CTA holds in its idle ring: every CTA's list
+// (grid * topk) plus at most topk^2 survivors of the head bound
+constexpr int kRingKeys = kStages * kStageBytes / 8;
+constexpr int kHeadRegs = 16;            // list heads per lane in the last CTA's registers
+constexpr int kMaxGrid = 32 * kHeadRegs; // so at most 512 CTAs
 
 // Running top-k of a warp: lane j holds rank j (score desc, index asc); every
 // lane also holds the current admission threshold (rank topk-1).
@@ -51,17 +62,37 @@ struct WarpTopk {
         thr_s = __shfl_sync(0xffffffffu, ts, topk - 1);
         thr_i = __shfl_sync(0xffffffffu, ti, topk - 1);
     }
-    // Offer 32 candidates at once (lane l holds one); only those that beat the
-    // threshold are inserted, in lane order.
-    __device__ __forceinline__ void offer32(int topk, float cs, int ci) {
-        unsigned m = __ballot_sync(0xffffffffu, ranks_before(cs, ci, thr_s, thr_i));
-        while (m) {
-            const int src = __ffs(m) - 1;
-            m &= m - 1;
-            offer(topk, __shfl_sync(0xffffffffu, cs, src), __shfl_sync(0xffffffffu, ci, src));
-        }
-    }
 };
+
+// Order-preserving key of a (score, index) pair: a larger key ranks earlier
+// (higher score, then lower index).  Keys of distinct indices are distinct, so
+// the rank of a candidate in a set is the number of larger keys in it.  Key 0
+// marks an empty list entry (it ranks after every real pair).
+__device__ __forceinline__ unsigned long long rank_key(float f, int i) {
+    const unsigned u = __float_as_uint(f);
+    const unsigned sk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(sk) << 32) | static_cast<unsigned>(~static_cast<unsigned>(i));
+}
+__device__ __forceinline__ float key_score(unsigned long long k) {
+    const unsigned sk = static_cast<unsigned>(k >> 32);
+    return __uint_as_float((sk & 0x80000000u) ? (sk & 0x7fffffffu) : ~sk);
+}
+__device__ __forceinline__ int key_index(unsigned long long k) {
+    return static_cast<int>(~static_cast<unsigned>(k & 0xffffffffull));
+}
+
+// Rank of key k among keys[0, n) (the number of larger keys), counted 32 keys
+// per ballot by the whole warp (k uniform across it); stops at `limit`.
+__device__ __forceinline__ int warp_rank(unsigned long long k, const unsigned long long* keys, int n,
+                                         int limit) {
+    const int lane = threadIdx.x & 31;
+    int r = 0;
+    for (int b0 = 0; b0 < n && r < limit; b0 += 32) {
+        const int e = b0 + lane;
+        r += __popc(__ballot_sync(0xffffffffu, e < n && keys[e] > k));
+    }
+    return r;
+}
 
 template <typename T>
 __device__ __forceinline__ float dot16(const uint4& raw, const float* qv);
@@ -89,6 +120,9 @@ struct __align__(8) DecodeBars {
     uint64_t full[kStages], empty[kStages];
     int abort;
     bool is_last;
+    unsigned long long bound;      // last CTA: key of the k-th best list head
+    int n_kept;                    // last CTA: survivors of the head bound
+    unsigned long long top[kMaxTopk];   // merged top-k keys by rank (0: none)
 };
 
 template <typename T, int VPL>
@@ -103,17 +137,18 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
                                                ~static_cast<uintptr_t>(127));
     float* qsh = reinterpret_cast<float*>(ring + kStages * kStageBytes);   // [D]
     __shared__ DecodeBars bars;
-    __shared__ float ws_s[kWarps][kMaxTopk];
-    __shared__ int ws_i[kWarps][kMaxTopk];
+    __shared__ unsigned long long wkeys[kWarps * kMaxTopk];   // the warps' lists as rank keys
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = D / kEPV;                           // vectors per row (<= 32 * VPL)
     const int row_bytes = nvec * 16;
     const int rows_per_stage = kStageBytes / row_bytes;
-    const int per_blk = (N + gridDim.x - 1) / gridDim.x;
-    const int r0 = min(N, blockIdx.x * per_blk);
-    const int r1 = min(N, r0 + per_blk);
-    const int n_stages_total = (r1 - r0 + rows_per_stage - 1) / rows_per_stage;
+    // Stage s of the table (rows s*rows_per_stage ...) belongs to CTA s % grid:
+    // at any moment all CTAs read within one contiguous front of the table.
+    const int total_stages = (N + rows_per_stage - 1) / rows_per_stage;
+    const int n_stages_total = (int)blockIdx.x < total_stages
+        ? (total_stages - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    auto stage_row = [&](int g) { return (g * (int)gridDim.x + (int)blockIdx.x) * rows_per_stage; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -121,16 +156,18 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
             tc::mbar_init(&bars.empty[i], kWarps);
         }
         bars.abort = 0;
+        bars.bound = 0ull;
+        bars.n_kept = 0;
         tc::fence_barrier_init();
     }
     for (int e = threadIdx.x; e < D; e += kThreads) qsh[e] = to_f(ql[e]);
     __syncthreads();
 
-    // Copies of stage g cover rows r0 + g*rows_per_stage ...
+    // Copies of this CTA's stage g: rows stage_row(g) ... (at most rows_per_stage)
     auto issue = [&](int g) {
         const int slot = g % kStages;
-        const int ra = r0 + g * rows_per_stage;
-        const int nr = min(rows_per_stage, r1 - ra);
+        const int ra = stage_row(g);
+        const int nr = min(rows_per_stage, N - ra);
         const uint32_t bytes = static_cast<uint32_t>(nr) * row_bytes;
         tc::mbar_arrive_expect_tx(&bars.full[slot], bytes);
         tcx::bulk_load(ring + slot * kStageBytes,
@@ -156,8 +193,8 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
         const int slot = g % kStages;
         const uint32_t par = static_cast<uint32_t>(g / kStages) & 1u;
         if (!tcx::wait_bar(&bars.abort, &bars.full[slot], par, status)) { ok = false; break; }
-        const int ra = r0 + g * rows_per_stage;
-        const int nr = min(rows_per_stage, r1 - ra);
+        const int ra = stage_row(g);
+        const int nr = min(rows_per_stage, N - ra);
         const uint4* st = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
         for (int rr = warp; rr < nr; rr += kWarps) {
             float acc = 0.f;
@@ -185,15 +222,27 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
             tc::mbar_wait(&bars.full[g % kStages], static_cast<uint32_t>(g / kStages) & 1u, nullptr,
                           100000000ull);
 
-    if (lane < kMaxTopk) { ws_s[warp][lane] = tk.ts; ws_i[warp][lane] = tk.ti; }
+    // CTA merge: every entry of the warps' lists is ranked among all of them
+    // by counting larger keys (keys are distinct); ranks below topk are the
+    // CTA's list, in order.
+    if (lane < topk) wkeys[warp * topk + lane] = tk.ti != 0x7fffffff ? rank_key(tk.ts, tk.ti) : 0ull;
+    if (threadIdx.x < kMaxTopk) bars.top[threadIdx.x] = 0ull;
+    __syncthreads();
+    {
+        const int nw = kWarps * topk;
+        for (int a = warp; a < nw; a += kWarps) {
+            const unsigned long long ka = wkeys[a];
+            if (ka == 0ull) continue;
+            const int r = warp_rank(ka, wkeys, nw, topk);
+            if (r < topk && lane == 0) bars.top[r] = ka;
+        }
+    }
     __syncthreads();
     if (warp == 0) {
-        for (int w = 1; w < kWarps; ++w)
-            tk.offer32(topk, lane < topk ? ws_s[w][lane] : -INFINITY,
-                       lane < topk ? ws_i[w][lane] : 0x7fffffff);
         if (lane < topk) {
-            blk_s[(size_t)blockIdx.x * topk + lane] = tk.ts;
-            blk_i[(size_t)blockIdx.x * topk + lane] = tk.ti;
+            const unsigned long long k = bars.top[lane];
+            blk_s[(size_t)blockIdx.x * topk + lane] = k ? key_score(k) : -INFINITY;
+            blk_i[(size_t)blockIdx.x * topk + lane] = k ? key_index(k) : 0x7fffffff;
         }
         __threadfence();
         if (lane == 0) bars.is_last = (atomicAdd(ticket, 1u) == gridDim.x - 1);
@@ -201,22 +250,79 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     __syncthreads();
     if (!bars.is_last) return;
 
-    // Last CTA: merge every CTA's list, 32 candidates per ballot.
+    // Last CTA.  (1) Every CTA's list lands in the idle ring as rank keys.
+    // (2) The k-th best list head bounds the global k-th best from below (the
+    // heads are a subset of all rows), and an entry ranking at or before it
+    // must come from a list whose head does too: at most topk lists, so at
+    // most topk^2 survivors.  (3) The survivors are ranked by counting.
     __threadfence();
-    tk.init();
-    const int total = gridDim.x * topk;
-    for (int base = warp * 32; base < total; base += kWarps * 32) {
-        const int e = base + lane;
-        const float cs = e < total ? __ldcg(blk_s + e) : -INFINITY;
-        const int ci = e < total ? __ldcg(blk_i + e) : 0x7fffffff;
-        tk.offer32(topk, cs, ci);
+    unsigned long long* rk = reinterpret_cast<unsigned long long*>(ring);
+    const int nb = gridDim.x;
+    const int total = nb * topk;
+    unsigned long long* surv = rk + total;
+    constexpr int kBatch = 8;       // independent loads in flight per thread
+    for (int b0 = threadIdx.x; b0 < total; b0 += kThreads * kBatch) {
+        float cs[kBatch];
+        int ci[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = b0 + u * kThreads;
+            cs[u] = e < total ? __ldcg(blk_s + e) : -INFINITY;
+            ci[u] = e < total ? __ldcg(blk_i + e) : 0x7fffffff;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int e = b0 + u * kThreads;
+            if (e < total) rk[e] = ci[u] != 0x7fffffff ? rank_key(cs[u], ci[u]) : 0ull;
+        }
     }
-    if (lane < kMaxTopk) { ws_s[warp][lane] = tk.ts; ws_i[warp][lane] = tk.ti; }
+    if (threadIdx.x < kMaxTopk) bars.top[threadIdx.x] = 0ull;
+    __syncthreads();
+    {
+        // heads in registers: lane l holds heads l, l + 32, ... (nb <= 32 * kHeadRegs)
+        unsigned long long hr[kHeadRegs];
+#pragma unroll
+        for (int j = 0; j < kHeadRegs; ++j) {
+            const int c = lane + 32 * j;
+            hr[j] = c < nb ? rk[(size_t)c * topk] : 0ull;
+        }
+        for (int c = warp; c < nb; c += kWarps) {
+            const unsigned long long kc = rk[(size_t)c * topk];
+            if (kc == 0ull) continue;
+            int cnt = 0;
+#pragma unroll
+            for (int j = 0; j < kHeadRegs; ++j) cnt += hr[j] > kc;
+            if (__reduce_add_sync(0xffffffffu, cnt) == topk - 1 && lane == 0) bars.bound = kc;
+        }
+    }
+    __syncthreads();
+    const unsigned long long bound = bars.bound;      // 0: fewer than topk non-empty lists
+    for (int b0 = warp * 32; b0 < total; b0 += kThreads) {
+        const int e = b0 + lane;
+        const unsigned long long ke = e < total ? rk[e] : 0ull;
+        const bool keep = ke != 0ull && ke >= bound;
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        int base = 0;
+        if (lane == 0 && m) base = atomicAdd(&bars.n_kept, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (keep) surv[base + __popc(m & ((1u << lane) - 1u))] = ke;
+    }
+    __syncthreads();
+    const int ns = bars.n_kept;
+    for (int a = warp; a < ns; a += kWarps) {
+        const unsigned long long ka = surv[a];
+        const int r = warp_rank(ka, surv, ns, topk);
+        if (r < topk && lane == 0) bars.top[r] = ka;
+    }
     __syncthreads();
     if (warp == 0) {
-        for (int w = 1; w < kWarps; ++w)
-            tk.offer32(topk, lane < topk ? ws_s[w][lane] : -INFINITY,
-                       lane < topk ? ws_i[w][lane] : 0x7fffffff);
+        if (lane < topk && bars.top[lane] != 0ull) {
+            tk.ts = key_score(bars.top[lane]);
+            tk.ti = key_index(bars.top[lane]);
+        } else {
+            tk.ts = -INFINITY;
+            tk.ti = 0x7fffffff;
+        }
         const int m = N < topk ? N : topk;
         const bool okl = lane < m;
         const float r = okl ? tk.ts * sscale : -INFINITY;
@@ -234,6 +340,7 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
         if (lane == 0) *ticket = 0u;     // leave the counter reset for the next call
     }
 }
+
 
 }  // namespace
 
@@ -268,6 +375,10 @@ cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, i
     const int cap = decode_max_blocks(N);
     if (nb > cap) nb = cap;
     unsigned* ticket = reinterpret_cast<unsigned*>(ws);
+    // the last CTA holds every list plus topk^2 survivors as keys in its ring
+    const int ring_cap = (kRingKeys - topk * topk) / topk;
+    if (nb > ring_cap) nb = ring_cap;
+    if (nb > kMaxGrid) nb = kMaxGrid;
     float* blk_s = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
     int* blk_i = reinterpret_cast<int*>(blk_s + (size_t)nb * topk);
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);

@@ -93,6 +93,14 @@ def test_decode_ties_across_blocks():
     assert idx.cpu().tolist() == [77777, 0, 1, 2, 3, 4, 5, 6]
 
 
+def test_decode_all_equal_full_table():
+    # every score ties at full size: the bound filter keeps every CTA's whole
+    # list, and the top-k must still be rows 0..k-1 in order
+    lm = torch.ones(262144, 8, dtype=torch.bfloat16)
+    idx = run_decode(lm, torch.ones(8, dtype=torch.bfloat16), 32, False)
+    assert idx.cpu().tolist() == list(range(32))
+
+
 def test_synth_fill_matches_host_generator():
     S, H, d = 64, 12, 64
     n = 5 * S * H * d
