@@ -430,19 +430,101 @@ def extra_workloads(lib, api, inputs, dev, hbm, tflops):
         dec["retrieve_plus_fwd_us"] = None
         dec["cache_error"] = str(exc)[:120]
     out["decode_16m"] = dec
+    out.update(next_rows(api, inputs, dev, hbm))
+    return out
+
+
+def _event_us(fn, n=50, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n * 1e3
+
+
+def next_rows(api, inputs, dev, hbm):
+    """The widened rows: noisy (Gumbel) top-k, landmark gradients, and the
+    reload of retrieved chunks from a K/V cache offloaded to page-locked host
+    memory, each timed alone with CUDA events on the current stream."""
+    import torch
+    out = {}
+    wl = inputs.WORKLOADS[WORKLOAD]
+    x = inputs.make(wl, with_dout=False)
+    lm = x["lm"].to(dev)
+    B, nC, D = lm.shape
+    g = torch.Generator(device="cpu").manual_seed(5)
+    u = torch.rand(B, nC, nC, generator=g).clamp_(1e-12, 1 - 1e-7)
+    noise = (-torch.log(-torch.log(u))).float().to(dev)           # Gumbel(0, 1)
+    kw = dict(S=wl.S, H=wl.H, d=wl.d, topk=wl.topk)
+    clean_us = _event_us(lambda i=0: api.score_topk(lm, **kw))
+    noisy_us = _event_us(lambda i=0: api.score_topk_noisy(lm, noise, **kw))
+    cand = B * nC * (nC - 1) // 2
+    out["noisy_topk_b8"] = {"kernel": "gca_score_topk_noisy", "us": round(noisy_us, 2),
+                            "clean_us": round(clean_us, 2),
+                            "roofline": {"bound": "hbm", "achieved": round((lm.numel() * 2 + cand * 4) / noisy_us / 1e3, 1),
+                                         "peak": hbm, "unit": "GB/s",
+                                         "frac": round((lm.numel() * 2 + cand * 4) / noisy_us / 1e3 / hbm, 4),
+                                         "note": "latency-bound: 2048 CTAs of one landmark row each"}}
+    idx, r, w = api.score_topk(lm, **kw)
+    dr = (torch.randn(B, nC, wl.topk, generator=g) * 0.1).float().to(dev) * (idx >= 0)
+    U = int((idx >= 0).sum().item())
+    lbw_us = _event_us(lambda i=0: api.landmark_bwd(lm, idx, dr, S=wl.S, H=wl.H, d=wl.d))
+    lb_bytes = 2 * lm.numel() * 2 + 2 * U * D * 2                 # rows in and out, two row reads per unit
+    out["landmark_bwd_b8"] = {"kernel": "gca_landmark_bwd", "us": round(lbw_us, 2), "valid_units": U,
+                              "roofline": {"bound": "hbm", "achieved": round(lb_bytes / lbw_us / 1e3, 1),
+                                           "peak": hbm, "unit": "GB/s",
+                                           "frac": round(lb_bytes / lbw_us / 1e3 / hbm, 4)}}
+    del x, lm, noise
+    # offloaded cache: 2048 chunks of K and of V (2 x 201 MB) in page-locked host memory
+    p = inputs.DECODE
+    S, H, d, k = p["S"], p["H"], p["d"], p["topk"]
+    n_src = 2048
+    ck = torch.empty(n_src, S, H, d, dtype=torch.bfloat16, device=dev)
+    cv = torch.empty_like(ck)
+    api.gca_synth_fill_hash(ck, p["seed"], 0)
+    api.gca_synth_fill_hash(cv, p["seed"], 1)
+    hk = torch.empty(ck.shape, dtype=ck.dtype, pin_memory=True)
+    hv = torch.empty(cv.shape, dtype=cv.dtype, pin_memory=True)
+    hk.copy_(ck)
+    hv.copy_(cv)
+    del ck, cv
+    n_it = 50
+    sets = torch.stack([torch.randperm(n_src, generator=g)[:k] for _ in range(n_it + 3)]).int().to(dev)
+    chunk = S * H * d * 2
+    dk = torch.empty(k * S, H, d, dtype=torch.bfloat16, device=dev)
+    dv = torch.empty_like(dk)
+    di = torch.empty(k, dtype=torch.int32, device=dev)
+    gat = lambda i=0: api.gca_gather_chunks(hk, hv, n_src, chunk, sets[i], k, dk, dv, di)
+    gat_us = _event_us(gat, n=n_it)
+    big_h = torch.empty(64 << 20, dtype=torch.float32, pin_memory=True)
+    big_d = torch.empty_like(big_h, device=dev)
+    copy_us = _event_us(lambda i=0: big_d.copy_(big_h, non_blocking=True), n=5, warm=1)
+    link = big_h.numel() * 4 / copy_us / 1e3
+    gb = 2 * k * chunk
+    out["offload_gather"] = {"kernel": "gca_gather_chunks", "us": round(gat_us, 2), "bytes": gb,
+                             "chunks": k, "source": "page-locked host memory (2 x 2048 chunks)",
+                             "roofline": {"bound": "host link", "achieved": round(gb / gat_us / 1e3, 1),
+                                          "peak": round(link, 1), "unit": "GB/s",
+                                          "frac": round(gb / gat_us / 1e3 / link, 4),
+                                          "peak_source": "cudaMemcpyAsync of 256 MB page-locked host -> device, same process"}}
     return out
 
 
 # --------------------------------------------------------------------------- oracle
-def oracle_step(L_sample):
-    """One oracle pass (score + fwd + bwd) on the first batch row of the
-    workload truncated to L_sample tokens.  Returns seconds."""
+def oracle_step(L_sample, B_sample=1):
+    """One oracle pass (score + fwd + bwd) on the first B_sample batch rows of
+    the workload truncated to L_sample tokens.  Returns seconds."""
     import numpy as np
 
     import oracle
     from retrieval_sparse_attention_gb300 import inputs
     wl = inputs.WORKLOADS[WORKLOAD]
-    x = inputs.make(wl, B=1, L=L_sample)
+    x = inputs.make(wl, B=B_sample, L=L_sample)
     f = {n: t.double().numpy() for n, t in x.items()}
     t0 = time.perf_counter()
     idx, r, w = oracle.score_topk(f["lm"], wl.topk, False, wl.off_by_one)
@@ -451,13 +533,13 @@ def oracle_step(L_sample):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(L_sample=8192):
+def cpu_baseline(L_sample=16384, B_sample=4):
     import oracle
     oracle.build()
-    t = oracle_step(L_sample)
-    return {"value": round(L_sample / t, 2), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": "fp64 oracle score+fwd+bwd on batch row 0, first %d tokens "
-            "(%d chunks) of the workload; %.2f s" % (L_sample, L_sample // 64, t)}
+    t = oracle_step(L_sample, B_sample)
+    return {"value": round(B_sample * L_sample / t, 2), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "fp64 oracle score+fwd+bwd on batch rows 0-%d (of 8), all %d "
+            "tokens each, of the workload; %.2f s" % (B_sample - 1, L_sample, t)}
 
 
 def run_reference(args):
