@@ -5,10 +5,12 @@
 //
 // The cache is [n_chunks, chunk_bytes] in memory the GPU can address: device
 // memory, or page-locked host memory (with unified addressing its host
-// pointer is valid on the device and is read over the CPU-GPU link).  One
-// CTA streams one retrieved chunk of K and of V with 16-byte loads into a
-// compact device pool [topk, chunk] and writes the slot's new index (j, or
-// -1 for an empty slot), so that gca_fwd can run on the compact pool.
+// pointer is valid on the device and is read over the CPU-GPU link).  The
+// retrieved chunks of K and of V are streamed with 16-byte loads into a
+// compact device pool [topk, chunk], and each slot's new index (j, or -1 for
+// an empty slot) is written, so that gca_fwd can run on the compact pool.
+// Each chunk is split over many CTAs, each issuing all its loads before its
+// stores, so the link's latency is paid about once per call.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,6 +18,7 @@ namespace gca {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 2;
 
 __global__ void __launch_bounds__(kThreads)
 gather_chunks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
@@ -29,17 +32,28 @@ gather_chunks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ 
         dst_idx[j] = ok ? j : -1;
         if (kap >= n_src) set_status(status, GCA_ERR_DEVICE_INDEX);
     }
-    const size_t per = (chunk_vecs + gridDim.y - 1) / gridDim.y;
-    const size_t lo = (size_t)blockIdx.y * per;
-    const size_t hi = lo + per < chunk_vecs ? lo + per : chunk_vecs;
+    // this CTA's piece: kThreads * kUnroll vectors of the chunk's K and of its V,
+    // every load issued before any store (the link's latency is paid once)
+    const size_t base = (size_t)blockIdx.y * kThreads * kUnroll + threadIdx.x;
     const uint4 z = make_uint4(0, 0, 0, 0);
     const uint4* sk = src_k + (size_t)(ok ? kap : 0) * chunk_vecs;
     const uint4* sv = src_v + (size_t)(ok ? kap : 0) * chunk_vecs;
+    uint4 a[kUnroll], c[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const size_t i = base + (size_t)u * kThreads;
+        a[u] = (ok && i < chunk_vecs) ? __ldcs(sk + i) : z;
+        c[u] = (ok && i < chunk_vecs) ? __ldcs(sv + i) : z;
+    }
     uint4* dk = dst_k + (size_t)j * chunk_vecs;
     uint4* dv = dst_v + (size_t)j * chunk_vecs;
-    for (size_t i = lo + threadIdx.x; i < hi; i += kThreads) {
-        dk[i] = ok ? __ldcs(sk + i) : z;
-        dv[i] = ok ? __ldcs(sv + i) : z;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const size_t i = base + (size_t)u * kThreads;
+        if (i < chunk_vecs) {
+            dk[i] = a[u];
+            dv[i] = c[u];
+        }
     }
 }
 
@@ -49,11 +63,12 @@ cudaError_t launch_gather_chunks(const void* src_k, const void* src_v, int n_src
                                  const int32_t* idx, int topk, void* dst_k, void* dst_v,
                                  int32_t* dst_idx, int* status, cudaStream_t st, int* launches) {
     const size_t vecs = chunk_bytes / 16;
-    // enough CTAs per chunk to keep many 16-byte reads in flight over the link
-    int split = (int)((vecs + 4095) / 4096);
-    if (split < 1) split = 1;
-    if (split > 64) split = 64;
-    dim3 grid(topk, split);
+    // one CTA per kThreads * kUnroll vectors of a chunk: the whole transfer is
+    // in flight at once for chunks of the usual size
+    const size_t per_cta = (size_t)kThreads * kUnroll;
+    const size_t split = (vecs + per_cta - 1) / per_cta;
+    if (split < 1 || split > 65535) return cudaErrorInvalidValue;
+    dim3 grid(topk, (unsigned)split);
     GCA_LAUNCH("gather_chunks", st,
                gather_chunks_kernel<<<grid, kThreads, 0, st>>>(
                    (const uint4*)src_k, (const uint4*)src_v, n_src, vecs, idx, topk, (uint4*)dst_k,

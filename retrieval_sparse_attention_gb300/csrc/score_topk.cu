@@ -5,10 +5,11 @@
 //
 // One CTA per (batch row, query chunk).  The landmark of chunk c-1 is staged
 // in shared memory as fp32; each warp scores a strided subset of the earlier
-// chunks (lanes split D, fp32 FMA, warp-shuffle sum: exact for integer
-// landmarks with |s| < 2^24), the scores stay in shared memory, and the
-// top-k is taken by k rounds of a block-wide arg-max under the order
-// (score descending, chunk ascending).  The whole landmark tensor of a row
+// chunks, two at a time (lanes split D in 16-byte vectors, fp32 FMA,
+// warp-shuffle sum: exact for integer landmarks with |s| < 2^24) and keeps a
+// running top-k of its keys in registers under the order (score descending,
+// chunk ascending); the eight warp lists are merged by counting, for each
+// entry, the entries ranking before it.  The whole landmark tensor of a row
 // is small (nC x D) and stays in L2, so the kernel is latency-bound.
 //
 // With a noise tensor (section 3.2: during training Gumbel noise is added to
@@ -20,6 +21,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace gca {
 namespace {
@@ -35,12 +37,11 @@ score_topk_kernel(const T* __restrict__ lm, const float* __restrict__ noise, int
                   float* __restrict__ weight) {
     extern __shared__ float sh[];
     float* lt = sh;            // [D]   landmark of chunk c-1
-    float* s = sh + D;         // [nC]  scores of the candidates
-    float* key = NOISY ? s + nC : s;   // [nC] selection keys
-    __shared__ float red_s[kWarps];
-    __shared__ int red_i[kWarps];
+    float* s = sh + D;         // [nC]  clean scores of the candidates
     __shared__ float sel_s[kMaxTopk];
     __shared__ int sel_i[kMaxTopk];
+    __shared__ unsigned long long wkeys[kWarps * kMaxTopk];   // the warps' lists as rank keys
+    __shared__ unsigned long long top[kMaxTopk];               // merged list by rank
 
     const int c = blockIdx.x, b = blockIdx.y;
     const int t = c - 1;
@@ -52,45 +53,76 @@ score_topk_kernel(const T* __restrict__ lm, const float* __restrict__ noise, int
         for (int e = threadIdx.x; e < D; e += kThreads) lt[e] = to_f(row[(size_t)t * D + e]);
     __syncthreads();
 
-    for (int kap = warp; kap < n; kap += kWarps) {
-        const T* lk = row + (size_t)kap * D;
-        float acc = 0.f;
-        for (int e = lane; e < D; e += 32) acc = fmaf(lt[e], to_f(lk[e]), acc);
-        acc = warp_sum(acc);
-        if (lane == 0) {
-            s[kap] = acc;
-            if (NOISY)
-                key[kap] = __fadd_rn(__fmul_rn(acc, sscale),
-                                     noise[((size_t)b * nC + c) * nC + kap]);
+    // scores: a warp per candidate, two candidates in flight (16-byte loads of
+    // the candidate rows when D allows it); each warp keeps a running top-k of
+    // the selection keys it produced, in registers
+    constexpr int kEPV = 16 / sizeof(T);
+    const bool vec = (D % kEPV) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0;
+    const float* nrow = NOISY ? noise + ((size_t)b * nC + c) * nC : nullptr;
+    WarpTopk tk;
+    tk.init();
+    auto record = [&](int kap, float acc) {
+        const float kv = NOISY ? __fadd_rn(__fmul_rn(acc, sscale), nrow[kap]) : acc;
+        if (lane == 0) s[kap] = acc;
+        tk.offer(topk, kv, kap);
+    };
+    for (int k0 = warp; k0 < n; k0 += 2 * kWarps) {
+        const int k1 = k0 + kWarps;
+        float a0 = 0.f, a1 = 0.f;
+        if (vec) {
+            const uint4* r0 = reinterpret_cast<const uint4*>(row + (size_t)k0 * D);
+            const uint4* r1 = reinterpret_cast<const uint4*>(row + (size_t)(k1 < n ? k1 : k0) * D);
+            const float4* l4 = reinterpret_cast<const float4*>(lt);
+            for (int v = lane; v < D / kEPV; v += 32) {
+                const uint4 x0 = __ldg(r0 + v), x1 = __ldg(r1 + v);
+                const T* e0 = reinterpret_cast<const T*>(&x0);
+                const T* e1 = reinterpret_cast<const T*>(&x1);
+#pragma unroll
+                for (int w4 = 0; w4 < kEPV / 4; ++w4) {
+                    const float4 q = l4[v * (kEPV / 4) + w4];
+                    const float qa[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        a0 = fmaf(qa[u], to_f(e0[4 * w4 + u]), a0);
+                        a1 = fmaf(qa[u], to_f(e1[4 * w4 + u]), a1);
+                    }
+                }
+            }
+        } else {
+            const T* r0 = row + (size_t)k0 * D;
+            const T* r1 = row + (size_t)(k1 < n ? k1 : k0) * D;
+            for (int e = lane; e < D; e += 32) {
+                a0 = fmaf(lt[e], to_f(r0[e]), a0);
+                a1 = fmaf(lt[e], to_f(r1[e]), a1);
+            }
+        }
+        record(k0, warp_sum(a0));
+        const float s1 = warp_sum(a1);
+        if (k1 < n) record(k1, s1);
+    }
+
+    // merge the warps' lists: an entry's place is the number of larger rank
+    // keys among all entries (keys are distinct), counted 32 per ballot
+    if (lane < topk) wkeys[warp * topk + lane] = tk.ti != 0x7fffffff ? rank_key(tk.ts, tk.ti) : 0ull;
+    if (threadIdx.x < kMaxTopk) top[threadIdx.x] = 0ull;
+    __syncthreads();
+    const int m = n < topk ? n : topk;
+    {
+        const int nw = kWarps * topk;
+        for (int a = warp; a < nw; a += kWarps) {
+            const unsigned long long ka = wkeys[a];
+            if (ka == 0ull) continue;
+            const int r = warp_rank(ka, wkeys, nw, topk);
+            if (r < topk && lane == 0) top[r] = ka;
         }
     }
     __syncthreads();
-
-    const int m = n < topk ? n : topk;
-    for (int j = 0; j < m; ++j) {
-        float bs = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int kap = threadIdx.x; kap < n; kap += kThreads) {
-            float v = key[kap];
-            if (v != -INFINITY && ranks_before(v, kap, bs, bi)) { bs = v; bi = kap; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ranks_before(os, oi, bs, bi)) { bs = os; bi = oi; }
-        }
-        if (lane == 0) { red_s[warp] = bs; red_i[warp] = bi; }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int w = 1; w < kWarps; ++w)
-                if (ranks_before(red_s[w], red_i[w], bs, bi)) { bs = red_s[w]; bi = red_i[w]; }
-            sel_s[j] = s[bi];    // the clean score
-            sel_i[j] = bi;
-            key[bi] = -INFINITY; // taken
-        }
-        __syncthreads();
+    if (threadIdx.x < m) {
+        const int kap = key_index(top[threadIdx.x]);
+        sel_i[threadIdx.x] = kap;
+        sel_s[threadIdx.x] = s[kap];       // the clean score
     }
+    __syncthreads();
 
     if (threadIdx.x == 0) {
         const size_t o = ((size_t)b * nC + c) * topk;
@@ -112,7 +144,7 @@ score_topk_kernel(const T* __restrict__ lm, const float* __restrict__ noise, int
 template <typename T, bool NOISY>
 void launch_typed(const Shape& sp, const void* lm, const float* noise, int32_t* idx, float* score,
                   float* weight, cudaStream_t st) {
-    const size_t smem = sizeof(float) * ((size_t)sp.D + (NOISY ? 2 : 1) * (size_t)sp.nQ);
+    const size_t smem = sizeof(float) * ((size_t)sp.D + (size_t)sp.nQ);
     dim3 grid(sp.nQ, sp.B);
     auto kern = score_topk_kernel<T, NOISY>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
