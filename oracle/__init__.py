@@ -10,8 +10,9 @@ Method source: "Efficient Length-Generalizable Attention via Causal Retrieval
 for Long-Context Language Modeling" (ICML 2025, arXiv 2410.01651): the
 rebuttal comment "Cmt 1" (G=1 form of Eq. 1, r = l_t^T l_k / sqrt(d)), the
 answers to W2 (Eq. 2 is the batch form of Figure 2) and Q4 (Eq. 3, softmax
-off by one), and the official README's "Model Architecture" (two-stage
-attention, weighted fusion).  Every function below is pinned by the
+off by one), the official README's "Model Architecture" (two-stage
+attention, weighted fusion), and sections 1 and 4.1.2 of the paper summary
+for the 512-token sliding-window self-attention that precedes GCA in a layer.  Every function below is pinned by the
 ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``.
 """
 from __future__ import annotations
@@ -56,6 +57,8 @@ def _load():
         lib.oracle_landmark_bwd.argtypes = [i32, i32, i32, i32, f64, vp, vp, vp, vp]
         lib.oracle_score_topk_noisy.argtypes = [i32, i32, i32, i32, i32, i32, f64, vp, vp, vp, vp, vp]
         lib.oracle_score_topk_noisy.restype = i32
+        lib.oracle_swa_fwd.argtypes = [i32] * 5 + [f64] + [vp] * 5
+        lib.oracle_swa_bwd.argtypes = [i32] * 5 + [f64] + [vp] * 7
         _lib = lib
     return _lib
 
@@ -197,3 +200,29 @@ def score_topk_noisy(lm, noise, topk: int, include_self: bool = False, off_by_on
     if rc != 0:
         raise ValueError("oracle_score_topk_noisy: topk must be in [1, 64]")
     return idx, r, w
+
+
+def swa_fwd(q, k, v, window: int, attn_scale: float | None = None):
+    """Sliding-window causal self-attention.  q, k, v [B, L, H, d]; token t
+    attends to keys max(0, t-window+1) .. t.  Returns (o [B,L,H,d], lse [B,L,H])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, L, H, d = q.shape
+    if attn_scale is None:
+        attn_scale = 1.0 / np.sqrt(d)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, L, H))
+    _load().oracle_swa_fwd(B, L, H, d, int(window), float(attn_scale), _ptr(q), _ptr(k), _ptr(v),
+                           _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def swa_bwd(q, k, v, dout, window: int, attn_scale: float | None = None):
+    """Gradients of sum(dout * swa_fwd(q, k, v).o): returns (dq, dk, dv)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, L, H, d = q.shape
+    if attn_scale is None:
+        attn_scale = 1.0 / np.sqrt(d)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    _load().oracle_swa_bwd(B, L, H, d, int(window), float(attn_scale), _ptr(q), _ptr(k), _ptr(v),
+                           _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv

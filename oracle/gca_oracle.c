@@ -453,3 +453,109 @@ int oracle_score_topk_noisy(int B, int nC, int D, int topk, int include_self, in
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Sliding-window self-attention ([P1] section 1: DRT combines top-k past  */
+/* chunks with fixed-size sliding-window self-attention; section 4.1.2:    */
+/* the window is 512 tokens; the GCA modules come after the attention      */
+/* modules of a layer).  Reading: token t of a sequence attends to the     */
+/* keys s with max(0, t - W + 1) <= s <= t (itself included), softmax of   */
+/* attn_scale * q_t . k_s per head, no other mask.                         */
+/* Layouts: q, k, v, o, dout, dq, dk, dv [B, L, H, d]; lse [B, L, H].      */
+/* ---------------------------------------------------------------------- */
+
+/* Forward: o_t = sum_s p_ts v_s with p_ts = exp(a_ts - lse_t),
+ * a_ts = attn_scale q_t . k_s, lse_t = ln sum_s exp(a_ts). */
+void oracle_swa_fwd(int B, int L, int H, int d, int W, double attn_scale, const double* q,
+                    const double* k, const double* v, double* o, double* lse)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double* a = (double*)malloc(sizeof(double) * (size_t)(W > 0 ? W : 1));
+            for (int t = 0; t < L; ++t) {
+                const int s0 = t - W + 1 > 0 ? t - W + 1 : 0;
+                const double* qt = q + (((size_t)b * L + t) * H + h) * d;
+                double m = -INFINITY;
+                for (int s = s0; s <= t; ++s) {
+                    const double* ks = k + (((size_t)b * L + s) * H + h) * d;
+                    double acc = 0.0;
+                    for (int e = 0; e < d; ++e) acc += qt[e] * ks[e];
+                    a[s - s0] = attn_scale * acc;
+                    if (a[s - s0] > m) m = a[s - s0];
+                }
+                double l = 0.0;
+                for (int s = s0; s <= t; ++s) l += exp(a[s - s0] - m);
+                double* ot = o + (((size_t)b * L + t) * H + h) * d;
+                for (int e = 0; e < d; ++e) ot[e] = 0.0;
+                for (int s = s0; s <= t; ++s) {
+                    const double p = exp(a[s - s0] - m) / l;
+                    const double* vs = v + (((size_t)b * L + s) * H + h) * d;
+                    for (int e = 0; e < d; ++e) ot[e] += p * vs[e];
+                }
+                lse[((size_t)b * L + t) * H + h] = m + log(l);
+            }
+            free(a);
+        }
+    }
+}
+
+/* Backward of oracle_swa_fwd for an upstream gradient dout:
+ *   delta_t = dout_t . o_t,  dp_ts = dout_t . v_s,  ds_ts = p_ts (dp_ts - delta_t),
+ *   dq_t = attn_scale sum_s ds_ts k_s,  dk_s = attn_scale sum_t ds_ts q_t,
+ *   dv_s = sum_t p_ts dout_t.
+ * p and o are recomputed here from q, k, v (nothing is taken from a forward). */
+void oracle_swa_bwd(int B, int L, int H, int d, int W, double attn_scale, const double* q,
+                    const double* k, const double* v, const double* dout, double* dq, double* dk,
+                    double* dv)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double* p = (double*)malloc(sizeof(double) * (size_t)(W > 0 ? W : 1));
+            double* ot = (double*)malloc(sizeof(double) * (size_t)d);
+            for (int t = 0; t < L; ++t) {
+                size_t ix = (((size_t)b * L + t) * H + h) * d;
+                for (int e = 0; e < d; ++e) { dk[ix + e] = 0.0; dv[ix + e] = 0.0; }
+            }
+            for (int t = 0; t < L; ++t) {
+                const int s0 = t - W + 1 > 0 ? t - W + 1 : 0;
+                const double* qt = q + (((size_t)b * L + t) * H + h) * d;
+                const double* gt = dout + (((size_t)b * L + t) * H + h) * d;
+                double m = -INFINITY;
+                for (int s = s0; s <= t; ++s) {
+                    const double* ks = k + (((size_t)b * L + s) * H + h) * d;
+                    double acc = 0.0;
+                    for (int e = 0; e < d; ++e) acc += qt[e] * ks[e];
+                    p[s - s0] = attn_scale * acc;
+                    if (p[s - s0] > m) m = p[s - s0];
+                }
+                double l = 0.0;
+                for (int s = s0; s <= t; ++s) { p[s - s0] = exp(p[s - s0] - m); l += p[s - s0]; }
+                for (int s = s0; s <= t; ++s) p[s - s0] /= l;
+                for (int e = 0; e < d; ++e) ot[e] = 0.0;
+                for (int s = s0; s <= t; ++s) {
+                    const double* vs = v + (((size_t)b * L + s) * H + h) * d;
+                    for (int e = 0; e < d; ++e) ot[e] += p[s - s0] * vs[e];
+                }
+                double delta = 0.0;
+                for (int e = 0; e < d; ++e) delta += gt[e] * ot[e];
+                double* dqt = dq + (((size_t)b * L + t) * H + h) * d;
+                for (int e = 0; e < d; ++e) dqt[e] = 0.0;
+                for (int s = s0; s <= t; ++s) {
+                    const size_t is = (((size_t)b * L + s) * H + h) * d;
+                    double dp = 0.0;
+                    for (int e = 0; e < d; ++e) dp += gt[e] * v[is + e];
+                    const double ds = p[s - s0] * (dp - delta);
+                    for (int e = 0; e < d; ++e) {
+                        dqt[e] += attn_scale * ds * k[is + e];
+                        dk[is + e] += attn_scale * ds * qt[e];
+                        dv[is + e] += p[s - s0] * gt[e];
+                    }
+                }
+            }
+            free(ot);
+            free(p);
+        }
+    }
+}
