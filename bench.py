@@ -49,7 +49,8 @@ def parse():
 #: small cases for profiler captures: (workload, batch rows, with backward)
 CASES = {"fwd_b4": ("gpt2s_fwd_b4", 4, False), "fwdbwd_b4": ("gpt2s_fwdbwd_b8", 4, True),
          "fwdbwd_b8": ("gpt2s_fwdbwd_b8", 8, True), "long_s64_k16": ("long64k_S64_k16", 1, True),
-         "long_s128_k8": ("long64k_S128_k8", 1, True), "decode": (None, 1, False)}
+         "long_s128_k8": ("long64k_S128_k8", 1, True), "decode": (None, 1, False),
+         "swa": ("swa", 8, False)}
 
 
 def peaks():
@@ -431,7 +432,41 @@ def extra_workloads(lib, api, inputs, dev, hbm, tflops):
         dec["cache_error"] = str(exc)[:120]
     out["decode_16m"] = dec
     out.update(next_rows(api, inputs, dev, hbm))
+    x = swa_inputs(dev)
+    us = _event_us(lambda i=0: api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW), n=20)
+    out["swa_fwd_b8_16k"] = {"kernel": "gca_swa_fwd", "B": 8, "L": 16384, "H": 12, "d": 64,
+                             "window": SWA_WINDOW, "us": round(us, 2),
+                             "query_tokens_per_s": round(8 * 16384 / (us / 1e6), 1),
+                             "roofline": swa_roofline(8, 16384, 12, 64, SWA_WINDOW, us / 1e3, hbm, tflops)}
+    del x
     return out
+
+
+SWA_WINDOW = 512
+
+
+def swa_inputs(dev, B=8, L=16384, H=12, d=64, seed=11):
+    """Q, K, V [B, L, H, d] ~ N(0, 1/64) in bf16 (the GCA workloads' recipe)."""
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    return [(torch.randn(B, L, H, d, generator=g) * 0.125).to(torch.bfloat16).to(dev) for _ in range(3)]
+
+
+def swa_roofline(B, L, H, d, W, ms, hbm, tflops):
+    """Slower of algorithmic bytes at HBM bandwidth and algorithmic FLOPs at
+    tensor peak.  Bytes: Q, K, V read and O written once (bf16), lse (fp32).
+    FLOPs: 4 d per (token, head, visible key); token t sees min(t + 1, W) keys."""
+    byts = 4 * B * L * H * d * 2 + B * L * H * 4
+    keys = W * (W + 1) // 2 + (L - W) * W if L >= W else L * (L + 1) // 2
+    flops = 4.0 * d * B * H * keys
+    t_hbm, t_tc = byts / (hbm * 1e9), flops / (tflops * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        ach, peak, unit = byts / (ms / 1e3) / 1e9, hbm, "GB/s"
+    else:
+        ach, peak, unit = flops / (ms / 1e3) / 1e12, tflops, "TFLOP/s"
+    return {"bound": bound, "achieved": round(ach, 1), "peak": peak, "unit": unit,
+            "frac": round(max(t_hbm, t_tc) / (ms / 1e3), 4), "alg_bytes": byts, "alg_flops": flops}
 
 
 def _event_us(fn, n=50, warm=3):
@@ -579,7 +614,10 @@ def run_case(args):
     name, B, backward = CASES[args.case]
     dev = torch.device("cuda", 0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if name is None:
+    if name == "swa":
+        x = swa_inputs(dev)
+        step = lambda: api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)
+    elif name is None:
         hx = inputs.decode_inputs()
         lm, ql = hx["lm"].to(dev), hx["ql"].to(dev)
         p = inputs.DECODE

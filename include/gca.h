@@ -225,6 +225,33 @@ gca_status_t gca_gather_chunks(const void* src_k, const void* src_v, int n_src,
                                void* dst_v, int32_t* dst_idx, void* stream);
 
 /*
+ * Sliding-window self-attention: the fixed-size window self-attention that a
+ * DRT layer runs before its GCA module.  Defines: paper summary section 1
+ * (DRT combines the top-k past chunks of GCA with fixed-size sliding-window
+ * self-attention) and section 4.1.2 (a 512-token window; the GCA modules are
+ * appended after the attention modules).  The norm and residual between the
+ * two modules are not part of this library.
+ *   Token t of a row attends to the keys max(0, t - window + 1) .. t:
+ *   o_t = sum_s softmax_s(attn_scale q_t . k_s) v_s per head.
+ */
+typedef struct {
+    int B, L, H, d;       /* q, k, v, o: [B, L, H, d], d contiguous                   */
+    int window;           /* W >= 1 (512 in the paper's model)                          */
+    gca_dtype_t dtype;    /* element type of q/k/v/o (GCA_BF16 with d = 64 supported)   */
+    float attn_scale;     /* 0 => 1/sqrt(d)                                             */
+} gca_swa_params_t;
+
+/*
+ * gca_swa_fwd -- sliding-window self-attention forward.
+ *   q, k, v, o [B, L, H, d] device pointers (16-byte aligned; o fully written).
+ *   lse [B, L, H] fp32 or NULL: ln sum_s exp(attn_scale q_t . k_s) over the
+ *   window; needed later by gca_swa_bwd.  fp32 accumulation, bf16 output.
+ *   Returns GCA_ERR_UNSUPPORTED for another dtype or head dimension.
+ */
+gca_status_t gca_swa_fwd(const gca_swa_params_t* params, const void* q, const void* k,
+                         const void* v, void* o, float* lse, void* stream);
+
+/*
  * gca_get_status -- synchronise `stream`, then return and clear the device
  * status word of the current device (GCA_OK if no device-side error was
  * recorded since the last call).

@@ -25,7 +25,7 @@ EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
             "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc",
             "gca_score_topk_noisy", "gca_landmark_bwd_workspace_size", "gca_landmark_bwd",
-            "gca_gather_chunks")
+            "gca_gather_chunks", "gca_swa_fwd")
 
 
 class GcaParams(ctypes.Structure):
@@ -36,6 +36,12 @@ class GcaParams(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("softmax_off_by_one", ctypes.c_int),
                 ("include_self", ctypes.c_int), ("score_scale", ctypes.c_float),
                 ("attn_scale", ctypes.c_float)]
+
+
+class GcaSwaParams(ctypes.Structure):
+    """Mirror of gca_swa_params_t."""
+    _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("H", ctypes.c_int), ("d", ctypes.c_int),
+                ("window", ctypes.c_int), ("dtype", ctypes.c_int), ("attn_scale", ctypes.c_float)]
 
 
 class GcaError(RuntimeError):
@@ -70,6 +76,7 @@ def load() -> ctypes.CDLL:
             "gca_decode_retrieve_noalloc": ([vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp],
                                             i32),
             "gca_gather_chunks": ([vp, vp, i32, sz, vp, i32, vp, vp, vp, vp], i32),
+            "gca_swa_fwd": ([ctypes.POINTER(GcaSwaParams), vp, vp, vp, vp, vp, vp], i32),
             "gca_get_status": ([vp], i32),
             "gca_status_string": ([i32], ctypes.c_char_p),
             "gca_last_launch_count": ([], i32),

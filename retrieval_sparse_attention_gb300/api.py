@@ -17,7 +17,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import GCA_BF16, GCA_F32, GcaError, GcaParams
+from ._lib import GCA_BF16, GCA_F32, GcaError, GcaParams, GcaSwaParams
 
 _DT = {torch.bfloat16: GCA_BF16, torch.float32: GCA_F32}
 
@@ -133,6 +133,26 @@ def gca_gather_chunks(src_k, src_v, n_src, chunk_bytes, idx, topk, dst_k, dst_v,
     _check("gca_gather_chunks", _lib.load().gca_gather_chunks(
         _pa(src_k), _pa(src_v), n_src, chunk_bytes, _p(idx), topk, _p(dst_k), _p(dst_v),
         _p(dst_idx), _stream(stream)))
+
+
+def make_swa_params(*, B, L, H, d, window, dtype=torch.bfloat16, attn_scale=0.0) -> GcaSwaParams:
+    return GcaSwaParams(B=B, L=L, H=H, d=d, window=window, dtype=dtype_code(dtype),
+                        attn_scale=float(attn_scale))
+
+
+def gca_swa_fwd(params: GcaSwaParams, q, k, v, o, lse, stream=None):
+    _check("gca_swa_fwd", _lib.load().gca_swa_fwd(ctypes.byref(params), _p(q), _p(k), _p(v), _p(o),
+                                                  _p(lse), _stream(stream)))
+
+
+def swa_fwd(q, k, v, *, window, attn_scale=0.0, with_lse=True):
+    """Sliding-window self-attention: q, k, v [B, L, H, d] -> (o, lse [B, L, H])."""
+    B, L, H, d = q.shape
+    p = make_swa_params(B=B, L=L, H=H, d=d, window=window, dtype=q.dtype, attn_scale=attn_scale)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, L, H, dtype=torch.float32, device=q.device) if with_lse else None
+    gca_swa_fwd(p, q, k, v, o, lse)
+    return o, lse
 
 
 def gather_chunks(cache_k, cache_v, idx):

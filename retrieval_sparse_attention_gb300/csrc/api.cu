@@ -191,6 +191,34 @@ gca_status_t gca_fwd(const gca_params_t* params, const void* q, const void* k, c
     return r;
 }
 
+namespace {
+gca_status_t swa_check(const gca_swa_params_t* p) {
+    if (!p) return GCA_ERR_INVALID_ARG;
+    if (p->B < 1 || p->L < 1 || p->H < 1 || p->d < 1 || p->window < 1) return GCA_ERR_INVALID_ARG;
+    if (p->dtype != GCA_BF16 && p->dtype != GCA_F32) return GCA_ERR_INVALID_ARG;
+    if (!(p->attn_scale >= 0.f)) return GCA_ERR_INVALID_ARG;
+    if (p->dtype != GCA_BF16 || p->d != 64) return GCA_ERR_UNSUPPORTED;
+    if ((long long)p->B * p->L >= (1ll << 31) || p->H > 1024) return GCA_ERR_UNSUPPORTED;
+    return GCA_OK;
+}
+}  // namespace
+
+gca_status_t gca_swa_fwd(const gca_swa_params_t* params, const void* q, const void* k,
+                         const void* v, void* o, float* lse, void* stream) {
+    gca_status_t r = swa_check(params);
+    if (r != GCA_OK) return r;
+    if ((r = check_ptrs({q, k, v, o})) != GCA_OK) return r;
+    if (lse && !aligned16(lse)) return GCA_ERR_INVALID_ARG;
+    int* st = status_ptr();
+    if (!st) return GCA_ERR_CUDA;
+    const float scale = params->attn_scale > 0.f ? params->attn_scale : 1.0f / sqrtf((float)params->d);
+    int n = 0;
+    r = from_cuda(launch_swa_fwd_tc(params->B, params->L, params->H, params->window, scale, q, k, v, o,
+                                    lse, st, static_cast<cudaStream_t>(stream), &n));
+    if (r == GCA_OK) t_launches = n;
+    return r;
+}
+
 size_t gca_bwd_workspace_size(const gca_params_t* params) {
     Shape s;
     if (make_shape(params, true, &s) != GCA_OK) return 0;

@@ -1,0 +1,434 @@
+// attn_swa_tc.cu -- sliding-window causal self-attention on the Blackwell tensor
+// cores (bf16, d = 64): the fixed-size window self-attention that a DRT layer
+// runs before its GCA module (paper summary section 1: top-k past chunks
+// combined with sliding-window self-attention; section 4.1.2: a 512-token
+// window; the GCA modules are appended after the attention modules).
+//
+// Token t of a sequence attends to the keys max(0, t - W + 1) .. t:
+//   o_t = sum_s softmax_s(attn_scale q_t . k_s) v_s,  lse_t = ln sum_s exp(...).
+//
+// Design (one persistent CTA per SM, 11 warps, warp-specialised):
+//   item       (batch row, 128-token query tile, head); keys come in tiles of
+//              128, so both products are M = 128 MMAs (full rate); for
+//              W = 512 an item needs at most 5 key tiles, of which only the
+//              first (window edge) and the last (causal diagonal) are masked.
+//   warp 0     producer: TMA of the Q tile and of each key tile's K and V
+//              (box 64 x 128, 128-byte swizzle) into a 3-stage ring.
+//   warp 1     S issuer and TMEM owner: S = Q K^T into the item's warpgroup's
+//              S buffer (128 columns).
+//   warp 2     P V issuer: O += P V into the warpgroup's O accumulator.
+//   warps 3-10 two softmax warpgroups owning alternate items (the online
+//              softmax of a row lives in one thread's registers); producer
+//              and issuers walk the two current items' tiles interleaved, so
+//              one warpgroup's softmax overlaps the other's products.
+// Online softmax with a stale running max: P = exp2(s' - m) is written
+// unnormalised; O (TMEM) and the running sum are rescaled only when a tile's
+// max exceeds m by more than 2^8, which keeps every P below 256 and the result
+// exact up to rounding.  The rescale reads, scales and writes O in TMEM after
+// the previous tile's P V has completed.
+// Every mbarrier wait is bounded (status GCA_ERR_TIMEOUT, then the CTA winds down).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace gca {
+namespace {
+
+using namespace tc;
+using tcx::fast_exp2;
+using tcx::kLn2;
+using tcx::kLog2e;
+using tcx::Ring;
+
+constexpr int kThreads = 352;          // producer, 2 MMA issuers, 2 softmax warpgroups
+constexpr int BM = 128;                // query rows per item (MMA M)
+constexpr int BN = 128;                // keys per tile (MMA N of S)
+constexpr int STAGES = 3;
+constexpr int TILE = 128 * 128;        // 128 rows x 64 bf16: a Q, K or V tile
+constexpr int STAGE_BYTES = 2 * TILE;  // K tile then V tile
+constexpr int P_BLOCK = BM * 128;      // 64 keys of P for the 128 rows
+constexpr int P_BYTES = 2 * P_BLOCK;   // 128 keys
+constexpr int OFF_Q = 0;               // one Q tile per warpgroup
+constexpr int OFF_KV = 2 * TILE;
+constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;   // one P buffer per warpgroup
+constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;        // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0;          // S buffer of warpgroup w at w * 128
+constexpr uint32_t COL_O = 256;        // O accumulator of warpgroup w at 256 + w * 64
+constexpr float kRescaleLog2 = 8.f;
+
+struct SwaArgs {
+    __nv_bfloat16* o;
+    float* lse;              // [B, L, H] or null
+    int* status;
+    int B, L, H, W, nQT;     // nQT = query tiles per row
+    float scale_log2;        // attn_scale * log2(e)
+    int n_items;
+};
+
+struct __align__(8) Bars {
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[STAGES], kv_empty[STAGES];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full[2], p_empty[2];
+    uint64_t o_full[2], o_empty[2];
+    uint64_t done, done2;
+    uint32_t tmem;
+    int abort;
+};
+
+__device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
+__device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
+
+// Item -> (batch row, query tile, head), its first key tile and key tile count.
+struct Item {
+    int b, qt, h, k0, nt;
+};
+__device__ __forceinline__ Item decode_item(const SwaArgs& a, int item) {
+    Item it;
+    it.h = item % a.H;
+    const int bq = item / a.H;
+    it.qt = bq % a.nQT;
+    it.b = bq / a.nQT;
+    int lo = it.qt * BM - a.W + 1;
+    if (lo < 0) lo = 0;
+    it.k0 = lo / BN;
+    it.nt = it.qt - it.k0 + 1;          // key tiles k0 .. qt (BN == BM)
+    return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const SwaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ Bars sb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
+    const int stride = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sb.q_full[i], 1);
+            mbar_init(&sb.q_empty[i], 1);
+            mbar_init(&sb.s_full[i], 1);
+            mbar_init(&sb.s_empty[i], 128);
+            mbar_init(&sb.p_full[i], 128);
+            mbar_init(&sb.p_empty[i], 1);
+            mbar_init(&sb.o_full[i], 1);
+            mbar_init(&sb.o_empty[i], 128);
+        }
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&sb.kv_full[i], 1);
+            mbar_init(&sb.kv_empty[i], 1);
+        }
+        mbar_init(&sb.done, 1);
+        mbar_init(&sb.done2, 1);
+        sb.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sb.tmem, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sb.tmem;
+
+    // The CTA's items are blockIdx.x + k * gridDim.x; pair p holds k = 2p (warpgroup 0)
+    // and k = 2p + 1 (warpgroup 1).  Producer and issuers walk a pair's tiles as
+    // (wg 0, tile 0), (wg 1, tile 0), (wg 0, tile 1), ...
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            Ring kv{0, 0};
+            int kq[2] = {0, 0};
+            bool kv_out[STAGES] = {}, q_out[2] = {false, false};
+            uint32_t kv_ph[STAGES] = {}, q_ph[2] = {0, 0};
+            bool ok = true;
+            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
+                Item it[2];
+                int n[2];
+                for (int w = 0; w < 2; ++w) {
+                    const int e = e0 + w * stride;
+                    n[w] = 0;
+                    if (e < a.n_items) { it[w] = decode_item(a, e); n[w] = it[w].nt; }
+                }
+                for (int w = 0; w < 2 && ok; ++w) {
+                    if (n[w] == 0) continue;
+                    if (!wait(&sb.q_empty[w], empty_par(kq[w]))) { ok = false; break; }
+                    mbar_arrive_expect_tx(&sb.q_full[w], TILE);
+                    tma_load_2d(sm + OFF_Q + w * TILE, &tq, &sb.q_full[w], it[w].h * 64,
+                                it[w].b * a.L + it[w].qt * BM);
+                    q_out[w] = true;
+                    q_ph[w] = full_par(kq[w]);
+                    ++kq[w];
+                }
+                const int nmax = n[0] > n[1] ? n[0] : n[1];
+                for (int j = 0; j < nmax && ok; ++j)
+                    for (int w = 0; w < 2; ++w) {
+                        if (j >= n[w]) continue;
+                        if (!wait(&sb.kv_empty[kv.i], kv.ph ^ 1u)) { ok = false; break; }
+                        uint8_t* stg = sm + OFF_KV + kv.i * STAGE_BYTES;
+                        const int y = it[w].b * a.L + (it[w].k0 + j) * BN;
+                        mbar_arrive_expect_tx(&sb.kv_full[kv.i], 2 * TILE);
+                        tma_load_2d(stg, &tk, &sb.kv_full[kv.i], it[w].h * 64, y);
+                        tma_load_2d(stg + TILE, &tv, &sb.kv_full[kv.i], it[w].h * 64, y);
+                        kv_out[kv.i] = true;
+                        kv_ph[kv.i] = kv.ph;
+                        kv.next(STAGES);
+                    }
+            }
+            // no copy may still be writing shared memory when the CTA exits
+            for (int i = 0; i < STAGES; ++i)
+                if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < 2; ++i)
+                if (q_out[i]) mbar_wait(&sb.q_full[i], q_ph[i], nullptr, 100000000ull);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ S issuer
+        if (lane == 0) {
+            Ring kv{0, 0};
+            int kq[2] = {0, 0}, ts[2] = {0, 0};
+            bool issued = false, ok = true;
+            const uint32_t id_s = idesc_bf16(BM, BN, false, false);
+            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
+                int n[2];
+                for (int w = 0; w < 2; ++w) {
+                    const int e = e0 + w * stride;
+                    n[w] = e < a.n_items ? decode_item(a, e).nt : 0;
+                }
+                const int nmax = n[0] > n[1] ? n[0] : n[1];
+                for (int j = 0; j < nmax && ok; ++j)
+                    for (int w = 0; w < 2; ++w) {
+                        if (j >= n[w]) continue;
+                        if ((j == 0 && !wait(&sb.q_full[w], full_par(kq[w]))) ||
+                            !wait(&sb.kv_full[kv.i], kv.ph) ||
+                            !wait(&sb.s_empty[w], empty_par(ts[w]))) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t qaddr = smem_u32(sm + OFF_Q + w * TILE);
+                        const uint32_t kaddr = smem_u32(sm + OFF_KV + kv.i * STAGE_BYTES);
+                        tcx::mma_kmajor_k64(tmem + COL_S + w * 128, qaddr, kaddr, id_s, 0);
+                        mma_commit(&sb.s_full[w]);
+                        issued = true;
+                        ++ts[w];
+                        if (j == n[w] - 1) {
+                            mma_commit(&sb.q_empty[w]);    // Q is read only by these products
+                            ++kq[w];
+                        }
+                        kv.next(STAGES);
+                    }
+            }
+            if (issued) {
+                mma_commit(&sb.done);
+                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ P V issuer
+        if (lane == 0) {
+            Ring kv{0, 0};
+            int ko[2] = {0, 0}, tp[2] = {0, 0};
+            bool issued = false, ok = true;
+            const uint32_t id_o = idesc_bf16(BM, 64, false, true);
+            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
+                int n[2];
+                for (int w = 0; w < 2; ++w) {
+                    const int e = e0 + w * stride;
+                    n[w] = e < a.n_items ? decode_item(a, e).nt : 0;
+                }
+                const int nmax = n[0] > n[1] ? n[0] : n[1];
+                for (int j = 0; j < nmax && ok; ++j)
+                    for (int w = 0; w < 2; ++w) {
+                        if (j >= n[w]) continue;
+                        if ((j == 0 && !wait(&sb.o_empty[w], empty_par(ko[w]))) ||
+                            !wait(&sb.p_full[w], full_par(tp[w]))) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t paddr = smem_u32(sm + OFF_P + w * P_BYTES);
+                        const uint32_t vaddr = smem_u32(sm + OFF_KV + kv.i * STAGE_BYTES + TILE);
+                        tcx::mma_kmajor_mnmajor<8>(tmem + COL_O + w * 64, paddr, P_BLOCK, vaddr, id_o,
+                                                   j > 0);
+                        // this tile's S is complete (its P exists): the stage may be reused
+                        mma_commit(&sb.kv_empty[kv.i]);
+                        mma_commit(&sb.p_empty[w]);
+                        issued = true;
+                        ++tp[w];
+                        if (j == n[w] - 1) {
+                            mma_commit(&sb.o_full[w]);
+                            ++ko[w];
+                        }
+                        kv.next(STAGES);
+                    }
+            }
+            if (issued) {
+                mma_commit(&sb.done2);
+                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int wg = (warp - 3) >> 2;
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;                 // TMEM lane = query row of the tile
+        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+        const uint32_t ts_addr = tmem + lane_base + COL_S + wg * 128;
+        const uint32_t to_addr = tmem + lane_base + COL_O + wg * 64;
+        int ts = 0, ko = 0;
+        bool ok = true;
+        for (int item = blockIdx.x + wg * stride; item < a.n_items && ok; item += 2 * stride) {
+            const Item it = decode_item(a, item);
+            const int t0 = it.qt * BM;
+            const int t = t0 + row;                     // this thread's token
+            float m = -INFINITY;                        // running max of s * scale * log2(e)
+            float l = 0.f;                              // running sum of exp2(. - m)
+            for (int j = 0; j < it.nt; ++j) {
+                if (!wait(&sb.s_full[wg], full_par(ts))) { ok = false; break; }
+                tc_fence_after();
+                float x[BN];
+#pragma unroll
+                for (int ci = 0; ci < BN / 16; ++ci) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(ts_addr + 16 * ci, r);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[u]);
+                }
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sb.s_empty[wg]);
+                const int kbase = (it.k0 + j) * BN;
+                if (kbase + BN - 1 > t0 || kbase < t0 + BM - a.W) {      // tile crosses a mask edge
+                    const int lo = t - a.W + 1;
+#pragma unroll
+                    for (int i = 0; i < BN; ++i) {
+                        const int s = kbase + i;
+                        if (s > t || s < lo) x[i] = -INFINITY;
+                    }
+                }
+                float mt = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < BN; ++i) mt = fmaxf(mt, x[i]);
+                const float mts = mt * a.scale_log2;
+                float alpha = 1.f;
+                bool resc = false;
+                if (mts > m + kRescaleLog2) {
+                    if (m != -INFINITY) {
+                        resc = true;
+                        alpha = fast_exp2(m - mts);
+                    }
+                    m = mts;
+                }
+                l *= alpha;
+                const float mu = (m == -INFINITY) ? 0.f : m;
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int i = 0; i < BN / 2; ++i) {
+                    const float p0 = fast_exp2(fmaf(x[2 * i], a.scale_log2, -mu));
+                    const float p1 = fast_exp2(fmaf(x[2 * i + 1], a.scale_log2, -mu));
+                    l += p0 + p1;
+                    pk[i] = tcx::pack_bf16(p0, p1);
+                }
+                // the previous tile's P V has completed: O is stable, P buffer free
+                if (!wait(&sb.p_empty[wg], empty_par(ts))) { ok = false; break; }
+                if (__any_sync(0xffffffffu, resc)) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ci = 0; ci < 4; ++ci) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(to_addr + 16 * ci, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
+                        tmem_st_32x32b_x16(to_addr + 16 * ci, r);
+                    }
+                    tmem_wait_st();
+                }
+                uint8_t* pbase = sm + OFF_P + wg * P_BYTES + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < BN / 8; ++ch) {
+                    const int blk = ch >> 3, cc = ch & 7;
+                    *reinterpret_cast<uint4*>(pbase + blk * P_BLOCK + ((cc ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&sb.p_full[wg]);
+                ++ts;
+            }
+            if (!ok) break;
+            // epilogue: O / l and lse of this thread's row
+            if (!wait(&sb.o_full[wg], full_par(ko))) break;
+            ++ko;
+            tc_fence_after();
+            uint32_t r[4][16];
+#pragma unroll
+            for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(to_addr + 16 * ci, r[ci]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&sb.o_empty[wg]);
+            if (t < a.L) {
+                const size_t tok = (size_t)it.b * a.L + t;
+                const float inv = 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(a.o + (tok * a.H + it.h) * 64);
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) {
+                    float f[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) f[u] = __uint_as_float(r[ci][u]);
+                    dst[2 * ci] = tcx::pack8(f, inv);
+                    dst[2 * ci + 1] = tcx::pack8(f + 8, inv);
+                }
+                if (a.lse) a.lse[tok * a.H + it.h] = (m + log2f(l)) * kLn2;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_swa_fwd_tc(int B, int L, int H, int W, float attn_scale, const void* q,
+                              const void* k, const void* v, void* o, float* lse, int* status,
+                              cudaStream_t st, int* launches) {
+    CUtensorMap tq, tk, tv;
+    const uint64_t rows = (uint64_t)B * L, cols = (uint64_t)H * 64;
+    if (!encode_bf16_rows(&tq, q, rows, cols, BM) || !encode_bf16_rows(&tk, k, rows, cols, BN) ||
+        !encode_bf16_rows(&tv, v, rows, cols, BN))
+        return cudaErrorInvalidValue;
+    SwaArgs a;
+    a.o = static_cast<__nv_bfloat16*>(o);
+    a.lse = lse;
+    a.status = status;
+    a.B = B; a.L = L; a.H = H; a.W = W;
+    a.nQT = (L + BM - 1) / BM;
+    a.scale_log2 = attn_scale * kLog2e;
+    a.n_items = B * a.nQT * H;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = a.n_items < sms ? a.n_items : sms;
+    cudaError_t e = cudaFuncSetAttribute(gca_swa_fwd_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    GCA_LAUNCH("swa_fwd_tc", st, gca_swa_fwd_tc_kernel<<<grid, kThreads, SMEM, st>>>(tq, tk, tv, a));
+    if ((e = cudaGetLastError()) == cudaSuccess) *launches += 1;
+    return e;
+}
+
+}  // namespace gca
