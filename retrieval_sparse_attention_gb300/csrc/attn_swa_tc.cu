@@ -12,8 +12,11 @@
 //              128, so both products are M = 128 MMAs (full rate); for
 //              W = 512 an item needs at most 5 key tiles, of which only the
 //              first (window edge) and the last (causal diagonal) are masked.
-//   warp 0     producer: TMA of the Q tile and of each key tile's K and V
-//              (box 64 x 128, 128-byte swizzle) into a 3-stage ring.
+//   warp 0     producer: TMA (3-D maps over [B, L, H*d]: rows outside a
+//              sequence read as zeros) of the Q tile (lane 0), each key
+//              tile's K (lane 0) and V (lane 1) into separate 4-stage rings:
+//              a K stage is free once its S product completes, long before
+//              the V stage, which waits for P V.
 //   warp 1     S issuer and TMEM owner: S = Q K^T into the item's warpgroup's
 //              S buffer (128 columns).
 //   warp 2     P V issuer: O += P V into the warpgroup's O accumulator.
@@ -26,6 +29,9 @@
 // max exceeds m by more than 2^8, which keeps every P below 256 and the result
 // exact up to rounding.  The rescale reads, scales and writes O in TMEM after
 // the previous tile's P V has completed.
+// Epilogue: O / l in bf16 is written into the warpgroup's idle P buffer in the
+// swizzled tile layout and stored with one TMA tensor store (rows past the
+// sequence end are clipped by the tensor map).
 // Every mbarrier wait is bounded (status GCA_ERR_TIMEOUT, then the CTA winds down).
 #include <math.h>
 
@@ -47,14 +53,14 @@ using tcx::Ring;
 constexpr int kThreads = 352;          // producer, 2 MMA issuers, 2 softmax warpgroups
 constexpr int BM = 128;                // query rows per item (MMA M)
 constexpr int BN = 128;                // keys per tile (MMA N of S)
-constexpr int STAGES = 3;
-constexpr int TILE = 128 * 128;        // 128 rows x 64 bf16: a Q, K or V tile
-constexpr int STAGE_BYTES = 2 * TILE;  // K tile then V tile
+constexpr int STAGES = 4;               // depth of the K ring and of the V ring
+constexpr int TILE = 128 * 128;        // 128 rows x 64 bf16: a Q, K, V or O tile
 constexpr int P_BLOCK = BM * 128;      // 64 keys of P for the 128 rows
 constexpr int P_BYTES = 2 * P_BLOCK;   // 128 keys
 constexpr int OFF_Q = 0;               // one Q tile per warpgroup
-constexpr int OFF_KV = 2 * TILE;
-constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;   // one P buffer per warpgroup
+constexpr int OFF_K = 2 * TILE;
+constexpr int OFF_V = OFF_K + STAGES * TILE;
+constexpr int OFF_P = OFF_V + STAGES * TILE;            // one P buffer per warpgroup
 constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;        // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;          // S buffer of warpgroup w at w * 128
@@ -72,7 +78,9 @@ struct SwaArgs {
 
 struct __align__(8) Bars {
     uint64_t q_full[2], q_empty[2];
-    uint64_t kv_full[STAGES], kv_empty[STAGES];
+    uint64_t k_full[STAGES], k_empty[STAGES];
+    uint64_t v_full[STAGES], v_empty[STAGES];
+    uint64_t epi_full[2], epi_free[2];    // O staged in the P buffer / its store has read it
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
@@ -103,7 +111,8 @@ __device__ __forceinline__ Item decode_item(const SwaArgs& a, int item) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const SwaArgs a) {
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                      const SwaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -124,8 +133,14 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             mbar_init(&sb.o_empty[i], 128);
         }
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&sb.kv_full[i], 1);
-            mbar_init(&sb.kv_empty[i], 1);
+            mbar_init(&sb.k_full[i], 1);
+            mbar_init(&sb.k_empty[i], 1);
+            mbar_init(&sb.v_full[i], 1);
+            mbar_init(&sb.v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sb.epi_full[i], 128);
+            mbar_init(&sb.epi_free[i], 1);
         }
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
@@ -136,6 +151,7 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+        prefetch_tmap(&to);
     }
     if (warp == 1) {
         tmem_alloc(&sb.tmem, TMEM_COLS);
@@ -151,11 +167,18 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     // (wg 0, tile 0), (wg 1, tile 0), (wg 0, tile 1), ...
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            Ring kv{0, 0};
+        // lane 0: Q tiles and the K ring; lane 1: the V ring (each walks the same
+        // sequence of positions and waits on its own barriers)
+        if (lane < 2) {
+            const bool kl = lane == 0;
+            Ring rg{0, 0};
             int kq[2] = {0, 0};
-            bool kv_out[STAGES] = {}, q_out[2] = {false, false};
-            uint32_t kv_ph[STAGES] = {}, q_ph[2] = {0, 0};
+            bool out[STAGES] = {}, q_out[2] = {false, false};
+            uint32_t ph[STAGES] = {}, q_ph[2] = {0, 0};
+            uint64_t* full = kl ? sb.k_full : sb.v_full;
+            uint64_t* empty = kl ? sb.k_empty : sb.v_empty;
+            const CUtensorMap* map = kl ? &tk : &tv;
+            uint8_t* ring = sm + (kl ? OFF_K : OFF_V);
             bool ok = true;
             for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
                 Item it[2];
@@ -165,34 +188,33 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     n[w] = 0;
                     if (e < a.n_items) { it[w] = decode_item(a, e); n[w] = it[w].nt; }
                 }
-                for (int w = 0; w < 2 && ok; ++w) {
-                    if (n[w] == 0) continue;
-                    if (!wait(&sb.q_empty[w], empty_par(kq[w]))) { ok = false; break; }
-                    mbar_arrive_expect_tx(&sb.q_full[w], TILE);
-                    tma_load_2d(sm + OFF_Q + w * TILE, &tq, &sb.q_full[w], it[w].h * 64,
-                                it[w].b * a.L + it[w].qt * BM);
-                    q_out[w] = true;
-                    q_ph[w] = full_par(kq[w]);
-                    ++kq[w];
-                }
+                if (kl)
+                    for (int w = 0; w < 2 && ok; ++w) {
+                        if (n[w] == 0) continue;
+                        if (!wait(&sb.q_empty[w], empty_par(kq[w]))) { ok = false; break; }
+                        mbar_arrive_expect_tx(&sb.q_full[w], TILE);
+                        tma_load_3d(sm + OFF_Q + w * TILE, &tq, &sb.q_full[w], it[w].h * 64,
+                                    it[w].qt * BM, it[w].b);
+                        q_out[w] = true;
+                        q_ph[w] = full_par(kq[w]);
+                        ++kq[w];
+                    }
                 const int nmax = n[0] > n[1] ? n[0] : n[1];
                 for (int j = 0; j < nmax && ok; ++j)
                     for (int w = 0; w < 2; ++w) {
                         if (j >= n[w]) continue;
-                        if (!wait(&sb.kv_empty[kv.i], kv.ph ^ 1u)) { ok = false; break; }
-                        uint8_t* stg = sm + OFF_KV + kv.i * STAGE_BYTES;
-                        const int y = it[w].b * a.L + (it[w].k0 + j) * BN;
-                        mbar_arrive_expect_tx(&sb.kv_full[kv.i], 2 * TILE);
-                        tma_load_2d(stg, &tk, &sb.kv_full[kv.i], it[w].h * 64, y);
-                        tma_load_2d(stg + TILE, &tv, &sb.kv_full[kv.i], it[w].h * 64, y);
-                        kv_out[kv.i] = true;
-                        kv_ph[kv.i] = kv.ph;
-                        kv.next(STAGES);
+                        if (!wait(&empty[rg.i], rg.ph ^ 1u)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&full[rg.i], TILE);
+                        tma_load_3d(ring + rg.i * TILE, map, &full[rg.i], it[w].h * 64,
+                                    (it[w].k0 + j) * BN, it[w].b);
+                        out[rg.i] = true;
+                        ph[rg.i] = rg.ph;
+                        rg.next(STAGES);
                     }
             }
             // no copy may still be writing shared memory when the CTA exits
             for (int i = 0; i < STAGES; ++i)
-                if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
+                if (out[i]) mbar_wait(&full[i], ph[i], nullptr, 100000000ull);
             for (int i = 0; i < 2; ++i)
                 if (q_out[i]) mbar_wait(&sb.q_full[i], q_ph[i], nullptr, 100000000ull);
         }
@@ -214,13 +236,14 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     for (int w = 0; w < 2; ++w) {
                         if (j >= n[w]) continue;
                         if ((j == 0 && !wait(&sb.q_full[w], full_par(kq[w]))) ||
-                            !wait(&sb.kv_full[kv.i], kv.ph) ||
+                            !wait(&sb.k_full[kv.i], kv.ph) ||
                             !wait(&sb.s_empty[w], empty_par(ts[w]))) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t qaddr = smem_u32(sm + OFF_Q + w * TILE);
-                        const uint32_t kaddr = smem_u32(sm + OFF_KV + kv.i * STAGE_BYTES);
+                        const uint32_t kaddr = smem_u32(sm + OFF_K + kv.i * TILE);
                         tcx::mma_kmajor_k64(tmem + COL_S + w * 128, qaddr, kaddr, id_s, 0);
                         mma_commit(&sb.s_full[w]);
+                        mma_commit(&sb.k_empty[kv.i]);     // K is read only by this product
                         issued = true;
                         ++ts[w];
                         if (j == n[w] - 1) {
@@ -253,14 +276,14 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     for (int w = 0; w < 2; ++w) {
                         if (j >= n[w]) continue;
                         if ((j == 0 && !wait(&sb.o_empty[w], empty_par(ko[w]))) ||
-                            !wait(&sb.p_full[w], full_par(tp[w]))) { ok = false; break; }
+                            !wait(&sb.p_full[w], full_par(tp[w])) ||
+                            !wait(&sb.v_full[kv.i], kv.ph)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t paddr = smem_u32(sm + OFF_P + w * P_BYTES);
-                        const uint32_t vaddr = smem_u32(sm + OFF_KV + kv.i * STAGE_BYTES + TILE);
+                        const uint32_t vaddr = smem_u32(sm + OFF_V + kv.i * TILE);
                         tcx::mma_kmajor_mnmajor<8>(tmem + COL_O + w * 64, paddr, P_BLOCK, vaddr, id_o,
                                                    j > 0);
-                        // this tile's S is complete (its P exists): the stage may be reused
-                        mma_commit(&sb.kv_empty[kv.i]);
+                        mma_commit(&sb.v_empty[kv.i]);
                         mma_commit(&sb.p_empty[w]);
                         issued = true;
                         ++tp[w];
@@ -311,8 +334,8 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     const int lo = t - a.W + 1;
 #pragma unroll
                     for (int i = 0; i < BN; ++i) {
-                        const int s = kbase + i;
-                        if (s > t || s < lo) x[i] = -INFINITY;
+                        const int sk = kbase + i;
+                        if (sk > t || sk < lo) x[i] = -INFINITY;
                     }
                 }
                 float mt = -INFINITY;
@@ -339,7 +362,9 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     pk[i] = tcx::pack_bf16(p0, p1);
                 }
                 // the previous tile's P V has completed: O is stable, P buffer free
-                if (!wait(&sb.p_empty[wg], empty_par(ts))) { ok = false; break; }
+                // (for a first tile: also the previous item's O store has read it)
+                if (!wait(&sb.p_empty[wg], empty_par(ts)) ||
+                    (j == 0 && ko > 0 && !wait(&sb.epi_free[wg], full_par(ko - 1)))) { ok = false; break; }
                 if (__any_sync(0xffffffffu, resc)) {
                     tc_fence_after();
 #pragma unroll
@@ -366,9 +391,9 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 ++ts;
             }
             if (!ok) break;
-            // epilogue: O / l and lse of this thread's row
+            // epilogue: O / l of this thread's row into the (idle) P buffer in the
+            // swizzled tile layout, then one TMA tensor store of the whole tile
             if (!wait(&sb.o_full[wg], full_par(ko))) break;
-            ++ko;
             tc_fence_after();
             uint32_t r[4][16];
 #pragma unroll
@@ -376,21 +401,32 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&sb.o_empty[wg]);
-            if (t < a.L) {
-                const size_t tok = (size_t)it.b * a.L + t;
-                const float inv = 1.f / l;
-                uint4* dst = reinterpret_cast<uint4*>(a.o + (tok * a.H + it.h) * 64);
+            uint8_t* obuf = sm + OFF_P + wg * P_BYTES;
+            const float inv = 1.f / l;
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci) {
-                    float f[16];
+            for (int ci = 0; ci < 4; ++ci) {
+                float f[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) f[u] = __uint_as_float(r[ci][u]);
-                    dst[2 * ci] = tcx::pack8(f, inv);
-                    dst[2 * ci + 1] = tcx::pack8(f + 8, inv);
-                }
-                if (a.lse) a.lse[tok * a.H + it.h] = (m + log2f(l)) * kLn2;
+                for (int u = 0; u < 16; ++u) f[u] = __uint_as_float(r[ci][u]);
+                *reinterpret_cast<uint4*>(obuf + row * 128 + (((2 * ci) ^ (row & 7)) << 4)) =
+                    tcx::pack8(f, inv);
+                *reinterpret_cast<uint4*>(obuf + row * 128 + (((2 * ci + 1) ^ (row & 7)) << 4)) =
+                    tcx::pack8(f + 8, inv);
             }
+            fence_proxy_async_smem();
+            mbar_arrive(&sb.epi_full[wg]);
+            if (t < a.L && a.lse) a.lse[((size_t)it.b * a.L + t) * a.H + it.h] = (m + log2f(l)) * kLn2;
+            if (qd == 0 && lane == 0) {          // one thread of the warpgroup stores the tile
+                if (!wait(&sb.epi_full[wg], full_par(ko))) break;
+                tma_store_3d(&to, obuf, it.h * 64, t0, it.b);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+                mbar_arrive(&sb.epi_free[wg]);
+            }
+            ++ko;
         }
+        // the last tile stores must be complete before the CTA exits
+        if (qd == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 
     tc_fence_before();
@@ -406,10 +442,10 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 cudaError_t launch_swa_fwd_tc(int B, int L, int H, int W, float attn_scale, const void* q,
                               const void* k, const void* v, void* o, float* lse, int* status,
                               cudaStream_t st, int* launches) {
-    CUtensorMap tq, tk, tv;
-    const uint64_t rows = (uint64_t)B * L, cols = (uint64_t)H * 64;
-    if (!encode_bf16_rows(&tq, q, rows, cols, BM) || !encode_bf16_rows(&tk, k, rows, cols, BN) ||
-        !encode_bf16_rows(&tv, v, rows, cols, BN))
+    CUtensorMap tq, tk, tv, to;
+    const uint64_t cols = (uint64_t)H * 64;
+    if (!encode_bf16_seq(&tq, q, B, L, cols, BM) || !encode_bf16_seq(&tk, k, B, L, cols, BN) ||
+        !encode_bf16_seq(&tv, v, B, L, cols, BN) || !encode_bf16_seq(&to, o, B, L, cols, BM))
         return cudaErrorInvalidValue;
     SwaArgs a;
     a.o = static_cast<__nv_bfloat16*>(o);
@@ -426,7 +462,7 @@ cudaError_t launch_swa_fwd_tc(int B, int L, int H, int W, float attn_scale, cons
     cudaError_t e = cudaFuncSetAttribute(gca_swa_fwd_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    GCA_LAUNCH("swa_fwd_tc", st, gca_swa_fwd_tc_kernel<<<grid, kThreads, SMEM, st>>>(tq, tk, tv, a));
+    GCA_LAUNCH("swa_fwd_tc", st, gca_swa_fwd_tc_kernel<<<grid, kThreads, SMEM, st>>>(tq, tk, tv, to, a));
     if ((e = cudaGetLastError()) == cudaSuccess) *launches += 1;
     return e;
 }

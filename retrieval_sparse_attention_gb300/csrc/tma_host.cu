@@ -46,6 +46,21 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool encode_bf16_seq(CUtensorMap* map, const void* base, uint64_t B, uint64_t L, uint64_t row_elems,
+                     uint32_t box_rows) {
+    std::call_once(g_once, resolve);
+    if (!g_encode) return false;
+    cuuint64_t dims[3] = {row_elems, L, B};
+    cuuint64_t strides[2] = {row_elems * 2, L * row_elems * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_f32_box(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
                     uint32_t box_cols, uint32_t box_rows) {
     std::call_once(g_once, resolve);
