@@ -50,7 +50,7 @@ def parse():
 CASES = {"fwd_b4": ("gpt2s_fwd_b4", 4, False), "fwdbwd_b4": ("gpt2s_fwdbwd_b8", 4, True),
          "fwdbwd_b8": ("gpt2s_fwdbwd_b8", 8, True), "long_s64_k16": ("long64k_S64_k16", 1, True),
          "long_s128_k8": ("long64k_S128_k8", 1, True), "decode": (None, 1, False),
-         "swa": ("swa", 8, False)}
+         "swa": ("swa", 8, False), "swa_bwd": ("swa", 8, True)}
 
 
 def peaks():
@@ -438,7 +438,14 @@ def extra_workloads(lib, api, inputs, dev, hbm, tflops):
                              "window": SWA_WINDOW, "us": round(us, 2),
                              "query_tokens_per_s": round(8 * 16384 / (us / 1e6), 1),
                              "roofline": swa_roofline(8, 16384, 12, 64, SWA_WINDOW, us / 1e3, hbm, tflops)}
-    del x
+    o, lse = api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)
+    g = swa_inputs(dev, seed=12)[0] * 8
+    us = _event_us(lambda i=0: api.swa_bwd(x[0], x[1], x[2], o, lse, g, window=SWA_WINDOW), n=10)
+    out["swa_bwd_b8_16k"] = {"kernel": "gca_swa_bwd", "B": 8, "L": 16384, "H": 12, "d": 64,
+                             "window": SWA_WINDOW, "us": round(us, 2),
+                             "roofline": swa_roofline(8, 16384, 12, 64, SWA_WINDOW, us / 1e3, hbm, tflops,
+                                                      backward=True)}
+    del x, o, lse, g
     return out
 
 
@@ -452,13 +459,15 @@ def swa_inputs(dev, B=8, L=16384, H=12, d=64, seed=11):
     return [(torch.randn(B, L, H, d, generator=g) * 0.125).to(torch.bfloat16).to(dev) for _ in range(3)]
 
 
-def swa_roofline(B, L, H, d, W, ms, hbm, tflops):
+def swa_roofline(B, L, H, d, W, ms, hbm, tflops, backward=False):
     """Slower of algorithmic bytes at HBM bandwidth and algorithmic FLOPs at
-    tensor peak.  Bytes: Q, K, V read and O written once (bf16), lse (fp32).
-    FLOPs: 4 d per (token, head, visible key); token t sees min(t + 1, W) keys."""
-    byts = 4 * B * L * H * d * 2 + B * L * H * 4
+    tensor peak.  Forward bytes: Q, K, V read and O written once (bf16), lse
+    (fp32); FLOPs: 4 d per (token, head, visible key), token t seeing
+    min(t + 1, W) keys.  Backward: Q, K, V, O, dO read and dQ, dK, dV written
+    once plus lse; 10 d FLOPs per (token, head, visible key)."""
+    byts = (8 if backward else 4) * B * L * H * d * 2 + B * L * H * 4
     keys = W * (W + 1) // 2 + (L - W) * W if L >= W else L * (L + 1) // 2
-    flops = 4.0 * d * B * H * keys
+    flops = (10.0 if backward else 4.0) * d * B * H * keys
     t_hbm, t_tc = byts / (hbm * 1e9), flops / (tflops * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     if bound == "hbm":
@@ -616,7 +625,12 @@ def run_case(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if name == "swa":
         x = swa_inputs(dev)
-        step = lambda: api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)
+        if backward:
+            o, lse = api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)
+            g = swa_inputs(dev, seed=12)[0] * 8
+            step = lambda: api.swa_bwd(x[0], x[1], x[2], o, lse, g, window=SWA_WINDOW)
+        else:
+            step = lambda: api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)
     elif name is None:
         hx = inputs.decode_inputs()
         lm, ql = hx["lm"].to(dev), hx["ql"].to(dev)

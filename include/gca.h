@@ -251,6 +251,23 @@ typedef struct {
 gca_status_t gca_swa_fwd(const gca_swa_params_t* params, const void* q, const void* k,
                          const void* v, void* o, float* lse, void* stream);
 
+/* Bytes of device workspace gca_swa_bwd needs. */
+size_t gca_swa_bwd_workspace_size(const gca_swa_params_t* params);
+
+/*
+ * gca_swa_bwd -- gradients of the sliding-window self-attention: for an
+ * upstream gradient dout, with p_ts the forward's probabilities,
+ * delta_t = dout_t . o_t and ds_ts = attn_scale p_ts (dout_t . v_s - delta_t):
+ *   dq_t = sum_s ds_ts k_s,  dk_s = sum_t ds_ts q_t,  dv_s = sum_t p_ts dout_t.
+ *   q, k, v, o, dout, dq, dk, dv [B, L, H, d]; lse [B, L, H] from gca_swa_fwd.
+ *   dq, dk, dv are fully overwritten; fp32 accumulation in a fixed order,
+ *   no atomics (bitwise reproducible).
+ *   workspace: >= gca_swa_bwd_workspace_size() bytes, 256-byte aligned.
+ */
+gca_status_t gca_swa_bwd(const gca_swa_params_t* params, const void* q, const void* k,
+                         const void* v, const void* o, const float* lse, const void* dout, void* dq,
+                         void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * gca_get_status -- synchronise `stream`, then return and clear the device
  * status word of the current device (GCA_OK if no device-side error was

@@ -25,7 +25,7 @@ EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
             "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc",
             "gca_score_topk_noisy", "gca_landmark_bwd_workspace_size", "gca_landmark_bwd",
-            "gca_gather_chunks", "gca_swa_fwd")
+            "gca_gather_chunks", "gca_swa_fwd", "gca_swa_bwd_workspace_size", "gca_swa_bwd")
 
 
 class GcaParams(ctypes.Structure):
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
                                             i32),
             "gca_gather_chunks": ([vp, vp, i32, sz, vp, i32, vp, vp, vp, vp], i32),
             "gca_swa_fwd": ([ctypes.POINTER(GcaSwaParams), vp, vp, vp, vp, vp, vp], i32),
+            "gca_swa_bwd_workspace_size": ([ctypes.POINTER(GcaSwaParams)], sz),
+            "gca_swa_bwd": ([ctypes.POINTER(GcaSwaParams)] + [vp] * 10 + [sz, vp], i32),
             "gca_get_status": ([vp], i32),
             "gca_status_string": ([i32], ctypes.c_char_p),
             "gca_last_launch_count": ([], i32),

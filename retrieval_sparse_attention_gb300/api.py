@@ -155,6 +155,27 @@ def swa_fwd(q, k, v, *, window, attn_scale=0.0, with_lse=True):
     return o, lse
 
 
+def gca_swa_bwd_workspace_size(params: GcaSwaParams) -> int:
+    return int(_lib.load().gca_swa_bwd_workspace_size(ctypes.byref(params)))
+
+
+def gca_swa_bwd(params: GcaSwaParams, q, k, v, o, lse, dout, dq, dk, dv, workspace, stream=None):
+    _check("gca_swa_bwd", _lib.load().gca_swa_bwd(
+        ctypes.byref(params), _p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv),
+        _p(workspace), workspace.numel(), _stream(stream)))
+
+
+def swa_bwd(q, k, v, o, lse, dout, *, window, attn_scale=0.0, workspace=None):
+    """Gradients of the sliding-window self-attention: returns (dq, dk, dv)."""
+    B, L, H, d = q.shape
+    p = make_swa_params(B=B, L=L, H=H, d=d, window=window, dtype=q.dtype, attn_scale=attn_scale)
+    if workspace is None:
+        workspace = torch.empty(gca_swa_bwd_workspace_size(p), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    gca_swa_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, workspace)
+    return dq, dk, dv
+
+
 def gather_chunks(cache_k, cache_v, idx):
     """cache_k/v [n_chunks, S, H, d] (device or pinned host) -> compact
     pools [1, topk*S, H, d] on the device and the remapped idx [1, 1, topk]."""

@@ -219,6 +219,30 @@ gca_status_t gca_swa_fwd(const gca_swa_params_t* params, const void* q, const vo
     return r;
 }
 
+size_t gca_swa_bwd_workspace_size(const gca_swa_params_t* params) {
+    if (swa_check(params) != GCA_OK) return 0;
+    return swa_bwd_workspace_bytes(params->B, params->L, params->H);
+}
+
+gca_status_t gca_swa_bwd(const gca_swa_params_t* params, const void* q, const void* k,
+                         const void* v, const void* o, const float* lse, const void* dout, void* dq,
+                         void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream) {
+    gca_status_t r = swa_check(params);
+    if (r != GCA_OK) return r;
+    if ((r = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != GCA_OK) return r;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GCA_ERR_WORKSPACE;
+    if (ws_bytes < swa_bwd_workspace_bytes(params->B, params->L, params->H)) return GCA_ERR_WORKSPACE;
+    int* st = status_ptr();
+    if (!st) return GCA_ERR_CUDA;
+    const float scale = params->attn_scale > 0.f ? params->attn_scale : 1.0f / sqrtf((float)params->d);
+    int n = 0;
+    r = from_cuda(launch_swa_bwd_tc(params->B, params->L, params->H, params->window, scale, q, k, v,
+                                    o, lse, dout, dq, dk, dv, workspace, st,
+                                    static_cast<cudaStream_t>(stream), &n));
+    if (r == GCA_OK) t_launches = n;
+    return r;
+}
+
 size_t gca_bwd_workspace_size(const gca_params_t* params) {
     Shape s;
     if (make_shape(params, true, &s) != GCA_OK) return 0;

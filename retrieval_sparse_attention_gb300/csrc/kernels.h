@@ -97,6 +97,11 @@ cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, vo
 cudaError_t launch_swa_fwd_tc(int B, int L, int H, int W, float attn_scale, const void* q,
                               const void* k, const void* v, void* o, float* lse, int* status,
                               cudaStream_t st, int* launches);
+size_t swa_bwd_workspace_bytes(int B, int L, int H);
+cudaError_t launch_swa_bwd_tc(int B, int L, int H, int W, float attn_scale, const void* q,
+                              const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, void* ws, int* status,
+                              cudaStream_t st, int* launches);
 cudaError_t launch_gather_chunks(const void* src_k, const void* src_v, int n_src, size_t chunk_bytes,
                                  const int32_t* idx, int topk, void* dst_k, void* dst_v,
                                  int32_t* dst_idx, int* status, cudaStream_t st, int* launches);

@@ -94,3 +94,67 @@ def test_unsupported_and_invalid():
     with pytest.raises(GcaError) as e:
         api.swa_fwd(q, k, v, window=0)
     assert e.value.code == 1
+
+
+def check_bwd(q, k, v, g, W):
+    qc, kc, vc, gc = (x.cuda() for x in (q, k, v, g))
+    o, lse = api.swa_fwd(qc, kc, vc, window=W)
+    dq, dk, dv = api.swa_bwd(qc, kc, vc, o, lse, gc, window=W)
+    torch.cuda.synchronize()
+    assert api.gca_get_status() == 0
+    rq, rk, rv = oracle.swa_bwd(f64(q), f64(k), f64(v), f64(g), W)
+    assert_close("dq", f64(dq), rq, BF16_ATOL, BF16_RTOL)
+    assert_close("dk", f64(dk), rk, BF16_ATOL, BF16_RTOL)
+    assert_close("dv", f64(dv), rv, BF16_ATOL, BF16_RTOL)
+    return dq, dk, dv
+
+
+def dout_like(q, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(q.shape, generator=g).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,L,H,W", [(2, 384, 2, 512), (1, 1000, 3, 200), (2, 640, 2, 64),
+                                     (1, 256, 1, 1), (1, 517, 2, 128), (1, 700, 2, 129),
+                                     (1, 1536, 4, 512), (3, 100, 1, 5000)])
+def test_bwd_every_element(B, L, H, W):
+    q, k, v = qkv(B, L, H, 64, seed=B * 1000 + L + W)
+    check_bwd(q, k, v, dout_like(q, 99), W)
+
+
+def test_bwd_full_size_sampled():
+    # dq of token t and dk/dv of key s depend only on the W-token neighbourhood:
+    # run the oracle on a slice that contains it and compare the row
+    B, L, H, d, W = 8, 16384, 12, 64, 512
+    q, k, v = qkv(B, L, H, d, seed=11)
+    g = dout_like(q, 12)
+    qc, kc, vc, gc = (x.cuda() for x in (q, k, v, g))
+    o, lse = api.swa_fwd(qc, kc, vc, window=W)
+    dq, dk, dv = api.swa_bwd(qc, kc, vc, o, lse, gc, window=W)
+    torch.cuda.synchronize()
+    assert api.gca_get_status() == 0
+    dq, dk, dv = f64(dq), f64(dk), f64(dv)
+    rng = np.random.default_rng(4)
+    picks = [(int(b), int(t)) for b, t in zip(rng.integers(0, B, 10), rng.integers(0, L, 10))]
+    picks += [(0, 0), (7, L - 1), (2, 511), (2, 512), (6, L - 512)]
+    for b, t in picks:
+        # dq_t needs tokens t-W+1 .. t; dk_t and dv_t need the queries t .. t+W-1
+        # and their windows: tokens t-W+1 .. t+W-1 (one more window of margin)
+        lo, s1 = max(0, t - 2 * W + 2), min(L, t + W)
+        sl = slice(lo, s1)
+        rq, rk, rv = oracle.swa_bwd(f64(q[b:b + 1, sl]), f64(k[b:b + 1, sl]), f64(v[b:b + 1, sl]),
+                                    f64(g[b:b + 1, sl]), W)
+        i = t - lo
+        assert_close("dq[%d,%d]" % (b, t), dq[b, t], rq[0, i], BF16_ATOL, BF16_RTOL)
+        assert_close("dk[%d,%d]" % (b, t), dk[b, t], rk[0, i], BF16_ATOL, BF16_RTOL)
+        assert_close("dv[%d,%d]" % (b, t), dv[b, t], rv[0, i], BF16_ATOL, BF16_RTOL)
+
+
+def test_bwd_deterministic():
+    q, k, v = (x.cuda() for x in qkv(2, 1024, 3, 64, seed=5))
+    g = dout_like(q, 6).cuda()
+    o, lse = api.swa_fwd(q, k, v, window=512)
+    a = api.swa_bwd(q, k, v, o, lse, g, window=512)
+    b = api.swa_bwd(q, k, v, o, lse, g, window=512)
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, b))
