@@ -50,7 +50,8 @@ def parse():
 CASES = {"fwd_b4": ("gpt2s_fwd_b4", 4, False), "fwdbwd_b4": ("gpt2s_fwdbwd_b8", 4, True),
          "fwdbwd_b8": ("gpt2s_fwdbwd_b8", 8, True), "long_s64_k16": ("long64k_S64_k16", 1, True),
          "long_s128_k8": ("long64k_S128_k8", 1, True), "decode": (None, 1, False),
-         "swa": ("swa", 8, False), "swa_bwd": ("swa", 8, True)}
+         "swa": ("swa", 8, False), "swa_bwd": ("swa", 8, True),
+         "swa_b2": ("swa", 2, False), "swa_bwd_b2": ("swa", 2, True)}
 
 
 def peaks():
@@ -624,10 +625,10 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if name == "swa":
-        x = swa_inputs(dev)
+        x = swa_inputs(dev, B=B)
         if backward:
             o, lse = api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)
-            g = swa_inputs(dev, seed=12)[0] * 8
+            g = swa_inputs(dev, B=B, seed=12)[0] * 8
             step = lambda: api.swa_bwd(x[0], x[1], x[2], o, lse, g, window=SWA_WINDOW)
         else:
             step = lambda: api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW)

@@ -318,29 +318,36 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             for (int j = 0; j < it.nt; ++j) {
                 if (!wait(&sb.s_full[wg], full_par(ts))) { ok = false; break; }
                 tc_fence_after();
-                float x[BN];
-#pragma unroll
-                for (int ci = 0; ci < BN / 16; ++ci) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(ts_addr + 16 * ci, r);
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[u]);
-                }
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.s_empty[wg]);
                 const int kbase = (it.k0 + j) * BN;
-                if (kbase + BN - 1 > t0 || kbase < t0 + BM - a.W) {      // tile crosses a mask edge
-                    const int lo = t - a.W + 1;
+                const bool edge = kbase + BN - 1 > t0 || kbase < t0 + BM - a.W;   // crosses a mask edge
+                const int lo = t - a.W + 1;
+                // the tile is read from TMEM twice, 64 columns at a time: first for the
+                // row max, then for the exponentials (few registers live at once)
+                float x[64];
+                auto load_half = [&](int hf) {
 #pragma unroll
-                    for (int i = 0; i < BN; ++i) {
-                        const int sk = kbase + i;
-                        if (sk > t || sk < lo) x[i] = -INFINITY;
+                    for (int ci = 0; ci < 4; ++ci) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(ts_addr + 64 * hf + 16 * ci, r);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[u]);
                     }
-                }
-                float mt = -INFINITY;
+                    tmem_wait_ld();
+                    if (edge) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) mt = fmaxf(mt, x[i]);
+                        for (int i = 0; i < 64; ++i) {
+                            const int sk = kbase + 64 * hf + i;
+                            if (sk > t || sk < lo) x[i] = -INFINITY;
+                        }
+                    }
+                };
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int hf = 0; hf < 2; ++hf) {
+                    load_half(hf);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                }
+                const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 const float mts = mt * a.scale_log2;
                 float alpha = 1.f;
                 bool resc = false;
@@ -353,14 +360,6 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 }
                 l *= alpha;
                 const float mu = (m == -INFINITY) ? 0.f : m;
-                uint32_t pk[BN / 2];
-#pragma unroll
-                for (int i = 0; i < BN / 2; ++i) {
-                    const float p0 = fast_exp2(fmaf(x[2 * i], a.scale_log2, -mu));
-                    const float p1 = fast_exp2(fmaf(x[2 * i + 1], a.scale_log2, -mu));
-                    l += p0 + p1;
-                    pk[i] = tcx::pack_bf16(p0, p1);
-                }
                 // the previous tile's P V has completed: O is stable, P buffer free
                 // (for a first tile: also the previous item's O store has read it)
                 if (!wait(&sb.p_empty[wg], empty_par(ts)) ||
@@ -379,12 +378,28 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     tmem_wait_st();
                 }
                 uint8_t* pbase = sm + OFF_P + wg * P_BYTES + row * 128;
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int hf = 0; hf < 2; ++hf) {
+                    load_half(hf);
+                    if (hf == 1) {                       // S fully read: the buffer is free
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty[wg]);
+                    }
 #pragma unroll
-                for (int ch = 0; ch < BN / 8; ++ch) {
-                    const int blk = ch >> 3, cc = ch & 7;
-                    *reinterpret_cast<uint4*>(pbase + blk * P_BLOCK + ((cc ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                    for (int cc = 0; cc < 8; ++cc) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float p0 = fast_exp2(fmaf(x[8 * cc + 2 * u], a.scale_log2, -mu));
+                            const float p1 = fast_exp2(fmaf(x[8 * cc + 2 * u + 1], a.scale_log2, -mu));
+                            l4[u] += p0 + p1;
+                            pk[u] = tcx::pack_bf16(p0, p1);
+                        }
+                        *reinterpret_cast<uint4*>(pbase + hf * P_BLOCK + ((cc ^ (row & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
                 }
+                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&sb.p_full[wg]);
