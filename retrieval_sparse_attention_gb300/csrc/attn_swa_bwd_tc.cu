@@ -362,31 +362,52 @@ swa_bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int j = 0; j < it.nt; ++j) {
                 if (!wait(&sb.s_full[wg], full_par(ts))) { ok = false; break; }
                 tc_fence_after();
-                float x[64], g[64];
-                load64(ts_addr, x);
-                load64(ts_addr + BT, g);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.s_empty[wg]);
                 const int kbase = (it.k0 + j) * BT;
                 const bool edge = kbase + BT - 1 > t0 || kbase < t0 + BM - a.W;
                 const int lo = t - a.W + 1;
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float d2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = 2 * i + u;
-                        float p = fast_exp2(fmaf(x[c], a.scale_log2, -lse2));
-                        if (edge && (kbase + c > t || kbase + c < lo)) p = 0.f;
-                        d2[u] = p * (g[c] - dlt) * a.scale;
-                    }
-                    pk[i] = tcx::pack_bf16(d2[0], d2[1]);
-                }
+                // the previous dQ product has read the dS buffer (for a first tile: the
+                // previous item's dQ store has read it too)
                 if (!wait(&sb.ds_empty[wg], empty_par(ts)) ||
                     (j == 0 && ko > 0 && !wait(&sb.epi_free[wg], full_par(ko - 1)))) { ok = false; break; }
-                put_row64(dsbuf, row, pk);
+                // 32 columns at a time: S and dP from TMEM, dS out 8 columns (16 bytes) at a time
+                for (int hf = 0; hf < 2; ++hf) {
+                    float x[32], g[32];
+#pragma unroll
+                    for (int ci = 0; ci < 2; ++ci) {
+                        uint32_t r[16], q[16];
+                        tmem_ld_32x32b_x16(ts_addr + 32 * hf + 16 * ci, r);
+                        tmem_ld_32x32b_x16(ts_addr + BT + 32 * hf + 16 * ci, q);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            x[16 * ci + u] = __uint_as_float(r[u]);
+                            g[16 * ci + u] = __uint_as_float(q[u]);
+                        }
+                    }
+                    tmem_wait_ld();
+                    if (hf == 1) {                      // S and dP fully read
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty[wg]);
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int u2 = 0; u2 < 4; ++u2) {
+                            float d2[2];
+#pragma unroll
+                            for (int v2 = 0; v2 < 2; ++v2) {
+                                const int xi = 8 * ch + 2 * u2 + v2, c = 32 * hf + xi;
+                                float p = fast_exp2(fmaf(x[xi], a.scale_log2, -lse2));
+                                if (edge && (kbase + c > t || kbase + c < lo)) p = 0.f;
+                                d2[v2] = p * (g[xi] - dlt) * a.scale;
+                            }
+                            pk[u2] = tcx::pack_bf16(d2[0], d2[1]);
+                        }
+                        const int chunk = 4 * hf + ch;
+                        *reinterpret_cast<uint4*>(dsbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
                 fence_proxy_async_smem();
                 mbar_arrive(&sb.ds_full[wg]);
                 ++ts;
@@ -699,39 +720,64 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     if (!wait(&sb.s_full[wg], full_par(ts)) || !wait(&sb.q_full[stg], stph) ||
                         !wait(&sb.d_full[stg], stph)) { ok = false; break; }
                     tc_fence_after();
-                    float x[64], g[64];
-                    load64(ts_addr, x);
-                    load64(ts_addr + BT, g);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&sb.s_empty[wg]);
                     const float4* l4 = reinterpret_cast<const float4*>(sm + OFF_Q + stg * STAGE + VEC);
                     const float4* d4 = reinterpret_cast<const float4*>(sm + OFF_DO + stg * STAGE + VEC);
                     const int qb = (mine.q0 + j) * BT;
                     const bool edge = qb < s || qb + BT - 1 > s + a.W - 1 || qb + BT > a.L;
-                    uint32_t pp[32], pd[32];
-#pragma unroll
-                    for (int i4 = 0; i4 < 16; ++i4) {
-                        const float4 lv = l4[i4], dv = d4[i4];
-                        const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
-                        float pv[4], dsv[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int c = 4 * i4 + u, tq = qb + c;
-                            float p = fast_exp2(fmaf(x[c], a.scale_log2, -la[u]));
-                            if (edge && (tq < s || tq > s + a.W - 1 || tq >= a.L)) p = 0.f;
-                            pv[u] = p;
-                            dsv[u] = p * (g[c] - da[u]) * a.scale;
-                        }
-                        pp[2 * i4] = tcx::pack_bf16(pv[0], pv[1]);
-                        pp[2 * i4 + 1] = tcx::pack_bf16(pv[2], pv[3]);
-                        pd[2 * i4] = tcx::pack_bf16(dsv[0], dsv[1]);
-                        pd[2 * i4 + 1] = tcx::pack_bf16(dsv[2], dsv[3]);
-                    }
+                    // the previous accumulation products have read the operand buffers
+                    // (for a first tile: the previous item's stores have read them too)
                     if (!wait(&sb.p_empty[wg], empty_par(ts)) ||
                         (j == 0 && ko > 0 && !wait(&sb.epi_free[wg], full_par(ko - 1)))) { ok = false; break; }
-                    put_row64(ptbuf, row, pp);
-                    put_row64(dsbuf, row, pd);
+                    // 32 columns at a time: S^T and dP^T from TMEM, P^T and dS^T out to the
+                    // operand buffers 8 columns (16 bytes) at a time
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float x[32], g[32];
+#pragma unroll
+                        for (int ci = 0; ci < 2; ++ci) {
+                            uint32_t r[16], q[16];
+                            tmem_ld_32x32b_x16(ts_addr + 32 * hf + 16 * ci, r);
+                            tmem_ld_32x32b_x16(ts_addr + BT + 32 * hf + 16 * ci, q);
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) {
+                                x[16 * ci + u] = __uint_as_float(r[u]);
+                                g[16 * ci + u] = __uint_as_float(q[u]);
+                            }
+                        }
+                        tmem_wait_ld();
+                        if (hf == 1) {                  // S^T and dP^T fully read
+                            tc_fence_before();
+                            mbar_arrive(&sb.s_empty[wg]);
+                        }
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {
+                            uint32_t pp[4], pd[4];
+#pragma unroll
+                            for (int h4 = 0; h4 < 2; ++h4) {
+                                const int i4 = 8 * hf + 2 * ch + h4;       // float4 index of the column
+                                const float4 lv = l4[i4], dv = d4[i4];
+                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+                                const float da[4] = {dv.x, dv.y, dv.z, dv.w};
+                                float pv[4], dsv[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int c = 4 * i4 + u, tq = qb + c;
+                                    const int xi = c - 32 * hf;
+                                    float p = fast_exp2(fmaf(x[xi], a.scale_log2, -la[u]));
+                                    if (edge && (tq < s || tq > s + a.W - 1 || tq >= a.L)) p = 0.f;
+                                    pv[u] = p;
+                                    dsv[u] = p * (g[xi] - da[u]) * a.scale;
+                                }
+                                pp[2 * h4] = tcx::pack_bf16(pv[0], pv[1]);
+                                pp[2 * h4 + 1] = tcx::pack_bf16(pv[2], pv[3]);
+                                pd[2 * h4] = tcx::pack_bf16(dsv[0], dsv[1]);
+                                pd[2 * h4 + 1] = tcx::pack_bf16(dsv[2], dsv[3]);
+                            }
+                            const int chunk = 4 * hf + ch;
+                            const int off = row * 128 + ((chunk ^ (row & 7)) << 4);
+                            *reinterpret_cast<uint4*>(ptbuf + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+                            *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+                        }
+                    }
                     fence_proxy_async_smem();
                     mbar_arrive(&sb.p_full[wg]);
                     ++ts;
