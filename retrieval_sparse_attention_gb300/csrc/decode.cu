@@ -39,7 +39,7 @@ constexpr int kMaxBlocks = 2048;
 constexpr int kStages = 2;
 constexpr int kStageBytes = 49152;
 // 64-bit rank keys the last CTA holds in its idle ring: every CTA's list
-// (grid * topk) plus at most topk^2 survivors of the head bound
+// (grid * topk) plus room for the survivors of the head bound (at least topk^2)
 constexpr int kRingKeys = kStages * kStageBytes / 8;
 constexpr int kHeadRegs = 16;            // list heads per lane in the last CTA's registers
 constexpr int kMaxGrid = 32 * kHeadRegs; // so at most 512 CTAs
@@ -73,6 +73,7 @@ struct __align__(8) DecodeBars {
     unsigned long long bound;      // last CTA: key of the k-th best list head
     int n_kept;                    // last CTA: survivors of the head bound
     unsigned long long top[kMaxTopk];   // merged top-k keys by rank (0: none)
+    int stage[kStages];                 // stage held by each slot (-1: no more)
 };
 
 template <typename T, int VPL>
@@ -80,7 +81,8 @@ __global__ void __launch_bounds__(kThreads)
 decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N, int D,
                        int topk, int off_by_one, float sscale, int32_t* __restrict__ out_idx,
                        float* __restrict__ out_score, float* __restrict__ out_weight,
-                       unsigned* ticket, float* blk_s, int* blk_i, int* status) {
+                       unsigned* ticket, unsigned* stage_ctr, float* blk_s, int* blk_i,
+                       int* status) {
     constexpr int kEPV = 16 / sizeof(T);                 // elements per 16-byte vector
     extern __shared__ uint8_t dsm_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 127) &
@@ -93,12 +95,11 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     const int nvec = D / kEPV;                           // vectors per row (<= 32 * VPL)
     const int row_bytes = nvec * 16;
     const int rows_per_stage = kStageBytes / row_bytes;
-    // Stage s of the table (rows s*rows_per_stage ...) belongs to CTA s % grid:
-    // at any moment all CTAs read within one contiguous front of the table.
+    // Stages of the table (rows s*rows_per_stage ...): each CTA's first kStages are
+    // dealt round-robin (stage i*grid + cta), later ones are taken from a global
+    // counter, so CTAs that run ahead take more and all finish together.
     const int total_stages = (N + rows_per_stage - 1) / rows_per_stage;
-    const int n_stages_total = (int)blockIdx.x < total_stages
-        ? (total_stages - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    auto stage_row = [&](int g) { return (g * (int)gridDim.x + (int)blockIdx.x) * rows_per_stage; };
+    const int dyn0 = kStages * (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -113,20 +114,33 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     for (int e = threadIdx.x; e < D; e += kThreads) qsh[e] = to_f(ql[e]);
     __syncthreads();
 
-    // Copies of this CTA's stage g: rows stage_row(g) ... (at most rows_per_stage)
-    auto issue = [&](int g) {
-        const int slot = g % kStages;
-        const int ra = stage_row(g);
-        const int nr = min(rows_per_stage, N - ra);
-        const uint32_t bytes = static_cast<uint32_t>(nr) * row_bytes;
-        tc::mbar_arrive_expect_tx(&bars.full[slot], bytes);
-        tcx::bulk_load(ring + slot * kStageBytes,
-                       reinterpret_cast<const uint8_t*>(lm) + (size_t)ra * row_bytes, bytes,
-                       &bars.full[slot]);
+    // Fill `slot` with stage `sidx` (rows sidx*rows_per_stage ...), or mark it
+    // "no more stages" (-1, the full barrier completed without a copy).  Stage
+    // indices handed to the slots only grow, so the first -1 ends the CTA's work.
+    bool out[kStages] = {};                              // thread 0: copy in flight
+    uint32_t oph[kStages] = {};
+    auto fill = [&](int slot, int sidx, uint32_t par) {
+        if (sidx < total_stages) {
+            const int ra = sidx * rows_per_stage;
+            const int nr = min(rows_per_stage, N - ra);
+            const uint32_t bytes = static_cast<uint32_t>(nr) * row_bytes;
+            bars.stage[slot] = sidx;
+            tc::mbar_arrive_expect_tx(&bars.full[slot], bytes);
+            tcx::bulk_load(ring + slot * kStageBytes,
+                           reinterpret_cast<const uint8_t*>(lm) + (size_t)ra * row_bytes, bytes,
+                           &bars.full[slot]);
+            out[slot] = true;
+            oph[slot] = par;
+        } else {
+            bars.stage[slot] = -1;
+            tc::mbar_arrive(&bars.full[slot]);
+        }
     };
-    int n_issued = 0;                                    // meaningful in thread 0 only
-    if (threadIdx.x == 0)
-        for (; n_issued < kStages && n_issued < n_stages_total; ++n_issued) issue(n_issued);
+    int pending = 0;                                     // thread 0: next dynamic stage
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) fill(i, i * (int)gridDim.x + (int)blockIdx.x, 0u);
+        pending = dyn0 + (int)atomicAdd(stage_ctr, 1u);
+    }
 
     float qv[VPL][kEPV];
 #pragma unroll
@@ -139,11 +153,14 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     WarpTopk tk;
     tk.init();
     bool ok = true;
-    for (int g = 0; g < n_stages_total; ++g) {
+    for (int g = 0;; ++g) {
         const int slot = g % kStages;
         const uint32_t par = static_cast<uint32_t>(g / kStages) & 1u;
         if (!tcx::wait_bar(&bars.abort, &bars.full[slot], par, status)) { ok = false; break; }
-        const int ra = stage_row(g);
+        const int sidx = *reinterpret_cast<volatile int*>(&bars.stage[slot]);
+        if (threadIdx.x == 0) out[slot] = false;
+        if (sidx < 0) break;
+        const int ra = sidx * rows_per_stage;
         const int nr = min(rows_per_stage, N - ra);
         const uint4* st = reinterpret_cast<const uint4*>(ring + slot * kStageBytes);
         for (int rr = warp; rr < nr; rr += kWarps) {
@@ -158,19 +175,18 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&bars.empty[slot]);
-        if (threadIdx.x == 0 && g + kStages < n_stages_total) {
+        if (threadIdx.x == 0) {
             // refill this slot once every warp has released it
             if (!tcx::wait_bar(&bars.abort, &bars.empty[slot], par, status)) { ok = false; break; }
-            issue(g + kStages);
-            ++n_issued;
+            const int nxt = pending;
+            if (nxt < total_stages) pending = dyn0 + (int)atomicAdd(stage_ctr, 1u);
+            fill(slot, nxt, par ^ 1u);
         }
     }
-    // Never leave a copy in flight behind an early exit: wait (bounded) for the
-    // last copy issued into each slot.
+    // Never leave a copy in flight behind an early exit: wait (bounded) for it.
     if (threadIdx.x == 0 && !ok)
-        for (int g = max(0, n_issued - kStages); g < n_issued; ++g)
-            tc::mbar_wait(&bars.full[g % kStages], static_cast<uint32_t>(g / kStages) & 1u, nullptr,
-                          100000000ull);
+        for (int i = 0; i < kStages; ++i)
+            if (out[i]) tc::mbar_wait(&bars.full[i], oph[i], nullptr, 100000000ull);
 
     // CTA merge: every entry of the warps' lists is ranked among all of them
     // by counting larger keys (keys are distinct); ranks below topk are the
@@ -201,10 +217,12 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     if (!bars.is_last) return;
 
     // Last CTA.  (1) Every CTA's list lands in the idle ring as rank keys.
-    // (2) The k-th best list head bounds the global k-th best from below (the
-    // heads are a subset of all rows), and an entry ranking at or before it
-    // must come from a list whose head does too: at most topk lists, so at
-    // most topk^2 survivors.  (3) The survivors are ranked by counting.
+    // (2) The k-th best of any set of list heads bounds the global k-th best
+    // from below (the heads are a subset of all rows); only entries ranking at
+    // or before it survive.  The best head of each of 32 lanes gives a cheap
+    // bound; if it leaves more survivors than fit, the k-th best of all heads
+    // is used, which leaves entries of at most topk lists (topk^2).  (3) The
+    // survivors are ranked by counting.
     __threadfence();
     unsigned long long* rk = reinterpret_cast<unsigned long long*>(ring);
     const int nb = gridDim.x;
@@ -228,9 +246,42 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     }
     if (threadIdx.x < kMaxTopk) bars.top[threadIdx.x] = 0ull;
     __syncthreads();
-    {
-        // heads in registers: lane l holds heads l, l + 32, ... (nb <= 32 * kHeadRegs)
-        unsigned long long hr[kHeadRegs];
+    const int cap = kRingKeys - total;                   // survivor room after the lists
+    // (2a) cheap bound: the k-th best of the 32 lanes' best heads (a subset of
+    // the heads, so still a lower bound on the global k-th best)
+    if (warp == 0) {
+        unsigned long long best = 0ull;
+        for (int c = lane; c < nb; c += 32) {
+            const unsigned long long kc = rk[(size_t)c * topk];
+            best = kc > best ? kc : best;
+        }
+        int r = 0;
+        for (int o = 0; o < 32; ++o) r += __shfl_sync(0xffffffffu, best, o) > best;
+        if (best != 0ull && r == topk - 1) bars.bound = best;
+    }
+    __syncthreads();
+    auto keep_survivors = [&](unsigned long long bound) {
+        for (int b0 = warp * 32; b0 < total; b0 += kThreads) {
+            const int e = b0 + lane;
+            const unsigned long long ke = e < total ? rk[e] : 0ull;
+            const bool keep = ke != 0ull && ke >= bound;
+            const unsigned m = __ballot_sync(0xffffffffu, keep);
+            int base = 0;
+            if (lane == 0 && m) base = atomicAdd(&bars.n_kept, __popc(m));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const int pos = base + __popc(m & ((1u << lane) - 1u));
+            if (keep && pos < cap) surv[pos] = ke;
+        }
+    };
+    keep_survivors(bars.bound);
+    __syncthreads();
+    if (bars.n_kept > cap) {
+        // (2b) too many survivors for the cheap bound: the exact k-th best head
+        // bounds them to at most topk lists (topk^2 entries)
+        __syncthreads();
+        if (threadIdx.x == 0) { bars.n_kept = 0; bars.bound = 0ull; }
+        __syncthreads();
+        unsigned long long hr[kHeadRegs];      // lane l holds heads l, l + 32, ... (nb <= 32 * kHeadRegs)
 #pragma unroll
         for (int j = 0; j < kHeadRegs; ++j) {
             const int c = lane + 32 * j;
@@ -244,20 +295,10 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
             for (int j = 0; j < kHeadRegs; ++j) cnt += hr[j] > kc;
             if (__reduce_add_sync(0xffffffffu, cnt) == topk - 1 && lane == 0) bars.bound = kc;
         }
+        __syncthreads();
+        keep_survivors(bars.bound);
+        __syncthreads();
     }
-    __syncthreads();
-    const unsigned long long bound = bars.bound;      // 0: fewer than topk non-empty lists
-    for (int b0 = warp * 32; b0 < total; b0 += kThreads) {
-        const int e = b0 + lane;
-        const unsigned long long ke = e < total ? rk[e] : 0ull;
-        const bool keep = ke != 0ull && ke >= bound;
-        const unsigned m = __ballot_sync(0xffffffffu, keep);
-        int base = 0;
-        if (lane == 0 && m) base = atomicAdd(&bars.n_kept, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (keep) surv[base + __popc(m & ((1u << lane) - 1u))] = ke;
-    }
-    __syncthreads();
     const int ns = bars.n_kept;
     for (int a = warp; a < ns; a += kWarps) {
         const unsigned long long ka = surv[a];
@@ -287,7 +328,7 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
             out_score[lane] = okl ? r : 0.f;
             out_weight[lane] = okl ? e / den : 0.f;
         }
-        if (lane == 0) *ticket = 0u;     // leave the counter reset for the next call
+        if (lane == 0) { *ticket = 0u; *stage_ctr = 0u; }     // leave both reset for the next call
     }
 }
 
@@ -331,12 +372,12 @@ cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, i
     if (nb > kMaxGrid) nb = kMaxGrid;
     float* blk_s = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + 256);
     int* blk_i = reinterpret_cast<int*>(blk_s + (size_t)nb * topk);
-    e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
+    e = cudaMemsetAsync(ticket, 0, 2 * sizeof(unsigned), st);      // ticket and stage counter
     if (e != cudaSuccess) return e;
     GCA_LAUNCH("decode_retrieve", st,
                kern<<<nb, kThreads, smem, st>>>((const T*)lm, (const T*)ql, N, D, topk, off_by_one,
-                                                score_scale, idx, score, weight, ticket, blk_s,
-                                                blk_i, status));
+                                                score_scale, idx, score, weight, ticket, ticket + 1,
+                                                blk_s, blk_i, status));
     return cudaGetLastError();
 }
 
