@@ -7,32 +7,41 @@
 // Token t of a sequence attends to the keys max(0, t - W + 1) .. t:
 //   o_t = sum_s softmax_s(attn_scale q_t . k_s) v_s,  lse_t = ln sum_s exp(...).
 //
-// Design (one persistent CTA per SM, 11 warps, warp-specialised):
+// Design (one persistent CTA per SM, 12 warps, warp-specialised):
 //   item       (batch row, 128-token query tile, head); keys come in tiles of
 //              128, so both products are M = 128 MMAs (full rate); for
 //              W = 512 an item needs at most 5 key tiles, of which only the
 //              first (window edge) and the last (causal diagonal) are masked.
 //   warp 0     producer: TMA (3-D maps over [B, L, H*d]: rows outside a
 //              sequence read as zeros) of the Q tile (lane 0), each key
-//              tile's K (lane 0) and V (lane 1) into separate 4-stage rings:
+//              tile's K (lane 0) and V (lane 1) into separate 3-stage rings:
 //              a K stage is free once its S product completes, long before
 //              the V stage, which waits for P V.
 //   warp 1     S issuer and TMEM owner: S = Q K^T into the item's warpgroup's
 //              S buffer (128 columns).
 //   warp 2     P V issuer: O += P V into the warpgroup's O accumulator.
-//   warps 3-10 two softmax warpgroups owning alternate items (the online
+//   warp 3     idle (completes the first warpgroup, which gives registers
+//              to the softmax warpgroups with setmaxnreg).
+//   warps 4-11 two softmax warpgroups owning alternate items (the online
 //              softmax of a row lives in one thread's registers); producer
 //              and issuers walk the two current items' tiles interleaved, so
 //              one warpgroup's softmax overlaps the other's products.
+// Masking: only the tiles that the window edge or the diagonal crosses are
+// masked, in registers, by straight-line selects (no per-chunk branches: the
+// unrolled exponential loop relies on interleaving across the whole row).
+// Softmax of one tile: the thread reads its row of S (128 columns) from TMEM
+// once and frees the buffer at once, so the next S product overlaps this
+// tile's arithmetic; the scaling and the row sum use packed f32x2 arithmetic.
 // Online softmax with a stale running max: P = exp2(s' - m) is written
 // unnormalised; O (TMEM) and the running sum are rescaled only when a tile's
 // max exceeds m by more than 2^8, which keeps every P below 256 and the result
 // exact up to rounding.  The rescale reads, scales and writes O in TMEM after
 // the previous tile's P V has completed.
-// Epilogue: O / l in bf16 is written into the warpgroup's idle P buffer in the
-// swizzled tile layout and stored with one TMA tensor store (rows past the
-// sequence end are clipped by the tensor map).
-// Every mbarrier wait is bounded (status GCA_ERR_TIMEOUT, then the CTA winds down).
+// Epilogue: O / l in bf16 goes into the warpgroup's own staging tile in the
+// swizzled layout and leaves with one TMA tensor store (rows past the sequence
+// end are clipped by the tensor map).  It runs after the next item's first
+// row max, so the wait for the last P V overlaps useful work; the store's read
+// of the staging tile is awaited only at the following epilogue.
 #include <math.h>
 
 #include "common.cuh"
@@ -50,10 +59,15 @@ using tcx::kLn2;
 using tcx::kLog2e;
 using tcx::Ring;
 
-constexpr int kThreads = 352;          // producer, 2 MMA issuers, 2 softmax warpgroups
+constexpr int kThreads = 384;          // control warpgroup + 2 softmax warpgroups
+constexpr int kRegsLaunch = 168;       // registers a thread at launch (384 x 168 <= 64K)
+constexpr int kRegsCtrl = 56;          // after setmaxnreg: producer / issuer warpgroup
+constexpr int kRegsSoftmax = 224;      //                   each softmax warpgroup
+static_assert(128 * kRegsCtrl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr int BM = 128;                // query rows per item (MMA M)
 constexpr int BN = 128;                // keys per tile (MMA N of S)
-constexpr int STAGES = 4;               // depth of the K ring and of the V ring
+constexpr int STAGES = 3;              // depth of the K ring and of the V ring
 constexpr int TILE = 128 * 128;        // 128 rows x 64 bf16: a Q, K, V or O tile
 constexpr int P_BLOCK = BM * 128;      // 64 keys of P for the 128 rows
 constexpr int P_BYTES = 2 * P_BLOCK;   // 128 keys
@@ -61,7 +75,8 @@ constexpr int OFF_Q = 0;               // one Q tile per warpgroup
 constexpr int OFF_K = 2 * TILE;
 constexpr int OFF_V = OFF_K + STAGES * TILE;
 constexpr int OFF_P = OFF_V + STAGES * TILE;            // one P buffer per warpgroup
-constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;        // + alignment slack
+constexpr int OFF_O = OFF_P + 2 * P_BYTES;              // one O staging tile per warpgroup
+constexpr int SMEM = OFF_O + 2 * TILE + 1024;           // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;          // S buffer of warpgroup w at w * 128
 constexpr uint32_t COL_O = 256;        // O accumulator of warpgroup w at 256 + w * 64
@@ -80,7 +95,7 @@ struct __align__(8) Bars {
     uint64_t q_full[2], q_empty[2];
     uint64_t k_full[STAGES], k_empty[STAGES];
     uint64_t v_full[STAGES], v_empty[STAGES];
-    uint64_t epi_full[2], epi_free[2];    // O staged in the P buffer / its store has read it
+    uint64_t epi_full[2], epi_free[2];    // O staged / the previous store has read the staging tile
     uint64_t s_full[2], s_empty[2];
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
@@ -107,6 +122,12 @@ __device__ __forceinline__ Item decode_item(const SwaArgs& a, int item) {
     it.k0 = lo / BN;
     it.nt = it.qt - it.k0 + 1;          // key tiles k0 .. qt (BN == BM)
     return it;
+}
+
+// Does key tile j of the item cross the window edge or the diagonal of any of its rows?
+__device__ __forceinline__ bool tile_masked(const SwaArgs& a, const Item& it, int j) {
+    const int kbase = (it.k0 + j) * BN, t0 = it.qt * BM;
+    return kbase + BN - 1 > t0 || kbase < t0 + BM - a.W;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -165,6 +186,10 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     // The CTA's items are blockIdx.x + k * gridDim.x; pair p holds k = 2p (warpgroup 0)
     // and k = 2p + 1 (warpgroup 1).  Producer and issuers walk a pair's tiles as
     // (wg 0, tile 0), (wg 1, tile 0), (wg 0, tile 1), ...
+    if (warp < 4) {
+    // each warpgroup's setmaxnreg heads its own branch: every warp of the group
+    // executes that one instruction, and it dominates the code that runs under it
+    setmaxnreg_dec<kRegsCtrl>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         // lane 0: Q tiles and the K ring; lane 1: the V ring (each walks the same
@@ -299,58 +324,67 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
             }
         }
+    }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int wg = (warp - 3) >> 2;
-        const int qd = warp & 3;
+        setmaxnreg_inc<kRegsSoftmax>();
+        const int wg = (warp - 4) >> 2;
+        const int qd = warp & 3;                        // TMEM lane quarter of this warp
         const int row = 32 * qd + lane;                 // TMEM lane = query row of the tile
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
         const uint32_t ts_addr = tmem + lane_base + COL_S + wg * 128;
         const uint32_t to_addr = tmem + lane_base + COL_O + wg * 64;
+        uint8_t* const pbuf = sm + OFF_P + wg * P_BYTES + row * 128;
+        uint8_t* const obuf = sm + OFF_O + wg * TILE;
+        const bool leader = qd == 0 && lane == 0;       // issues this warpgroup's O stores
+        const float sl = a.scale_log2;
+        // warp-uniform result: the TMEM accesses and votes after a wait are warp-collective,
+        // so a wait that gave up in one lane (abort) must give up in all of them
+        auto wwait = [&](uint64_t* bar, uint32_t par) { return __all_sync(0xffffffffu, wait(bar, par)); };
+
         int ts = 0, ko = 0;
-        bool ok = true;
-        for (int item = blockIdx.x + wg * stride; item < a.n_items && ok; item += 2 * stride) {
-            const Item it = decode_item(a, item);
-            const int t0 = it.qt * BM;
-            const int t = t0 + row;                     // this thread's token
-            float m = -INFINITY;                        // running max of s * scale * log2(e)
-            float l = 0.f;                              // running sum of exp2(. - m)
-            for (int j = 0; j < it.nt; ++j) {
-                if (!wait(&sb.s_full[wg], full_par(ts))) { ok = false; break; }
+        int item = blockIdx.x + wg * stride, j = 0;
+        Item it{};
+        if (item < a.n_items) it = decode_item(a, item);
+        float m = -INFINITY;                            // running max of s * scale * log2(e)
+        float l = 0.f;                                  // running sum of exp2(. - m)
+        // the finished item whose O still sits in TMEM
+        bool pend = false;
+        Item pit{};
+        float pm = 0.f, pl = 1.f;
+        while (true) {
+            const bool have = item < a.n_items;
+            float alpha = 1.f;
+            bool resc = false;
+            float x[128];
+            if (have) {
+                if (!wwait(&sb.s_full[wg], full_par(ts))) break;
                 tc_fence_after();
-                const int kbase = (it.k0 + j) * BN;
-                const bool edge = kbase + BN - 1 > t0 || kbase < t0 + BM - a.W;   // crosses a mask edge
-                const int lo = t - a.W + 1;
-                // the tile is read from TMEM twice, 64 columns at a time: first for the
-                // row max, then for the exponentials (few registers live at once)
-                float x[64];
-                auto load_half = [&](int hf) {
+                {
+                    uint32_t r[8][16];
 #pragma unroll
-                    for (int ci = 0; ci < 4; ++ci) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(ts_addr + 64 * hf + 16 * ci, r);
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[u]);
-                    }
+                    for (int ci = 0; ci < 8; ++ci) tmem_ld_32x32b_x16(ts_addr + 16 * ci, r[ci]);
                     tmem_wait_ld();
-                    if (edge) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            const int sk = kbase + 64 * hf + i;
-                            if (sk > t || sk < lo) x[i] = -INFINITY;
-                        }
-                    }
-                };
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                for (int hf = 0; hf < 2; ++hf) {
-                    load_half(hf);
+                    for (int ci = 0; ci < 8; ++ci)
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                        for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[ci][u]);
                 }
-                const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                const float mts = mt * a.scale_log2;
-                float alpha = 1.f;
-                bool resc = false;
+                tc_fence_before();
+                mbar_arrive(&sb.s_empty[wg]);           // S is in registers: the buffer is free
+                if (tile_masked(a, it, j)) {
+                    // row t sees the keys t - W + 1 .. t: columns c_lo .. c_lo + W - 1
+                    // (a select per column; a conditional store here becomes a branch)
+                    const int c_lo = it.qt * BM + row - a.W + 1 - (it.k0 + j) * BN;
+                    const uint32_t span = static_cast<uint32_t>(a.W - 1);
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        x[i] = static_cast<uint32_t>(i - c_lo) > span ? -INFINITY : x[i];
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                const float mts = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl;
                 if (mts > m + kRescaleLog2) {
                     if (m != -INFINITY) {
                         resc = true;
@@ -359,89 +393,111 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     m = mts;
                 }
                 l *= alpha;
-                const float mu = (m == -INFINITY) ? 0.f : m;
-                // the previous tile's P V has completed: O is stable, P buffer free
-                // (for a first tile: also the previous item's O store has read it)
-                if (!wait(&sb.p_empty[wg], empty_par(ts)) ||
-                    (j == 0 && ko > 0 && !wait(&sb.epi_free[wg], full_par(ko - 1)))) { ok = false; break; }
-                if (__any_sync(0xffffffffu, resc)) {
-                    tc_fence_after();
+            }
+            // the previous item's output leaves after the next item's first row max,
+            // which gives its last P V time to complete
+            if ((j == 0 || !have) && pend) {
+                if (!wwait(&sb.o_full[wg], full_par(ko))) break;
+                tc_fence_after();
+                uint32_t r[4][16];
 #pragma unroll
-                    for (int ci = 0; ci < 4; ++ci) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(to_addr + 16 * ci, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
-                        tmem_st_32x32b_x16(to_addr + 16 * ci, r);
-                    }
-                    tmem_wait_st();
-                }
-                uint8_t* pbase = sm + OFF_P + wg * P_BYTES + row * 128;
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int hf = 0; hf < 2; ++hf) {
-                    load_half(hf);
-                    if (hf == 1) {                       // S fully read: the buffer is free
-                        tc_fence_before();
-                        mbar_arrive(&sb.s_empty[wg]);
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float p0 = fast_exp2(fmaf(x[8 * cc + 2 * u], a.scale_log2, -mu));
-                            const float p1 = fast_exp2(fmaf(x[8 * cc + 2 * u + 1], a.scale_log2, -mu));
-                            l4[u] += p0 + p1;
-                            pk[u] = tcx::pack_bf16(p0, p1);
-                        }
-                        *reinterpret_cast<uint4*>(pbase + hf * P_BLOCK + ((cc ^ (row & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
-                }
-                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-                fence_proxy_async_smem();
+                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(to_addr + 16 * ci, r[ci]);
+                tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(&sb.p_full[wg]);
-                ++ts;
+                mbar_arrive(&sb.o_empty[wg]);
+                // the previous store of this warpgroup must have read the staging tile
+                if (ko > 0) {
+                    if (leader) {
+                        bulk_wait_group_read0();
+                        mbar_arrive(&sb.epi_free[wg]);
+                    }
+                    if (!wwait(&sb.epi_free[wg], full_par(ko - 1))) break;
+                }
+                const float inv = 1.f / pl;
+                uint8_t* orow = obuf + row * 128;
+#pragma unroll
+                for (int ci = 0; ci < 4; ++ci) {
+                    float f[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) f[u] = __uint_as_float(r[ci][u]);
+                    *reinterpret_cast<uint4*>(orow + (((2 * ci) ^ (row & 7)) << 4)) = tcx::pack8(f, inv);
+                    *reinterpret_cast<uint4*>(orow + (((2 * ci + 1) ^ (row & 7)) << 4)) =
+                        tcx::pack8(f + 8, inv);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&sb.epi_full[wg]);
+                const int t = pit.qt * BM + row;
+                if (t < a.L && a.lse) a.lse[((size_t)pit.b * a.L + t) * a.H + pit.h] = (pm + log2f(pl)) * kLn2;
+                if (leader) {
+                    if (!wait(&sb.epi_full[wg], full_par(ko))) break;
+                    tma_store_3d(&to, obuf, pit.h * 64, pit.qt * BM, pit.b);
+                    bulk_commit_group();
+                }
+                ++ko;
+                pend = false;
             }
-            if (!ok) break;
-            // epilogue: O / l of this thread's row into the (idle) P buffer in the
-            // swizzled tile layout, then one TMA tensor store of the whole tile
-            if (!wait(&sb.o_full[wg], full_par(ko))) break;
-            tc_fence_after();
-            uint32_t r[4][16];
+            if (!have) break;
+            const float mu = (m == -INFINITY) ? 0.f : m;
+            // the previous tile's P V has completed: O is stable, P buffer free
+            if (!wwait(&sb.p_empty[wg], empty_par(ts))) break;
+            if (__any_sync(0xffffffffu, resc)) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int ci = 0; ci < 4; ++ci) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(to_addr + 16 * ci, r);
+                    tmem_wait_ld();
 #pragma unroll
-            for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(to_addr + 16 * ci, r[ci]);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&sb.o_empty[wg]);
-            uint8_t* obuf = sm + OFF_P + wg * P_BYTES;
-            const float inv = 1.f / l;
-#pragma unroll
-            for (int ci = 0; ci < 4; ++ci) {
-                float f[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) f[u] = __uint_as_float(r[ci][u]);
-                *reinterpret_cast<uint4*>(obuf + row * 128 + (((2 * ci) ^ (row & 7)) << 4)) =
-                    tcx::pack8(f, inv);
-                *reinterpret_cast<uint4*>(obuf + row * 128 + (((2 * ci + 1) ^ (row & 7)) << 4)) =
-                    tcx::pack8(f + 8, inv);
+                    for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * alpha);
+                    tmem_st_32x32b_x16(to_addr + 16 * ci, r);
+                }
+                tmem_wait_st();
             }
+            // p = exp2(s * scale * log2(e) - m); the scaling and the row sum run on
+            // column pairs (packed f32x2 FMA and add: one instruction for two columns)
+            const uint64_t sl2 = tcx::f2_pack(sl, sl), nmu2 = tcx::f2_pack(-mu, -mu);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float y0, y1;
+                    const uint64_t s2 = tcx::f2_pack(x[16 * c + 2 * u], x[16 * c + 2 * u + 1]);
+                    tcx::f2_unpack(tcx::ffma2(s2, sl2, nmu2), y0, y1);
+                    const float e0 = fast_exp2(y0);
+                    const float e1 = fast_exp2(y1);
+                    acc2[u & 3] = tcx::fadd2(acc2[u & 3], tcx::f2_pack(e0, e1));
+                    pk[u] = tcx::pack_bf16(e0, e1);
+                }
+                uint8_t* dst = pbuf + (c >> 2) * P_BLOCK;
+                const int p0 = 2 * (c & 3);             // 16-byte pieces of the 128-byte row
+                *reinterpret_cast<uint4*>(dst + ((p0 ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(dst + (((p0 + 1) ^ (row & 7)) << 4)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+            float l4[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tcx::f2_unpack(acc2[u], l4[2 * u], l4[2 * u + 1]);
+            l += ((l4[0] + l4[1]) + (l4[2] + l4[3])) + ((l4[4] + l4[5]) + (l4[6] + l4[7]));
             fence_proxy_async_smem();
-            mbar_arrive(&sb.epi_full[wg]);
-            if (t < a.L && a.lse) a.lse[((size_t)it.b * a.L + t) * a.H + it.h] = (m + log2f(l)) * kLn2;
-            if (qd == 0 && lane == 0) {          // one thread of the warpgroup stores the tile
-                if (!wait(&sb.epi_full[wg], full_par(ko))) break;
-                tma_store_3d(&to, obuf, it.h * 64, t0, it.b);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-                mbar_arrive(&sb.epi_free[wg]);
+            tc_fence_before();
+            mbar_arrive(&sb.p_full[wg]);
+            ++ts;
+            if (++j == it.nt) {                         // item done: its O is written out later
+                pend = true;
+                pit = it;
+                pm = m;
+                pl = l;
+                m = -INFINITY;
+                l = 0.f;
+                j = 0;
+                item += 2 * stride;
+                if (item < a.n_items) it = decode_item(a, item);
             }
-            ++ko;
         }
         // the last tile stores must be complete before the CTA exits
-        if (qd == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 
     tc_fence_before();
@@ -474,7 +530,13 @@ cudaError_t launch_swa_fwd_tc(int B, int L, int H, int W, float attn_scale, cons
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = a.n_items < sms ? a.n_items : sms;
-    cudaError_t e = cudaFuncSetAttribute(gca_swa_fwd_tc_kernel,
+    // the setmaxnreg split needs the whole launch allocation: refuse to launch a
+    // build that gave the kernel fewer registers a thread (its warps would wait forever)
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, gca_swa_fwd_tc_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 128 * kRegsCtrl + 256 * kRegsSoftmax) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(gca_swa_fwd_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     GCA_LAUNCH("swa_fwd_tc", st, gca_swa_fwd_tc_kernel<<<grid, kThreads, SMEM, st>>>(tq, tk, tv, to, a));
