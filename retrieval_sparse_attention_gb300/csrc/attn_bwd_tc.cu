@@ -510,30 +510,40 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(&sb.s_empty[sbuf]);
-                    float pr[32], gv[32];
+                    // column pairs in packed f32x2 arithmetic: p = exp2(s sl - L2) as
+                    // exp2(-(L2 - s sl)), delta = sum p g, dA = p (g - delta) w scale
+                    const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
+                    const uint64_t l2_2 = tcx::f2_pack(L2, L2);
+                    uint64_t pr2[16], gv2[16];
+                    uint64_t dacc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        pr[t] = fast_exp2(fmaf(__uint_as_float(r0[t]), a.scale_log2, -L2));
-                        pr[16 + t] = fast_exp2(fmaf(__uint_as_float(r1[t]), a.scale_log2, -L2));
-                        gv[t] = __uint_as_float(r2[t]);
-                        gv[16 + t] = __uint_as_float(r3[t]);
+                    for (int p = 0; p < 16; ++p) {
+                        const uint32_t* rs = p < 8 ? r0 : r1;
+                        const uint32_t* rg = p < 8 ? r2 : r3;
+                        const int t = 2 * (p & 7);
+                        float y0, y1;
+                        tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(__uint_as_float(rs[t]), __uint_as_float(rs[t + 1])),
+                                                  nsl2, l2_2), y0, y1);
+                        pr2[p] = tcx::f2_pack(fast_exp2(-y0), fast_exp2(-y1));
+                        gv2[p] = tcx::f2_pack(__uint_as_float(rg[t]), __uint_as_float(rg[t + 1]));
+                        dacc[p & 3] = tcx::ffma2(pr2[p], gv2[p], dacc[p & 3]);
                     }
                     float d8[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) d8[i] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) d8[i & 7] = fmaf(pr[i], gv[i], d8[i & 7]);
+                    for (int i = 0; i < 4; ++i) tcx::f2_unpack(dacc[i], d8[2 * i], d8[2 * i + 1]);
                     dl = ((d8[0] + d8[1]) + (d8[2] + d8[3])) + ((d8[4] + d8[5]) + (d8[6] + d8[7]));
                     dl += __shfl_xor_sync(0xffffffffu, dl, 16);     // the row's other 32 keys
                     emit_rows(dl);
+                    const uint64_t wsc2 = tcx::f2_pack(wsc, wsc), ndl2 = tcx::f2_pack(-dl * wsc, -dl * wsc);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int p = 0; p < 16; ++p)
+                        pk[p] = tcx::pack_bf16x2(tcx::fmul2(pr2[p], tcx::ffma2(gv2[p], wsc2, ndl2)));
                     if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        float v8[8];
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) v8[t] = pr[8 * c4 + t] * (gv[8 * c4 + t] - dl);
-                        *reinterpret_cast<uint4*>(pb + sw128_off(row, 4 * u + c4)) = pack8(v8, wsc);
-                    }
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        *reinterpret_cast<uint4*>(pb + sw128_off(row, 4 * u + c4)) =
+                            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
                 } else {
                     // this thread: one token row, all 128 keys in two 64-key chunks
                     float x[64];
@@ -946,34 +956,36 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(&sb.s_empty[sbuf]);
-                    float xs[32], xg[32];
+                    // token pairs in packed f32x2 arithmetic: p = exp2(s sl - lse2) as
+                    // exp2(-(lse2 - s sl)); w P^T and dA^T = w scale p (g - delta)
+                    const ulonglong2* l2v = reinterpret_cast<const ulonglong2*>(vec + 32 * u);
+                    const ulonglong2* d2v = reinterpret_cast<const ulonglong2*>(vec + S + 32 * u);
+                    const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
+                    const uint64_t wsc2 = tcx::f2_pack(wsc, wsc), wv2 = tcx::f2_pack(wv, wv);
+                    uint32_t pa[16], pp[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        xs[t] = __uint_as_float(r0[t]);
-                        xs[16 + t] = __uint_as_float(r1[t]);
-                        xg[t] = __uint_as_float(r2[t]);
-                        xg[16 + t] = __uint_as_float(r3[t]);
-                    }
-                    const float4* l4 = reinterpret_cast<const float4*>(vec + 32 * u);
-                    const float4* d4 = reinterpret_cast<const float4*>(vec + S + 32 * u);
-#pragma unroll
-                    for (int i4 = 0; i4 < 8; ++i4) {
-                        const float4 lv = l4[i4], dv = d4[i4];
-                        const float la[4] = {lv.x, lv.y, lv.z, lv.w}, da[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const int i = 4 * i4 + t;
-                            const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -la[t]));
-                            xs[i] = pr * (xg[i] - da[t]);       // dA^T / (w s)
-                            xg[i] = pr;                         // P^T / w
-                        }
+                    for (int p = 0; p < 16; ++p) {
+                        const uint32_t* rs = p < 8 ? r0 : r1;
+                        const uint32_t* rg = p < 8 ? r2 : r3;
+                        const int t = 2 * (p & 7);
+                        const ulonglong2 lv = l2v[p >> 1], dv = d2v[p >> 1];
+                        float y0, y1;
+                        tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(__uint_as_float(rs[t]), __uint_as_float(rs[t + 1])),
+                                                  nsl2, (p & 1) ? lv.y : lv.x), y0, y1);
+                        const uint64_t pr2 = tcx::f2_pack(fast_exp2(-y0), fast_exp2(-y1));
+                        const uint64_t g2 = tcx::f2_pack(__uint_as_float(rg[t]), __uint_as_float(rg[t + 1]));
+                        pp[p] = tcx::pack_bf16x2(tcx::fmul2(pr2, wv2));
+                        pa[p] = tcx::pack_bf16x2(
+                            tcx::fmul2(tcx::fmul2(pr2, wsc2), tcx::fsub2(g2, (p & 1) ? dv.y : dv.x)));
                     }
                     if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
                         const uint32_t off = sw128_off(row, 4 * u + c4);
-                        *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c4, wsc);
-                        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c4, wv);
+                        *reinterpret_cast<uint4*>(pb + off) =
+                            make_uint4(pa[4 * c4], pa[4 * c4 + 1], pa[4 * c4 + 2], pa[4 * c4 + 3]);
+                        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) =
+                            make_uint4(pp[4 * c4], pp[4 * c4 + 1], pp[4 * c4 + 2], pp[4 * c4 + 3]);
                     }
                 } else {
                     if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
