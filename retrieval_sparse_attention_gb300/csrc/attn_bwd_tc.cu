@@ -1055,6 +1055,413 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     }
 }
 
+// ============================================================================ pass B, S = 64
+// Item = (row, pool chunk, head) as above; a group is a PAIR of inverse-index
+// entries (two query chunks that retrieved this chunk, or one for an odd
+// tail).  Their Q tiles (and dO tiles) sit one above the other in the stage, so
+// S = [Q_1; Q_2] K^T and G = [dO_1; dO_2] V^T are M = 128 products (full rate,
+// all 128 TMEM lanes, four MMAs each per pair instead of eight per entry at
+// M = 64).  A math thread owns one query row of the pair: its lse and delta are
+// scalars, and it writes its 64 keys of w P and dA as one 128-byte row, which
+// the accumulation products read as MN-major A operands:
+// dK += dA^T [Q_1; Q_2] and dV += (w P)^T [dO_1; dO_2] over K = 128 queries
+// (64 for a single entry).
+struct CfgP {
+    static constexpr int S = 64;
+    static constexpr int TILE = 64 * 128;                 // 64 rows x 64 bf16
+    static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
+    static constexpr int STAGES = 3;                      // 6 entries in flight
+    static constexpr int Q_OFF = 0;                       // Q of entries 0 and 1 (rows 0-63, 64-127)
+    static constexpr int DO_OFF = 2 * TILE;               // dO of entries 0 and 1
+    static constexpr int VEC_OFF = 4 * TILE;              // lse2[2][64], then delta[2][64]
+    static constexpr int ENT_OFF = VEC_OFF + 1024;        // EntryInfo[2]
+    static constexpr int STAGE_BYTES = VEC_OFF + 2048;
+    static constexpr int ENTRY_TX = 2 * TILE + 2 * 64 * 4;
+    static constexpr int P_BYTES = 128 * 128;             // one operand: 128 query rows x 64 keys
+    static constexpr int OFF_IT = 0;
+    static constexpr int OFF_ST = 2 * ITEM_BYTES;
+    static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
+    static constexpr int SMEM = OFF_P + 2 * 2 * P_BYTES + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t SGW = 128;                  // S (64 columns), then G
+    static constexpr uint32_t COL_ACC = 2 * SGW;          // dK, dV: 2 x (64 + 64)
+};
+static_assert(CfgP::STAGES <= 6, "barrier arrays");
+
+// D (+)= A^T B over ksteps*16 rows of K, A and B MN-major 128-byte-swizzled
+// tiles with 128-byte K rows (A: [K x 64 M], B: [K x 64 N]).
+__device__ __forceinline__ void mma_mnmajor_mnmajor(uint32_t d, uint32_t a_addr, uint32_t b_addr,
+                                                    uint32_t idesc, int ksteps, uint32_t acc_first) {
+    const uint64_t ad = tc::desc_mnmajor_sw128(a_addr);
+    const uint64_t bd = tc::desc_mnmajor_sw128(b_addr);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        if (ks == ksteps) break;
+        tc::mma_bf16(d, ad + (uint64_t)(ks * 128), bd + (uint64_t)(ks * 128), idesc, ks == 0 ? acc_first : 1u);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                       const BwdArgs a) {
+    using C = CfgP;
+    constexpr int S = C::S;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ BarsB sb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
+    const int nE = a.nQ * a.topk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kInfo; ++i) {
+            mbar_init(&sb.info_full[i], 1);
+            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + math threads
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sb.it_full[i], 1);
+            mbar_init(&sb.it_empty[i], 1);
+            mbar_init(&sb.p_full[i], 128);
+            mbar_init(&sb.p_empty[i], 1);
+            mbar_init(&sb.o_full[i], 1);
+            mbar_init(&sb.o_empty[i], 128);
+            mbar_init(&sb.s_full[i], 1);
+            mbar_init(&sb.s_empty[i], 128);
+        }
+        for (int i = 0; i < C::STAGES; ++i) {
+            mbar_init(&sb.st_full[i], 1);
+            mbar_init(&sb.st_empty[i], 1);
+        }
+        mbar_init(&sb.done, 1);
+        mbar_init(&sb.done2, 1);
+        sb.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tdo);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(&sb.tmem, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sb.tmem;
+
+    if (warp == 0) {
+        // Producer: the whole warp walks the items; lane 0 alone waits and issues
+        // the copies.  Item offsets and entry records are fetched 32 at a time, one
+        // per lane; entries are staged in pairs (lanes u, u + 1 of a batch of 32).
+        constexpr unsigned kAll = 0xffffffffu;
+        Ring st{0, 0}, it{0, 0}, inf{0, 0};
+        bool st_out[C::STAGES] = {}, it_out[2] = {false, false};
+        uint32_t st_ph[C::STAGES] = {}, it_ph[2] = {0, 0};
+        auto lane0_wait = [&](uint64_t* bar, uint32_t par) {
+            int r = 0;
+            if (lane == 0) r = wait(bar, par) ? 1 : 0;
+            return __shfl_sync(kAll, r, 0) != 0;
+        };
+        int my_e0 = 0, my_ne = 0;
+        int n_item = 0;
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_item) {
+            if ((n_item & 31) == 0) {
+                const int it_l = item + lane * gridDim.x;
+                my_e0 = my_ne = 0;
+                if (it_l < a.n_items) {
+                    const int bk_l = it_l / a.H, kap_l = bk_l % a.nP, b_l = bk_l / a.nP;
+                    const int* off = a.offset + (size_t)b_l * (a.nP + 1) + kap_l;
+                    my_e0 = off[0];
+                    my_ne = off[1] - my_e0;
+                }
+            }
+            const int e0 = __shfl_sync(kAll, my_e0, n_item & 31);
+            const int ne = __shfl_sync(kAll, my_ne, n_item & 31);
+            const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
+            if (!lane0_wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
+            if (lane == 0) {
+                ItemInfoB& I = sb.info[inf.i];
+                I.b = b; I.kap = kap; I.h = h; I.ne = ne;
+                mbar_arrive(&sb.info_full[inf.i]);
+            }
+            inf.next(kInfo);
+            if (ne <= 0) continue;
+            const int* ent = a.entry + (size_t)b * nE + e0;
+            if (!lane0_wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
+            if (lane == 0) {
+                uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
+                mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
+                tma_load_2d(ib, &tk, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
+                tma_load_2d(ib + C::TILE, &tv, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
+            }
+            it_out[it.i] = true;
+            it_ph[it.i] = it.ph;
+            it.next(2);
+            bool ok = true;
+            for (int base = 0; base < ne && ok; base += 32) {
+                int my_c = 0, my_j = 0;
+                float my_w = 0.f;
+                if (base + lane < ne) {
+                    const int e = ent[base + lane];
+                    my_c = e / a.topk;
+                    my_j = e % a.topk;
+                    my_w = a.w[((size_t)b * a.nQ + my_c) * a.topk + my_j];
+                }
+                const int cnt = min(32, ne - base);
+                for (int u = 0; u < cnt; u += 2) {
+                    const int n2 = (u + 1 < cnt) ? 2 : 1;
+                    int cc[2], jj[2];
+                    float ww[2];
+                    for (int x = 0; x < 2; ++x) {
+                        const int src = (x < n2) ? u + x : u;
+                        cc[x] = __shfl_sync(kAll, my_c, src);
+                        jj[x] = __shfl_sync(kAll, my_j, src);
+                        ww[x] = __shfl_sync(kAll, my_w, src);
+                    }
+                    if (!lane0_wait(&sb.st_empty[st.i], st.ph ^ 1u)) { ok = false; break; }
+                    if (lane == 0) {
+                        uint8_t* stg = sm + C::OFF_ST + st.i * C::STAGE_BYTES;
+                        EntryInfo* ei = reinterpret_cast<EntryInfo*>(stg + C::ENT_OFF);
+                        mbar_arrive_expect_tx(&sb.st_full[st.i], n2 * C::ENTRY_TX);
+                        for (int x = 0; x < n2; ++x) {
+                            ei[x].c = cc[x]; ei[x].j = jj[x]; ei[x].w = ww[x];
+                            tma_load_2d(stg + C::Q_OFF + x * C::TILE, &tq, &sb.st_full[st.i], h * 64,
+                                        b * a.Lq + cc[x] * S);
+                            tma_load_2d(stg + C::DO_OFF + x * C::TILE, &tdo, &sb.st_full[st.i], h * 64,
+                                        b * a.Lq + cc[x] * S);
+                            const size_t rb = ((((size_t)b * a.nQ + cc[x]) * a.topk + jj[x]) * a.H + h) * S;
+                            tcx::bulk_load(stg + C::VEC_OFF + x * 256, a.lse2_rows + rb, S * 4, &sb.st_full[st.i]);
+                            tcx::bulk_load(stg + C::VEC_OFF + 512 + x * 256, a.delta_rows + rb, S * 4,
+                                           &sb.st_full[st.i]);
+                        }
+                    }
+                    st_out[st.i] = true;
+                    st_ph[st.i] = st.ph;
+                    st.next(C::STAGES);
+                }
+            }
+            if (!ok) break;
+        }
+        if (lane == 0) {
+            for (int i = 0; i < C::STAGES; ++i)
+                if (st_out[i]) mbar_wait(&sb.st_full[i], st_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < 2; ++i)
+                if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
+        }
+    } else if (warp == 1) {
+        // S = [Q_1; Q_2] K^T and G = [dO_1; dO_2] V^T of each pair (M = 128, N = 64)
+        if (lane == 0) {
+            Ring st{0, 0}, it{0, 0}, inf{0, 0};
+            int q = 0;
+            bool issued = false;
+            const uint32_t id_s = idesc_bf16(128, S, false, false);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+                const int ne = sb.info[inf.i].ne;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (ne <= 0) continue;
+                const int ng = (ne + 1) >> 1;
+                if (!wait(&sb.it_full[it.i], it.ph)) break;
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
+                const uint32_t vaddr = kaddr + C::TILE;
+                bool ok = true;
+                for (int g = 0; g < ng; ++g) {
+                    const int qq = q + g, sbuf = qq & 1;
+                    if (!wait(&sb.st_full[st.i], st.ph) || !wait(&sb.s_empty[sbuf], empty_par(qq >> 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, stg + C::Q_OFF, kaddr, id_s, 0);
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, vaddr, id_s, 0);
+                    mma_commit(&sb.s_full[sbuf]);
+                    issued = true;
+                    st.next(C::STAGES);
+                }
+                if (!ok) break;
+                mma_commit(&sb.it_empty[it.i]);     // K and V are read only by these products
+                it.next(2);
+                q += ng;
+            }
+            if (issued) {
+                mma_commit(&sb.done);
+                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+            }
+        }
+    } else if (warp == 2) {
+        // dK += dA^T [Q_1; Q_2] and dV += (w P)^T [dO_1; dO_2] (M = 64 keys, K = the pair's queries)
+        if (lane == 0) {
+            Ring st{0, 0}, inf{0, 0};
+            int q = 0, e = 0;
+            bool issued = false;
+            const uint32_t id_acc = idesc_bf16(64, 64, true, true);
+            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+                if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+                const int ne = sb.info[inf.i].ne;
+                mbar_arrive(&sb.info_empty[inf.i]);
+                inf.next(kInfo);
+                if (ne <= 0) continue;
+                const int ng = (ne + 1) >> 1;
+                const int ob = e & 1;
+                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
+                tc_fence_after();
+                const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
+                const uint32_t d_dv = d_dk + 64;
+                bool ok = true;
+                for (int g = 0; g < ng; ++g) {
+                    const int qq = q + g, pbuf = qq & 1;
+                    const int ksteps = (2 * g + 1 < ne) ? 8 : 4;
+                    if (!wait(&sb.p_full[pbuf], full_par(qq >> 1))) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
+                    const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
+                    mma_mnmajor_mnmajor(d_dk, paddr, stg + C::Q_OFF, id_acc, ksteps, g > 0 ? 1u : 0u);
+                    mma_mnmajor_mnmajor(d_dv, paddr + C::P_BYTES, stg + C::DO_OFF, id_acc, ksteps,
+                                        g > 0 ? 1u : 0u);
+                    mma_commit(&sb.st_empty[st.i]);
+                    mma_commit(&sb.p_empty[pbuf]);
+                    issued = true;
+                    st.next(C::STAGES);
+                }
+                if (!ok) break;
+                mma_commit(&sb.o_full[ob]);
+                q += ng;
+                ++e;
+            }
+            if (issued) {
+                mma_commit(&sb.done2);
+                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+            }
+        }
+    } else {
+        const int wg = (warp - 3) >> 2;
+        const int qd = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+        const int prow = 32 * qd + lane;            // query row of the pair (M = 128 layout)
+        const int pe = prow >> 6, ptr = prow & 63;  // its entry and token row
+        const int erow = 16 * qd + (lane & 15);     // key row of the dK/dV accumulators (M = 64)
+        const int eu = lane >> 4;
+        const float* vec0 = nullptr;
+        Ring inf{0, 0}, st{0, 0};
+        int q = 0, e = 0, n_all = 0, kg = 0;
+        const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
+        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_all) {
+            if (!wait(&sb.info_full[inf.i], inf.ph)) break;
+            const ItemInfoB I = sb.info[inf.i];
+            mbar_arrive(&sb.info_empty[inf.i]);
+            inf.next(kInfo);
+            const size_t krow = (size_t)(I.b * a.nP + I.kap) * S + erow;
+            __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * 64;
+            __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * 64;
+            if (I.ne <= 0) {
+                if ((n_all & 1) == wg) {
+                    zero_row64<S>(dkrow, eu);
+                    zero_row64<S>(dvrow, eu);
+                }
+                continue;
+            }
+            const int ng = (I.ne + 1) >> 1;
+            bool ok = true;
+            for (int g = 0; g < ng; ++g) {
+                const int qq = q + g;
+                const int stage = st.i;
+                const uint32_t stph = st.ph;
+                st.next(C::STAGES);
+                if ((qq & 1) != wg) continue;
+                const int sbuf = qq & 1;
+                // our own s_full first: its completion implies this pair's stage copy
+                // has landed, so the stage barrier's phase below is unambiguous
+                if (!wait(&sb.s_full[sbuf], full_par(kg)) || !wait(&sb.st_full[stage], stph)) { ok = false; break; }
+                tc_fence_after();
+                const uint8_t* stg = sm + C::OFF_ST + stage * C::STAGE_BYTES;
+                // a single-entry pair leaves rows 64-127 unused (the products read K = 64)
+                const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[pe];
+                vec0 = reinterpret_cast<const float*>(stg + C::VEC_OFF);
+                const float lse2 = vec0[pe * 64 + ptr], dlt = vec0[128 + pe * 64 + ptr];
+                const float wv = ei.w, wsc = wv * a.attn_scale;
+                const uint64_t l2 = tcx::f2_pack(lse2, lse2), dl2 = tcx::f2_pack(dlt, dlt);
+                const uint64_t wv2 = tcx::f2_pack(wv, wv), wsc2 = tcx::f2_pack(wsc, wsc);
+                uint8_t* pa_buf = sm + C::OFF_P + wg * 2 * C::P_BYTES;
+                uint8_t* pp_buf = pa_buf + C::P_BYTES;
+                const uint32_t ts0 = tmem + lane_base + sbuf * C::SGW;
+                const uint32_t tg0 = ts0 + 64;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    // keys 32 hf .. 32 hf + 31 of this query row
+                    uint32_t r0[16], r1[16], r2[16], r3[16];
+                    tmem_ld_32x32b_x16(ts0 + 32 * hf, r0);
+                    tmem_ld_32x32b_x16(ts0 + 32 * hf + 16, r1);
+                    tmem_ld_32x32b_x16(tg0 + 32 * hf, r2);
+                    tmem_ld_32x32b_x16(tg0 + 32 * hf + 16, r3);
+                    tmem_wait_ld();
+                    if (hf == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty[sbuf]);
+                    }
+                    // key pairs in packed f32x2 arithmetic: p = exp2(-(lse2 - s sl)),
+                    // w P and dA = w scale p (g - delta)
+                    uint32_t pa[16], pp[16];
+#pragma unroll
+                    for (int p = 0; p < 16; ++p) {
+                        const uint32_t* rs = p < 8 ? r0 : r1;
+                        const uint32_t* rg = p < 8 ? r2 : r3;
+                        const int t = 2 * (p & 7);
+                        float y0, y1;
+                        tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(__uint_as_float(rs[t]), __uint_as_float(rs[t + 1])),
+                                                  nsl2, l2), y0, y1);
+                        const uint64_t pr2 = tcx::f2_pack(fast_exp2(-y0), fast_exp2(-y1));
+                        const uint64_t g2 = tcx::f2_pack(__uint_as_float(rg[t]), __uint_as_float(rg[t + 1]));
+                        pp[p] = tcx::pack_bf16x2(tcx::fmul2(pr2, wv2));
+                        pa[p] = tcx::pack_bf16x2(tcx::fmul2(tcx::fmul2(pr2, wsc2), tcx::fsub2(g2, dl2)));
+                    }
+                    if (hf == 0 && !wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const uint32_t off = sw128_off(prow, 4 * hf + c4);
+                        *reinterpret_cast<uint4*>(pa_buf + off) =
+                            make_uint4(pa[4 * c4], pa[4 * c4 + 1], pa[4 * c4 + 2], pa[4 * c4 + 3]);
+                        *reinterpret_cast<uint4*>(pp_buf + off) =
+                            make_uint4(pp[4 * c4], pp[4 * c4 + 1], pp[4 * c4 + 2], pp[4 * c4 + 3]);
+                    }
+                }
+                if (!ok) break;
+                fence_proxy_async_smem();
+                mbar_arrive(&sb.p_full[wg]);
+                ++kg;
+            }
+            if (!ok) break;
+            q += ng;
+            const bool mine = (e & 1) == wg;
+            const int ob = e & 1, ko = e >> 1;
+            ++e;
+            if (!mine) continue;
+            if (!wait(&sb.o_full[ob], full_par(ko))) break;
+            tc_fence_after();
+            const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 128;
+            store_row64<S>(acc, dkrow, eu);
+            store_row64<S>(acc + 64, dvrow, eu);
+            tc_fence_before();
+            mbar_arrive(&sb.o_empty[ob]);
+        }
+        (void)vec0;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, CfgP::TMEM_COLS);
+    }
+}
+
 // ============================================================================ launch
 template <int S>
 cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const void* v,
@@ -1104,11 +1511,18 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     a.n_items = sp.B * sp.nP * sp.H;
-    auto kb = gca_bwd_kv_tc_kernel<S>;
-    e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S>::SMEM);
-    if (e != cudaSuccess) return e;
     grid = a.n_items < sms ? a.n_items : sms;
-    GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgB<S>::SMEM, st>>>(tq, tdo, tk, tv, a));
+    if constexpr (S == 64) {
+        auto kb = gca_bwd_kv_pair_kernel;
+        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgP::SMEM);
+        if (e != cudaSuccess) return e;
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgP::SMEM, st>>>(tq, tdo, tk, tv, a));
+    } else {
+        auto kb = gca_bwd_kv_tc_kernel<S>;
+        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S>::SMEM);
+        if (e != cudaSuccess) return e;
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgB<S>::SMEM, st>>>(tq, tdo, tk, tv, a));
+    }
     return cudaGetLastError();
 }
 
