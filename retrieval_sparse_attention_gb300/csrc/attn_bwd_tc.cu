@@ -60,6 +60,7 @@ struct BwdArgs {
     float* dwpart;             // [B, nQ, H, 4, topk]: per TMEM lane quadrant
     const int* offset;         // [B, nP + 1]
     const int* entry;          // [B, nQ * topk]
+    const float* entry_w;      // [B, nQ * topk]: the weight of each entry
     __nv_bfloat16* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -1156,8 +1157,10 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
 
     if (warp == 0) {
         // Producer: the whole warp walks the items; lane 0 alone waits and issues
-        // the copies.  Item offsets and entry records are fetched 32 at a time, one
-        // per lane; entries are staged in pairs (lanes u, u + 1 of a batch of 32).
+        // the copies.  Item offsets are fetched 32 items at a time and entry records
+        // (entry, weight) 32 entries at a time, one per lane; the next item's offsets
+        // and first records are loaded while this item is staged, so no dependent
+        // global load sits between two items.  Entries are staged in pairs.
         constexpr unsigned kAll = 0xffffffffu;
         Ring st{0, 0}, it{0, 0}, inf{0, 0};
         bool st_out[C::STAGES] = {}, it_out[2] = {false, false};
@@ -1167,22 +1170,44 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             if (lane == 0) r = wait(bar, par) ? 1 : 0;
             return __shfl_sync(kAll, r, 0) != 0;
         };
-        int my_e0 = 0, my_ne = 0;
-        int n_item = 0;
-        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_item) {
-            if ((n_item & 31) == 0) {
-                const int it_l = item + lane * gridDim.x;
-                my_e0 = my_ne = 0;
-                if (it_l < a.n_items) {
-                    const int bk_l = it_l / a.H, kap_l = bk_l % a.nP, b_l = bk_l / a.nP;
-                    const int* off = a.offset + (size_t)b_l * (a.nP + 1) + kap_l;
-                    my_e0 = off[0];
-                    my_ne = off[1] - my_e0;
-                }
+        int my_e0 = 0, my_ne = 0;           // lane l: offsets of the batch's l-th item
+        auto load_offsets = [&](int item0) {
+            const int it_l = item0 + lane * gridDim.x;
+            my_e0 = my_ne = 0;
+            if (it_l < a.n_items) {
+                const int bk_l = it_l / a.H, kap_l = bk_l % a.nP, b_l = bk_l / a.nP;
+                const int* off = a.offset + (size_t)b_l * (a.nP + 1) + kap_l;
+                my_e0 = off[0];
+                my_ne = off[1] - my_e0;
             }
-            const int e0 = __shfl_sync(kAll, my_e0, n_item & 31);
-            const int ne = __shfl_sync(kAll, my_ne, n_item & 31);
+        };
+        auto fetch = [&](int b_, int e0_, int ne_, int base, int& e_out, float& w_out) {
+            e_out = 0;
+            w_out = 0.f;
+            if (base + lane < ne_) {
+                const size_t at = (size_t)b_ * nE + e0_ + base + lane;
+                e_out = a.entry[at];
+                w_out = a.entry_w[at];
+            }
+        };
+        int item = blockIdx.x, n_item = 0;
+        if (item < a.n_items) load_offsets(item);
+        int nx_e0 = __shfl_sync(kAll, my_e0, 0), nx_ne = __shfl_sync(kAll, my_ne, 0);
+        int nx_e = 0;
+        float nx_w = 0.f;
+        if (item < a.n_items) fetch(item / a.H / a.nP, nx_e0, nx_ne, 0, nx_e, nx_w);
+        for (; item < a.n_items; item += gridDim.x, ++n_item) {
             const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
+            const int e0 = nx_e0, ne = nx_ne;
+            int bat_e = nx_e;
+            float bat_w = nx_w;
+            {
+                const int nn = n_item + 1, nitem = item + gridDim.x;
+                if ((nn & 31) == 0 && nitem < a.n_items) load_offsets(nitem);
+                nx_e0 = __shfl_sync(kAll, my_e0, nn & 31);
+                nx_ne = __shfl_sync(kAll, my_ne, nn & 31);
+                if (nitem < a.n_items) fetch(nitem / a.H / a.nP, nx_e0, nx_ne, 0, nx_e, nx_w);
+            }
             if (!lane0_wait(&sb.info_empty[inf.i], inf.ph ^ 1u)) break;
             if (lane == 0) {
                 ItemInfoB& I = sb.info[inf.i];
@@ -1191,7 +1216,6 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             }
             inf.next(kInfo);
             if (ne <= 0) continue;
-            const int* ent = a.entry + (size_t)b * nE + e0;
             if (!lane0_wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
             if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
@@ -1204,14 +1228,9 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             it.next(2);
             bool ok = true;
             for (int base = 0; base < ne && ok; base += 32) {
-                int my_c = 0, my_j = 0;
-                float my_w = 0.f;
-                if (base + lane < ne) {
-                    const int e = ent[base + lane];
-                    my_c = e / a.topk;
-                    my_j = e % a.topk;
-                    my_w = a.w[((size_t)b * a.nQ + my_c) * a.topk + my_j];
-                }
+                if (base > 0) fetch(b, e0, ne, base, bat_e, bat_w);
+                const int my_c = bat_e / a.topk, my_j = bat_e % a.topk;
+                const float my_w = bat_w;
                 const int cnt = min(32, ne - base);
                 for (int u = 0; u < cnt; u += 2) {
                     const int n2 = (u + 1 < cnt) ? 2 : 1;
@@ -1483,6 +1502,7 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     a.dwpart = reinterpret_cast<float*>(base + L.dwpart_off);
     a.offset = reinterpret_cast<const int*>(base + L.offset_off);
     a.entry = reinterpret_cast<const int*>(base + L.entry_off);
+    a.entry_w = reinterpret_cast<const float*>(base + L.entry_w_off);
     a.dq = static_cast<__nv_bfloat16*>(dq);
     a.dk = static_cast<__nv_bfloat16*>(dk);
     a.dv = static_cast<__nv_bfloat16*>(dv);
@@ -1532,7 +1552,7 @@ cudaError_t launch_bwd_tc(const Shape& sp, const void* q, const void* k, const v
                           const int32_t* idx, const float* w, const float* lse, const void* dout,
                           void* dq, void* dk, void* dv, float* dscore, void* ws, int* status,
                           cudaStream_t st, int* launches) {
-    cudaError_t e = launch_inverse_index(sp, idx, ws, st, launches);
+    cudaError_t e = launch_inverse_index(sp, idx, w, ws, st, launches);
     if (e != cudaSuccess) return e;
     e = (sp.S == 64) ? launch_bwd_s<64>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st)
                      : launch_bwd_s<128>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);

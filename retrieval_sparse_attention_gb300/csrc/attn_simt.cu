@@ -285,7 +285,7 @@ cudaError_t launch_bwd_simt(const Shape& sp, const void* q, const void* k, const
                             const int32_t* idx, const float* w, const float* lse,
                             const void* dout, void* dq, void* dk, void* dv, float* dscore,
                             void* ws, int* status, cudaStream_t st, int* launches) {
-    cudaError_t e = launch_inverse_index(sp, idx, ws, st, launches);
+    cudaError_t e = launch_inverse_index(sp, idx, w, ws, st, launches);
     if (e != cudaSuccess) return e;
     e = cudaErrorInvalidValue;
     if (sp.dtype == GCA_F32) {

@@ -22,6 +22,7 @@ BwdWorkspace bwd_workspace_layout(const Shape& s) {
     w.count_off = off;  off += align256(sizeof(int) * (size_t)s.B * s.nP);
     w.offset_off = off; off += align256(sizeof(int) * (size_t)s.B * (s.nP + 1));
     w.entry_off = off;  off += align256(sizeof(int) * (size_t)s.B * s.nQ * s.topk);
+    w.entry_w_off = off; off += align256(sizeof(float) * (size_t)s.B * s.nQ * s.topk);
     w.total = off;
     return w;
 }
@@ -70,9 +71,12 @@ __global__ void inv_scan_kernel(const int* __restrict__ count, int nP, int* __re
 }
 
 // One warp per (b, kappa): write the entries e = c*topk + j with
-// idx[b][e] == kappa, in ascending e, into the CSR bucket of kappa.
+// idx[b][e] == kappa, in ascending e, into the CSR bucket of kappa (and, if
+// entry_w is given, the weight w[b][e] beside each, so that a reader of the
+// bucket needs no dependent load).
 __global__ void inv_fill_kernel(const int32_t* __restrict__ idx, int B, int nE, int nP,
-                                const int* __restrict__ offset, int* __restrict__ entry) {
+                                const int* __restrict__ offset, int* __restrict__ entry,
+                                const float* __restrict__ w, float* __restrict__ entry_w) {
     const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (gw >= B * nP) return;
@@ -85,7 +89,11 @@ __global__ void inv_fill_kernel(const int32_t* __restrict__ idx, int B, int nE, 
         const int e = e0 + lane;
         const bool hit = e < nE && row[e] == kap;
         const unsigned m = __ballot_sync(0xffffffffu, hit);
-        if (hit) out[pos + __popc(m & below)] = e;
+        if (hit) {
+            const int at = pos + __popc(m & below);
+            out[at] = e;
+            if (entry_w) entry_w[(size_t)b * nE + at] = w[(size_t)b * nE + e];
+        }
         pos += __popc(m);
     }
 }
@@ -117,13 +125,14 @@ __global__ void dscore_kernel(const int32_t* __restrict__ idx, const float* __re
 
 }  // namespace
 
-cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, cudaStream_t st,
-                                 int* launches) {
+cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, const float* w, void* ws,
+                                 cudaStream_t st, int* launches) {
     const BwdWorkspace L = bwd_workspace_layout(s);
     char* base = static_cast<char*>(ws);
     return launch_inverse_index_to(s, idx, reinterpret_cast<int*>(base + L.count_off),
                                    reinterpret_cast<int*>(base + L.offset_off),
-                                   reinterpret_cast<int*>(base + L.entry_off), st, launches);
+                                   reinterpret_cast<int*>(base + L.entry_off), w,
+                                   reinterpret_cast<float*>(base + L.entry_w_off), st, launches);
 }
 
 size_t inverse_index_bytes(int B, int nQ, int nP, int topk) {
@@ -132,13 +141,15 @@ size_t inverse_index_bytes(int B, int nQ, int nP, int topk) {
 }
 
 cudaError_t launch_inverse_index_to(const Shape& s, const int32_t* idx, int* count, int* offset,
-                                    int* entry, cudaStream_t st, int* launches) {
+                                    int* entry, const float* w, float* entry_w, cudaStream_t st,
+                                    int* launches) {
     const int nE = s.nQ * s.topk;
     const int warps = s.B * s.nP;
     const int blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     GCA_LAUNCH("inv_count", st, inv_count_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, count));
     GCA_LAUNCH("inv_scan", st, inv_scan_kernel<<<s.B, 1024, 0, st>>>(count, s.nP, offset));
-    GCA_LAUNCH("inv_fill", st, inv_fill_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, offset, entry));
+    GCA_LAUNCH("inv_fill", st, inv_fill_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, offset, entry,
+                                                                                   w, w ? entry_w : nullptr));
     *launches += 3;
     return cudaGetLastError();
 }

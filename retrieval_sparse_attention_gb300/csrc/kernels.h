@@ -43,6 +43,7 @@ struct BwdWorkspace {
     size_t count_off;     // int32 [B, nP]: how many (c, j) retrieved each pool chunk
     size_t offset_off;    // int32 [B, nP + 1]: CSR offsets of the inverse index
     size_t entry_off;     // int32 [B, nQ * topk]: entries c * topk + j, ascending
+    size_t entry_w_off;   // fp32 [B, nQ * topk]: the fusion weight w[b][c][j] of each entry
     size_t total;
 };
 BwdWorkspace bwd_workspace_layout(const Shape& s);
@@ -86,11 +87,14 @@ cudaError_t launch_bwd_tc(const Shape& s, const void* q, const void* k, const vo
                           void* ws, int* status, cudaStream_t st, int* launches);
 
 // Shared backward pieces (inverse index, score gradient).
-cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, void* ws, cudaStream_t st,
-                                 int* launches);
-// Inverse index into explicit buffers: count [B, nP], offset [B, nP+1], entry [B, nQ*topk].
+// (w [B, nQ, topk]: the fusion weights, copied beside the entries into the workspace)
+cudaError_t launch_inverse_index(const Shape& s, const int32_t* idx, const float* w, void* ws,
+                                 cudaStream_t st, int* launches);
+// Inverse index into explicit buffers: count [B, nP], offset [B, nP+1], entry [B, nQ*topk],
+// and, when both are given, entry_w[i] = w at entry i's (b, c, j).
 cudaError_t launch_inverse_index_to(const Shape& s, const int32_t* idx, int* count, int* offset,
-                                    int* entry, cudaStream_t st, int* launches);
+                                    int* entry, const float* w, float* entry_w, cudaStream_t st,
+                                    int* launches);
 cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, void* ws,
                           float* dscore, cudaStream_t st, int* launches);
 

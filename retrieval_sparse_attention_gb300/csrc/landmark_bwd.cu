@@ -60,7 +60,7 @@ cudaError_t launch_landmark_bwd(const Shape& s, const void* lm, const int32_t* i
     int* offset = reinterpret_cast<int*>(base + c_bytes);
     const size_t o_bytes = ((sizeof(int) * (size_t)p.B * (p.nP + 1)) + 255) / 256 * 256;
     int* entry = reinterpret_cast<int*>(base + c_bytes + o_bytes);
-    cudaError_t e = launch_inverse_index_to(p, idx, count, offset, entry, st, launches);
+    cudaError_t e = launch_inverse_index_to(p, idx, count, offset, entry, nullptr, nullptr, st, launches);
     if (e != cudaSuccess) return e;
     dim3 grid(p.nQ, p.B);
     if (p.dtype == GCA_BF16)
