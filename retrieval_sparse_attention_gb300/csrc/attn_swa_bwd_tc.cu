@@ -359,6 +359,10 @@ swa_bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             const size_t vrow = ((size_t)it.b * a.H + it.h) * a.Lp + t;   // t < Lp
             const float lse2 = a.lse2T[vrow];
             const float dlt = a.deltaT[vrow];
+            const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2), l2 = tcx::f2_pack(lse2, lse2);
+            const uint64_t sc2 = tcx::f2_pack(a.scale, a.scale);
+            const uint64_t ndsc2 = tcx::f2_pack(-dlt * a.scale, -dlt * a.scale);
+            const uint32_t span = static_cast<uint32_t>(a.W - 1);
             for (int j = 0; j < it.nt; ++j) {
                 if (!wait(&sb.s_full[wg], full_par(ts))) { ok = false; break; }
                 tc_fence_after();
@@ -388,24 +392,32 @@ swa_bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                         tc_fence_before();
                         mbar_arrive(&sb.s_empty[wg]);
                     }
+                    // column pairs in packed f32x2 arithmetic: p = exp2(-(lse2 - s sl)),
+                    // dS = p (dP - delta) scale; on a tile that the window edge or the
+                    // diagonal crosses, key t0 + c outside [lo, t] gets p = 0 (a select)
+                    uint32_t pk[16];
+                    const int cb = kbase + 32 * hf - lo;          // column 0 relative to lo
+                    auto body = [&](bool msk) {
+#pragma unroll
+                        for (int pi = 0; pi < 16; ++pi) {
+                            float y0, y1;
+                            tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(x[2 * pi], x[2 * pi + 1]), nsl2, l2), y0, y1);
+                            float p0 = fast_exp2(-y0), p1 = fast_exp2(-y1);
+                            if (msk) {
+                                p0 = static_cast<uint32_t>(cb + 2 * pi) > span ? 0.f : p0;
+                                p1 = static_cast<uint32_t>(cb + 2 * pi + 1) > span ? 0.f : p1;
+                            }
+                            const uint64_t gd = tcx::ffma2(tcx::f2_pack(g[2 * pi], g[2 * pi + 1]), sc2, ndsc2);
+                            pk[pi] = tcx::pack_bf16x2(tcx::fmul2(tcx::f2_pack(p0, p1), gd));
+                        }
+                    };
+                    if (edge) body(true);
+                    else body(false);
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int u2 = 0; u2 < 4; ++u2) {
-                            float d2[2];
-#pragma unroll
-                            for (int v2 = 0; v2 < 2; ++v2) {
-                                const int xi = 8 * ch + 2 * u2 + v2, c = 32 * hf + xi;
-                                float p = fast_exp2(fmaf(x[xi], a.scale_log2, -lse2));
-                                if (edge && (kbase + c > t || kbase + c < lo)) p = 0.f;
-                                d2[v2] = p * (g[xi] - dlt) * a.scale;
-                            }
-                            pk[u2] = tcx::pack_bf16(d2[0], d2[1]);
-                        }
                         const int chunk = 4 * hf + ch;
                         *reinterpret_cast<uint4*>(dsbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
                     }
                 }
                 fence_proxy_async_smem();
@@ -709,6 +721,10 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             if (n[wg] == 0) break;                    // no more items for this warpgroup
             const int s = mine.kt * BM + row;         // this thread's key
+            const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
+            const uint64_t sc2 = tcx::f2_pack(a.scale, a.scale);
+            // queries s .. min(s + W - 1, L - 1) see this key (rows past L are never stored)
+            const uint32_t span = static_cast<uint32_t>(min(a.W - 1, a.L - 1 - s));
             const int nmax = n[0] > n[1] ? n[0] : n[1];
             for (int j = 0; j < nmax && ok; ++j)
                 for (int w = 0; w < 2; ++w) {
@@ -723,7 +739,8 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     const float4* l4 = reinterpret_cast<const float4*>(sm + OFF_Q + stg * STAGE + VEC);
                     const float4* d4 = reinterpret_cast<const float4*>(sm + OFF_DO + stg * STAGE + VEC);
                     const int qb = (mine.q0 + j) * BT;
-                    const bool edge = qb < s || qb + BT - 1 > s + a.W - 1 || qb + BT > a.L;
+                    // warp-uniform: the selects below are exact per lane
+                    const bool edge = __any_sync(0xffffffffu, qb < s || qb + BT - 1 > s + a.W - 1 || qb + BT > a.L);
                     // the previous accumulation products have read the operand buffers
                     // (for a first tile: the previous item's stores have read them too)
                     if (!wait(&sb.p_empty[wg], empty_par(ts)) ||
@@ -748,34 +765,42 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             tc_fence_before();
                             mbar_arrive(&sb.s_empty[wg]);
                         }
+                        // query pairs in packed f32x2 arithmetic: P^T = exp2(-(lse2 - s sl)),
+                        // dS^T = p (dP - delta) scale; on a tile that the window edges cross,
+                        // query tq outside [s, min(s + W - 1, L - 1)] gets p = 0 (a select)
+                        const ulonglong2* l2v = reinterpret_cast<const ulonglong2*>(l4) + 8 * hf;
+                        const ulonglong2* d2v = reinterpret_cast<const ulonglong2*>(d4) + 8 * hf;
+                        const int cb = qb + 32 * hf - s;            // column 0 relative to s
+                        uint32_t pp[16], pd[16];
+                        auto body = [&](bool msk) {
+#pragma unroll
+                            for (int pi = 0; pi < 16; ++pi) {
+                                const ulonglong2 lv = l2v[pi >> 1], dv = d2v[pi >> 1];
+                                float y0, y1;
+                                tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(x[2 * pi], x[2 * pi + 1]), nsl2,
+                                                          (pi & 1) ? lv.y : lv.x), y0, y1);
+                                float p0 = fast_exp2(-y0), p1 = fast_exp2(-y1);
+                                if (msk) {
+                                    p0 = static_cast<uint32_t>(cb + 2 * pi) > span ? 0.f : p0;
+                                    p1 = static_cast<uint32_t>(cb + 2 * pi + 1) > span ? 0.f : p1;
+                                }
+                                const uint64_t p2 = tcx::f2_pack(p0, p1);
+                                const uint64_t g2 = tcx::f2_pack(g[2 * pi], g[2 * pi + 1]);
+                                pp[pi] = tcx::pack_bf16x2(p2);
+                                pd[pi] = tcx::pack_bf16x2(
+                                    tcx::fmul2(tcx::fmul2(p2, sc2), tcx::fsub2(g2, (pi & 1) ? dv.y : dv.x)));
+                            }
+                        };
+                        if (edge) body(true);
+                        else body(false);
 #pragma unroll
                         for (int ch = 0; ch < 4; ++ch) {
-                            uint32_t pp[4], pd[4];
-#pragma unroll
-                            for (int h4 = 0; h4 < 2; ++h4) {
-                                const int i4 = 8 * hf + 2 * ch + h4;       // float4 index of the column
-                                const float4 lv = l4[i4], dv = d4[i4];
-                                const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-                                const float da[4] = {dv.x, dv.y, dv.z, dv.w};
-                                float pv[4], dsv[4];
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int c = 4 * i4 + u, tq = qb + c;
-                                    const int xi = c - 32 * hf;
-                                    float p = fast_exp2(fmaf(x[xi], a.scale_log2, -la[u]));
-                                    if (edge && (tq < s || tq > s + a.W - 1 || tq >= a.L)) p = 0.f;
-                                    pv[u] = p;
-                                    dsv[u] = p * (g[xi] - da[u]) * a.scale;
-                                }
-                                pp[2 * h4] = tcx::pack_bf16(pv[0], pv[1]);
-                                pp[2 * h4 + 1] = tcx::pack_bf16(pv[2], pv[3]);
-                                pd[2 * h4] = tcx::pack_bf16(dsv[0], dsv[1]);
-                                pd[2 * h4 + 1] = tcx::pack_bf16(dsv[2], dsv[3]);
-                            }
                             const int chunk = 4 * hf + ch;
                             const int off = row * 128 + ((chunk ^ (row & 7)) << 4);
-                            *reinterpret_cast<uint4*>(ptbuf + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
-                            *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+                            *reinterpret_cast<uint4*>(ptbuf + off) =
+                                make_uint4(pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2], pp[4 * ch + 3]);
+                            *reinterpret_cast<uint4*>(dsbuf + off) =
+                                make_uint4(pd[4 * ch], pd[4 * ch + 1], pd[4 * ch + 2], pd[4 * ch + 3]);
                         }
                     }
                     fence_proxy_async_smem();
