@@ -98,28 +98,132 @@ __global__ void inv_fill_kernel(const int32_t* __restrict__ idx, int B, int nE, 
     }
 }
 
-// One thread per (b, c): reduce the partial dw (per head and per quarter of
-// the chunk's tokens) in a fixed order, then
-// apply the softmax Jacobian (same form for the vanilla and off-by-one
-// softmax, whose Jacobians are both diag(w) - w w^T).
+// One warp per (b, c): lane l sums the partials (head, token quarter) l, l + 32, ... of
+// every slot, a shuffle tree over the warp (fixed order, lane 0's result broadcast)
+// gives the slot totals dw_j, then the softmax Jacobian (same form for the vanilla
+// and off-by-one softmax, whose Jacobians are both diag(w) - w w^T):
+// dr_j = w_j (dw_j - sum_i w_i dw_i).
 __global__ void dscore_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w,
                               const float* __restrict__ dwpart, int n_rows, int H, int topk,
                               int nP, float* __restrict__ dscore) {
-    const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     if (row >= n_rows) return;
-    float dw[kMaxTopk];
-    float wdw = 0.f;
-    for (int j = 0; j < topk; ++j) {
-        float acc = 0.f;
-        for (int hq = 0; hq < 4 * H; ++hq) acc += dwpart[((size_t)row * 4 * H + hq) * topk + j];
-        dw[j] = acc;
-        const int kap = idx[(size_t)row * topk + j];
-        if (kap >= 0 && kap < nP) wdw += w[(size_t)row * topk + j] * acc;
+    const float* dp = dwpart + (size_t)row * 4 * H * topk;
+    float acc[kMaxTopk];
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) acc[j] = 0.f;
+    for (int hq = lane; hq < 4 * H; hq += 32) {
+#pragma unroll
+        for (int j = 0; j < kMaxTopk; ++j)
+            if (j < topk) acc[j] += dp[(size_t)hq * topk + j];
     }
-    for (int j = 0; j < topk; ++j) {
-        const size_t o = (size_t)row * topk + j;
+    float wdw = 0.f, mine = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) {
+        if (j >= topk) break;
+        float v = acc[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+        v = __shfl_sync(0xffffffffu, v, 0);
+        if (lane == j) mine = v;
+        const int kap = idx[(size_t)row * topk + j];
+        if (kap >= 0 && kap < nP) wdw += w[(size_t)row * topk + j] * v;
+    }
+    if (lane < topk) {
+        const size_t o = (size_t)row * topk + lane;
         const int kap = idx[o];
-        dscore[o] = (kap >= 0 && kap < nP) ? w[o] * (dw[j] - wdw) : 0.f;
+        dscore[o] = (kap >= 0 && kap < nP) ? w[o] * (mine - wdw) : 0.f;
+    }
+}
+
+// The whole inverse index of one batch row in one CTA (a stable counting sort of
+// the row's entries by retrieved chunk).  The row's idx is staged in shared
+// memory and cut into one contiguous segment per warp.  (1) Each warp counts its
+// segment per chunk: lanes that hold the same chunk form a __match_any_sync
+// group whose highest lane adds the group size (each warp owns its count row:
+// no atomics).  (2) Per chunk, the warps' counts become exclusive prefixes over
+// the warps, and the chunk totals are scanned into offsets.  (3) Each warp places
+// its segment in ascending entry order: slot = offset + its warps' prefix + rank in
+// the group.  (4) The CTA writes the entries out, each with its weight.
+__global__ void inv_index_kernel(const int32_t* __restrict__ idx, int nE, int nP, int nw,
+                                 int* __restrict__ count, int* __restrict__ offset,
+                                 int* __restrict__ entry, const float* __restrict__ w,
+                                 float* __restrict__ entry_w) {
+    extern __shared__ int sh[];
+    int* ent = sh;                          // [nE]: the row's idx
+    int* fill = sh + nE;                    // [nE]: the entries in bucket order
+    int* off = sh + 2 * nE;                 // [nP + 1]: bucket offsets
+    int* wc = sh + 2 * nE + nP + 1;         // [nw][nP]: per-warp counts, then prefixes
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t* row = idx + (size_t)b * nE;
+    const int seg = ((nE + nw - 1) / nw + 31) / 32 * 32;
+    for (int i = tid; i < nw * nP; i += blockDim.x) wc[i] = 0;
+    for (int e = tid; e < nE; e += blockDim.x) ent[e] = row[e];
+    __syncthreads();
+    const unsigned below = (1u << lane) - 1u;
+    if (warp < nw) {
+        int* mine = wc + (size_t)warp * nP;
+        for (int e0 = warp * seg; e0 < min(nE, (warp + 1) * seg); e0 += 32) {
+            const int e = e0 + lane;
+            const int k = e < nE ? ent[e] : -1;
+            const bool valid = k >= 0 && k < nP;
+            const unsigned grp = __match_any_sync(0xffffffffu, valid ? k : -1);
+            if (valid && lane == 31 - __clz(grp)) mine[k] += __popc(grp);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int k = tid; k < nP; k += blockDim.x) {      // per chunk: prefix over the warps
+        int run = 0;
+        for (int v = 0; v < nw; ++v) {
+            const int c = wc[(size_t)v * nP + k];
+            wc[(size_t)v * nP + k] = run;
+            run += c;
+        }
+        off[k] = run;                                 // the chunk's total, scanned below
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int base = 0; base < nP; base += 32) {
+            const int i = base + lane;
+            const int v = i < nP ? off[i] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (i < nP) {
+                count[(size_t)b * nP + i] = v;
+                off[i] = run + incl - v;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) off[nP] = run;
+    }
+    __syncthreads();
+    for (int i = tid; i <= nP; i += blockDim.x) offset[(size_t)b * (nP + 1) + i] = off[i];
+    if (warp < nw) {
+        int* mine = wc + (size_t)warp * nP;
+        for (int e0 = warp * seg; e0 < min(nE, (warp + 1) * seg); e0 += 32) {
+            const int e = e0 + lane;
+            const int k = e < nE ? ent[e] : -1;
+            const bool valid = k >= 0 && k < nP;
+            const unsigned grp = __match_any_sync(0xffffffffu, valid ? k : -1);
+            if (valid) fill[off[k] + mine[k] + __popc(grp & below)] = e;
+            __syncwarp();
+            if (valid && lane == 31 - __clz(grp)) mine[k] += __popc(grp);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    const int n = off[nP];
+    for (int i = tid; i < n; i += blockDim.x) {
+        const int e = fill[i];
+        entry[(size_t)b * nE + i] = e;
+        if (entry_w) entry_w[(size_t)b * nE + i] = w[(size_t)b * nE + e];
     }
 }
 
@@ -144,6 +248,20 @@ cudaError_t launch_inverse_index_to(const Shape& s, const int32_t* idx, int* cou
                                     int* entry, const float* w, float* entry_w, cudaStream_t st,
                                     int* launches) {
     const int nE = s.nQ * s.topk;
+    // one CTA per row while its staging fits shared memory: 32 warps' count rows for
+    // up to 512 chunks, 8 for more
+    const int nw = s.nP <= 512 ? 32 : 8;
+    const size_t smem = sizeof(int) * (2 * (size_t)nE + (size_t)s.nP + 1 + (size_t)nw * s.nP);
+    if (smem <= 160 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(inv_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        GCA_LAUNCH("inv_index", st, inv_index_kernel<<<s.B, 1024, smem, st>>>(idx, nE, s.nP, nw, count, offset,
+                                                                               entry, w, w ? entry_w : nullptr));
+        *launches += 1;
+        return cudaGetLastError();
+    }
+    // rows too long for one CTA's shared memory: count, scan and fill as three passes
     const int warps = s.B * s.nP;
     const int blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     GCA_LAUNCH("inv_count", st, inv_count_kernel<<<blocks, 32 * kWarpsPerBlock, 0, st>>>(idx, s.B, nE, s.nP, count));
@@ -159,7 +277,8 @@ cudaError_t launch_dscore(const Shape& s, const int32_t* idx, const float* w, vo
     const BwdWorkspace L = bwd_workspace_layout(s);
     const float* dwpart = reinterpret_cast<const float*>(static_cast<char*>(ws) + L.dwpart_off);
     const int rows = s.B * s.nQ;
-    GCA_LAUNCH("dscore", st, dscore_kernel<<<(rows + 127) / 128, 128, 0, st>>>(idx, w, dwpart, rows, s.H, s.topk, s.nP, dscore));
+    GCA_LAUNCH("dscore", st, dscore_kernel<<<(rows + kWarpsPerBlock - 1) / kWarpsPerBlock, 32 * kWarpsPerBlock, 0, st>>>(
+                                 idx, w, dwpart, rows, s.H, s.topk, s.nP, dscore));
     *launches += 1;
     return cudaGetLastError();
 }
