@@ -17,18 +17,20 @@
 //     sums per quarter of the chunk's tokens.
 //   pass B, key-major, item = (batch row, pool chunk, head): walks the inverse
 //     index of (query chunk, slot) entries that retrieved the chunk, gathers
-//     their Q/dO tiles and delta/lse rows, recomputes S^T = K Q^T and
-//     G^T = V dO^T, and accumulates dK += dA^T Q and dV += (w P)^T dO in TMEM.
-// A group is one retrieved chunk of an item (pass A: one slot; pass B: one
-// entry).  Warp roles: warp 0 producer (the whole warp fetches the item
-// metadata -- slot rows, inverse-index entries -- 32 at a time into shared
-// memory; lane 0 issues the TMA / bulk copies; pass A's item lse block rides
-// on the info barrier as a TMA transaction); warp 1 issues the score products
-// (S and G, or S^T and G^T) into a ring of TMEM buffers (S = 64: three in
-// pass A, two in pass B) and owns TMEM; warp 2 issues the accumulation
-// products (dQ, or dK and dV), so neither kind of product waits behind the
-// other's issue; warps 3-10 are two math warpgroups taking alternate groups
-// and alternate item epilogues.
+//     their Q/dO tiles and delta/lse rows, recomputes the scores and dP, and
+//     accumulates dK += dA^T Q and dV += (w P)^T dO in TMEM.  For S = 64 a
+//     group is a pair of entries whose tiles are stacked into M = 128 products
+//     (gca_bwd_kv_pair_kernel); for S = 128 a group is one entry
+//     (S^T = K Q^T, G^T = V dO^T, already M = 128).
+// Warp roles: warp 0 producer (the whole warp fetches the item metadata --
+// slot rows, inverse-index entries and weights -- 32 at a time; lane 0 issues
+// the TMA / bulk copies; pass A's item lse block rides on the info barrier as a
+// TMA transaction); warp 1 issues the score products into a ring of TMEM
+// buffers and owns TMEM; warp 2 issues the accumulation products (dQ, or dK
+// and dV), so neither kind of product waits behind the other's issue; warps
+// 3-10 are math warpgroups (two, one for the S = 128 key-major pass) taking
+// alternate groups and alternate item epilogues; the S = 64 math runs on
+// column pairs in packed f32x2 arithmetic.
 #include <math.h>
 
 #include "common.cuh"
@@ -637,13 +639,16 @@ struct EntryInfo {
     int pad;
 };
 
+// The key-major pass for S = 128 (S = 64 uses the entry-pair kernel below): a
+// group is one inverse-index entry and the products are already M = 128.
 template <int S>
 struct CfgB {
+    static_assert(S == 128, "S = 64 runs gca_bwd_kv_pair_kernel");
     static constexpr int M = S;                           // keys of the item
     static constexpr int NG = S;                          // tokens per group
-    static constexpr int NWG = (S == 64) ? 2 : 1;         // math warpgroups in use
-    static constexpr int NSB = (S == 64) ? 2 : 1;         // S^T/G^T TMEM buffers
-    static constexpr int STAGES = (S == 64) ? 6 : 2;
+    static constexpr int NWG = 1;                         // math warpgroups in use
+    static constexpr int NSB = 1;                         // S^T/G^T TMEM buffers
+    static constexpr int STAGES = 2;
     static constexpr int TILE = S * 128;
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
     static constexpr int VEC_OFF = 2 * TILE;              // after the Q and dO tiles
@@ -907,8 +912,8 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     } else {
         const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
-        const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
-        const int u = (S == 64) ? (lane >> 4) : 0;
+        const int row = 32 * qd + lane;
+        const int u = 0;
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
         Ring inf{0, 0}, st{0, 0};
         int q = 0, e = 0, n_all = 0, kg = 0;
@@ -947,85 +952,42 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 uint8_t* pb = sm + C::OFF_P + wg * 2 * C::P_BYTES;
                 const uint32_t ts0 = tmem + lane_base + sbuf * C::SGW;
                 const uint32_t tg0 = ts0 + S;
-                if constexpr (S == 64) {
-                    // this thread: one key row, tokens u*32 .. u*32+31 of the entry
-                    uint32_t r0[16], r1[16], r2[16], r3[16];
-                    tmem_ld_16x32bx2_x16<32>(ts0, r0);
-                    tmem_ld_16x32bx2_x16<32>(ts0 + 16, r1);
-                    tmem_ld_16x32bx2_x16<32>(tg0, r2);
-                    tmem_ld_16x32bx2_x16<32>(tg0 + 16, r3);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&sb.s_empty[sbuf]);
-                    // token pairs in packed f32x2 arithmetic: p = exp2(s sl - lse2) as
-                    // exp2(-(lse2 - s sl)); w P^T and dA^T = w scale p (g - delta)
-                    const ulonglong2* l2v = reinterpret_cast<const ulonglong2*>(vec + 32 * u);
-                    const ulonglong2* d2v = reinterpret_cast<const ulonglong2*>(vec + S + 32 * u);
-                    const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
-                    const uint64_t wsc2 = tcx::f2_pack(wsc, wsc), wv2 = tcx::f2_pack(wv, wv);
-                    uint32_t pa[16], pp[16];
+                if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                // this thread: one key row, all 128 tokens in four 32-token pieces
+                for (int pc = 0; pc < 4; ++pc) {
+                    float xs[32], xg[32];
+                    {
+                        uint32_t r0[16], r1[16], r2[16], r3[16];
+                        issue_cols16<S>(ts0 + 32 * pc, r0);
+                        issue_cols16<S>(ts0 + 32 * pc + 16, r1);
+                        issue_cols16<S>(tg0 + 32 * pc, r2);
+                        issue_cols16<S>(tg0 + 32 * pc + 16, r3);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int p = 0; p < 16; ++p) {
-                        const uint32_t* rs = p < 8 ? r0 : r1;
-                        const uint32_t* rg = p < 8 ? r2 : r3;
-                        const int t = 2 * (p & 7);
-                        const ulonglong2 lv = l2v[p >> 1], dv = d2v[p >> 1];
-                        float y0, y1;
-                        tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(__uint_as_float(rs[t]), __uint_as_float(rs[t + 1])),
-                                                  nsl2, (p & 1) ? lv.y : lv.x), y0, y1);
-                        const uint64_t pr2 = tcx::f2_pack(fast_exp2(-y0), fast_exp2(-y1));
-                        const uint64_t g2 = tcx::f2_pack(__uint_as_float(rg[t]), __uint_as_float(rg[t + 1]));
-                        pp[p] = tcx::pack_bf16x2(tcx::fmul2(pr2, wv2));
-                        pa[p] = tcx::pack_bf16x2(
-                            tcx::fmul2(tcx::fmul2(pr2, wsc2), tcx::fsub2(g2, (p & 1) ? dv.y : dv.x)));
+                        for (int t = 0; t < 16; ++t) {
+                            xs[t] = __uint_as_float(r0[t]);
+                            xs[16 + t] = __uint_as_float(r1[t]);
+                            xg[t] = __uint_as_float(r2[t]);
+                            xg[16 + t] = __uint_as_float(r3[t]);
+                        }
                     }
-                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                    if (pc == 3) {
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty[sbuf]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * pc + i;
+                        const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -vec[t]));
+                        xs[i] = pr * (xg[i] - vec[S + t]);
+                        xg[i] = pr;
+                    }
+                    const int blk = pc >> 1;
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint32_t off = sw128_off(row, 4 * u + c4);
-                        *reinterpret_cast<uint4*>(pb + off) =
-                            make_uint4(pa[4 * c4], pa[4 * c4 + 1], pa[4 * c4 + 2], pa[4 * c4 + 3]);
-                        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) =
-                            make_uint4(pp[4 * c4], pp[4 * c4 + 1], pp[4 * c4 + 2], pp[4 * c4 + 3]);
-                    }
-                } else {
-                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
-                    // this thread: one key row, all 128 tokens in four 32-token pieces
-                    for (int pc = 0; pc < 4; ++pc) {
-                        float xs[32], xg[32];
-                        {
-                            uint32_t r0[16], r1[16], r2[16], r3[16];
-                            issue_cols16<S>(ts0 + 32 * pc, r0);
-                            issue_cols16<S>(ts0 + 32 * pc + 16, r1);
-                            issue_cols16<S>(tg0 + 32 * pc, r2);
-                            issue_cols16<S>(tg0 + 32 * pc + 16, r3);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int t = 0; t < 16; ++t) {
-                                xs[t] = __uint_as_float(r0[t]);
-                                xs[16 + t] = __uint_as_float(r1[t]);
-                                xg[t] = __uint_as_float(r2[t]);
-                                xg[16 + t] = __uint_as_float(r3[t]);
-                            }
-                        }
-                        if (pc == 3) {
-                            tc_fence_before();
-                            mbar_arrive(&sb.s_empty[sbuf]);
-                        }
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int t = 32 * pc + i;
-                            const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -vec[t]));
-                            xs[i] = pr * (xg[i] - vec[S + t]);
-                            xg[i] = pr;
-                        }
-                        const int blk = pc >> 1;
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            const uint32_t off = blk * C::P_BLOCK + sw128_off(row, (pc & 1) * 4 + c4);
-                            *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c4, wsc);
-                            *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c4, wv);
-                        }
+                        const uint32_t off = blk * C::P_BLOCK + sw128_off(row, (pc & 1) * 4 + c4);
+                        *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c4, wsc);
+                        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c4, wv);
                     }
                 }
                 fence_proxy_async_smem();
