@@ -51,6 +51,7 @@ using tcx::Ring;
 using tcx::sw128_off;
 
 constexpr int kThreads = 352;         // producer, 2 MMA issuers, 2 math warpgroups
+constexpr int kThreadsA = 384;        // + warp 11, which issues the G products (pass A, S = 64 pass B)
 constexpr int kInfo = 4;
 
 struct BwdArgs {
@@ -214,14 +215,14 @@ struct __align__(8) BarsA {
     uint64_t s_full[3], s_empty[3];    // per S/G buffer (per warpgroup when one buffer)
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
-    uint64_t done, done2;
+    uint64_t done, done2, done3;
     uint32_t tmem;
     int abort;
     ItemInfoA info[kInfo];
 };
 
 template <int S>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsA, 1)
 gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const __grid_constant__ CUtensorMap tl, const BwdArgs a) {
@@ -236,11 +237,11 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInfo; ++i) {
             mbar_init(&sb.info_full[i], 1);
-            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + math threads
+            mbar_init(&sb.info_empty[i], 3 + 256);     // three MMA issuers + math threads
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
-            mbar_init(&sb.it_empty[i], 1);
+            mbar_init(&sb.it_empty[i], 2);            // Q read by the S products, dO by the G products
             mbar_init(&sb.p_full[i], 128);
             mbar_init(&sb.p_empty[i], 1);
             mbar_init(&sb.o_full[i], 1);
@@ -250,10 +251,11 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             mbar_init(&sb.kv_full[i], 1);
             mbar_init(&sb.kv_empty[i], 1);
         }
-        for (int i = 0; i < 3; ++i) mbar_init(&sb.s_full[i], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&sb.s_full[i], 2);   // S issuer + G issuer
         for (int i = 0; i < C::NSB; ++i) mbar_init(&sb.s_empty[i], 128);
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
+        mbar_init(&sb.done3, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -362,8 +364,10 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             for (int i = 0; i < kInfo; ++i)
                 if (inf_out[i]) mbar_wait(&sb.info_full[i], inf_ph[i], nullptr, 100000000ull);
         }
-    } else if (warp == 1) {
-        // S / G products: S = Q K^T and G = dO V^T of each group
+    } else if (warp == 1 || warp == 11) {
+        // warp 1: S = Q K^T, warp 11: G = dO V^T of each group (two issuing
+        // threads: M = 64 products issue faster from two than from one)
+        const bool gs = warp == 11;
         if (lane == 0) {
             Ring kv{0, 0}, it{0, 0}, inf{0, 0};
             int q = 0;
@@ -388,20 +392,21 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
                     const uint32_t vaddr = kaddr + C::TILE;
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, qaddr, kaddr, id_s, 0);
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + S, doaddr, vaddr, id_s, 0);
+                    if (gs) tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + S, doaddr, vaddr, id_s, 0);
+                    else tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, qaddr, kaddr, id_s, 0);
                     mma_commit(&sb.s_full[C::sfull_index(qq)]);
                     issued = true;
                     kv.next(C::STAGES);
                 }
                 if (!ok) break;
-                mma_commit(&sb.it_empty[it.i]);     // Q and dO are read only by these products
+                mma_commit(&sb.it_empty[it.i]);     // Q (dO) is read only by these products
                 it.next(2);
                 q += n;
             }
             if (issued) {
-                mma_commit(&sb.done);
-                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+                uint64_t* dn = gs ? &sb.done3 : &sb.done;
+                mma_commit(dn);
+                mbar_wait(dn, 0, nullptr, 100000000ull);
             }
         }
     } else if (warp == 2) {
@@ -445,7 +450,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
             }
         }
-    } else {
+    } else if (warp < 11) {
         const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
         const int row = (S == 64) ? 16 * qd + (lane & 15) : 32 * qd + lane;
@@ -672,7 +677,7 @@ struct __align__(8) BarsB {
     uint64_t s_full[2], s_empty[2];    // s_full per math warpgroup, s_empty per S/G buffer
     uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
-    uint64_t done, done2;
+    uint64_t done, done2, done3;
     uint32_t tmem;
     int abort;
     ItemInfoB info[kInfo];
@@ -1064,7 +1069,7 @@ __device__ __forceinline__ void mma_mnmajor_mnmajor(uint32_t d, uint32_t a_addr,
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsA, 1)
 gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const BwdArgs a) {
@@ -1081,16 +1086,16 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInfo; ++i) {
             mbar_init(&sb.info_full[i], 1);
-            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + math threads
+            mbar_init(&sb.info_empty[i], 3 + 256);     // three MMA issuers + math threads
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
-            mbar_init(&sb.it_empty[i], 1);
+            mbar_init(&sb.it_empty[i], 2);            // K read by the S products, V by the G products
             mbar_init(&sb.p_full[i], 128);
             mbar_init(&sb.p_empty[i], 1);
             mbar_init(&sb.o_full[i], 1);
             mbar_init(&sb.o_empty[i], 128);
-            mbar_init(&sb.s_full[i], 1);
+            mbar_init(&sb.s_full[i], 2);              // S issuer + G issuer
             mbar_init(&sb.s_empty[i], 128);
         }
         for (int i = 0; i < C::STAGES; ++i) {
@@ -1099,6 +1104,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         }
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
+        mbar_init(&sb.done3, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -1234,8 +1240,10 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             for (int i = 0; i < 2; ++i)
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
-    } else if (warp == 1) {
-        // S = [Q_1; Q_2] K^T and G = [dO_1; dO_2] V^T of each pair (M = 128, N = 64)
+    } else if (warp == 1 || warp == 11) {
+        // warp 1: S = [Q_1; Q_2] K^T, warp 11: G = [dO_1; dO_2] V^T of each pair
+        // (M = 128, N = 64; two issuing threads)
+        const bool gs = warp == 11;
         if (lane == 0) {
             Ring st{0, 0}, it{0, 0}, inf{0, 0};
             int q = 0;
@@ -1261,8 +1269,8 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                     }
                     tc_fence_after();
                     const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, stg + C::Q_OFF, kaddr, id_s, 0);
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, vaddr, id_s, 0);
+                    if (gs) tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, vaddr, id_s, 0);
+                    else tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, stg + C::Q_OFF, kaddr, id_s, 0);
                     mma_commit(&sb.s_full[sbuf]);
                     issued = true;
                     st.next(C::STAGES);
@@ -1273,8 +1281,9 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 q += ng;
             }
             if (issued) {
-                mma_commit(&sb.done);
-                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+                uint64_t* dn = gs ? &sb.done3 : &sb.done;
+                mma_commit(dn);
+                mbar_wait(dn, 0, nullptr, 100000000ull);
             }
         }
     } else if (warp == 2) {
@@ -1322,7 +1331,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
             }
         }
-    } else {
+    } else if (warp < 11) {
         const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
@@ -1489,7 +1498,7 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgA<S>::SMEM);
     if (e != cudaSuccess) return e;
     int grid = a.n_items < sms ? a.n_items : sms;
-    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreads, CfgA<S>::SMEM, st>>>(tq, tdo, tk, tv, tl, a));
+    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreadsA, CfgA<S>::SMEM, st>>>(tq, tdo, tk, tv, tl, a));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     a.n_items = sp.B * sp.nP * sp.H;
@@ -1498,7 +1507,7 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
         auto kb = gca_bwd_kv_pair_kernel;
         e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgP::SMEM);
         if (e != cudaSuccess) return e;
-        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgP::SMEM, st>>>(tq, tdo, tk, tv, a));
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, CfgP::SMEM, st>>>(tq, tdo, tk, tv, a));
     } else {
         auto kb = gca_bwd_kv_tc_kernel<S>;
         e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S>::SMEM);
