@@ -26,11 +26,12 @@
 // slot rows, inverse-index entries and weights -- 32 at a time; lane 0 issues
 // the TMA / bulk copies; pass A's item lse block rides on the info barrier as a
 // TMA transaction); warp 1 issues the score products into a ring of TMEM
-// buffers and owns TMEM; warp 2 issues the accumulation products (dQ, or dK
-// and dV), so neither kind of product waits behind the other's issue; warps
-// 3-10 are math warpgroups (two, one for the S = 128 key-major pass) taking
-// alternate groups and alternate item epilogues; the S = 64 math runs on
-// column pairs in packed f32x2 arithmetic.
+// buffers and owns TMEM (in pass A and the S = 64 pass B the G products come
+// from warp 11, a second issuing thread); warp 2 issues the accumulation
+// products (dQ, or dK and dV), so neither kind of product waits behind the
+// other's issue; warps 3-10 are math warpgroups (two, one for the S = 128
+// key-major pass) taking alternate groups and alternate item epilogues; the
+// S = 64 math runs on column pairs in packed f32x2 arithmetic.
 #include <math.h>
 
 #include "common.cuh"
