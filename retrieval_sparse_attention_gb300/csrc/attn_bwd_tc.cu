@@ -79,18 +79,6 @@ struct BwdArgs {
 __device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
 __device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
 
-// 16 consecutive fp32 TMEM columns of this thread's row (S = 64: the 16x32bx2
-// shape, whose second half starts 64 columns on; S = 128: 32x32b).
-template <int S>
-__device__ __forceinline__ void load_cols16(uint32_t taddr, float* x) {
-    uint32_t r[16];
-    if (S == 64) tmem_ld_16x32bx2_x16<64>(taddr, r);
-    else tmem_ld_32x32b_x16(taddr, r);
-    tmem_wait_ld();
-#pragma unroll
-    for (int t = 0; t < 16; ++t) x[t] = __uint_as_float(r[t]);
-}
-
 template <int S>
 __device__ __forceinline__ void issue_cols16(uint32_t taddr, uint32_t (&r)[16]) {
     if (S == 64) tmem_ld_16x32bx2_x16<64>(taddr, r);
@@ -106,28 +94,6 @@ __device__ __forceinline__ void load_cols64(uint32_t taddr, float* x) {
         else tmem_ld_32x32b_x16(taddr + 16 * ci, r);
 #pragma unroll
         for (int t = 0; t < 16; ++t) x[16 * ci + t] = __uint_as_float(r[t]);
-    }
-    tmem_wait_ld();
-}
-
-// TMEM loads of one 64-column chunk of S and of G for this thread's row.
-template <int S>
-__device__ __forceinline__ void load_sg(uint32_t ts, uint32_t tg, float* xs, float* xg) {
-#pragma unroll
-    for (int ci = 0; ci < 4; ++ci) {
-        uint32_t r1[16], r2[16];
-        if (S == 64) {
-            tmem_ld_16x32bx2_x16<64>(ts + 16 * ci, r1);
-            tmem_ld_16x32bx2_x16<64>(tg + 16 * ci, r2);
-        } else {
-            tmem_ld_32x32b_x16(ts + 16 * ci, r1);
-            tmem_ld_32x32b_x16(tg + 16 * ci, r2);
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            xs[16 * ci + t] = __uint_as_float(r1[t]);
-            xg[16 * ci + t] = __uint_as_float(r2[t]);
-        }
     }
     tmem_wait_ld();
 }
@@ -1340,7 +1306,6 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         const int pe = prow >> 6, ptr = prow & 63;  // its entry and token row
         const int erow = 16 * qd + (lane & 15);     // key row of the dK/dV accumulators (M = 64)
         const int eu = lane >> 4;
-        const float* vec0 = nullptr;
         Ring inf{0, 0}, st{0, 0};
         int q = 0, e = 0, n_all = 0, kg = 0;
         const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
@@ -1375,8 +1340,8 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 const uint8_t* stg = sm + C::OFF_ST + stage * C::STAGE_BYTES;
                 // a single-entry pair leaves rows 64-127 unused (the products read K = 64)
                 const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[pe];
-                vec0 = reinterpret_cast<const float*>(stg + C::VEC_OFF);
-                const float lse2 = vec0[pe * 64 + ptr], dlt = vec0[128 + pe * 64 + ptr];
+                const float* vec = reinterpret_cast<const float*>(stg + C::VEC_OFF);
+                const float lse2 = vec[pe * 64 + ptr], dlt = vec[128 + pe * 64 + ptr];
                 const float wv = ei.w, wsc = wv * a.attn_scale;
                 const uint64_t l2 = tcx::f2_pack(lse2, lse2), dl2 = tcx::f2_pack(dlt, dlt);
                 const uint64_t wv2 = tcx::f2_pack(wv, wv), wsc2 = tcx::f2_pack(wsc, wsc);
@@ -1442,7 +1407,6 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             tc_fence_before();
             mbar_arrive(&sb.o_empty[ob]);
         }
-        (void)vec0;
     }
 
     tc_fence_before();

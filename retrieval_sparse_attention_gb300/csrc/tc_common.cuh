@@ -138,9 +138,6 @@ __device__ __forceinline__ void mma_kmajor_mnmajor(uint32_t d, uint32_t p_addr, 
                      xd + (uint64_t)(ks * 128), idesc, ks == 0 ? acc_first : 1u);
 }
 
-// Named barrier over the 128 softmax/epilogue threads (warps 2-5).
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 // Untiled bulk copy global -> shared, completing on an mbarrier (16-byte
 // aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
