@@ -432,6 +432,7 @@ def extra_workloads(lib, api, inputs, dev, hbm, tflops):
         dec["retrieve_plus_fwd_us"] = None
         dec["cache_error"] = str(exc)[:120]
     out["decode_16m"] = dec
+    out.update(sweep_rows(lib, api, inputs, dev, hbm))
     out.update(next_rows(api, inputs, dev, hbm))
     x = swa_inputs(dev)
     us = _event_us(lambda i=0: api.swa_fwd(x[0], x[1], x[2], window=SWA_WINDOW), n=20)
@@ -447,6 +448,71 @@ def extra_workloads(lib, api, inputs, dev, hbm, tflops):
                              "roofline": swa_roofline(8, 16384, 12, 64, SWA_WINDOW, us / 1e3, hbm, tflops,
                                                       backward=True)}
     del x, o, lse, g
+    return out
+
+
+def sweep_rows(lib, api, inputs, dev, hbm, steps=10, warm=3):
+    """The chunk-size / top-k sweep at long context: B=1, L=65536, H=12, d=64,
+    S in {64, 128}, top-k in {4, 8, 16}, vanilla softmax, one fwd+bwd step
+    (gca_score_topk + gca_fwd + gca_bwd) per point.  Each row gives query
+    tokens/s, the step against its gathered-bytes roofline (three gathers of
+    2 S D bf16 per valid unit: K/V in the forward, K/V and Q/dO in the
+    backward) and every kernel against its own algorithmic bytes."""
+    import torch
+    out = {}
+    for S in (64, 128):
+        base = inputs.WORKLOADS["long64k_S%d_k4" % S]
+        x = {n: t.to(dev) for n, t in inputs.make(base).items()}
+        B, L, H, d = base.B, base.L, base.H, base.d
+        D, nC = H * d, L // S
+        for k in (4, 8, 16):
+            wl = inputs.WORKLOADS["long64k_S%d_k%d" % (S, k)]
+            p = api.make_params(B=B, Lq=L, S=S, H=H, d=d, topk=k, dtype=torch.bfloat16)
+            idx = torch.empty(B, nC, k, dtype=torch.int32, device=dev)
+            r, w, ds = (torch.empty(B, nC, k, dtype=torch.float32, device=dev) for _ in range(3))
+            o, dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(4))
+            lse = torch.empty(B, L, H, k, dtype=torch.float32, device=dev)
+            wsb = torch.empty(api.gca_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+
+            def step():
+                api.gca_score_topk(p, x["lm"], idx, r, w)
+                api.gca_fwd(p, x["q"], x["k"], x["v"], idx, w, o, lse)
+                api.gca_bwd(p, x["q"], x["k"], x["v"], idx, w, lse, x["dout"], dq, dk, dv, ds, wsb)
+            for _ in range(warm):
+                step()
+            torch.cuda.synchronize()
+            lib.gca_prof_read(0, None, None, None)
+            lib.gca_prof_enable(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            lib.gca_prof_enable(0)
+            prof = read_prof(lib)
+            assert api.gca_get_status() == 0, "device-side error in the sweep"
+            ms = e0.elapsed_time(e1) / steps
+            U = int((idx >= 0).sum().item())
+            ab = alg_bytes(wl, U, H, D, k)
+            gathered = 3 * U * 2 * S * D * 2
+            kern = {}
+            for n, (t, c) in sorted(prof.items()):
+                fam = "bwd_kv" if "kv" in n else ("bwd_q" if "bwd_q" in n else ("fwd" if "fwd" in n else None))
+                row = {"ms": round(t / c, 4)}
+                if fam is not None:
+                    row["frac"] = round(ab[fam] / (t / c / 1e3) / 1e9 / hbm, 4)
+                kern[n] = row
+            out["sweep_64k_S%d_k%d" % (S, k)] = {
+                "step": "gca_score_topk + gca_fwd + gca_bwd", "B": B, "L": L, "S": S, "topk": k,
+                "valid_units": U, "ms": round(ms, 4), "query_tokens_per_s": round(B * L / (ms / 1e3), 1),
+                "roofline": {"bound": "hbm", "gathered_bytes": gathered,
+                             "achieved": round(gathered / ms / 1e6, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(gathered / ms / 1e6 / hbm, 4)},
+                "kernels": kern}
+            del idx, r, w, ds, o, dq, dk, dv, lse, wsb
+        del x
+        torch.cuda.empty_cache()
     return out
 
 

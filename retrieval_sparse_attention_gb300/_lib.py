@@ -25,7 +25,8 @@ EXPORTED = ("gca_score_topk", "gca_fwd", "gca_bwd_workspace_size", "gca_bwd",
             "gca_status_string", "gca_last_launch_count", "gca_synth_fill_hash",
             "gca_prof_enable", "gca_prof_read", "gca_decode_retrieve_noalloc",
             "gca_score_topk_noisy", "gca_landmark_bwd_workspace_size", "gca_landmark_bwd",
-            "gca_gather_chunks", "gca_swa_fwd", "gca_swa_bwd_workspace_size", "gca_swa_bwd")
+            "gca_gather_chunks", "gca_swa_fwd", "gca_swa_bwd_workspace_size", "gca_swa_bwd",
+            "gca_debug_stall_next_decode")
 
 
 class GcaParams(ctypes.Structure):
@@ -82,6 +83,7 @@ def load() -> ctypes.CDLL:
             "gca_get_status": ([vp], i32),
             "gca_status_string": ([i32], ctypes.c_char_p),
             "gca_last_launch_count": ([], i32),
+            "gca_debug_stall_next_decode": ([ctypes.c_uint64], i32),
             "gca_synth_fill_hash": ([vp, sz, i32, ctypes.c_uint64, ctypes.c_uint64,
                                      ctypes.c_uint64, vp], i32),
             "gca_prof_enable": ([i32], None),

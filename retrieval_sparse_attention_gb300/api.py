@@ -194,6 +194,12 @@ def gca_get_status(stream=None) -> int:
     return int(_lib.load().gca_get_status(_stream(stream)))
 
 
+def gca_debug_stall_next_decode(wait_ns: int):
+    """Test-only: the next decode launch on this thread withholds one stage and
+    bounds its waits by ``wait_ns`` (include/gca_debug.h)."""
+    _check("gca_debug_stall_next_decode", _lib.load().gca_debug_stall_next_decode(int(wait_ns)))
+
+
 def gca_last_launch_count() -> int:
     return int(_lib.load().gca_last_launch_count())
 

@@ -1,7 +1,10 @@
 // api.cu -- the C ABI declared in include/gca.h: argument validation,
 // defaults, the per-device status word and kernel dispatch.
+#include <cuda.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "gca.h"
@@ -17,18 +20,59 @@ namespace {
 __device__ int g_status_word;           // first device-side error since the last read
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices];         // per-device address of g_status_word
+struct StatusCache {
+    std::mutex mu;
+    unsigned long long ctx[kMaxDevices];   // context the address was looked up in
+    int* ptr[kMaxDevices];                 // device address of g_status_word
+} g_status_cache;
 
-int* status_ptr() {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
+
+void resolve_ctx_fns() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+        g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+}
+
+}  // namespace
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, resolve_ctx_fns);
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext c = nullptr;
+    if (g_ctx_get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+int* status_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_status_ptr[dev]) {
+    std::lock_guard<std::mutex> lock(g_status_cache.mu);
+    const unsigned long long ctx = current_context_id();
+    if (!g_status_cache.ptr[dev] || ctx == 0 || ctx != g_status_cache.ctx[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-        g_status_ptr[dev] = static_cast<int*>(p);
+        g_status_cache.ptr[dev] = static_cast<int*>(p);
+        g_status_cache.ctx[dev] = current_context_id();   // the lookup made a context current
     }
-    return g_status_ptr[dev];
+    return g_status_cache.ptr[dev];
 }
+
+void set_launch_count(int n) { t_launches = n; }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -124,7 +168,7 @@ gca_status_t gca_score_topk(const gca_params_t* params, const void* landmarks, i
     if (r != GCA_OK) return r;
     if ((r = check_ptrs({landmarks, idx, score, weight})) != GCA_OK) return r;
     if (sizeof(float) * ((size_t)s.D + s.nQ) > 200 * 1024) return GCA_ERR_UNSUPPORTED;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     r = from_cuda(launch_score_topk(s, landmarks, nullptr, idx, score, weight, st,
@@ -141,7 +185,7 @@ gca_status_t gca_score_topk_noisy(const gca_params_t* params, const void* landma
     if (r != GCA_OK) return r;
     if ((r = check_ptrs({landmarks, noise, idx, score, weight})) != GCA_OK) return r;
     if (sizeof(float) * ((size_t)s.D + 2 * (size_t)s.nQ) > 200 * 1024) return GCA_ERR_UNSUPPORTED;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     r = from_cuda(launch_score_topk(s, landmarks, noise, idx, score, weight, st,
@@ -180,7 +224,7 @@ gca_status_t gca_fwd(const gca_params_t* params, const void* q, const void* k, c
     if ((r = attn_supported(s)) != GCA_OK) return r;
     if ((r = check_ptrs({q, k, v, idx, weight, o})) != GCA_OK) return r;
     if (lse && !aligned16(lse)) return GCA_ERR_INVALID_ARG;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -209,7 +253,7 @@ gca_status_t gca_swa_fwd(const gca_swa_params_t* params, const void* q, const vo
     if (r != GCA_OK) return r;
     if ((r = check_ptrs({q, k, v, o})) != GCA_OK) return r;
     if (lse && !aligned16(lse)) return GCA_ERR_INVALID_ARG;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     const float scale = params->attn_scale > 0.f ? params->attn_scale : 1.0f / sqrtf((float)params->d);
     int n = 0;
@@ -232,7 +276,7 @@ gca_status_t gca_swa_bwd(const gca_swa_params_t* params, const void* q, const vo
     if ((r = check_ptrs({q, k, v, o, lse, dout, dq, dk, dv})) != GCA_OK) return r;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GCA_ERR_WORKSPACE;
     if (ws_bytes < swa_bwd_workspace_bytes(params->B, params->L, params->H)) return GCA_ERR_WORKSPACE;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     const float scale = params->attn_scale > 0.f ? params->attn_scale : 1.0f / sqrtf((float)params->d);
     int n = 0;
@@ -260,7 +304,7 @@ gca_status_t gca_bwd(const gca_params_t* params, const void* q, const void* k, c
     if ((r = check_ptrs({q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore})) != GCA_OK) return r;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GCA_ERR_WORKSPACE;
     if (ws_bytes < bwd_workspace_layout(s).total) return GCA_ERR_WORKSPACE;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -292,7 +336,7 @@ gca_status_t gca_decode_retrieve(const void* landmarks, const void* query_landma
     if (r != GCA_OK) return r;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GCA_ERR_WORKSPACE;
     if (ws_bytes < decode_workspace_bytes(N, topk)) return GCA_ERR_WORKSPACE;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     const float sc = score_scale > 0.f ? score_scale : 1.0f / sqrtf((float)D);
     int n = 0;
@@ -310,7 +354,7 @@ gca_status_t gca_gather_chunks(const void* src_k, const void* src_v, int n_src,
     if (topk > kMaxTopk) return GCA_ERR_UNSUPPORTED;
     gca_status_t r = check_ptrs({src_k, src_v, idx, dst_k, dst_v, dst_idx});
     if (r != GCA_OK) return r;
-    int* st = status_ptr();
+    int* st = status_word();
     if (!st) return GCA_ERR_CUDA;
     int n = 0;
     r = from_cuda(launch_gather_chunks(src_k, src_v, n_src, chunk_bytes, idx, topk, dst_k, dst_v,

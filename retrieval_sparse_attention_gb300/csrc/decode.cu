@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gca_debug.h"
 #include "kernels.h"
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
@@ -82,7 +83,7 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
                        int topk, int off_by_one, float sscale, int32_t* __restrict__ out_idx,
                        float* __restrict__ out_score, float* __restrict__ out_weight,
                        unsigned* ticket, unsigned* stage_ctr, float* blk_s, int* blk_i,
-                       int* status) {
+                       int* status, uint64_t wait_ns, int stall) {
     constexpr int kEPV = 16 / sizeof(T);                 // elements per 16-byte vector
     extern __shared__ uint8_t dsm_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 127) &
@@ -138,7 +139,12 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     };
     int pending = 0;                                     // thread 0: next dynamic stage
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) fill(i, i * (int)gridDim.x + (int)blockIdx.x, 0u);
+        for (int i = 0; i < kStages; ++i) {
+            // fault injection (test only): CTA 0 withholds its first stage, so its
+            // bounded waits run out and the timeout path below is taken
+            if (stall && blockIdx.x == 0 && i == 0) continue;
+            fill(i, i * (int)gridDim.x + (int)blockIdx.x, 0u);
+        }
         pending = dyn0 + (int)atomicAdd(stage_ctr, 1u);
     }
 
@@ -156,7 +162,7 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
     for (int g = 0;; ++g) {
         const int slot = g % kStages;
         const uint32_t par = static_cast<uint32_t>(g / kStages) & 1u;
-        if (!tcx::wait_bar(&bars.abort, &bars.full[slot], par, status)) { ok = false; break; }
+        if (!tcx::wait_bar_ns(&bars.abort, &bars.full[slot], par, status, wait_ns)) { ok = false; break; }
         const int sidx = *reinterpret_cast<volatile int*>(&bars.stage[slot]);
         if (threadIdx.x == 0) out[slot] = false;
         if (sidx < 0) break;
@@ -177,7 +183,7 @@ decode_retrieve_kernel(const T* __restrict__ lm, const T* __restrict__ ql, int N
         if (lane == 0) tc::mbar_arrive(&bars.empty[slot]);
         if (threadIdx.x == 0) {
             // refill this slot once every warp has released it
-            if (!tcx::wait_bar(&bars.abort, &bars.empty[slot], par, status)) { ok = false; break; }
+            if (!tcx::wait_bar_ns(&bars.abort, &bars.empty[slot], par, status, wait_ns)) { ok = false; break; }
             const int nxt = pending;
             if (nxt < total_stages) pending = dyn0 + (int)atomicAdd(stage_ctr, 1u);
             fill(slot, nxt, par ^ 1u);
@@ -350,6 +356,10 @@ size_t decode_workspace_bytes(int N, int topk) {
 
 namespace {
 
+// Test-only fault injection (gca_debug.h): nonzero = the next decode launch on
+// this host thread withholds one stage and bounds its waits by this many ns.
+thread_local uint64_t t_stall_wait_ns = 0;
+
 template <typename T, int VPL>
 cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, int off_by_one,
                        float score_scale, int32_t* idx, float* score, float* weight, void* ws,
@@ -374,10 +384,13 @@ cudaError_t launch_vpl(const void* lm, const void* ql, int N, int D, int topk, i
     int* blk_i = reinterpret_cast<int*>(blk_s + (size_t)nb * topk);
     e = cudaMemsetAsync(ticket, 0, 2 * sizeof(unsigned), st);      // ticket and stage counter
     if (e != cudaSuccess) return e;
+    const uint64_t stall_ns = t_stall_wait_ns;
+    t_stall_wait_ns = 0;
+    const uint64_t wait_ns = stall_ns ? stall_ns : tcx::kWaitNs;
     GCA_LAUNCH("decode_retrieve", st,
                kern<<<nb, kThreads, smem, st>>>((const T*)lm, (const T*)ql, N, D, topk, off_by_one,
                                                 score_scale, idx, score, weight, ticket, ticket + 1,
-                                                blk_s, blk_i, status));
+                                                blk_s, blk_i, status, wait_ns, stall_ns ? 1 : 0));
     return cudaGetLastError();
 }
 
@@ -424,22 +437,27 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[GCA_DECODE_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDev = 64;
-void* g_scratch_ptr[kMaxDev];
+void* g_scratch_ptr[kMaxDev];                 // device address of g_decode_scratch per device
+unsigned long long g_scratch_ctx[kMaxDev];    // the CUDA context it was looked up in
 std::mutex g_scratch_mu;
 
-// Device address of g_decode_scratch on the current device (looked up once
-// per device).  In host code the array's name is only a host-side stand-in.
+// Device address of g_decode_scratch on the current device, looked up with
+// that device current the first time it is used there (and again if the
+// device's context has changed since, e.g. after cudaDeviceReset).  In host
+// code the array's name is only a host-side stand-in, never a device address.
 cudaError_t static_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_ptr[dev] || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        e = cudaGetSymbolAddress((void**)&p, g_decode_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();   // the lookup made a context current
     }
     *out = g_scratch_ptr[dev];
     return cudaSuccess;
@@ -467,11 +485,21 @@ extern "C" gca_status_t gca_decode_retrieve_noalloc(const void* landmarks,
     if (decode_workspace_bytes(N, topk) > GCA_DECODE_STATIC_SCRATCH_BYTES) return GCA_ERR_WORKSPACE;
     void* ws = nullptr;
     if (static_scratch(&ws) != cudaSuccess) return GCA_ERR_CUDA;
+    int* st = status_word();            // device errors go to the same word as every entry's
+    if (!st) return GCA_ERR_CUDA;
     const float sc = score_scale > 0.f ? score_scale : 1.0f / sqrtf((float)D);
     int n = 0;
     const cudaError_t e = launch_decode_retrieve(landmarks, query_landmark, N, D, topk, dtype,
                                                  softmax_off_by_one ? 1 : 0, sc, idx, score,
-                                                 weight, ws, nullptr,
+                                                 weight, ws, st,
                                                  static_cast<cudaStream_t>(stream), &n);
-    return e == cudaSuccess ? GCA_OK : GCA_ERR_CUDA;
+    if (e != cudaSuccess) return GCA_ERR_CUDA;
+    set_launch_count(n);
+    return GCA_OK;
+}
+
+extern "C" gca_status_t gca_debug_stall_next_decode(uint64_t wait_ns) {
+    if (wait_ns < 1000ull || wait_ns > 1000000000ull) return GCA_ERR_INVALID_ARG;
+    gca::t_stall_wait_ns = wait_ns;
+    return GCA_OK;
 }

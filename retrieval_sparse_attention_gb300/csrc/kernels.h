@@ -20,6 +20,18 @@ void prof_end(cudaStream_t st);
         ::gca::prof_end((st));             \
     } while (0)
 
+// Device address of the status word of the current device (looked up once
+// per device and CUDA context), or nullptr if the lookup failed.
+int* status_word();
+// Record the launch count of the call that just succeeded, for
+// gca_last_launch_count() (per host thread).
+void set_launch_count(int n);
+// Identity of the CUDA context current on this host thread (cuCtxGetId), or
+// 0 if none is current or it cannot be read.  Per-device caches of symbol
+// addresses compare it so that they are looked up again in a new context
+// (after cudaDeviceReset, for instance).
+unsigned long long current_context_id();
+
 // Validated, defaulted parameters of one call.
 struct Shape {
     int B, Lq, S, H, d, topk;

@@ -84,20 +84,26 @@ __device__ __forceinline__ uint4 pack8u(const uint32_t* r) {
                       pack_bf16(__uint_as_float(r[6]), __uint_as_float(r[7])));
 }
 
-// Bounded wait that also gives up once another role of the CTA has aborted.
-__device__ __forceinline__ bool wait_bar(int* abort_flag, uint64_t* bar, uint32_t parity,
-                                         int* status) {
+// Bounded wait that also gives up once another role of the CTA has aborted:
+// after `limit_ns` it records GCA_ERR_TIMEOUT, raises the CTA's abort flag and
+// returns false.
+__device__ __forceinline__ bool wait_bar_ns(int* abort_flag, uint64_t* bar, uint32_t parity,
+                                            int* status, uint64_t limit_ns) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = tc::global_timer_ns();
     while (true) {
         if (tc::mbar_try_wait(bar, parity)) return true;
         if (*((volatile int*)abort_flag)) return false;
-        if (tc::global_timer_ns() - t0 > kWaitNs) {
+        if (tc::global_timer_ns() - t0 > limit_ns) {
             set_status(status, GCA_ERR_TIMEOUT);
             *((volatile int*)abort_flag) = 1;
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bar(int* abort_flag, uint64_t* bar, uint32_t parity,
+                                         int* status) {
+    return wait_bar_ns(abort_flag, bar, parity, status, kWaitNs);
 }
 
 // Address of the 16-byte chunk `ch` (0..7 within a 64-element row block) of

@@ -32,11 +32,13 @@ struct WarpTopk {
 };
 
 // Order-preserving key of a (score, index) pair: a larger key ranks earlier
-// (higher score, then lower index).  Keys of distinct indices are distinct, so
+// (higher score, then lower index; -0 and +0 are one score).  Keys of distinct
+// indices are distinct, so
 // the rank of a candidate in a set is the number of larger keys in it.  Key 0
 // marks an empty list entry (it ranks after every real pair).
 __device__ __forceinline__ unsigned long long rank_key(float f, int i) {
-    const unsigned u = __float_as_uint(f);
+    unsigned u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;     // -0 ranks as +0 (they compare equal in ranks_before)
     const unsigned sk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return (static_cast<unsigned long long>(sk) << 32) | static_cast<unsigned>(~static_cast<unsigned>(i));
 }

@@ -108,6 +108,12 @@ def test_score_topk_validation(lib):
                               None) == UNSUPPORTED
 
 
+def test_debug_stall_validation(lib):
+    assert lib.gca_debug_stall_next_decode(0) == INVALID
+    assert lib.gca_debug_stall_next_decode(999) == INVALID
+    assert lib.gca_debug_stall_next_decode(2_000_000_000) == INVALID
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert lib.gca_status_string(code).decode() == name

@@ -40,6 +40,9 @@ SMALL = [
     ("long64k_S128_k8", 1, 4096, False, False),
     ("long64k_S128_k4", 2, 1664, True, True),
     ("long64k_S64_k16", 1, 2304, False, False),
+    ("long64k_S128_k16", 1, 3328, False, False),
+    ("long64k_S128_k16", 1, 2560, True, True),
+    ("long64k_S64_k4", 1, 1984, False, True),
 ]
 
 
@@ -62,8 +65,8 @@ def test_fwd_bwd_every_element(name, B, L, off_by_one, include_self):
     assert_close("dscore", f64(got["ds"]), ds, atol, rtol)
 
 
-FULL = [("gpt2s_fwd_b4", True, False), ("gpt2s_fwdbwd_b8", False, True),
-        ("long64k_S64_k16", False, True), ("long64k_S128_k8", False, True)]
+FULL = [("gpt2s_fwd_b4", True, False), ("gpt2s_fwdbwd_b8", False, True)] + \
+    [("long64k_S%d_k%d" % (S, k), False, True) for S in (64, 128) for k in (4, 8, 16)]
 
 
 @pytest.mark.parametrize("name,off_by_one,backward", FULL)

@@ -66,5 +66,10 @@ def test_landmark_grad_after_backward_pipeline():
     oi, orr, ow = oracle.score_topk(f64(x["lm"]), wl.topk)
     _, _, _, ods = oracle.bwd(f64(x["q"]), f64(x["k"]), f64(x["v"]), oi, ow, f64(x["dout"]), wl.S)
     want = oracle.landmark_bwd(f64(x["lm"]), oi, ods)
-    scale = np.abs(want).max()
-    assert_close("dlandmarks", f64(dl), want, 2e-2 * scale, 2e-2)
+    assert_close("dscore", f64(ds), ods, 2e-2, 2e-2)
+    # the landmark kernel itself, fed the GPU's own d(score): fp32 accumulation,
+    # then one rounding to bf16 (relative error at most 2^-9)
+    assert_close("dlandmarks | gpu dscore", f64(dl), oracle.landmark_bwd(f64(x["lm"]), oi, f64(ds)),
+                 1e-4, 4e-3)
+    # and the whole chain against the oracle, at the bf16 bound
+    assert_close("dlandmarks", f64(dl), want, 2e-2, 2e-2)

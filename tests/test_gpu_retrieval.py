@@ -111,3 +111,20 @@ def test_synth_fill_matches_host_generator():
     for i in range(5):
         want = inputs.decode_cache_chunk_np(4, 1, 3 + i, S, H, d)
         np.testing.assert_array_equal(got[i], want)
+
+
+def test_signed_zero_scores_tie_toward_lower_index():
+    # all scores are zero, some from negative zeros: -0 and +0 are one score,
+    # so the slots go to the lowest indices in order (scoring and decode)
+    lm = torch.zeros(1, 40, 16)
+    lm[0, 1::2] = -0.0
+    lm[0, 6, 3] = 2.0                 # orthogonal to every other landmark
+    oi, ow = run_score(lm, 64, 1, 16, 8, False, False)
+    assert list(oi[0, 39]) == list(range(8))
+    tab = torch.zeros(70000, 16)
+    tab[1::3] = -0.0
+    tab[5, 0] = 1.0
+    q = torch.zeros(16)
+    q[1:] = -0.0
+    idx = run_decode(tab, q, 8, False)
+    assert idx.cpu().tolist() == list(range(8))

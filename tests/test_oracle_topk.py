@@ -65,6 +65,25 @@ def test_hand_worked_example():
     assert list(idx2[0, 3]) == [1, 2]                             # 4 == 4: tie -> lower index
 
 
+def test_signed_zero_scores_tie_toward_lower_index():
+    # Every score is zero, some computed from negative zeros (-0 * x, -0 + -0):
+    # -0 and +0 are the same score, so every slot goes to the lowest indices, in
+    # order, and the vanilla weights are uniform.
+    lm = np.zeros((1, 9, 4))
+    lm[0, 1::2] = -0.0
+    lm[0, 2, 0] = 3.0                 # chunk 2 is orthogonal to every other landmark
+    lm[0, 4, :] = np.array([-0.0, 0.0, -0.0, 0.0])
+    assert np.signbit(lm[0, 1]).all()
+    idx, r, w = oracle.score_topk(lm, 3, include_self=False, off_by_one=False, score_scale=1.0)
+    for c in range(4, 9):
+        assert list(idx[0, c]) == [0, 1, 2], c
+        assert (r[0, c] == 0).all()
+        assert np.allclose(w[0, c], 1.0 / 3.0, rtol=1e-15)
+    di, dr, dw = oracle.decode_retrieve(lm[0], -lm[0, 1], 4)
+    assert list(di) == [0, 1, 2, 3]
+    assert np.allclose(dw, 0.25, rtol=1e-15)
+
+
 @pytest.mark.parametrize("include_self", [False, True])
 @pytest.mark.parametrize("off_by_one", [False, True])
 @pytest.mark.parametrize("shape", [(1, 1, 4, 1), (1, 2, 3, 2), (2, 5, 8, 3), (3, 17, 130, 5),

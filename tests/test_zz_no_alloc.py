@@ -39,6 +39,7 @@ def test_noalloc_matches_workspace_entry_point():
     lm, ql = x["lm"].cuda(), x["ql"].cuda()
     ref = api.decode_retrieve(lm, ql, topk=8)
     first = noalloc(lm, ql, 8, False)
+    assert api.gca_last_launch_count() == 1
     second = noalloc(lm, ql, 8, False)                # the array keeps the first call's contents
     torch.cuda.synchronize()
     check_same(first, ref)
@@ -59,3 +60,19 @@ def test_noalloc_refuses_requests_beyond_its_array():
     with pytest.raises(GcaError) as e:
         noalloc(lm, ql, 32, False)                    # 2048 CTAs x 32 ranks > the array
     assert e.value.code == 3                          # GCA_ERR_WORKSPACE
+
+
+def test_noalloc_reports_device_errors_through_the_status_word():
+    # a bounded wait that runs out inside this entry point is recorded in the
+    # same per-device status word as every other entry's (test-only stall
+    # switch), and the next call is normal again
+    x = inputs.decode_inputs(N=65536)
+    lm, ql = x["lm"].cuda(), x["ql"].cuda()
+    ref = api.decode_retrieve(lm, ql, topk=8)
+    assert api.gca_get_status() == 0
+    api.gca_debug_stall_next_decode(200_000)
+    noalloc(lm, ql, 8, False)
+    assert api.gca_last_launch_count() == 1
+    assert api.gca_get_status() == 5                  # GCA_ERR_TIMEOUT
+    check_same(noalloc(lm, ql, 8, False), ref)
+    assert api.gca_get_status() == 0
