@@ -1057,17 +1057,17 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
-            mbar_init(&sb.it_empty[i], 2);            // K read by the S products, V by the G products
+            mbar_init(&sb.it_empty[i], 1);            // K and V read by the S and G products
             mbar_init(&sb.p_full[i], 128);
-            mbar_init(&sb.p_empty[i], 1);
-            mbar_init(&sb.o_full[i], 1);
+            mbar_init(&sb.p_empty[i], 2);             // the dK issuer + the dV issuer
+            mbar_init(&sb.o_full[i], 2);
             mbar_init(&sb.o_empty[i], 128);
-            mbar_init(&sb.s_full[i], 2);              // S issuer + G issuer
+            mbar_init(&sb.s_full[i], 1);
             mbar_init(&sb.s_empty[i], 128);
         }
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&sb.st_full[i], 1);
-            mbar_init(&sb.st_empty[i], 1);
+            mbar_init(&sb.st_empty[i], 2);            // Q read by the dK products, dO by the dV products
         }
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
@@ -1207,10 +1207,8 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             for (int i = 0; i < 2; ++i)
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
-    } else if (warp == 1 || warp == 11) {
-        // warp 1: S = [Q_1; Q_2] K^T, warp 11: G = [dO_1; dO_2] V^T of each pair
-        // (M = 128, N = 64; two issuing threads)
-        const bool gs = warp == 11;
+    } else if (warp == 1) {
+        // S = [Q_1; Q_2] K^T and G = [dO_1; dO_2] V^T of each pair (M = 128, N = 64)
         if (lane == 0) {
             Ring st{0, 0}, it{0, 0}, inf{0, 0};
             int q = 0;
@@ -1236,8 +1234,8 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                     }
                     tc_fence_after();
                     const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    if (gs) tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, vaddr, id_s, 0);
-                    else tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, stg + C::Q_OFF, kaddr, id_s, 0);
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, stg + C::Q_OFF, kaddr, id_s, 0);
+                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, vaddr, id_s, 0);
                     mma_commit(&sb.s_full[sbuf]);
                     issued = true;
                     st.next(C::STAGES);
@@ -1248,13 +1246,14 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 q += ng;
             }
             if (issued) {
-                uint64_t* dn = gs ? &sb.done3 : &sb.done;
-                mma_commit(dn);
-                mbar_wait(dn, 0, nullptr, 100000000ull);
+                mma_commit(&sb.done);
+                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
             }
         }
-    } else if (warp == 2) {
-        // dK += dA^T [Q_1; Q_2] and dV += (w P)^T [dO_1; dO_2] (M = 64 keys, K = the pair's queries)
+    } else if (warp == 2 || warp == 11) {
+        // warp 2: dK += dA^T [Q_1; Q_2], warp 11: dV += (w P)^T [dO_1; dO_2] (M = 64 keys,
+        // K = the pair's queries): M = 64 products issue faster from two threads than one
+        const bool dvi = warp == 11;
         if (lane == 0) {
             Ring st{0, 0}, inf{0, 0};
             int q = 0, e = 0;
@@ -1280,9 +1279,11 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
                     const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    mma_mnmajor_mnmajor(d_dk, paddr, stg + C::Q_OFF, id_acc, ksteps, g > 0 ? 1u : 0u);
-                    mma_mnmajor_mnmajor(d_dv, paddr + C::P_BYTES, stg + C::DO_OFF, id_acc, ksteps,
-                                        g > 0 ? 1u : 0u);
+                    if (dvi)
+                        mma_mnmajor_mnmajor(d_dv, paddr + C::P_BYTES, stg + C::DO_OFF, id_acc, ksteps,
+                                            g > 0 ? 1u : 0u);
+                    else
+                        mma_mnmajor_mnmajor(d_dk, paddr, stg + C::Q_OFF, id_acc, ksteps, g > 0 ? 1u : 0u);
                     mma_commit(&sb.st_empty[st.i]);
                     mma_commit(&sb.p_empty[pbuf]);
                     issued = true;
@@ -1294,8 +1295,9 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 ++e;
             }
             if (issued) {
-                mma_commit(&sb.done2);
-                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+                uint64_t* dn = dvi ? &sb.done3 : &sb.done2;
+                mma_commit(dn);
+                mbar_wait(dn, 0, nullptr, 100000000ull);
             }
         }
     } else if (warp < 11) {
