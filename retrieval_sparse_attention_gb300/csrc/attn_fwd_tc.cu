@@ -55,26 +55,34 @@ using tcx::pack_bf16;
 using tcx::kLog2e;
 using tcx::kLn2;
 
-template <int S>
+template <int S, int DH>
 struct Cfg {
+    using G = tcx::HeadGeom<DH>;
     static constexpr int M = S;                         // tokens per item = MMA M
     static constexpr int GS = 128 / S;                  // slots per group
     static constexpr int NG = 128;                      // keys per full group
-    static constexpr int STAGES = (S == 64) ? 4 : 3;    // K/V ring depth
-    static constexpr int TILE = S * 128;                // one slot's K (or V) tile, bytes
-    static constexpr int Q_BYTES = S * 128;
-    static constexpr int STAGE_BYTES = 2 * NG * 128;    // K half then V half
+    // K/V ring depth and Q buffers: what fits beside the P buffers
+    static constexpr int STAGES = DH == 128 ? 2 : ((S == 64) ? 4 : 3);
+    static constexpr int QBUF = (S == 128 && DH == 128) ? 1 : 2;
+    static constexpr int TILE = G::tile_bytes(S);       // one slot's K (or V) tile, bytes
+    static constexpr int Q_BYTES = G::tile_bytes(S);
+    // K half then V half; in each, sub-tile s holds the NG key rows of the
+    // group's slots (slot u at rows u*S ..), so a group's K is one B operand
+    static constexpr int HALF_BYTES = G::tile_bytes(NG);
+    static constexpr int STAGE_BYTES = 2 * HALF_BYTES;
     static constexpr int P_BLOCK = M * 128;             // 64 keys of P for all M rows
     static constexpr int P_BYTES = M * NG * 2;
     static constexpr int VALS = (S == 64) ? 64 : 128;   // S values per softmax thread
     // shared-memory carve-up (all 1024-byte aligned)
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = OFF_Q + 2 * Q_BYTES;
+    static constexpr int OFF_KV = OFF_Q + QBUF * Q_BYTES;
     static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
     static constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;                // two S buffers of 128 columns
-    static constexpr uint32_t COL_O = 256;              // two O buffers of 64 columns
+    static constexpr uint32_t COL_O = 256;              // two O buffers of DH columns
+    static_assert(SMEM <= 232448 - 1024, "shared memory");
+    static_assert(COL_O + 2 * DH <= TMEM_COLS, "tensor memory");
 };
 
 struct FwdArgs {
@@ -118,11 +126,12 @@ __device__ __forceinline__ bool wait_bar(Bars& sb, uint64_t* bar, uint32_t parit
 __device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
 __device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
 
-template <int S>
+template <int S, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
 gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
-    using C = Cfg<S>;
+    using C = Cfg<S, DH>;
+    using HG = tcx::HeadGeom<DH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -196,11 +205,12 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (n == 0) continue;
                 if (!wait_bar(sb, &sb.q_empty[qr.i], qr.ph ^ 1u, a.status)) break;
                 mbar_arrive_expect_tx(&sb.q_full[qr.i], C::Q_BYTES);
-                tma_load_2d(sm + C::OFF_Q + qr.i * C::Q_BYTES, &tq, &sb.q_full[qr.i], h * 64,
-                            b * a.Lq + c * S);
+                for (int sub = 0; sub < HG::SUB; ++sub)
+                    tma_load_2d(sm + C::OFF_Q + qr.i * C::Q_BYTES + sub * S * HG::ROW_BYTES, &tq,
+                                &sb.q_full[qr.i], h * DH + sub * 64, b * a.Lq + c * S);
                 q_out[qr.i] = true;
                 q_ph[qr.i] = qr.ph;
-                qr.next(2);
+                qr.next(C::QBUF);
                 bool ok = true;
                 for (int g = 0; g * C::GS < n; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
@@ -209,9 +219,12 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     mbar_arrive_expect_tx(&sb.kv_full[kv.i], ns * 2 * C::TILE);
                     for (int u = 0; u < ns; ++u) {
                         const int y = (b * a.nP + I.kaps[g * C::GS + u]) * S;
-                        tma_load_2d(stg + u * C::TILE, &tk, &sb.kv_full[kv.i], h * 64, y);
-                        tma_load_2d(stg + C::NG * 128 + u * C::TILE, &tv, &sb.kv_full[kv.i],
-                                    h * 64, y);
+                        for (int sub = 0; sub < HG::SUB; ++sub) {
+                            const int off = (sub * C::NG + u * S) * HG::ROW_BYTES;
+                            tma_load_2d(stg + off, &tk, &sb.kv_full[kv.i], h * DH + sub * 64, y);
+                            tma_load_2d(stg + C::HALF_BYTES + off, &tv, &sb.kv_full[kv.i],
+                                        h * DH + sub * 64, y);
+                        }
                     }
                     kv_out[kv.i] = true;
                     kv_ph[kv.i] = kv.ph;
@@ -222,7 +235,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // no copy may still be writing shared memory when the CTA exits
             for (int i = 0; i < C::STAGES; ++i)
                 if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < C::QBUF; ++i)
                 if (q_out[i]) mbar_wait(&sb.q_full[i], q_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
@@ -252,15 +265,15 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         !wait_bar(sb, &sb.s_empty[sbuf], empty_par(qq >> 1), a.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    tcx::mma_kmajor_k64(tmem + C::COL_S + sbuf * 128, qaddr, kaddr,
-                                        (ns * S == 128) ? id_s128 : id_s64, 0);
+                    tcx::mma_kmajor_dh<DH>(tmem + C::COL_S + sbuf * 128, qaddr, S, kaddr, C::NG,
+                                           (ns * S == 128) ? id_s128 : id_s64, 0);
                     mma_commit(&sb.s_full[sbuf]);
                     issued = true;
                     kv.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.q_empty[qr.i]);     // Q is read only by these products
-                qr.next(2);
+                qr.next(C::QBUF);
                 q += G;
             }
             if (issued) {
@@ -275,7 +288,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             Ring kv{0, 0}, inf{0, 0};
             int q = 0, e = 0;
             bool issued = false;
-            const uint32_t id_o = idesc_bf16(C::M, 64, false, true);
+            const uint32_t id_o = idesc_bf16(C::M, HG::SUB_COLS, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait_bar(sb, &sb.info_full[inf.i], inf.ph, a.status)) break;
                 const int n = sb.info[inf.i].n;
@@ -286,7 +299,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const int ob = e & 1;
                 if (!wait_bar(sb, &sb.o_empty[ob], empty_par(e >> 1), a.status)) break;
                 tc_fence_after();
-                const uint32_t d_o = tmem + C::COL_O + ob * 64;
+                const uint32_t d_o = tmem + C::COL_O + ob * DH;
                 bool ok = true;
                 for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
@@ -294,11 +307,11 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     if (!wait_bar(sb, &sb.p_full[pbuf], full_par(qq >> 1), a.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * C::P_BYTES);
-                    const uint32_t vaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES + C::NG * 128);
+                    const uint32_t vaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES + C::HALF_BYTES);
                     if (ns * S == 128)
-                        tcx::mma_kmajor_mnmajor<8>(d_o, paddr, C::P_BLOCK, vaddr, id_o, g > 0);
+                        tcx::mma_kmajor_mn_dh<DH, 8>(d_o, paddr, C::P_BLOCK, vaddr, C::NG, id_o, g > 0);
                     else
-                        tcx::mma_kmajor_mnmajor<4>(d_o, paddr, C::P_BLOCK, vaddr, id_o, g > 0);
+                        tcx::mma_kmajor_mn_dh<DH, 4>(d_o, paddr, C::P_BLOCK, vaddr, C::NG, id_o, g > 0);
                     // S_g is complete (its P exists), so the whole stage may be reused
                     mma_commit(&sb.kv_empty[kv.i]);
                     mma_commit(&sb.p_empty[pbuf]);
@@ -330,7 +343,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const ItemInfo& I = sb.info[inf.i];
             const int b = I.b, c = I.c, h = I.h, n = I.n;
             const size_t tok = (size_t)b * a.Lq + (size_t)c * S + row;
-            __nv_bfloat16* orow = a.o + (tok * a.H + h) * 64;
+            __nv_bfloat16* orow = a.o + (tok * a.H + h) * DH;
             float* lrow = a.lse ? a.lse + (tok * a.H + h) * a.topk : nullptr;
             // the epilogue of an item is done by one warpgroup, alternating
             const bool my_epi = (n == 0) ? ((n_all & 1) == wg) : ((e & 1) == wg);
@@ -343,16 +356,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (n == 0) {
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
-                if (my_epi) {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-                    if (S == 64) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) reinterpret_cast<uint4*>(orow + u * 32)[q4] = z;
-                    } else {
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) reinterpret_cast<uint4*>(orow)[q4] = z;
-                    }
-                }
+                if (my_epi) tcx::zero_acc_row<S, DH>(orow, u);
                 continue;
             }
             const int G = (n + C::GS - 1) / C::GS;
@@ -425,29 +429,22 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (!wait_bar(sb, &sb.o_full[wg], full_par(ko), a.status)) break;
             ++ko;
             tc_fence_after();
-            const uint32_t oaddr = tmem + lane_base + C::COL_O + wg * 64;
-            if (S == 64) {
-                uint32_t r0[16], r1[16];
-                tmem_ld_16x32bx2_x16<32>(oaddr, r0);
-                tmem_ld_16x32bx2_x16<32>(oaddr + 16, r1);
+            const uint32_t oaddr = tmem + lane_base + C::COL_O + wg * DH;
+            {
+                // O rows of this warp's lanes to registers, release the buffer, then store
+                constexpr int NR = (S == 64 ? DH / 2 : DH) / 16;
+                uint32_t r[NR][16];
+#pragma unroll
+                for (int ci = 0; ci < NR; ++ci) {
+                    if (S == 64) tmem_ld_16x32bx2_x16<DH / 2>(oaddr + 16 * ci, r[ci]);
+                    else tmem_ld_32x32b_x16(oaddr + 16 * ci, r[ci]);
+                }
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&sb.o_empty[wg]);
-                uint4* dst = reinterpret_cast<uint4*>(orow + u * 32);
-                dst[0] = tcx::pack8u(r0);
-                dst[1] = tcx::pack8u(r0 + 8);
-                dst[2] = tcx::pack8u(r1);
-                dst[3] = tcx::pack8u(r1 + 8);
-            } else {
-                uint32_t r[4][16];
+                uint4* dst = reinterpret_cast<uint4*>(orow + (S == 64 ? u * (DH / 2) : 0));
 #pragma unroll
-                for (int ci = 0; ci < 4; ++ci) tmem_ld_32x32b_x16(oaddr + 16 * ci, r[ci]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.o_empty[wg]);
-                uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-                for (int ci = 0; ci < 4; ++ci) {
+                for (int ci = 0; ci < NR; ++ci) {
                     dst[2 * ci] = tcx::pack8u(r[ci]);
                     dst[2 * ci + 1] = tcx::pack8u(r[ci] + 8);
                 }
@@ -459,19 +456,20 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, Cfg<S>::TMEM_COLS);
+        tmem_dealloc(tmem, Cfg<S, DH>::TMEM_COLS);
     }
 }
 
-template <int S>
+template <int S, int DH>
 cudaError_t launch_s(const Shape& sp, const void* q, const void* k, const void* v,
                      const int32_t* idx, const float* w, void* o, float* lse, int* status,
                      cudaStream_t st) {
     CUtensorMap tq, tk, tv;
-    const uint64_t cols = (uint64_t)sp.H * 64;
-    if (!encode_bf16_rows(&tq, q, (uint64_t)sp.B * sp.Lq, cols, S) ||
-        !encode_bf16_rows(&tk, k, (uint64_t)sp.B * sp.nP * S, cols, S) ||
-        !encode_bf16_rows(&tv, v, (uint64_t)sp.B * sp.nP * S, cols, S))
+    const uint64_t cols = (uint64_t)sp.H * DH;
+    constexpr uint32_t bc = tcx::HeadGeom<DH>::SUB_COLS;
+    if (!encode_bf16_rows_box(&tq, q, (uint64_t)sp.B * sp.Lq, cols, bc, S) ||
+        !encode_bf16_rows_box(&tk, k, (uint64_t)sp.B * sp.nP * S, cols, bc, S) ||
+        !encode_bf16_rows_box(&tv, v, (uint64_t)sp.B * sp.nP * S, cols, bc, S))
         return cudaErrorInvalidValue;
     FwdArgs a;
     a.idx = idx; a.w = w; a.o = static_cast<__nv_bfloat16*>(o); a.lse = lse; a.status = status;
@@ -482,10 +480,10 @@ cudaError_t launch_s(const Shape& sp, const void* q, const void* k, const void* 
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = a.n_items < sms ? a.n_items : sms;
-    auto kern = gca_fwd_tc_kernel<S>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<S>::SMEM);
+    auto kern = gca_fwd_tc_kernel<S, DH>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<S, DH>::SMEM);
     if (e != cudaSuccess) return e;
-    GCA_LAUNCH("fwd_tc", st, kern<<<grid, kThreads, Cfg<S>::SMEM, st>>>(tq, tk, tv, a));
+    GCA_LAUNCH("fwd_tc", st, kern<<<grid, kThreads, Cfg<S, DH>::SMEM, st>>>(tq, tk, tv, a));
     return cudaGetLastError();
 }
 
@@ -494,8 +492,16 @@ cudaError_t launch_s(const Shape& sp, const void* q, const void* k, const void* 
 cudaError_t launch_fwd_tc(const Shape& sp, const void* q, const void* k, const void* v,
                           const int32_t* idx, const float* w, void* o, float* lse, int* status,
                           cudaStream_t st, int* launches) {
-    cudaError_t e = (sp.S == 64) ? launch_s<64>(sp, q, k, v, idx, w, o, lse, status, st)
-                                 : launch_s<128>(sp, q, k, v, idx, w, o, lse, status, st);
+    cudaError_t e;
+    if (sp.S == 64) {
+        e = sp.d == 32 ? launch_s<64, 32>(sp, q, k, v, idx, w, o, lse, status, st)
+          : sp.d == 128 ? launch_s<64, 128>(sp, q, k, v, idx, w, o, lse, status, st)
+                        : launch_s<64, 64>(sp, q, k, v, idx, w, o, lse, status, st);
+    } else {
+        e = sp.d == 32 ? launch_s<128, 32>(sp, q, k, v, idx, w, o, lse, status, st)
+          : sp.d == 128 ? launch_s<128, 128>(sp, q, k, v, idx, w, o, lse, status, st)
+                        : launch_s<128, 64>(sp, q, k, v, idx, w, o, lse, status, st);
+    }
     if (e == cudaSuccess) *launches += 1;
     return e;
 }

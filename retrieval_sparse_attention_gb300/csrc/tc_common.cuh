@@ -144,6 +144,128 @@ __device__ __forceinline__ void mma_kmajor_mnmajor(uint32_t d, uint32_t p_addr, 
                      xd + (uint64_t)(ks * 128), idesc, ks == 0 ? acc_first : 1u);
 }
 
+// ---------------------------------------------------------------------------
+// Head tiles of DH = 32, 64 or 128 columns.  A [rows x DH] bf16 tile is held
+// in shared memory as SUB sub-tiles, each [rows x SUB_COLS] with rows of
+// ROW_BYTES bytes, exactly as one TMA box of SUB_COLS x rows writes it:
+// DH = 64 and 128 use 64-column sub-tiles (128-byte rows, 128-byte swizzle),
+// DH = 32 one 32-column tile (64-byte rows, 64-byte swizzle).  Sub-tile s of a
+// tile whose sub-tiles hold R rows starts at s * R * ROW_BYTES.
+// ---------------------------------------------------------------------------
+template <int DH>
+struct HeadGeom {
+    static_assert(DH == 32 || DH == 64 || DH == 128, "head dimension 32, 64 or 128");
+    static constexpr int SUB = DH == 128 ? 2 : 1;
+    static constexpr int SUB_COLS = DH == 32 ? 32 : 64;
+    static constexpr int ROW_BYTES = SUB_COLS * 2;
+    static constexpr uint32_t SWZ = DH == 32 ? 4u : 2u;      // descriptor layout: 64B / 128B swizzle
+    static constexpr uint32_t SBO = 8u * ROW_BYTES;           // bytes between 8-row groups
+    static constexpr int KSTEPS_SUB = ROW_BYTES / 32;         // K = 16 steps along one row
+    static constexpr uint32_t KROW16 = 16u * ROW_BYTES;       // bytes of 16 rows (MN-major K step)
+    __host__ __device__ static constexpr int tile_bytes(int rows) { return rows * DH * 2; }
+};
+
+template <int DH>
+__device__ __forceinline__ uint64_t desc_head(uint32_t saddr) {
+    return tc::smem_desc(saddr, 16, HeadGeom<DH>::SBO, HeadGeom<DH>::SWZ);
+}
+
+// D (+)= A B^T contracted over the DH columns of two K-major head tiles whose
+// sub-tiles hold a_rows and b_rows rows.
+template <int DH>
+__device__ __forceinline__ void mma_kmajor_dh(uint32_t d, uint32_t a_addr, int a_rows, uint32_t b_addr,
+                                              int b_rows, uint32_t idesc, uint32_t acc_first) {
+    using G = HeadGeom<DH>;
+#pragma unroll
+    for (int s = 0; s < G::SUB; ++s) {
+        const uint64_t ad = desc_head<DH>(a_addr + s * a_rows * G::ROW_BYTES);
+        const uint64_t bd = desc_head<DH>(b_addr + s * b_rows * G::ROW_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < G::KSTEPS_SUB; ++ks)
+            tc::mma_bf16(d, ad + 2 * ks, bd + 2 * ks, idesc, (s == 0 && ks == 0) ? acc_first : 1u);
+    }
+}
+
+// D (+)= P X over KSTEPS*16 rows of K: P K-major (128-byte swizzle, blocks of 64
+// K elements p_block bytes apart), X an MN-major head tile (K along its rows,
+// x_rows rows per sub-tile).  Sub-tile s accumulates into TMEM columns
+// d + s * SUB_COLS; idesc must give N = SUB_COLS.
+template <int DH, int KSTEPS>
+__device__ __forceinline__ void mma_kmajor_mn_dh(uint32_t d, uint32_t p_addr, uint32_t p_block,
+                                                 uint32_t x_addr, int x_rows, uint32_t idesc,
+                                                 uint32_t acc_first) {
+    using G = HeadGeom<DH>;
+    const uint64_t pd = tc::desc_kmajor_sw128(p_addr);
+#pragma unroll
+    for (int s = 0; s < G::SUB; ++s) {
+        const uint64_t xd = desc_head<DH>(x_addr + s * x_rows * G::ROW_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+            tc::mma_bf16(d + s * G::SUB_COLS, pd + (uint64_t)(((ks >> 2) * p_block + (ks & 3) * 32) >> 4),
+                         xd + (uint64_t)(ks * (G::KROW16 >> 4)), idesc, ks == 0 ? acc_first : 1u);
+    }
+}
+
+// D (+)= A^T X over ksteps*16 rows of K: A MN-major with 128-byte rows (64
+// elements along M), X an MN-major head tile (x_rows rows per sub-tile).
+template <int DH>
+__device__ __forceinline__ void mma_mn_mn_dh(uint32_t d, uint32_t a_addr, uint32_t x_addr, int x_rows,
+                                             uint32_t idesc, int ksteps, uint32_t acc_first) {
+    using G = HeadGeom<DH>;
+    const uint64_t ad = tc::desc_mnmajor_sw128(a_addr);
+#pragma unroll
+    for (int s = 0; s < G::SUB; ++s) {
+        const uint64_t xd = desc_head<DH>(x_addr + s * x_rows * G::ROW_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            if (ks == ksteps) break;
+            tc::mma_bf16(d + s * G::SUB_COLS, ad + (uint64_t)(ks * 128), xd + (uint64_t)(ks * (G::KROW16 >> 4)),
+                         idesc, ks == 0 ? acc_first : 1u);
+        }
+    }
+}
+
+// Store DH fp32 TMEM columns of one accumulator row as bf16.  M = 64 layout
+// (16x32bx2 reads): this thread holds half the row (u = 0: columns 0 .. DH/2-1,
+// u = 1: the rest) of row lane%16 (+16 per lane quadrant); M = 128 layout: the
+// whole row of its lane.
+template <int M, int DH>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, __nv_bfloat16* dst_row, int u) {
+    if constexpr (M == 64) {
+        constexpr int HALF = DH / 2;
+        uint32_t r[DH / 32][16];
+#pragma unroll
+        for (int i = 0; i < DH / 32; ++i) tc::tmem_ld_16x32bx2_x16<HALF>(taddr + 16 * i, r[i]);
+        tc::tmem_wait_ld();
+        uint4* dst = reinterpret_cast<uint4*>(dst_row + u * HALF);
+#pragma unroll
+        for (int i = 0; i < DH / 32; ++i) {
+            dst[2 * i] = pack8u(r[i]);
+            dst[2 * i + 1] = pack8u(r[i] + 8);
+        }
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+        for (int ci = 0; ci < DH / 16; ++ci) {
+            uint32_t r[16];
+            tc::tmem_ld_32x32b_x16(taddr + 16 * ci, r);
+            tc::tmem_wait_ld();
+            dst[2 * ci] = pack8u(r);
+            dst[2 * ci + 1] = pack8u(r + 8);
+        }
+    }
+}
+
+// Zero one accumulator row's share (layout as store_acc_row).
+template <int M, int DH>
+__device__ __forceinline__ void zero_acc_row(__nv_bfloat16* dst_row, int u) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    constexpr int n16 = (M == 64 ? DH / 2 : DH) / 8;
+    uint4* dst = reinterpret_cast<uint4*>(dst_row + (M == 64 ? u * (DH / 2) : 0));
+#pragma unroll
+    for (int q4 = 0; q4 < n16; ++q4) dst[q4] = z;
+}
+
 // Untiled bulk copy global -> shared, completing on an mbarrier (16-byte
 // aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -29,21 +29,26 @@ void resolve() {
 
 }  // namespace
 
-bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
-                      uint32_t box_rows) {
+bool encode_bf16_rows_box(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                          uint32_t box_cols, uint32_t box_rows) {
     std::call_once(g_once, resolve);
-    if (!g_encode) return false;
-    // 2-D view [rows, row_elems] of bf16, box = 64 elements (128 bytes) x box_rows,
-    // written to shared memory with the 128-byte swizzle.
+    if (!g_encode || (box_cols != 64 && box_cols != 32)) return false;
+    // 2-D view [rows, row_elems] of bf16, box = box_cols x box_rows, written to
+    // shared memory with the swizzle whose span is one box row (128 or 64 bytes).
     cuuint64_t dims[2] = {row_elems, rows};
     cuuint64_t strides[1] = {row_elems * 2};
-    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                      uint32_t box_rows) {
+    return encode_bf16_rows_box(map, base, rows, row_elems, 64, box_rows);
 }
 
 bool encode_bf16_seq(CUtensorMap* map, const void* base, uint64_t B, uint64_t L, uint64_t row_elems,

@@ -13,6 +13,11 @@ namespace gca {
 bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
                       uint32_t box_rows);
 
+// The same view with a box of box_cols (64 or 32) columns: 64 columns use the
+// 128-byte swizzle, 32 columns the 64-byte swizzle (one box row per swizzle span).
+bool encode_bf16_rows_box(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                          uint32_t box_cols, uint32_t box_rows);
+
 // Tensor map over bf16 sequences [B, L, row_elems] (row stride row_elems * 2
 // bytes, a multiple of 16), box of 64 columns x box_rows rows x 1 sequence,
 // 128-byte swizzle.  Rows outside [0, L) of a sequence are out of bounds:

@@ -63,7 +63,9 @@ def test_fwd_validation(lib):
     assert fwd(lib, params(dtype=7)) == INVALID
     assert fwd(lib, params(score_scale=-1.0)) == INVALID
     assert fwd(lib, params(topk=33)) == UNSUPPORTED
-    assert fwd(lib, params(d=48)) == UNSUPPORTED                     # bf16 path is d = 64
+    assert fwd(lib, params(d=48)) == UNSUPPORTED                     # bf16 path: d in {32, 64, 128}
+    assert fwd(lib, params(d=16)) == UNSUPPORTED
+    assert fwd(lib, params(d=256)) == UNSUPPORTED
     assert fwd(lib, params(S=32)) == UNSUPPORTED
     assert fwd(lib, params(dtype=1, d=128, S=64)) == UNSUPPORTED
 
