@@ -25,7 +25,7 @@
  *  - Pointers must be 16-byte aligned.
  *
  * Supported shapes (anything else returns GCA_ERR_UNSUPPORTED):
- *  - dtype GCA_BF16: d = 64, S in {64, 128}            (tensor-core path)
+ *  - dtype GCA_BF16: d in {32, 64, 128}, S in {64, 128} (tensor-core path)
  *  - dtype GCA_F32 : d in {16, 32, 64}, S in {16, 32, 64} (fp32 FFMA path)
  *  - 1 <= topk <= 32, landmark dimension <= 8192, chunks per row <= 16384.
  */

@@ -112,12 +112,11 @@ gca_status_t make_shape(const gca_params_t* p, bool need_pool, Shape* out) {
     return GCA_OK;
 }
 
-// Shapes the kernels of a pass support: bf16 runs the tensor-core kernels
-// (head dimension 32, 64 or 128 in the forward, 64 in the backward; S in
-// {64, 128}), fp32 the FFMA kernels.
-gca_status_t attn_supported(const Shape& s, bool backward) {
+// Shapes the attention kernels support: bf16 runs the tensor-core kernels
+// (head dimension 32, 64 or 128; S in {64, 128}), fp32 the FFMA kernels.
+gca_status_t attn_supported(const Shape& s) {
     if (s.dtype == GCA_BF16) {
-        const bool dim_ok = s.d == 64 || (!backward && (s.d == 32 || s.d == 128));
+        const bool dim_ok = s.d == 32 || s.d == 64 || s.d == 128;
         if (!dim_ok || (s.S != 64 && s.S != 128)) return GCA_ERR_UNSUPPORTED;
     } else {
         if ((s.d != 16 && s.d != 32 && s.d != 64) || !is_pow2(s.S) || s.S < 16 || s.S > 64)
@@ -225,7 +224,7 @@ gca_status_t gca_fwd(const gca_params_t* params, const void* q, const void* k, c
     Shape s;
     gca_status_t r = make_shape(params, true, &s);
     if (r != GCA_OK) return r;
-    if ((r = attn_supported(s, false)) != GCA_OK) return r;
+    if ((r = attn_supported(s)) != GCA_OK) return r;
     if ((r = check_ptrs({q, k, v, idx, weight, o})) != GCA_OK) return r;
     if (lse && !aligned16(lse)) return GCA_ERR_INVALID_ARG;
     int* st = status_word();
@@ -304,7 +303,7 @@ gca_status_t gca_bwd(const gca_params_t* params, const void* q, const void* k, c
     Shape s;
     gca_status_t r = make_shape(params, true, &s);
     if (r != GCA_OK) return r;
-    if ((r = attn_supported(s, true)) != GCA_OK) return r;
+    if ((r = attn_supported(s)) != GCA_OK) return r;
     if ((r = check_ptrs({q, k, v, idx, weight, lse, dout, dq, dk, dv, dscore})) != GCA_OK) return r;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GCA_ERR_WORKSPACE;
     if (ws_bytes < bwd_workspace_layout(s).total) return GCA_ERR_WORKSPACE;

@@ -1,4 +1,5 @@
-// attn_bwd_tc.cu -- GCA backward on the Blackwell tensor cores (bf16, d = 64).
+// attn_bwd_tc.cu -- GCA backward on the Blackwell tensor cores (bf16, head
+// dimension d = 32, 64 or 128).
 //
 // App. B backward (gradients for Q, K, V and the weights) of the forward
 // O_t = sum_j w_j softmax(s q_t K_j^T) V_j.  With p = exp(s q.k - lse_j),
@@ -32,6 +33,12 @@
 // other's issue; warps 3-10 are math warpgroups (two, one for the S = 128
 // key-major pass) taking alternate groups and alternate item epilogues; the
 // S = 64 math runs on column pairs in packed f32x2 arithmetic.
+// Head tiles of d = 64 and 128 are 64-column sub-tiles (128-byte swizzle), of
+// d = 32 one 32-column tile (64-byte swizzle); products contract over every
+// sub-tile and products with N = d issue one product per sub-tile.  Stage
+// counts, item buffers and the number of dK/dV accumulators are chosen per
+// (S, d) to fit shared memory and the 512 TMEM columns; at d = 128 the S = 64
+// key-major pass shares one operand pair between its math warpgroups.
 #include <math.h>
 
 #include "common.cuh"
@@ -98,41 +105,6 @@ __device__ __forceinline__ void load_cols64(uint32_t taddr, float* x) {
     tmem_wait_ld();
 }
 
-// Store 64 (S = 64: this thread's half) or 64 (S = 128: the full row) fp32
-// TMEM columns as bf16 into a [.., 64] row.
-template <int S>
-__device__ __forceinline__ void store_row64(uint32_t taddr, __nv_bfloat16* dst_row, int u) {
-    if (S == 64) {
-        uint32_t r0[16], r1[16];
-        tmem_ld_16x32bx2_x16<32>(taddr, r0);
-        tmem_ld_16x32bx2_x16<32>(taddr + 16, r1);
-        tmem_wait_ld();
-        uint4* dst = reinterpret_cast<uint4*>(dst_row + u * 32);
-        dst[0] = pack8u(r0);
-        dst[1] = pack8u(r0 + 8);
-        dst[2] = pack8u(r1);
-        dst[3] = pack8u(r1 + 8);
-    } else {
-        uint4* dst = reinterpret_cast<uint4*>(dst_row);
-#pragma unroll
-        for (int ci = 0; ci < 4; ++ci) {
-            uint32_t r[16];
-            tmem_ld_32x32b_x16(taddr + 16 * ci, r);
-            tmem_wait_ld();
-            dst[2 * ci] = pack8u(r);
-            dst[2 * ci + 1] = pack8u(r + 8);
-        }
-    }
-}
-
-template <int S>
-__device__ __forceinline__ void zero_row64(__nv_bfloat16* dst_row, int u) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    const int nq = (S == 64) ? 4 : 8;
-    uint4* dst = reinterpret_cast<uint4*>(dst_row + ((S == 64) ? u * 32 : 0));
-    for (int q4 = 0; q4 < nq; ++q4) dst[q4] = z;
-}
-
 // ============================================================================ pass A
 struct ItemInfoA {
     int b, c, h, n;
@@ -142,19 +114,22 @@ struct ItemInfoA {
     int8_t code[kMaxTopk];     // 0 valid, otherwise an empty or out-of-range slot
 };
 
-template <int S>
+template <int S, int DH>
 struct CfgA {
+    using G = tcx::HeadGeom<DH>;
     static constexpr int M = S;
     static constexpr int NG = S;                           // keys per group
-    static constexpr int NSB = (S == 64) ? 3 : 1;          // S/G TMEM buffers
-    static constexpr int STAGES = (S == 64) ? 8 : 2;
-    static constexpr int TILE = S * 128;
+    static constexpr int NSB = (S == 64) ? (DH == 128 ? 2 : 3) : 1;   // S/G TMEM buffers
+    // K/V ring depth and Q/dO buffers: what fits beside the P and lse buffers
+    static constexpr int STAGES = (S == 64) ? (DH == 128 ? 3 : 8) : (DH == 32 ? 4 : (DH == 64 ? 2 : 1));
+    static constexpr int IBUF = (S == 128 && DH == 128) ? 1 : 2;
+    static constexpr int TILE = G::tile_bytes(S);
     static constexpr int ITEM_BYTES = 2 * TILE;            // Q then dO
     static constexpr int STAGE_BYTES = 2 * TILE;           // K then V of one slot
     static constexpr int P_BLOCK = M * 128;
     static constexpr int P_BYTES = M * NG * 2;
     static constexpr int OFF_IT = 0;
-    static constexpr int OFF_KV = 2 * ITEM_BYTES;
+    static constexpr int OFF_KV = IBUF * ITEM_BYTES;
     static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
     // per info-ring entry: the item's lse block, S rows of topk floats
     static constexpr int LSE_TOPK_MAX = (S == 64) ? 16 : 8;
@@ -163,7 +138,9 @@ struct CfgA {
     static constexpr int SMEM = OFF_LSE + kInfo * LSE_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t SGW = 2 * S;                 // columns of one S/G buffer
-    static constexpr uint32_t COL_DQ = NSB * SGW;          // two dQ accumulators of 64 columns
+    static constexpr uint32_t COL_DQ = NSB * SGW;          // two dQ accumulators of DH columns
+    static_assert(COL_DQ + 2 * DH <= TMEM_COLS, "tensor memory");
+    static_assert(STAGES <= 8, "barrier arrays");
     // S/G-full barrier of group qq and the parity of its phase.  With one
     // buffer the two warpgroups alternate on it, so each has its own barrier
     // (kg = the warpgroup's group count).  With several buffers the issuer may
@@ -188,12 +165,13 @@ struct __align__(8) BarsA {
     ItemInfoA info[kInfo];
 };
 
-template <int S>
+template <int S, int DH>
 __global__ void __launch_bounds__(kThreadsA, 1)
 gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                     const __grid_constant__ CUtensorMap tl, const BwdArgs a) {
-    using C = CfgA<S>;
+    using C = CfgA<S, DH>;
+    using HG = tcx::HeadGeom<DH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -301,12 +279,16 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
                 mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
-                tma_load_2d(ib, &tq, &sb.it_full[it.i], h * 64, b * a.Lq + c * S);
-                tma_load_2d(ib + C::TILE, &tdo, &sb.it_full[it.i], h * 64, b * a.Lq + c * S);
+                for (int sub = 0; sub < HG::SUB; ++sub) {
+                    const int off = sub * S * HG::ROW_BYTES;
+                    tma_load_2d(ib + off, &tq, &sb.it_full[it.i], h * DH + sub * 64, b * a.Lq + c * S);
+                    tma_load_2d(ib + C::TILE + off, &tdo, &sb.it_full[it.i], h * DH + sub * 64,
+                                b * a.Lq + c * S);
+                }
             }
             it_out[it.i] = true;
             it_ph[it.i] = it.ph;
-            it.next(2);
+            it.next(C::IBUF);
             bool ok = true;
             for (int g = 0; g < n; ++g) {
                 if (!lane0_wait(&sb.kv_empty[kv.i], kv.ph ^ 1u)) { ok = false; break; }
@@ -314,8 +296,11 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     uint8_t* stg = sm + C::OFF_KV + kv.i * C::STAGE_BYTES;
                     const int y = (b * a.nP + I.kaps[g]) * S;
                     mbar_arrive_expect_tx(&sb.kv_full[kv.i], 2 * C::TILE);
-                    tma_load_2d(stg, &tk, &sb.kv_full[kv.i], h * 64, y);
-                    tma_load_2d(stg + C::TILE, &tv, &sb.kv_full[kv.i], h * 64, y);
+                    for (int sub = 0; sub < HG::SUB; ++sub) {
+                        const int off = sub * S * HG::ROW_BYTES;
+                        tma_load_2d(stg + off, &tk, &sb.kv_full[kv.i], h * DH + sub * 64, y);
+                        tma_load_2d(stg + C::TILE + off, &tv, &sb.kv_full[kv.i], h * DH + sub * 64, y);
+                    }
                 }
                 kv_out[kv.i] = true;
                 kv_ph[kv.i] = kv.ph;
@@ -326,7 +311,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         if (lane == 0) {
             for (int i = 0; i < C::STAGES; ++i)
                 if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < C::IBUF; ++i)
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
             for (int i = 0; i < kInfo; ++i)
                 if (inf_out[i]) mbar_wait(&sb.info_full[i], inf_ph[i], nullptr, 100000000ull);
@@ -359,15 +344,15 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
                     const uint32_t vaddr = kaddr + C::TILE;
-                    if (gs) tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + S, doaddr, vaddr, id_s, 0);
-                    else tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, qaddr, kaddr, id_s, 0);
+                    if (gs) tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW + S, doaddr, S, vaddr, S, id_s, 0);
+                    else tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW, qaddr, S, kaddr, S, id_s, 0);
                     mma_commit(&sb.s_full[C::sfull_index(qq)]);
                     issued = true;
                     kv.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.it_empty[it.i]);     // Q (dO) is read only by these products
-                it.next(2);
+                it.next(C::IBUF);
                 q += n;
             }
             if (issued) {
@@ -382,7 +367,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             Ring kv{0, 0}, inf{0, 0};
             int q = 0, e = 0;
             bool issued = false;
-            const uint32_t id_dq = idesc_bf16(C::M, 64, false, true);
+            const uint32_t id_dq = idesc_bf16(C::M, HG::SUB_COLS, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int n = sb.info[inf.i].n;
@@ -392,7 +377,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 const int ob = e & 1;
                 if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
                 tc_fence_after();
-                const uint32_t d_dq = tmem + C::COL_DQ + ob * 64;
+                const uint32_t d_dq = tmem + C::COL_DQ + ob * DH;
                 bool ok = true;
                 for (int g = 0; g < n; ++g) {
                     const int qq = q + g, pb = qq & 1;
@@ -400,7 +385,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     tc_fence_after();
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    tcx::mma_kmajor_mnmajor<S / 16>(d_dq, paddr, C::P_BLOCK, kaddr, id_dq, g > 0);
+                    tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dq, paddr, C::P_BLOCK, kaddr, S, id_dq, g > 0);
                     // the S / G products of this group are complete (their P exists)
                     mma_commit(&sb.kv_empty[kv.i]);
                     mma_commit(&sb.p_empty[pb]);
@@ -430,7 +415,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             const ItemInfoA& I = sb.info[inf.i];
             const int b = I.b, c = I.c, h = I.h, n = I.n;
             const size_t tok = (size_t)b * a.Lq + (size_t)c * S + row;
-            __nv_bfloat16* dqrow = a.dq + (tok * a.H + h) * 64;
+            __nv_bfloat16* dqrow = a.dq + (tok * a.H + h) * DH;
             const bool my_epi = (n == 0) ? ((n_all & 1) == wg) : ((e & 1) == wg);
             float* dwp = a.dwpart + (((size_t)b * a.nQ + c) * a.H + h) * 4 * a.topk;
             if (my_epi && threadIdx.x == 96 + wg * 128)
@@ -440,7 +425,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             if (n == 0) {
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
-                if (my_epi) zero_row64<S>(dqrow, u);
+                if (my_epi) tcx::zero_acc_row<S, DH>(dqrow, u);
                 continue;
             }
             const float* lse_s = reinterpret_cast<const float*>(sm + C::OFF_LSE + inf.i * C::LSE_BYTES);
@@ -586,7 +571,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             if (!wait(&sb.o_full[wg], full_par(ko))) break;
             ++ko;
             tc_fence_after();
-            store_row64<S>(tmem + lane_base + C::COL_DQ + wg * 64, dqrow, u);
+            tcx::store_acc_row<S, DH>(tmem + lane_base + C::COL_DQ + wg * DH, dqrow, u);
             tc_fence_before();
             mbar_arrive(&sb.o_empty[wg]);
         }
@@ -596,7 +581,7 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, CfgA<S>::TMEM_COLS);
+        tmem_dealloc(tmem, CfgA<S, DH>::TMEM_COLS);
     }
 }
 
@@ -613,15 +598,19 @@ struct EntryInfo {
 
 // The key-major pass for S = 128 (S = 64 uses the entry-pair kernel below): a
 // group is one inverse-index entry and the products are already M = 128.
-template <int S>
+template <int S, int DH>
 struct CfgB {
     static_assert(S == 128, "S = 64 runs gca_bwd_kv_pair_kernel");
+    using G = tcx::HeadGeom<DH>;
     static constexpr int M = S;                           // keys of the item
     static constexpr int NG = S;                          // tokens per group
     static constexpr int NWG = 1;                         // math warpgroups in use
     static constexpr int NSB = 1;                         // S^T/G^T TMEM buffers
-    static constexpr int STAGES = 2;
-    static constexpr int TILE = S * 128;
+    // what fits beside the operand pair: stages, K/V item buffers, dK/dV accumulators
+    static constexpr int STAGES = DH == 32 ? 4 : (DH == 64 ? 2 : 1);
+    static constexpr int IBUF = DH == 128 ? 1 : 2;
+    static constexpr int NACC = DH == 128 ? 1 : 2;
+    static constexpr int TILE = G::tile_bytes(S);
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
     static constexpr int VEC_OFF = 2 * TILE;              // after the Q and dO tiles
     static constexpr int ENT_OFF = VEC_OFF + 1024;        // lse2/delta rows, then entry info
@@ -629,12 +618,14 @@ struct CfgB {
     static constexpr int P_BLOCK = M * 128;
     static constexpr int P_BYTES = M * NG * 2;            // one operand (dA^T or wP^T)
     static constexpr int OFF_IT = 0;
-    static constexpr int OFF_ST = 2 * ITEM_BYTES;
+    static constexpr int OFF_ST = IBUF * ITEM_BYTES;
     static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
     static constexpr int SMEM = OFF_P + NWG * 2 * P_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t SGW = 2 * S;                // columns of one S^T/G^T buffer
-    static constexpr uint32_t COL_ACC = NSB * SGW;        // dK, dV: 2 x (64 + 64)
+    static constexpr uint32_t COL_ACC = NSB * SGW;        // dK then dV (DH columns each) per buffer
+    static_assert(COL_ACC + NACC * 2 * DH <= TMEM_COLS, "tensor memory");
+    static_assert(STAGES <= 6, "barrier arrays");
 };
 
 struct __align__(8) BarsB {
@@ -650,12 +641,13 @@ struct __align__(8) BarsB {
     ItemInfoB info[kInfo];
 };
 
-template <int S>
+template <int S, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
 gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                      const BwdArgs a) {
-    using C = CfgB<S>;
+    using C = CfgB<S, DH>;
+    using HG = tcx::HeadGeom<DH>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -747,12 +739,16 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
                 mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
-                tma_load_2d(ib, &tk, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
-                tma_load_2d(ib + C::TILE, &tv, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
+                for (int sub = 0; sub < HG::SUB; ++sub) {
+                    const int off = sub * S * HG::ROW_BYTES;
+                    tma_load_2d(ib + off, &tk, &sb.it_full[it.i], h * DH + sub * 64, (b * a.nP + kap) * S);
+                    tma_load_2d(ib + C::TILE + off, &tv, &sb.it_full[it.i], h * DH + sub * 64,
+                                (b * a.nP + kap) * S);
+                }
             }
             it_out[it.i] = true;
             it_ph[it.i] = it.ph;
-            it.next(2);
+            it.next(C::IBUF);
             bool ok = true;
             for (int base = 0; base < ne && ok; base += 32) {
                 int my_c = 0, my_j = 0;
@@ -774,8 +770,12 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                         EntryInfo* ei = reinterpret_cast<EntryInfo*>(stg + C::ENT_OFF);
                         ei->c = c; ei->j = j; ei->w = wv;
                         mbar_arrive_expect_tx(&sb.st_full[st.i], 2 * C::TILE + 2 * S * 4);
-                        tma_load_2d(stg, &tq, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
-                        tma_load_2d(stg + C::TILE, &tdo, &sb.st_full[st.i], h * 64, b * a.Lq + c * S);
+                        for (int sub = 0; sub < HG::SUB; ++sub) {
+                            const int off = sub * S * HG::ROW_BYTES;
+                            tma_load_2d(stg + off, &tq, &sb.st_full[st.i], h * DH + sub * 64, b * a.Lq + c * S);
+                            tma_load_2d(stg + C::TILE + off, &tdo, &sb.st_full[st.i], h * DH + sub * 64,
+                                        b * a.Lq + c * S);
+                        }
                         const size_t rb = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S;
                         tcx::bulk_load(stg + C::VEC_OFF, a.lse2_rows + rb, S * 4, &sb.st_full[st.i]);
                         tcx::bulk_load(stg + C::VEC_OFF + S * 4, a.delta_rows + rb, S * 4,
@@ -791,7 +791,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
         if (lane == 0) {
             for (int i = 0; i < C::STAGES; ++i)
                 if (st_out[i]) mbar_wait(&sb.st_full[i], st_ph[i], nullptr, 100000000ull);
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < C::IBUF; ++i)
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
@@ -820,15 +820,15 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                     tc_fence_after();
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
                     const uint32_t doaddr = qaddr + C::TILE;
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, kaddr, qaddr, id_s, 0);
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + S, vaddr, doaddr, id_s, 0);
+                    tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW, kaddr, S, qaddr, S, id_s, 0);
+                    tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW + S, vaddr, S, doaddr, S, id_s, 0);
                     mma_commit(&sb.s_full[qq % C::NWG]);
                     issued = true;
                     st.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.it_empty[it.i]);     // K and V are read only by these products
-                it.next(2);
+                it.next(C::IBUF);
                 q += ne;
             }
             if (issued) {
@@ -842,18 +842,18 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             Ring st{0, 0}, inf{0, 0};
             int q = 0, e = 0;
             bool issued = false;
-            const uint32_t id_acc = idesc_bf16(C::M, 64, false, true);
+            const uint32_t id_acc = idesc_bf16(C::M, HG::SUB_COLS, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
                 mbar_arrive(&sb.info_empty[inf.i]);
                 inf.next(kInfo);
                 if (ne <= 0) continue;
-                const int ob = e & 1;
-                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
+                const int ob = e % C::NACC;
+                if (!wait(&sb.o_empty[ob], empty_par(e / C::NACC))) break;
                 tc_fence_after();
-                const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
-                const uint32_t d_dv = d_dk + 64;
+                const uint32_t d_dk = tmem + C::COL_ACC + ob * 2 * DH;
+                const uint32_t d_dv = d_dk + DH;
                 bool ok = true;
                 for (int g = 0; g < ne; ++g) {
                     const int qq = q + g, pbuf = qq % C::NWG;
@@ -862,9 +862,9 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                     const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
                     const uint32_t doaddr = qaddr + C::TILE;
-                    tcx::mma_kmajor_mnmajor<S / 16>(d_dk, paddr, C::P_BLOCK, qaddr, id_acc, g > 0);
-                    tcx::mma_kmajor_mnmajor<S / 16>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, id_acc,
-                                                    g > 0);
+                    tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dk, paddr, C::P_BLOCK, qaddr, S, id_acc, g > 0);
+                    tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, S,
+                                                      id_acc, g > 0);
                     // the S^T / G^T products of this group are complete (their P exists)
                     mma_commit(&sb.st_empty[st.i]);
                     mma_commit(&sb.p_empty[pbuf]);
@@ -895,12 +895,12 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             mbar_arrive(&sb.info_empty[inf.i]);
             inf.next(kInfo);
             const size_t krow = (size_t)(I.b * a.nP + I.kap) * S + row;
-            __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * 64;
-            __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * 64;
+            __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * DH;
+            __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * DH;
             if (I.ne <= 0) {
                 if ((n_all % C::NWG) == wg) {
-                    zero_row64<S>(dkrow, u);
-                    zero_row64<S>(dvrow, u);
+                    tcx::zero_acc_row<S, DH>(dkrow, u);
+                    tcx::zero_acc_row<S, DH>(dvrow, u);
                 }
                 continue;
             }
@@ -969,14 +969,14 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             if (!ok) break;
             q += I.ne;
             const bool mine = (e % C::NWG) == wg;
-            const int ob = e & 1, ko = e >> 1;
+            const int ob = e % C::NACC, ko = e / C::NACC;
             ++e;
             if (!mine) continue;
             if (!wait(&sb.o_full[ob], full_par(ko))) break;
             tc_fence_after();
-            const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 128;
-            store_row64<S>(acc, dkrow, u);
-            store_row64<S>(acc + 64, dvrow, u);
+            const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 2 * DH;
+            tcx::store_acc_row<S, DH>(acc, dkrow, u);
+            tcx::store_acc_row<S, DH>(acc + DH, dvrow, u);
             tc_fence_before();
             mbar_arrive(&sb.o_empty[ob]);
         }
@@ -986,7 +986,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, CfgB<S>::TMEM_COLS);
+        tmem_dealloc(tmem, CfgB<S, DH>::TMEM_COLS);
     }
 }
 
@@ -1001,46 +1001,45 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 // the accumulation products read as MN-major A operands:
 // dK += dA^T [Q_1; Q_2] and dV += (w P)^T [dO_1; dO_2] over K = 128 queries
 // (64 for a single entry).
+template <int DH>
 struct CfgP {
+    using G = tcx::HeadGeom<DH>;
     static constexpr int S = 64;
-    static constexpr int TILE = 64 * 128;                 // 64 rows x 64 bf16
+    static constexpr int TILE = G::tile_bytes(64);        // 64 rows x DH bf16
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
-    static constexpr int STAGES = 3;                      // 6 entries in flight
-    static constexpr int Q_OFF = 0;                       // Q of entries 0 and 1 (rows 0-63, 64-127)
-    static constexpr int DO_OFF = 2 * TILE;               // dO of entries 0 and 1
+    // what fits: d = 128 keeps one K/V item buffer and one operand pair shared
+    // by both math warpgroups, and a single dK/dV accumulator in TMEM
+    static constexpr int STAGES = DH == 32 ? 4 : (DH == 64 ? 3 : 2);
+    static constexpr int IBUF = DH == 128 ? 1 : 2;
+    static constexpr bool SHARED_P = DH == 128;
+    static constexpr int NACC = DH == 128 ? 1 : 2;
+    // Q of entries 0 and 1: sub-tile s holds rows 0-63 (entry 0) then 64-127
+    // (entry 1), so [Q_1; Q_2] is one 128-row operand per sub-tile
+    static constexpr int Q_OFF = 0;
+    static constexpr int DO_OFF = 2 * TILE;               // dO of entries 0 and 1, likewise
     static constexpr int VEC_OFF = 4 * TILE;              // lse2[2][64], then delta[2][64]
     static constexpr int ENT_OFF = VEC_OFF + 1024;        // EntryInfo[2]
     static constexpr int STAGE_BYTES = VEC_OFF + 2048;
     static constexpr int ENTRY_TX = 2 * TILE + 2 * 64 * 4;
     static constexpr int P_BYTES = 128 * 128;             // one operand: 128 query rows x 64 keys
     static constexpr int OFF_IT = 0;
-    static constexpr int OFF_ST = 2 * ITEM_BYTES;
+    static constexpr int OFF_ST = IBUF * ITEM_BYTES;
     static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
-    static constexpr int SMEM = OFF_P + 2 * 2 * P_BYTES + 1024;
+    static constexpr int SMEM = OFF_P + (SHARED_P ? 1 : 2) * 2 * P_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t SGW = 128;                  // S (64 columns), then G
-    static constexpr uint32_t COL_ACC = 2 * SGW;          // dK, dV: 2 x (64 + 64)
+    static constexpr uint32_t COL_ACC = 2 * SGW;          // dK then dV (DH columns each) per buffer
+    static_assert(COL_ACC + NACC * 2 * DH <= TMEM_COLS, "tensor memory");
+    static_assert(STAGES <= 6, "barrier arrays");
 };
-static_assert(CfgP::STAGES <= 6, "barrier arrays");
 
-// D (+)= A^T B over ksteps*16 rows of K, A and B MN-major 128-byte-swizzled
-// tiles with 128-byte K rows (A: [K x 64 M], B: [K x 64 N]).
-__device__ __forceinline__ void mma_mnmajor_mnmajor(uint32_t d, uint32_t a_addr, uint32_t b_addr,
-                                                    uint32_t idesc, int ksteps, uint32_t acc_first) {
-    const uint64_t ad = tc::desc_mnmajor_sw128(a_addr);
-    const uint64_t bd = tc::desc_mnmajor_sw128(b_addr);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        if (ks == ksteps) break;
-        tc::mma_bf16(d, ad + (uint64_t)(ks * 128), bd + (uint64_t)(ks * 128), idesc, ks == 0 ? acc_first : 1u);
-    }
-}
-
+template <int DH>
 __global__ void __launch_bounds__(kThreadsA, 1)
 gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const BwdArgs a) {
-    using C = CfgP;
+    using C = CfgP<DH>;
+    using HG = tcx::HeadGeom<DH>;
     constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1155,12 +1154,16 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
                 mbar_arrive_expect_tx(&sb.it_full[it.i], C::ITEM_BYTES);
-                tma_load_2d(ib, &tk, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
-                tma_load_2d(ib + C::TILE, &tv, &sb.it_full[it.i], h * 64, (b * a.nP + kap) * S);
+                for (int sub = 0; sub < HG::SUB; ++sub) {
+                    const int off = sub * S * HG::ROW_BYTES;
+                    tma_load_2d(ib + off, &tk, &sb.it_full[it.i], h * DH + sub * 64, (b * a.nP + kap) * S);
+                    tma_load_2d(ib + C::TILE + off, &tv, &sb.it_full[it.i], h * DH + sub * 64,
+                                (b * a.nP + kap) * S);
+                }
             }
             it_out[it.i] = true;
             it_ph[it.i] = it.ph;
-            it.next(2);
+            it.next(C::IBUF);
             bool ok = true;
             for (int base = 0; base < ne && ok; base += 32) {
                 if (base > 0) fetch(b, e0, ne, base, bat_e, bat_w);
@@ -1184,10 +1187,13 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                         mbar_arrive_expect_tx(&sb.st_full[st.i], n2 * C::ENTRY_TX);
                         for (int x = 0; x < n2; ++x) {
                             ei[x].c = cc[x]; ei[x].j = jj[x]; ei[x].w = ww[x];
-                            tma_load_2d(stg + C::Q_OFF + x * C::TILE, &tq, &sb.st_full[st.i], h * 64,
-                                        b * a.Lq + cc[x] * S);
-                            tma_load_2d(stg + C::DO_OFF + x * C::TILE, &tdo, &sb.st_full[st.i], h * 64,
-                                        b * a.Lq + cc[x] * S);
+                            for (int sub = 0; sub < HG::SUB; ++sub) {
+                                const int off = (sub * 128 + x * 64) * HG::ROW_BYTES;
+                                tma_load_2d(stg + C::Q_OFF + off, &tq, &sb.st_full[st.i], h * DH + sub * 64,
+                                            b * a.Lq + cc[x] * S);
+                                tma_load_2d(stg + C::DO_OFF + off, &tdo, &sb.st_full[st.i], h * DH + sub * 64,
+                                            b * a.Lq + cc[x] * S);
+                            }
                             const size_t rb = ((((size_t)b * a.nQ + cc[x]) * a.topk + jj[x]) * a.H + h) * S;
                             tcx::bulk_load(stg + C::VEC_OFF + x * 256, a.lse2_rows + rb, S * 4, &sb.st_full[st.i]);
                             tcx::bulk_load(stg + C::VEC_OFF + 512 + x * 256, a.delta_rows + rb, S * 4,
@@ -1204,7 +1210,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         if (lane == 0) {
             for (int i = 0; i < C::STAGES; ++i)
                 if (st_out[i]) mbar_wait(&sb.st_full[i], st_ph[i], nullptr, 100000000ull);
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < C::IBUF; ++i)
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
@@ -1234,15 +1240,15 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                     }
                     tc_fence_after();
                     const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW, stg + C::Q_OFF, kaddr, id_s, 0);
-                    tcx::mma_kmajor_k64(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, vaddr, id_s, 0);
+                    tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW, stg + C::Q_OFF, 128, kaddr, S, id_s, 0);
+                    tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW + 64, stg + C::DO_OFF, 128, vaddr, S, id_s, 0);
                     mma_commit(&sb.s_full[sbuf]);
                     issued = true;
                     st.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.it_empty[it.i]);     // K and V are read only by these products
-                it.next(2);
+                it.next(C::IBUF);
                 q += ng;
             }
             if (issued) {
@@ -1258,7 +1264,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             Ring st{0, 0}, inf{0, 0};
             int q = 0, e = 0;
             bool issued = false;
-            const uint32_t id_acc = idesc_bf16(64, 64, true, true);
+            const uint32_t id_acc = idesc_bf16(64, HG::SUB_COLS, true, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
@@ -1266,31 +1272,34 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 inf.next(kInfo);
                 if (ne <= 0) continue;
                 const int ng = (ne + 1) >> 1;
-                const int ob = e & 1;
-                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
+                const int ob = e % C::NACC;
+                if (!wait(&sb.o_empty[ob], empty_par(e / C::NACC))) break;
                 tc_fence_after();
-                const uint32_t d_dk = tmem + C::COL_ACC + ob * 128;
-                const uint32_t d_dv = d_dk + 64;
+                const uint32_t d_dk = tmem + C::COL_ACC + ob * 2 * DH;
+                const uint32_t d_dv = d_dk + DH;
                 bool ok = true;
                 for (int g = 0; g < ng; ++g) {
                     const int qq = q + g, pbuf = qq & 1;
                     const int ksteps = (2 * g + 1 < ne) ? 8 : 4;
                     if (!wait(&sb.p_full[pbuf], full_par(qq >> 1))) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
+                    const uint32_t paddr = smem_u32(sm + C::OFF_P + (C::SHARED_P ? 0 : pbuf * 2 * C::P_BYTES));
                     const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
                     if (dvi)
-                        mma_mnmajor_mnmajor(d_dv, paddr + C::P_BYTES, stg + C::DO_OFF, id_acc, ksteps,
-                                            g > 0 ? 1u : 0u);
+                        tcx::mma_mn_mn_dh<DH>(d_dv, paddr + C::P_BYTES, stg + C::DO_OFF, 128, id_acc, ksteps,
+                                              g > 0 ? 1u : 0u);
                     else
-                        mma_mnmajor_mnmajor(d_dk, paddr, stg + C::Q_OFF, id_acc, ksteps, g > 0 ? 1u : 0u);
+                        tcx::mma_mn_mn_dh<DH>(d_dk, paddr, stg + C::Q_OFF, 128, id_acc, ksteps, g > 0 ? 1u : 0u);
                     mma_commit(&sb.st_empty[st.i]);
                     mma_commit(&sb.p_empty[pbuf]);
                     issued = true;
                     st.next(C::STAGES);
                 }
                 if (!ok) break;
-                mma_commit(&sb.o_full[ob]);
+                // the full barrier belongs to the warpgroup that stores this item (item
+                // parity), whatever the TMEM buffer: with one accumulator, a barrier
+                // shared by both warpgroups could be awaited two phases behind
+                mma_commit(&sb.o_full[e & 1]);
                 q += ng;
                 ++e;
             }
@@ -1317,12 +1326,12 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             mbar_arrive(&sb.info_empty[inf.i]);
             inf.next(kInfo);
             const size_t krow = (size_t)(I.b * a.nP + I.kap) * S + erow;
-            __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * 64;
-            __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * 64;
+            __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * DH;
+            __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * DH;
             if (I.ne <= 0) {
                 if ((n_all & 1) == wg) {
-                    zero_row64<S>(dkrow, eu);
-                    zero_row64<S>(dvrow, eu);
+                    tcx::zero_acc_row<64, DH>(dkrow, eu);
+                    tcx::zero_acc_row<64, DH>(dvrow, eu);
                 }
                 continue;
             }
@@ -1347,7 +1356,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 const float wv = ei.w, wsc = wv * a.attn_scale;
                 const uint64_t l2 = tcx::f2_pack(lse2, lse2), dl2 = tcx::f2_pack(dlt, dlt);
                 const uint64_t wv2 = tcx::f2_pack(wv, wv), wsc2 = tcx::f2_pack(wsc, wsc);
-                uint8_t* pa_buf = sm + C::OFF_P + wg * 2 * C::P_BYTES;
+                uint8_t* pa_buf = sm + C::OFF_P + (C::SHARED_P ? 0 : wg * 2 * C::P_BYTES);
                 uint8_t* pp_buf = pa_buf + C::P_BYTES;
                 const uint32_t ts0 = tmem + lane_base + sbuf * C::SGW;
                 const uint32_t tg0 = ts0 + 64;
@@ -1380,7 +1389,17 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                         pp[p] = tcx::pack_bf16x2(tcx::fmul2(pr2, wv2));
                         pa[p] = tcx::pack_bf16x2(tcx::fmul2(tcx::fmul2(pr2, wsc2), tcx::fsub2(g2, dl2)));
                     }
-                    if (hf == 0 && !wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
+                    if (hf == 0) {
+                        // own operand pair: free once this warpgroup's previous pair was read.
+                        // Shared pair: pair qq overwrites it once the products of pair qq - 1
+                        // (the other warpgroup's) have read it; that barrier completes only for
+                        // the other warpgroup's pairs, and its next phase needs this pair's
+                        // products, so it is at most one phase from the one awaited.
+                        const bool pw = C::SHARED_P
+                            ? (qq == 0 || wait(&sb.p_empty[wg ^ 1], full_par((qq - 1) >> 1)))
+                            : wait(&sb.p_empty[wg], empty_par(kg));
+                        if (!pw) { ok = false; break; }
+                    }
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
                         const uint32_t off = sw128_off(prow, 4 * hf + c4);
@@ -1398,14 +1417,14 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             if (!ok) break;
             q += ng;
             const bool mine = (e & 1) == wg;
-            const int ob = e & 1, ko = e >> 1;
+            const int ob = e % C::NACC, ko = e >> 1;     // TMEM buffer; this warpgroup's epilogue count
             ++e;
             if (!mine) continue;
-            if (!wait(&sb.o_full[ob], full_par(ko))) break;
+            if (!wait(&sb.o_full[wg], full_par(ko))) break;
             tc_fence_after();
-            const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 128;
-            store_row64<S>(acc, dkrow, eu);
-            store_row64<S>(acc + 64, dvrow, eu);
+            const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 2 * DH;
+            tcx::store_acc_row<64, DH>(acc, dkrow, eu);
+            tcx::store_acc_row<64, DH>(acc + DH, dvrow, eu);
             tc_fence_before();
             mbar_arrive(&sb.o_empty[ob]);
         }
@@ -1415,21 +1434,27 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, CfgP::TMEM_COLS);
+        tmem_dealloc(tmem, CfgP<DH>::TMEM_COLS);
     }
 }
 
 // ============================================================================ launch
-template <int S>
+// Dynamic plus static shared memory of each kernel within the 227 KB a CTA may use.
+constexpr int kSmemMax = 232448;
+template <int S, int DH>
 cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const void* v,
                          const int32_t* idx, const float* w, const float* lse, const void* dout,
                          void* dq, void* dk, void* dv, void* ws, int* status, cudaStream_t st) {
+    static_assert(CfgA<S, DH>::SMEM + sizeof(BarsA) <= kSmemMax, "shared memory (query-major pass)");
+    if constexpr (S == 64) static_assert(CfgP<DH>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
+    else static_assert(CfgB<S, DH>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (key-major pass)");
     CUtensorMap tq, tdo, tk, tv;
-    const uint64_t cols = (uint64_t)sp.H * 64;
-    if (!encode_bf16_rows(&tq, q, (uint64_t)sp.B * sp.Lq, cols, S) ||
-        !encode_bf16_rows(&tdo, dout, (uint64_t)sp.B * sp.Lq, cols, S) ||
-        !encode_bf16_rows(&tk, k, (uint64_t)sp.B * sp.nP * S, cols, S) ||
-        !encode_bf16_rows(&tv, v, (uint64_t)sp.B * sp.nP * S, cols, S))
+    const uint64_t cols = (uint64_t)sp.H * DH;
+    constexpr uint32_t bc = tcx::HeadGeom<DH>::SUB_COLS;
+    if (!encode_bf16_rows_box(&tq, q, (uint64_t)sp.B * sp.Lq, cols, bc, S) ||
+        !encode_bf16_rows_box(&tdo, dout, (uint64_t)sp.B * sp.Lq, cols, bc, S) ||
+        !encode_bf16_rows_box(&tk, k, (uint64_t)sp.B * sp.nP * S, cols, bc, S) ||
+        !encode_bf16_rows_box(&tv, v, (uint64_t)sp.B * sp.nP * S, cols, bc, S))
         return cudaErrorInvalidValue;
     const BwdWorkspace L = bwd_workspace_layout(sp);
     char* base = static_cast<char*>(ws);
@@ -1451,7 +1476,7 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     // pass A stages each item's lse block [S x topk] by TMA when its rows are
     // 16-byte granular and the block fits the per-item staging area
     CUtensorMap tl;
-    a.lse_smem = (sp.topk % 4 == 0 && sp.topk <= CfgA<S>::LSE_TOPK_MAX &&
+    a.lse_smem = (sp.topk % 4 == 0 && sp.topk <= CfgA<S, DH>::LSE_TOPK_MAX &&
                   (reinterpret_cast<uintptr_t>(lse) & 15) == 0 &&
                   encode_f32_box(&tl, lse, (uint64_t)sp.B * sp.Lq, (uint64_t)sp.H * sp.topk,
                                  (uint32_t)sp.topk, S)) ? 1 : 0;
@@ -1461,25 +1486,25 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
     a.n_items = sp.B * sp.nQ * sp.H;
-    auto ka = gca_bwd_q_tc_kernel<S>;
-    cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgA<S>::SMEM);
+    auto ka = gca_bwd_q_tc_kernel<S, DH>;
+    cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgA<S, DH>::SMEM);
     if (e != cudaSuccess) return e;
     int grid = a.n_items < sms ? a.n_items : sms;
-    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreadsA, CfgA<S>::SMEM, st>>>(tq, tdo, tk, tv, tl, a));
+    GCA_LAUNCH("bwd_q_tc", st, ka<<<grid, kThreadsA, CfgA<S, DH>::SMEM, st>>>(tq, tdo, tk, tv, tl, a));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     a.n_items = sp.B * sp.nP * sp.H;
     grid = a.n_items < sms ? a.n_items : sms;
     if constexpr (S == 64) {
-        auto kb = gca_bwd_kv_pair_kernel;
-        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgP::SMEM);
+        auto kb = gca_bwd_kv_pair_kernel<DH>;
+        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgP<DH>::SMEM);
         if (e != cudaSuccess) return e;
-        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, CfgP::SMEM, st>>>(tq, tdo, tk, tv, a));
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, CfgP<DH>::SMEM, st>>>(tq, tdo, tk, tv, a));
     } else {
-        auto kb = gca_bwd_kv_tc_kernel<S>;
-        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S>::SMEM);
+        auto kb = gca_bwd_kv_tc_kernel<S, DH>;
+        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S, DH>::SMEM);
         if (e != cudaSuccess) return e;
-        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgB<S>::SMEM, st>>>(tq, tdo, tk, tv, a));
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgB<S, DH>::SMEM, st>>>(tq, tdo, tk, tv, a));
     }
     return cudaGetLastError();
 }
@@ -1492,8 +1517,10 @@ cudaError_t launch_bwd_tc(const Shape& sp, const void* q, const void* k, const v
                           cudaStream_t st, int* launches) {
     cudaError_t e = launch_inverse_index(sp, idx, w, ws, st, launches);
     if (e != cudaSuccess) return e;
-    e = (sp.S == 64) ? launch_bwd_s<64>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st)
-                     : launch_bwd_s<128>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st);
+#define GCA_BWD_S(S_, DH_) launch_bwd_s<S_, DH_>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st)
+    if (sp.S == 64) e = sp.d == 32 ? GCA_BWD_S(64, 32) : (sp.d == 128 ? GCA_BWD_S(64, 128) : GCA_BWD_S(64, 64));
+    else e = sp.d == 32 ? GCA_BWD_S(128, 32) : (sp.d == 128 ? GCA_BWD_S(128, 128) : GCA_BWD_S(128, 64));
+#undef GCA_BWD_S
     if (e != cudaSuccess) return e;
     *launches += 2;
     return launch_dscore(sp, idx, w, ws, dscore, st, launches);

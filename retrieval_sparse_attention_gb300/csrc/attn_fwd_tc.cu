@@ -1,4 +1,5 @@
-// attn_fwd_tc.cu -- GCA forward on the Blackwell tensor cores (bf16, d = 64).
+// attn_fwd_tc.cu -- GCA forward on the Blackwell tensor cores (bf16, head
+// dimension d = 32, 64 or 128).
 //
 // GCA (README "Model Architecture"; Figure 1/2; Eq. 2 as the batch form of
 // Figure 2): every token t of query chunk c attends separately to each
@@ -32,6 +33,10 @@
 //          slots; each softmax thread owns one (token, slot) row of 64 keys.
 // S = 128: M = 128 MMAs (row r at lane r); a group is one slot; each softmax
 //          thread owns one token row of 128 keys.
+// Head tiles: d = 64 and 128 as 64-column sub-tiles with the 128-byte swizzle
+// (a TMA box each), d = 32 as one 32-column tile with the 64-byte swizzle; the
+// score product contracts over every sub-tile, P V issues one N = 64 (or 32)
+// product per sub-tile into adjacent TMEM columns.
 // Every mbarrier wait is bounded (status GCA_ERR_TIMEOUT, then the CTA winds
 // down); indices outside [0, n_pool_chunks) are skipped and reported.
 #include <math.h>
@@ -81,7 +86,6 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;                // two S buffers of 128 columns
     static constexpr uint32_t COL_O = 256;              // two O buffers of DH columns
-    static_assert(SMEM <= 232448 - 1024, "shared memory");
     static_assert(COL_O + 2 * DH <= TMEM_COLS, "tensor memory");
 };
 
@@ -464,6 +468,7 @@ template <int S, int DH>
 cudaError_t launch_s(const Shape& sp, const void* q, const void* k, const void* v,
                      const int32_t* idx, const float* w, void* o, float* lse, int* status,
                      cudaStream_t st) {
+    static_assert(Cfg<S, DH>::SMEM + sizeof(Bars) <= 232448, "shared memory: dynamic + static");
     CUtensorMap tq, tk, tv;
     const uint64_t cols = (uint64_t)sp.H * DH;
     constexpr uint32_t bc = tcx::HeadGeom<DH>::SUB_COLS;
