@@ -66,9 +66,15 @@ struct Cfg {
     static constexpr int M = S;                         // tokens per item = MMA M
     static constexpr int GS = 128 / S;                  // slots per group
     static constexpr int NG = 128;                      // keys per full group
-    // K/V ring depth and Q buffers: what fits beside the P buffers
-    static constexpr int STAGES = DH == 128 ? 2 : ((S == 64) ? 4 : 3);
-    static constexpr int QBUF = (S == 128 && DH == 128) ? 1 : 2;
+    // S = 128 keeps P in tensor memory over its own S row (the softmax thread
+    // owns TMEM lane = row, which is the A operand layout of P V), so it needs
+    // no shared-memory P buffers; an S buffer is then held until its P V
+    // products complete, and three of them rotate (two at d = 128).
+    static constexpr bool TP = (S == 128);
+    static constexpr int NSB = TP ? (DH == 128 ? 2 : 3) : 2;
+    // K/V ring depth: what fits beside Q (and the P buffers when S = 64)
+    static constexpr int STAGES = TP ? (DH == 32 ? 6 : (DH == 64 ? 5 : 2)) : (DH == 128 ? 2 : 4);
+    static constexpr int QBUF = 2;
     static constexpr int TILE = G::tile_bytes(S);       // one slot's K (or V) tile, bytes
     static constexpr int Q_BYTES = G::tile_bytes(S);
     // K half then V half; in each, sub-tile s holds the NG key rows of the
@@ -82,10 +88,11 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + QBUF * Q_BYTES;
     static constexpr int OFF_P = OFF_KV + STAGES * STAGE_BYTES;
-    static constexpr int SMEM = OFF_P + 2 * P_BYTES + 1024;   // + alignment slack
+    static constexpr int SMEM = OFF_P + (TP ? 0 : 2 * P_BYTES) + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0;                // two S buffers of 128 columns
-    static constexpr uint32_t COL_O = 256;              // two O buffers of DH columns
+    static constexpr uint32_t COL_S = 0;                // NSB S buffers of 128 columns
+    static constexpr uint32_t COL_O = NSB * 128;        // two O buffers of DH columns
+    static_assert(STAGES <= 6 && NSB <= 3, "barrier arrays");
     static_assert(COL_O + 2 * DH <= TMEM_COLS, "tensor memory");
 };
 
@@ -111,9 +118,9 @@ struct ItemInfo {
 struct __align__(8) Bars {
     uint64_t info_full[kInfo], info_empty[kInfo];
     uint64_t q_full[2], q_empty[2];
-    uint64_t kv_full[4], kv_empty[4];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full[2], p_empty[2];
+    uint64_t kv_full[6], kv_empty[6];
+    uint64_t s_full[3], s_empty[3];
+    uint64_t p_full[4], p_empty[2];
     uint64_t o_full[2], o_empty[2];
     uint64_t done, done2;
     uint32_t tmem;
@@ -129,6 +136,18 @@ __device__ __forceinline__ bool wait_bar(Bars& sb, uint64_t* bar, uint32_t parit
 // barriers complete once per use, "empty" ones start out released.
 __device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
 __device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
+
+// P-full barrier of group qq and the phase it completes.  With P in shared
+// memory a warpgroup's next P waits for the previous one's products, so one
+// barrier per warpgroup suffices.  With P in TMEM nothing holds a fast warp
+// back from its warpgroup's next group: its arrival for group qq + 2 could
+// then count toward group qq's phase, so each warpgroup alternates two
+// barriers (a warp reaches group qq + 4 only after P V of qq + 1 was issued,
+// which needed group qq's phase complete).
+template <bool TP>
+__device__ __forceinline__ int pfull_index(int qq) { return TP ? (qq & 3) : (qq & 1); }
+template <bool TP>
+__device__ __forceinline__ uint32_t pfull_par(int qq) { return full_par(TP ? (qq >> 2) : (qq >> 1)); }
 
 template <int S, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -147,12 +166,16 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(&sb.info_full[i], 1);
             mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + every softmax thread
         }
+        for (int i = 0; i < C::NSB; ++i) {
+            mbar_init(&sb.s_full[i], 1);
+            // released by the softmax threads' reads, or (P in TMEM) by the P V products
+            mbar_init(&sb.s_empty[i], C::TP ? 1 : 128);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.q_full[i], 1);
             mbar_init(&sb.q_empty[i], 1);
-            mbar_init(&sb.s_full[i], 1);
-            mbar_init(&sb.s_empty[i], 128);
             mbar_init(&sb.p_full[i], 128);
+            mbar_init(&sb.p_full[2 + i], 128);
             mbar_init(&sb.p_empty[i], 1);
             mbar_init(&sb.o_full[i], 1);
             mbar_init(&sb.o_empty[i], 128);
@@ -184,8 +207,8 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             Ring kv{0, 0}, qr{0, 0}, inf{0, 0};
-            bool kv_out[4] = {false, false, false, false}, q_out[2] = {false, false};
-            uint32_t kv_ph[4] = {0, 0, 0, 0}, q_ph[2] = {0, 0};
+            bool kv_out[6] = {}, q_out[2] = {false, false};
+            uint32_t kv_ph[6] = {}, q_ph[2] = {0, 0};
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 const int h = item % a.H, bc = item / a.H, c = bc % a.nQ, b = bc / a.nQ;
                 if (!wait_bar(sb, &sb.info_empty[inf.i], inf.ph ^ 1u, a.status)) break;
@@ -264,9 +287,9 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 bool ok = true;
                 for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
-                    const int qq = q + g, sbuf = qq & 1;
+                    const int qq = q + g, sbuf = qq % C::NSB;
                     if (!wait_bar(sb, &sb.kv_full[kv.i], kv.ph, a.status) ||
-                        !wait_bar(sb, &sb.s_empty[sbuf], empty_par(qq >> 1), a.status)) { ok = false; break; }
+                        !wait_bar(sb, &sb.s_empty[sbuf], empty_par(qq / C::NSB), a.status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
                     tcx::mma_kmajor_dh<DH>(tmem + C::COL_S + sbuf * 128, qaddr, S, kaddr, C::NG,
@@ -308,17 +331,28 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 for (int g = 0; g < G; ++g) {
                     const int ns = min(C::GS, n - g * C::GS);
                     const int qq = q + g, pbuf = qq & 1;
-                    if (!wait_bar(sb, &sb.p_full[pbuf], full_par(qq >> 1), a.status)) { ok = false; break; }
+                    if (!wait_bar(sb, &sb.p_full[pfull_index<C::TP>(qq)], pfull_par<C::TP>(qq), a.status)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * C::P_BYTES);
                     const uint32_t vaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES + C::HALF_BYTES);
-                    if (ns * S == 128)
-                        tcx::mma_kmajor_mn_dh<DH, 8>(d_o, paddr, C::P_BLOCK, vaddr, C::NG, id_o, g > 0);
-                    else
-                        tcx::mma_kmajor_mn_dh<DH, 4>(d_o, paddr, C::P_BLOCK, vaddr, C::NG, id_o, g > 0);
-                    // S_g is complete (its P exists), so the whole stage may be reused
-                    mma_commit(&sb.kv_empty[kv.i]);
-                    mma_commit(&sb.p_empty[pbuf]);
+                    if constexpr (C::TP) {
+                        // P_g sits in its S buffer's first 64 columns (bf16 pairs)
+                        const int sbuf = qq % C::NSB;
+                        tcx::mma_ts_mn_dh<DH, 8>(d_o, tmem + C::COL_S + sbuf * 128, vaddr, C::NG, id_o, g > 0);
+                        mma_commit(&sb.kv_empty[kv.i]);
+                        mma_commit(&sb.s_empty[sbuf]);
+                    } else {
+                        const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * C::P_BYTES);
+                        if (ns * S == 128)
+                            tcx::mma_kmajor_mn_dh<DH, 8>(d_o, paddr, C::P_BLOCK, vaddr, C::NG, id_o, g > 0);
+                        else
+                            tcx::mma_kmajor_mn_dh<DH, 4>(d_o, paddr, C::P_BLOCK, vaddr, C::NG, id_o, g > 0);
+                        // S_g is complete (its P exists), so the whole stage may be reused
+                        mma_commit(&sb.kv_empty[kv.i]);
+                        mma_commit(&sb.p_empty[pbuf]);
+                    }
                     issued = true;
                     kv.next(C::STAGES);
                 }
@@ -372,10 +406,11 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const bool active = u < ns;
                 const int j = active ? I.js[g * C::GS + u] : 0;
                 const float wj = active ? I.w[g * C::GS + u] : 0.f;
-                if (!wait_bar(sb, &sb.s_full[wg], full_par(kg), a.status)) { ok = false; break; }
+                const int sbuf = qq % C::NSB;
+                if (!wait_bar(sb, &sb.s_full[sbuf], full_par(qq / C::NSB), a.status)) { ok = false; break; }
                 tc_fence_after();
                 float x[C::VALS];
-                const uint32_t taddr = tmem + lane_base + C::COL_S + wg * 128;
+                const uint32_t taddr = tmem + lane_base + C::COL_S + sbuf * 128;
                 if (S == 64) {
 #pragma unroll
                     for (int ci = 0; ci < C::VALS / 16; ++ci) {
@@ -394,8 +429,10 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     }
                 }
                 tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&sb.s_empty[wg]);
+                if constexpr (!C::TP) {
+                    tc_fence_before();
+                    mbar_arrive(&sb.s_empty[sbuf]);
+                }
                 float mx = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < C::VALS; ++i) mx = fmaxf(mx, x[i]);
@@ -408,19 +445,33 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 const float coef = active ? wj / l : 0.f;
                 if (active && lrow) lrow[j] = (mb + log2f(l)) * kLn2;
-                if (!wait_bar(sb, &sb.p_empty[wg], empty_par(kg), a.status)) { ok = false; break; }
-                if (active) {
-                    uint8_t* pbase = sm + C::OFF_P + wg * C::P_BYTES + row * 128;
+                if constexpr (C::TP) {
+                    // P over the first 64 columns of this row's S buffer, two keys per column
 #pragma unroll
-                    for (int ch = 0; ch < C::VALS / 8; ++ch) {
-                        const int blk = (S == 64) ? u : (ch >> 3);
-                        const int cc = ch & 7;
-                        *reinterpret_cast<uint4*>(pbase + blk * C::P_BLOCK + ((cc ^ (row & 7)) << 4)) =
-                            tcx::pack8(x + 8 * ch, coef);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            pk[t] = tcx::pack_bf16(x[32 * ch + 2 * t] * coef, x[32 * ch + 2 * t + 1] * coef);
+                        tmem_st_32x32b_x16(taddr + 16 * ch, pk);
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                } else {
+                    if (!wait_bar(sb, &sb.p_empty[wg], empty_par(kg), a.status)) { ok = false; break; }
+                    if (active) {
+                        uint8_t* pbase = sm + C::OFF_P + wg * C::P_BYTES + row * 128;
+#pragma unroll
+                        for (int ch = 0; ch < C::VALS / 8; ++ch) {
+                            const int blk = (S == 64) ? u : (ch >> 3);
+                            const int cc = ch & 7;
+                            *reinterpret_cast<uint4*>(pbase + blk * C::P_BLOCK + ((cc ^ (row & 7)) << 4)) =
+                                tcx::pack8(x + 8 * ch, coef);
+                        }
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(&sb.p_full[wg]);
+                mbar_arrive(&sb.p_full[pfull_index<C::TP>(qq)]);
                 ++kg;
             }
             mbar_arrive(&sb.info_empty[inf.i]);

@@ -206,6 +206,24 @@ __device__ __forceinline__ void mma_kmajor_mn_dh(uint32_t d, uint32_t p_addr, ui
     }
 }
 
+// D (+)= P X over KSTEPS*16 rows of K with P in tensor memory (p_tmem: column
+// of K = 0, lane 0; 8 columns per K = 16 step) and X an MN-major head tile
+// (x_rows rows per sub-tile).  Sub-tile s accumulates into TMEM columns
+// d + s * SUB_COLS; idesc must give N = SUB_COLS and a K-major A.
+template <int DH, int KSTEPS>
+__device__ __forceinline__ void mma_ts_mn_dh(uint32_t d, uint32_t p_tmem, uint32_t x_addr, int x_rows,
+                                             uint32_t idesc, uint32_t acc_first) {
+    using G = HeadGeom<DH>;
+#pragma unroll
+    for (int s = 0; s < G::SUB; ++s) {
+        const uint64_t xd = desc_head<DH>(x_addr + s * x_rows * G::ROW_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+            tc::mma_bf16_ts(d + s * G::SUB_COLS, p_tmem + 8 * ks, xd + (uint64_t)(ks * (G::KROW16 >> 4)),
+                            idesc, ks == 0 ? acc_first : 1u);
+    }
+}
+
 // D (+)= A^T X over ksteps*16 rows of K: A MN-major with 128-byte rows (64
 // elements along M), X an MN-major head tile (x_rows rows per sub-tile).
 template <int DH>
