@@ -433,16 +433,38 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     tc_fence_before();
                     mbar_arrive(&sb.s_empty[sbuf]);
                 }
-                float mx = -INFINITY;
+                // row max and row sum (S = 128: eight independent chains, combined in a fixed order)
+                float mx, l;
+                if constexpr (S == 128) {
+                    float m8[8], l8[8];
 #pragma unroll
-                for (int i = 0; i < C::VALS; ++i) mx = fmaxf(mx, x[i]);
-                const float mb = mx * a.scale_log2;
-                float l = 0.f;
+                    for (int i = 0; i < 8; ++i) m8[i] = x[i];
 #pragma unroll
-                for (int i = 0; i < C::VALS; ++i) {
-                    x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -mb));
-                    l += x[i];
+                    for (int i = 8; i < C::VALS; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    const float mb = mx * a.scale_log2;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < C::VALS; ++i) {
+                        x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -mb));
+                        l8[i & 7] += x[i];
+                    }
+                    l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+                } else {
+                    mx = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < C::VALS; ++i) mx = fmaxf(mx, x[i]);
+                    const float mb = mx * a.scale_log2;
+                    l = 0.f;
+#pragma unroll
+                    for (int i = 0; i < C::VALS; ++i) {
+                        x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -mb));
+                        l += x[i];
+                    }
                 }
+                const float mb = mx * a.scale_log2;
                 const float coef = active ? wj / l : 0.f;
                 if (active && lrow) lrow[j] = (mb + log2f(l)) * kLn2;
                 if constexpr (C::TP) {
