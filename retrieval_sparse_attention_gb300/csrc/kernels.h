@@ -69,6 +69,11 @@ cudaError_t launch_score_topk(const Shape& s, const void* lm, const float* noise
                               float* score, float* weight, int* status, cudaStream_t st,
                               int* launches);
 
+// The same on the tensor cores (bf16 landmarks, D a multiple of 64, at least two chunks, k <= 16).
+bool score_topk_tc_supported(const Shape& s);
+cudaError_t launch_score_topk_tc(const Shape& s, const void* lm, const float* noise, int32_t* idx,
+                                 float* score, float* weight, int* status, cudaStream_t st);
+
 // Landmark gradients; ws holds an inverse index (inverse_index_bytes()).
 size_t inverse_index_bytes(int B, int nQ, int nP, int topk);
 cudaError_t launch_landmark_bwd(const Shape& s, const void* lm, const int32_t* idx,

@@ -159,7 +159,12 @@ void launch_typed(const Shape& sp, const void* lm, const float* noise, int32_t* 
 cudaError_t launch_score_topk(const Shape& sp, const void* lm, const float* noise, int32_t* idx,
                               float* score, float* weight, int* status, cudaStream_t st,
                               int* launches) {
-    (void)status;
+    if (score_topk_tc_supported(sp)) {
+        // bf16 landmarks with D a multiple of 64: scores from the tensor cores
+        const cudaError_t e = launch_score_topk_tc(sp, lm, noise, idx, score, weight, status, st);
+        if (e == cudaSuccess) *launches += 1;
+        return e;
+    }
     if (sp.dtype == GCA_BF16) {
         if (noise) launch_typed<__nv_bfloat16, true>(sp, lm, noise, idx, score, weight, st);
         else launch_typed<__nv_bfloat16, false>(sp, lm, noise, idx, score, weight, st);

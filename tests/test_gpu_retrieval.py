@@ -128,3 +128,31 @@ def test_signed_zero_scores_tie_toward_lower_index():
     q[1:] = -0.0
     idx = run_decode(tab, q, 8, False)
     assert idx.cpu().tolist() == list(range(8))
+
+
+@pytest.mark.parametrize("B,nC,D,k", [(16, 200, 64, 8), (8, 256, 768, 16), (4, 520, 128, 5)])
+@pytest.mark.parametrize("include_self", [False, True])
+@pytest.mark.parametrize("off_by_one", [False, True])
+def test_score_topk_tensor_core_path(B, nC, D, k, include_self, off_by_one):
+    # shapes with at least 16 row tiles of 128 landmarks (bf16, D a multiple of 64,
+    # k <= 16) take the tensor-core scorer; values in {-1, 0, 1} make many ties
+    g = torch.Generator().manual_seed(B * nC + D)
+    lm = torch.randint(-1, 2, (B, nC, D), generator=g).to(torch.bfloat16)
+    run_score(lm, 64, 1, D, k, off_by_one, include_self)
+
+
+@pytest.mark.parametrize("include_self", [False, True])
+def test_noisy_topk_tensor_core_path(include_self):
+    B, nC, D, k = 16, 256, 128, 8
+    g = torch.Generator().manual_seed(7)
+    lm = torch.randint(-2, 3, (B, nC, D), generator=g).to(torch.bfloat16)
+    u = torch.rand(B, nC, nC, generator=g, dtype=torch.float64).clamp_(1e-12, 1 - 1e-12)
+    noise = (-torch.log(-torch.log(u))).to(torch.float32)
+    idx, r, w = api.score_topk_noisy(lm.cuda(), noise.cuda(), S=64, H=1, d=D, topk=k,
+                                     include_self=include_self)
+    torch.cuda.synchronize()
+    assert api.gca_get_status() == 0
+    oi, orr, ow = oracle.score_topk_noisy(f64(lm), noise.numpy(), k, include_self, False)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oi)
+    assert_close("score", f64(r), orr, 1e-5, 1e-6)
+    assert_close("weight", f64(w), ow, 1e-6, 1e-5)
