@@ -596,38 +596,6 @@ struct EntryInfo {
     int pad;
 };
 
-// The key-major pass for S = 128 (S = 64 uses the entry-pair kernel below): a
-// group is one inverse-index entry and the products are already M = 128.
-template <int S, int DH>
-struct CfgB {
-    static_assert(S == 128, "S = 64 runs gca_bwd_kv_pair_kernel");
-    using G = tcx::HeadGeom<DH>;
-    static constexpr int M = S;                           // keys of the item
-    static constexpr int NG = S;                          // tokens per group
-    static constexpr int NWG = 1;                         // math warpgroups in use
-    static constexpr int NSB = 1;                         // S^T/G^T TMEM buffers
-    // what fits beside the operand pair: stages, K/V item buffers, dK/dV accumulators
-    static constexpr int STAGES = DH == 32 ? 4 : (DH == 64 ? 2 : 1);
-    static constexpr int IBUF = DH == 128 ? 1 : 2;
-    static constexpr int NACC = DH == 128 ? 1 : 2;
-    static constexpr int TILE = G::tile_bytes(S);
-    static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
-    static constexpr int VEC_OFF = 2 * TILE;              // after the Q and dO tiles
-    static constexpr int ENT_OFF = VEC_OFF + 1024;        // lse2/delta rows, then entry info
-    static constexpr int STAGE_BYTES = VEC_OFF + 2048;
-    static constexpr int P_BLOCK = M * 128;
-    static constexpr int P_BYTES = M * NG * 2;            // one operand (dA^T or wP^T)
-    static constexpr int OFF_IT = 0;
-    static constexpr int OFF_ST = IBUF * ITEM_BYTES;
-    static constexpr int OFF_P = OFF_ST + STAGES * STAGE_BYTES;
-    static constexpr int SMEM = OFF_P + NWG * 2 * P_BYTES + 1024;
-    static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t SGW = 2 * S;                // columns of one S^T/G^T buffer
-    static constexpr uint32_t COL_ACC = NSB * SGW;        // dK then dV (DH columns each) per buffer
-    static_assert(COL_ACC + NACC * 2 * DH <= TMEM_COLS, "tensor memory");
-    static_assert(STAGES <= 6, "barrier arrays");
-};
-
 struct __align__(8) BarsB {
     uint64_t info_full[kInfo], info_empty[kInfo];
     uint64_t it_full[2], it_empty[2];
@@ -641,17 +609,64 @@ struct __align__(8) BarsB {
     ItemInfoB info[kInfo];
 };
 
-template <int S, int DH>
-__global__ void __launch_bounds__(kThreads, 1)
-gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+// The key-major pass for S = 128 (S = 64 uses the entry-pair kernel below).
+// Work unit = (inverse-index entry, half of its 128 query tokens).  Per unit
+// S^T = K Q_h^T and G^T = V dO_h^T are M = 128 (keys) x N = 64 (tokens)
+// products into a 128-column TMEM half-buffer (S^T, then G^T).  A math thread
+// owns one key row: it reads its 64 scores and 64 G values in two pieces of 32
+// tokens and writes dA^T (bf16 pairs) over the S^T columns and w P^T over the
+// G^T columns it has already read -- the row of key s is TMEM lane s, exactly
+// the layout of an A operand -- so dK += dA^T Q_h and dV += (w P)^T dO_h read A
+// from tensor memory (K = 64 tokens) and no shared-memory operand buffer
+// exists.  Two math warpgroups take alternate units; dK and dV are issued by
+// two threads, S^T and G^T by one.
+template <int DH>
+struct CfgK {
+    using G = tcx::HeadGeom<DH>;
+    static constexpr int S = 128;
+    static constexpr int TILE = G::tile_bytes(S);         // 128 rows x DH
+    static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
+    static constexpr int IBUF = DH == 128 ? 1 : 2;
+    static constexpr int VEC_OFF = 2 * TILE;              // after the Q and dO tiles
+    static constexpr int ENT_OFF = VEC_OFF + 1024;        // lse2[128], delta[128], then entry info
+    static constexpr int STAGE_BYTES = VEC_OFF + 2048;
+    static constexpr int STAGES = DH == 32 ? 6 : (DH == 64 ? 4 : 2);
+    static constexpr int OFF_IT = 0;
+    static constexpr int OFF_ST = IBUF * ITEM_BYTES;
+    static constexpr int SMEM = OFF_ST + STAGES * STAGE_BYTES + 1024;
+    static constexpr int NHB = DH == 32 ? 3 : 2;          // TMEM half-buffers of 128 columns
+    static constexpr int NACC = DH == 128 ? 1 : 2;        // dK/dV accumulators
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_ACC = NHB * 128;        // dK then dV (DH columns each) per accumulator
+    static_assert(COL_ACC + NACC * 2 * DH <= TMEM_COLS, "tensor memory");
+    static_assert(STAGES <= 6, "barrier arrays");
+};
+
+struct __align__(8) BarsK {
+    uint64_t info_full[kInfo], info_empty[kInfo];
+    uint64_t it_full[2], it_empty[2];
+    uint64_t st_full[6], st_empty[6];
+    uint64_t s_full[3], s_empty[3];    // per TMEM half-buffer
+    uint64_t p_full[4];                // per unit, cycling four (two per warpgroup)
+    uint64_t o_full[2], o_empty[2];    // o_full per storing warpgroup, o_empty per accumulator
+    uint64_t done, done2, done3;
+    uint32_t tmem;
+    int abort;
+    ItemInfoB info[kInfo];
+};
+
+template <int DH>
+__global__ void __launch_bounds__(kThreadsA, 1)
+gca_bwd_kv128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                      const BwdArgs a) {
-    using C = CfgB<S, DH>;
+    using C = CfgK<DH>;
     using HG = tcx::HeadGeom<DH>;
+    constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-    __shared__ BarsB sb;
+    __shared__ BarsK sb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
     const int nE = a.nQ * a.topk;
@@ -659,25 +674,26 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInfo; ++i) {
             mbar_init(&sb.info_full[i], 1);
-            mbar_init(&sb.info_empty[i], 2 + 256);     // two MMA issuers + math threads
+            mbar_init(&sb.info_empty[i], 3 + 256);     // three MMA issuers + math threads
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
             mbar_init(&sb.it_empty[i], 1);
-            mbar_init(&sb.p_full[i], 128);
-            mbar_init(&sb.p_empty[i], 1);
-            mbar_init(&sb.o_full[i], 1);
+            mbar_init(&sb.o_full[i], 2);              // the dK issuer + the dV issuer
             mbar_init(&sb.o_empty[i], 128);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(&sb.p_full[i], 128);
+        for (int i = 0; i < C::NHB; ++i) {
+            mbar_init(&sb.s_full[i], 1);
+            mbar_init(&sb.s_empty[i], 2);             // freed by the dK and dV products
         }
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&sb.st_full[i], 1);
-            mbar_init(&sb.st_empty[i], 1);
+            mbar_init(&sb.st_empty[i], 2);
         }
-        mbar_init(&sb.s_full[0], 1);
-        mbar_init(&sb.s_full[1], 1);
-        for (int i = 0; i < C::NSB; ++i) mbar_init(&sb.s_empty[i], 128);
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
+        mbar_init(&sb.done3, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -697,10 +713,9 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     const uint32_t tmem = sb.tmem;
 
     if (warp == 0) {
-        // The whole warp walks the items; lane 0 alone waits on barriers and
-        // issues the copies.  The other lanes fetch the item offsets and the
-        // entry records (query chunk, slot, weight) 32 at a time, so those
-        // dependent global loads are paid once per 32 instead of once each.
+        // Producer: the whole warp walks the items; lane 0 alone waits on barriers
+        // and issues the copies.  The other lanes fetch the item offsets and the
+        // entry records (entry, weight) 32 at a time.
         constexpr unsigned kAll = 0xffffffffu;
         Ring st{0, 0}, it{0, 0}, inf{0, 0};
         bool st_out[C::STAGES] = {}, it_out[2] = {false, false};
@@ -734,7 +749,6 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             }
             inf.next(kInfo);
             if (ne <= 0) continue;
-            const int* ent = a.entry + (size_t)b * nE + e0;
             if (!lane0_wait(&sb.it_empty[it.i], it.ph ^ 1u)) break;
             if (lane == 0) {
                 uint8_t* ib = sm + C::OFF_IT + it.i * C::ITEM_BYTES;
@@ -754,10 +768,11 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 int my_c = 0, my_j = 0;
                 float my_w = 0.f;
                 if (base + lane < ne) {
-                    const int e = ent[base + lane];
+                    const size_t at = (size_t)b * nE + e0 + base + lane;
+                    const int e = a.entry[at];
                     my_c = e / a.topk;
                     my_j = e % a.topk;
-                    my_w = a.w[((size_t)b * a.nQ + my_c) * a.topk + my_j];
+                    my_w = a.entry_w[at];
                 }
                 const int cnt = min(32, ne - base);
                 for (int u = 0; u < cnt; ++u) {
@@ -778,8 +793,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                         }
                         const size_t rb = ((((size_t)b * a.nQ + c) * a.topk + j) * a.H + h) * S;
                         tcx::bulk_load(stg + C::VEC_OFF, a.lse2_rows + rb, S * 4, &sb.st_full[st.i]);
-                        tcx::bulk_load(stg + C::VEC_OFF + S * 4, a.delta_rows + rb, S * 4,
-                                       &sb.st_full[st.i]);
+                        tcx::bulk_load(stg + C::VEC_OFF + S * 4, a.delta_rows + rb, S * 4, &sb.st_full[st.i]);
                     }
                     st_out[st.i] = true;
                     st_ph[st.i] = st.ph;
@@ -795,12 +809,12 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
-        // S^T / G^T products: S^T = K Q^T and G^T = V dO^T of each group
+        // S^T = K Q_h^T and G^T = V dO_h^T of each unit (M = 128 keys, N = 64 tokens)
         if (lane == 0) {
             Ring st{0, 0}, it{0, 0}, inf{0, 0};
-            int q = 0;
+            int u = 0;                          // units issued
             bool issued = false;
-            const uint32_t id_s = idesc_bf16(C::M, S, false, false);
+            const uint32_t id_s = idesc_bf16(128, 64, false, false);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
@@ -812,37 +826,39 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 const uint32_t kaddr = smem_u32(sm + C::OFF_IT + it.i * C::ITEM_BYTES);
                 const uint32_t vaddr = kaddr + C::TILE;
                 bool ok = true;
-                for (int g = 0; g < ne; ++g) {
-                    const int qq = q + g;
-                    const int sbuf = qq % C::NSB;
-                    if (!wait(&sb.st_full[st.i], st.ph) ||
-                        !wait(&sb.s_empty[sbuf], empty_par(qq / C::NSB))) { ok = false; break; }
-                    tc_fence_after();
+                for (int g = 0; g < ne && ok; ++g) {
+                    if (!wait(&sb.st_full[st.i], st.ph)) { ok = false; break; }
                     const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
                     const uint32_t doaddr = qaddr + C::TILE;
-                    tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW, kaddr, S, qaddr, S, id_s, 0);
-                    tcx::mma_kmajor_dh<DH>(tmem + sbuf * C::SGW + S, vaddr, S, doaddr, S, id_s, 0);
-                    mma_commit(&sb.s_full[qq % C::NWG]);
-                    issued = true;
+                    for (int hf = 0; hf < 2; ++hf, ++u) {
+                        const int hb = u % C::NHB;
+                        if (!wait(&sb.s_empty[hb], empty_par(u / C::NHB))) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t d = tmem + hb * 128;
+                        tcx::mma_kmajor_dh<DH>(d, kaddr, S, qaddr + 64 * hf * HG::ROW_BYTES, S, id_s, 0);
+                        tcx::mma_kmajor_dh<DH>(d + 64, vaddr, S, doaddr + 64 * hf * HG::ROW_BYTES, S, id_s, 0);
+                        mma_commit(&sb.s_full[hb]);
+                        issued = true;
+                    }
                     st.next(C::STAGES);
                 }
                 if (!ok) break;
                 mma_commit(&sb.it_empty[it.i]);     // K and V are read only by these products
                 it.next(C::IBUF);
-                q += ne;
             }
             if (issued) {
                 mma_commit(&sb.done);
                 mbar_wait(&sb.done, 0, nullptr, 100000000ull);
             }
         }
-    } else if (warp == 2) {
-        // accumulation products: dK += dA^T Q and dV += (w P)^T dO of each group
+    } else if (warp == 2 || warp == 11) {
+        // warp 2: dK += dA^T Q_h, warp 11: dV += (w P)^T dO_h, A from TMEM (K = 64 tokens)
+        const bool dvi = warp == 11;
         if (lane == 0) {
             Ring st{0, 0}, inf{0, 0};
-            int q = 0, e = 0;
+            int u = 0, e = 0;
             bool issued = false;
-            const uint32_t id_acc = idesc_bf16(C::M, HG::SUB_COLS, false, true);
+            const uint32_t id_acc = idesc_bf16(128, HG::SUB_COLS, false, true);
             for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
@@ -852,43 +868,43 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
                 const int ob = e % C::NACC;
                 if (!wait(&sb.o_empty[ob], empty_par(e / C::NACC))) break;
                 tc_fence_after();
-                const uint32_t d_dk = tmem + C::COL_ACC + ob * 2 * DH;
-                const uint32_t d_dv = d_dk + DH;
+                const uint32_t d_acc = tmem + C::COL_ACC + ob * 2 * DH + (dvi ? DH : 0);
                 bool ok = true;
-                for (int g = 0; g < ne; ++g) {
-                    const int qq = q + g, pbuf = qq % C::NWG;
-                    if (!wait(&sb.p_full[pbuf], full_par(qq / C::NWG))) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pbuf * 2 * C::P_BYTES);
-                    const uint32_t qaddr = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
-                    const uint32_t doaddr = qaddr + C::TILE;
-                    tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dk, paddr, C::P_BLOCK, qaddr, S, id_acc, g > 0);
-                    tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dv, paddr + C::P_BYTES, C::P_BLOCK, doaddr, S,
-                                                      id_acc, g > 0);
-                    // the S^T / G^T products of this group are complete (their P exists)
+                for (int g = 0; g < ne && ok; ++g) {
+                    const uint32_t stg = smem_u32(sm + C::OFF_ST + st.i * C::STAGE_BYTES);
+                    const uint32_t xaddr = stg + (dvi ? C::TILE : 0);    // Q (dK) or dO (dV)
+                    for (int hf = 0; hf < 2; ++hf, ++u) {
+                        const int hb = u % C::NHB;
+                        if (!wait(&sb.p_full[u & 3], full_par(u >> 2))) { ok = false; break; }
+                        tc_fence_after();
+                        tcx::mma_ts_mn_dh<DH, 4>(d_acc, tmem + hb * 128 + (dvi ? 64 : 0),
+                                                 xaddr + 64 * hf * HG::ROW_BYTES, S, id_acc,
+                                                 (g > 0 || hf > 0) ? 1u : 0u);
+                        mma_commit(&sb.s_empty[hb]);
+                        issued = true;
+                    }
+                    if (!ok) break;
                     mma_commit(&sb.st_empty[st.i]);
-                    mma_commit(&sb.p_empty[pbuf]);
-                    issued = true;
                     st.next(C::STAGES);
                 }
                 if (!ok) break;
-                mma_commit(&sb.o_full[ob]);
-                q += ne;
+                // the full barrier belongs to the warpgroup that stores this item
+                mma_commit(&sb.o_full[e & 1]);
                 ++e;
             }
             if (issued) {
-                mma_commit(&sb.done2);
-                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+                uint64_t* dn = dvi ? &sb.done3 : &sb.done2;
+                mma_commit(dn);
+                mbar_wait(dn, 0, nullptr, 100000000ull);
             }
         }
-    } else {
+    } else if (warp < 11) {
         const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
-        const int row = 32 * qd + lane;
-        const int u = 0;
+        const int row = 32 * qd + lane;             // key row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
         Ring inf{0, 0}, st{0, 0};
-        int q = 0, e = 0, n_all = 0, kg = 0;
+        int u = 0, e = 0, n_all = 0;
         for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_all) {
             if (!wait(&sb.info_full[inf.i], inf.ph)) break;
             const ItemInfoB I = sb.info[inf.i];
@@ -898,85 +914,73 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
             __nv_bfloat16* dkrow = a.dk + (krow * a.H + I.h) * DH;
             __nv_bfloat16* dvrow = a.dv + (krow * a.H + I.h) * DH;
             if (I.ne <= 0) {
-                if ((n_all % C::NWG) == wg) {
-                    tcx::zero_acc_row<S, DH>(dkrow, u);
-                    tcx::zero_acc_row<S, DH>(dvrow, u);
+                if ((n_all & 1) == wg) {
+                    tcx::zero_acc_row<128, DH>(dkrow, 0);
+                    tcx::zero_acc_row<128, DH>(dvrow, 0);
                 }
                 continue;
             }
             bool ok = true;
-            for (int g = 0; g < I.ne; ++g) {
-                const int qq = q + g;
+            for (int g = 0; g < I.ne && ok; ++g) {
                 const int stage = st.i;
                 const uint32_t stph = st.ph;
                 st.next(C::STAGES);
-                if ((qq % C::NWG) != wg) continue;
-                const int sbuf = qq % C::NSB;
-                // our own s_full first: its completion implies this group's stage copy
-                // has landed, so the stage barrier's phase below is unambiguous
-                if (!wait(&sb.s_full[wg], full_par(kg)) || !wait(&sb.st_full[stage], stph)) { ok = false; break; }
-                tc_fence_after();
-                const uint8_t* stg = sm + C::OFF_ST + stage * C::STAGE_BYTES;
-                const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[0];
-                const float wv = ei.w;
-                const float wsc = wv * a.attn_scale;
-                const float* vec = reinterpret_cast<const float*>(stg + C::VEC_OFF);   // lse2[S], delta[S]
-                uint8_t* pb = sm + C::OFF_P + wg * 2 * C::P_BYTES;
-                const uint32_t ts0 = tmem + lane_base + sbuf * C::SGW;
-                const uint32_t tg0 = ts0 + S;
-                if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
-                // this thread: one key row, all 128 tokens in four 32-token pieces
-                for (int pc = 0; pc < 4; ++pc) {
-                    float xs[32], xg[32];
-                    {
+                for (int hf = 0; hf < 2; ++hf, ++u) {
+                    if ((u & 1) != wg) continue;
+                    const int hb = u % C::NHB;
+                    // own s_full first: its completion implies this entry's stage has
+                    // landed, so the stage barrier's phase below is unambiguous
+                    if (!wait(&sb.s_full[hb], full_par(u / C::NHB)) || !wait(&sb.st_full[stage], stph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint8_t* stg = sm + C::OFF_ST + stage * C::STAGE_BYTES;
+                    const EntryInfo ei = reinterpret_cast<const EntryInfo*>(stg + C::ENT_OFF)[0];
+                    const float wv = ei.w, wsc = wv * a.attn_scale;
+                    const float* vec = reinterpret_cast<const float*>(stg + C::VEC_OFF) + 64 * hf;
+                    const uint32_t tb = tmem + lane_base + hb * 128;
+#pragma unroll
+                    for (int pc = 0; pc < 2; ++pc) {
+                        // tokens 64 hf + 32 pc .. + 31 of this key row
                         uint32_t r0[16], r1[16], r2[16], r3[16];
-                        issue_cols16<S>(ts0 + 32 * pc, r0);
-                        issue_cols16<S>(ts0 + 32 * pc + 16, r1);
-                        issue_cols16<S>(tg0 + 32 * pc, r2);
-                        issue_cols16<S>(tg0 + 32 * pc + 16, r3);
+                        tmem_ld_32x32b_x16(tb + 32 * pc, r0);
+                        tmem_ld_32x32b_x16(tb + 32 * pc + 16, r1);
+                        tmem_ld_32x32b_x16(tb + 64 + 32 * pc, r2);
+                        tmem_ld_32x32b_x16(tb + 64 + 32 * pc + 16, r3);
                         tmem_wait_ld();
+                        uint32_t pa[16], pp[16];
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            xs[t] = __uint_as_float(r0[t]);
-                            xs[16 + t] = __uint_as_float(r1[t]);
-                            xg[t] = __uint_as_float(r2[t]);
-                            xg[16 + t] = __uint_as_float(r3[t]);
+                        for (int p2 = 0; p2 < 16; ++p2) {
+                            const uint32_t* rs = p2 < 8 ? r0 : r1;
+                            const uint32_t* rg = p2 < 8 ? r2 : r3;
+                            const int tt = 2 * (p2 & 7);
+                            const int t0 = 32 * pc + 2 * p2;
+                            const float pr0 = fast_exp2(fmaf(__uint_as_float(rs[tt]), a.scale_log2, -vec[t0]));
+                            const float pr1 = fast_exp2(fmaf(__uint_as_float(rs[tt + 1]), a.scale_log2, -vec[t0 + 1]));
+                            pa[p2] = tcx::pack_bf16(pr0 * (__uint_as_float(rg[tt]) - vec[128 + t0]) * wsc,
+                                                    pr1 * (__uint_as_float(rg[tt + 1]) - vec[128 + t0 + 1]) * wsc);
+                            pp[p2] = tcx::pack_bf16(pr0 * wv, pr1 * wv);
                         }
+                        // dA^T over S^T columns 16 pc .., w P^T over G^T columns 16 pc .. (both read)
+                        tmem_st_32x32b_x16(tb + 16 * pc, pa);
+                        tmem_st_32x32b_x16(tb + 64 + 16 * pc, pp);
                     }
-                    if (pc == 3) {
-                        tc_fence_before();
-                        mbar_arrive(&sb.s_empty[sbuf]);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * pc + i;
-                        const float pr = fast_exp2(fmaf(xs[i], a.scale_log2, -vec[t]));
-                        xs[i] = pr * (xg[i] - vec[S + t]);
-                        xg[i] = pr;
-                    }
-                    const int blk = pc >> 1;
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint32_t off = blk * C::P_BLOCK + sw128_off(row, (pc & 1) * 4 + c4);
-                        *reinterpret_cast<uint4*>(pb + off) = pack8(xs + 8 * c4, wsc);
-                        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = pack8(xg + 8 * c4, wv);
-                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&sb.p_full[u & 3]);
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(&sb.p_full[wg]);
-                ++kg;
             }
             if (!ok) break;
-            q += I.ne;
-            const bool mine = (e % C::NWG) == wg;
-            const int ob = e % C::NACC, ko = e / C::NACC;
+            const bool mine = (e & 1) == wg;
+            const int ob = e % C::NACC, ko = e >> 1;
             ++e;
             if (!mine) continue;
-            if (!wait(&sb.o_full[ob], full_par(ko))) break;
+            if (!wait(&sb.o_full[wg], full_par(ko))) break;
             tc_fence_after();
             const uint32_t acc = tmem + lane_base + C::COL_ACC + ob * 2 * DH;
-            tcx::store_acc_row<S, DH>(acc, dkrow, u);
-            tcx::store_acc_row<S, DH>(acc + DH, dvrow, u);
+            tcx::store_acc_row<128, DH>(acc, dkrow, 0);
+            tcx::store_acc_row<128, DH>(acc + DH, dvrow, 0);
             tc_fence_before();
             mbar_arrive(&sb.o_empty[ob]);
         }
@@ -986,7 +990,7 @@ gca_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, CfgB<S, DH>::TMEM_COLS);
+        tmem_dealloc(tmem, CfgK<DH>::TMEM_COLS);
     }
 }
 
@@ -1447,7 +1451,7 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
                          void* dq, void* dk, void* dv, void* ws, int* status, cudaStream_t st) {
     static_assert(CfgA<S, DH>::SMEM + sizeof(BarsA) <= kSmemMax, "shared memory (query-major pass)");
     if constexpr (S == 64) static_assert(CfgP<DH>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
-    else static_assert(CfgB<S, DH>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (key-major pass)");
+    else static_assert(CfgK<DH>::SMEM + sizeof(BarsK) <= kSmemMax, "shared memory (key-major pass)");
     CUtensorMap tq, tdo, tk, tv;
     const uint64_t cols = (uint64_t)sp.H * DH;
     constexpr uint32_t bc = tcx::HeadGeom<DH>::SUB_COLS;
@@ -1501,10 +1505,10 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
         if (e != cudaSuccess) return e;
         GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, CfgP<DH>::SMEM, st>>>(tq, tdo, tk, tv, a));
     } else {
-        auto kb = gca_bwd_kv_tc_kernel<S, DH>;
-        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgB<S, DH>::SMEM);
+        auto kb = gca_bwd_kv128_kernel<DH>;
+        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgK<DH>::SMEM);
         if (e != cudaSuccess) return e;
-        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreads, CfgB<S, DH>::SMEM, st>>>(tq, tdo, tk, tv, a));
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, CfgK<DH>::SMEM, st>>>(tq, tdo, tk, tv, a));
     }
     return cudaGetLastError();
 }
