@@ -634,8 +634,8 @@ struct CfgK {
     static constexpr int OFF_IT = 0;
     static constexpr int OFF_ST = IBUF * ITEM_BYTES;
     static constexpr int SMEM = OFF_ST + STAGES * STAGE_BYTES + 1024;
-    static constexpr int NHB = DH == 32 ? 3 : 2;          // TMEM half-buffers of 128 columns
-    static constexpr int NACC = DH == 128 ? 1 : 2;        // dK/dV accumulators
+    static constexpr int NHB = DH == 128 ? 2 : 3;         // TMEM half-buffers of 128 columns
+    static constexpr int NACC = DH == 32 ? 2 : 1;         // dK/dV accumulators
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_ACC = NHB * 128;        // dK then dV (DH columns each) per accumulator
     static_assert(COL_ACC + NACC * 2 * DH <= TMEM_COLS, "tensor memory");
