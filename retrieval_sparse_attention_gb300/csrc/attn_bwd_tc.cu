@@ -1013,8 +1013,8 @@ struct CfgP {
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
     // what fits: d = 128 keeps one K/V item buffer and one operand pair shared
     // by both math warpgroups, and a single dK/dV accumulator in TMEM
-    static constexpr int STAGES = DH == 32 ? 4 : (DH == 64 ? 3 : 2);
-    static constexpr int IBUF = DH == 128 ? 1 : 2;
+    static constexpr int STAGES = DH == 32 ? 4 : (DH == 64 ? 4 : 2);
+    static constexpr int IBUF = DH == 32 ? 2 : 1;
     static constexpr bool SHARED_P = DH == 128;
     static constexpr int NACC = DH == 128 ? 1 : 2;
     // Q of entries 0 and 1: sub-tile s holds rows 0-63 (entry 0) then 64-127
