@@ -69,9 +69,10 @@ struct Cfg {
     // S = 128 keeps P in tensor memory over its own S row (the softmax thread
     // owns TMEM lane = row, which is the A operand layout of P V), so it needs
     // no shared-memory P buffers; an S buffer is then held until its P V
-    // products complete, and three of them rotate (two at d = 128).
+    // products complete.  Three S buffers rotate (two at d = 128, where the O
+    // buffers take 256 columns).
     static constexpr bool TP = (S == 128);
-    static constexpr int NSB = TP ? (DH == 128 ? 2 : 3) : 2;
+    static constexpr int NSB = DH == 128 ? 2 : 3;
     // K/V ring depth: what fits beside Q (and the P buffers when S = 64)
     static constexpr int STAGES = TP ? (DH == 32 ? 6 : (DH == 64 ? 5 : 2)) : (DH == 128 ? 2 : 4);
     static constexpr int QBUF = 2;
