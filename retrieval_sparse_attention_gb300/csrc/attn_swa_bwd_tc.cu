@@ -6,24 +6,38 @@
 // With p_ts = exp(attn_scale q_t . k_s - lse_t) over the window of t,
 // delta_t = dO_t . O_t, dp_ts = dO_t . v_s and ds_ts = attn_scale p_ts (dp_ts - delta_t):
 //   dQ_t = sum_s ds_ts k_s,   dK_s = sum_t ds_ts q_t,   dV_s = sum_t p_ts dO_t.
-// Three launches, no atomics (every output row is written by one CTA):
-//   swa_delta    delta and lse * log2(e) per (token, head), stored as [B, H, Lp]
-//                rows so that 64 consecutive tokens are one bulk copy.
-//   pass A       query-major, item = (batch row, 128-token query tile, head):
-//                for each 64-key tile S = Q K^T and dP = dO V^T (M = 128,
-//                N = 64) into the warpgroup's TMEM buffer, ds in registers,
-//                dQ += dS K accumulated in TMEM.
-//   pass B       key-major, item = (batch row, 128-key tile, head): for each
-//                64-query tile S^T = K Q^T and dP^T = V dO^T, then
-//                dV += P^T dO and dK += dS^T Q accumulated in TMEM.
-// Warp roles as in the forward: warp 0 producer (lane 0 and lane 1 feed two
-// rings), warp 1 score-product issuer and TMEM owner, warp 2 accumulation
-// issuer, warps 3-10 two math warpgroups owning alternate items; producer and
-// issuers walk the two current items' tiles interleaved.  Outputs are staged
-// in the warpgroup's idle operand buffer and written with TMA tensor stores
-// (3-D maps over [B, L, H*d]: rows past a sequence end are read as zeros and
-// never written).  Every mbarrier wait is bounded.
+// Two launches, no atomics (every output row is written by one CTA):
+//   pass A  query-major, item = (batch row, 128-token query tile, head).  The
+//           item's Q, dO and O tiles land once; each math thread forms delta_t
+//           of its token row from the dO and O rows in shared memory, and the
+//           item's storing warpgroup writes -lse_t log2(e) and -attn_scale
+//           delta_t as [B, H, Lp] rows for pass B.  Unit = one 64-key tile:
+//           S = Q K^T and dP = dO V^T (M = 128 tokens, N = 64 keys) into a
+//           128-column TMEM buffer.  A math thread owns token row t, which is
+//           TMEM lane t -- the layout of an A operand -- so it writes ds (bf16
+//           pairs) over the S columns it has read and dQ += dS K reads A from
+//           tensor memory.
+//   pass B  key-major, item = (batch row, 128-key tile, head).  Unit = 64
+//           queries, half of a 128-query stage that also carries those queries'
+//           two pass-A rows: S^T = K Q^T and dP^T = V dO^T (M = 128 keys); a math
+//           thread owns key row s, writes dS^T over S^T and P^T over dP^T, and
+//           dK += dS^T Q, dV += P^T dO read A from tensor memory (two issuing
+//           threads).
+// In both passes the two math warpgroups take alternate units of the same
+// item, three TMEM buffers rotate, the accumulation products release a buffer
+// when they have read it, and no shared-memory operand buffer exists.
+// A CTA walks a contiguous run of items, tile index fastest, so consecutive
+// items of a (batch row, head) strip share most of their units' tiles (K/V
+// tiles in pass A, Q/dO stages in pass B): a shared tile stays in its ring
+// slot and only the new ones are loaded (2 of 10 K/V tiles, 1 of 5 stages at
+// W = 512).  Slots are filled and released in load order; the host checks for
+// the window at hand that no item waits for a slot a later item still holds,
+// and otherwise every item loads all its tiles.  Tensor maps are 3-D over
+// [B, L, H*d], so rows past a sequence end read as zeros; output rows past it
+// are never written.  Every mbarrier wait is bounded.
 #include <math.h>
+
+#include <vector>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -39,165 +53,178 @@ using tcx::fast_exp2;
 using tcx::kLog2e;
 using tcx::Ring;
 
-constexpr int kThreads = 352;
 constexpr int BM = 128;                  // item rows = MMA M
-constexpr int BT = 64;                   // inner tile = MMA N of the score products
-constexpr int STAGES = 4;
+constexpr int BT = 64;                   // unit width = MMA N of the score products
 constexpr int TILE128 = 128 * 128;       // 128 rows x 64 bf16
 constexpr int TILE64 = 64 * 128;         // 64 rows x 64 bf16
-constexpr int OPB = BM * 128;            // one operand buffer: 128 rows x 64 bf16
+// Tensor memory: an X ring of 64-column slots holds a unit's S (S^T) and then
+// the bf16 operands the math writes over it, until the accumulation products
+// have read them; a Y ring holds its dP (dP^T) and is free as soon as the math
+// has read it; the accumulators follow.
+constexpr int NX = 4;
+constexpr int NY = 2;
+constexpr uint32_t COL_X = 0;
+constexpr uint32_t COL_Y = NX * 64;
+constexpr uint32_t COL_ACC = COL_Y + NY * 64;
 constexpr uint32_t TMEM_COLS = 512;
+static_assert(COL_ACC + 128 <= TMEM_COLS, "tensor memory");
+constexpr int kSmemMax = 232448;
 
 struct SwaBwdArgs {
-    const float* lse2T;      // [B, H, Lp]: lse * log2(e)
-    const float* deltaT;     // [B, H, Lp]
+    const float* lse;        // [B, L, H] (forward output)
+    float* nlse2T;           // [B, H, Lp]: -lse * log2(e)       (written by pass A)
+    float* ndscT;            // [B, H, Lp]: -attn_scale * delta  (written by pass A)
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
     int* status;
     int B, L, H, W, Lp;
-    int nQT, nKT, nQ64;      // 128-token query tiles, 128-key tiles, 64-token query tiles per row
+    int nQT, nKT;            // 128-token query tiles, 128-key tiles per row
     float scale_log2;        // attn_scale * log2(e)
     float scale;             // attn_scale
     int n_items;
+    int chunk;               // items per CTA (a contiguous run)
+    int slide;               // keep shared tiles of consecutive items resident
+};
+
+// Ring bookkeeping shared by the producer and the consumers of a ring whose
+// entries are the tiles of items (k0 .. k1 per item, increasing within a strip).
+// Ring position of a tile = the order in which it was loaded; slot = position
+// % NSLOT.  begin() returns the first tile of the item that must be loaded:
+// k0, or the one after the last tile of the previous item when that item kept
+// its tiles k0 .. for this one.
+struct Slide {
+    int strip, klast, nload;
+    __device__ __forceinline__ int begin(bool kept, int strip_, int k0, int k1) {
+        const int from = (kept && strip_ == strip && k0 <= klast + 1) ? klast + 1 : k0;
+        nload += k1 - from + 1;
+        klast = k1;
+        strip = strip_;
+        return from;
+    }
+    __device__ __forceinline__ int pos(int k1, int k) const { return nload - 1 - (k1 - k); }
 };
 
 __device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
 __device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
 
-// ---------------------------------------------------------------- delta
-__global__ void swa_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                 const __nv_bfloat16* __restrict__ dout,
-                                 const float* __restrict__ lse, int B, int L, int H, int Lp,
-                                 float* __restrict__ lse2T, float* __restrict__ deltaT) {
-    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const size_t total = (size_t)B * H * Lp;
-    if (idx >= total) return;
-    const int t = (int)(idx % Lp);
-    const size_t bh = idx / Lp;
-    const int h = (int)(bh % H), b = (int)(bh / H);
-    float dl = 0.f, l2 = 0.f;
-    if (t < L) {
-        const size_t row = ((size_t)b * L + t) * H + h;
-        const uint4* po = reinterpret_cast<const uint4*>(o + row * 64);
-        const uint4* pg = reinterpret_cast<const uint4*>(dout + row * 64);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const uint4 a = __ldg(po + v), g = __ldg(pg + v);
-            const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&g);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 fa = __bfloat1622float2(ha[u]), fg = __bfloat1622float2(hg[u]);
-                acc[2 * u] = fmaf(fa.x, fg.x, acc[2 * u]);
-                acc[2 * u + 1] = fmaf(fa.y, fg.y, acc[2 * u + 1]);
-            }
-        }
-        dl = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-        l2 = lse[row] * kLog2e;
-    }
-    deltaT[idx] = dl;
-    lse2T[idx] = l2;
+// A global load issued where it stands: the compiler may not sink it to the
+// value's first use (an item later), so its latency overlaps a whole item.
+__device__ __forceinline__ float ld_early(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
 }
 
-// Row of `x` (64 fp32 values of one thread) -> bf16 into a swizzled 128-row x
-// 64-column operand tile (row r at r * 128 bytes, 16-byte chunk c at c ^ (r & 7)).
-__device__ __forceinline__ void put_row64(uint8_t* buf, int row, const uint32_t (&pk)[32]) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(buf + row * 128 + ((c ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-}
-
-// 64 TMEM columns of this thread's lane -> fp32 registers.
-__device__ __forceinline__ void load64(uint32_t taddr, float (&x)[64]) {
+// 64 fp32 accumulator columns of this thread's lane -> 32 bf16 pairs (the TMEM
+// reads are warp-collective).
+__device__ __forceinline__ void load_row64(uint32_t taddr, uint32_t (&pk)[32]) {
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
         uint32_t r[16];
         tmem_ld_32x32b_x16(taddr + 16 * ci, r);
+        tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[u]);
+        for (int u = 0; u < 8; ++u)
+            pk[8 * ci + u] = tcx::pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
     }
 }
+__device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const uint32_t (&pk)[32]) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) d4[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
 
-// ============================================================================ pass A (dQ)
+// ============================================================================ pass A (dQ, delta)
 namespace pa {
-constexpr int OFF_QD = 0;                        // per warpgroup: Q tile, dO tile
-constexpr int OFF_K = 2 * 2 * TILE128;
-constexpr int OFF_V = OFF_K + STAGES * TILE64;
-constexpr int OFF_DS = OFF_V + STAGES * TILE64;  // per warpgroup: dS operand (and dQ staging)
-constexpr int SMEM = OFF_DS + 2 * OPB + 1024;
-constexpr uint32_t COL_S = 0;                    // warpgroup w: S at w*128, dP at w*128 + 64
-constexpr uint32_t COL_DQ = 256;                 // warpgroup w: dQ at 256 + w*64
+constexpr int kThreads = 384;                    // producer, S, dQ and dP issuers, 8 math warps
+constexpr int IBUF = 2;
+constexpr int ITEM = 3 * TILE128;                // Q, dO, O
+constexpr int NSLOT = 8;                         // K/V tile slots
+constexpr int SLOT = 2 * TILE64;                 // K, V
+constexpr int OFF_IT = 0;
+constexpr int OFF_KV = IBUF * ITEM;
+constexpr int SMEM = OFF_KV + NSLOT * SLOT + 1024;
 
 struct Item {
-    int b, qt, h, k0, nt;    // key tiles of 64: k0 .. k0 + nt - 1
+    int b, qt, h, strip, k0, k1;     // 64-key tiles k0 .. k1
 };
+// item = (b * H + h) * nQT + qt
 __device__ __forceinline__ Item decode(const SwaBwdArgs& a, int item) {
     Item it;
-    it.h = item % a.H;
-    const int bq = item / a.H;
-    it.qt = bq % a.nQT;
-    it.b = bq / a.nQT;
+    it.qt = item % a.nQT;
+    it.strip = item / a.nQT;
+    it.h = it.strip % a.H;
+    it.b = it.strip / a.H;
     int lo = it.qt * BM - a.W + 1;
     if (lo < 0) lo = 0;
     it.k0 = lo / BT;
-    it.nt = (it.qt * BM + BM - 1) / BT - it.k0 + 1;
+    it.k1 = (it.qt * BM + BM - 1) / BT;
     return it;
+}
+// Does this item keep its tiles k >= next.k0 resident for the next item of the run?
+__device__ __forceinline__ bool keeps(const SwaBwdArgs& a, const Item& I, int item, int c1, Item& nx) {
+    if (!a.slide || item + 1 >= c1) return false;
+    nx = decode(a, item + 1);
+    return nx.strip == I.strip;
 }
 
 struct __align__(8) Bars {
-    uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t ds_full[2], ds_empty[2];
-    uint64_t o_full[2], o_empty[2];
-    uint64_t epi_full[2], epi_free[2];
-    uint64_t done, done2;
+    uint64_t it_full[IBUF], it_empty[IBUF];
+    uint64_t kv_full[NSLOT], kv_empty[NSLOT];
+    uint64_t x_full[NX], x_empty[NX], y_empty[NY];
+    uint64_t p_full[4];                  // per unit, cycling four (two per warpgroup)
+    uint64_t o_full[2], o_empty[2];      // per dQ accumulator = per storing warpgroup
+    uint64_t done, done2, done3;
     uint32_t tmem;
     int abort;
 };
+static_assert(SMEM + sizeof(Bars) <= kSmemMax, "shared memory (pass A)");
 
 __global__ void __launch_bounds__(kThreads, 1)
 swa_bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                 const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                 const __grid_constant__ CUtensorMap tdq, const SwaBwdArgs a) {
+                 const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tk,
+                 const __grid_constant__ CUtensorMap tv, const SwaBwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
     __shared__ Bars sb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
-    const int stride = gridDim.x;
+    const int c0 = static_cast<int>((long long)blockIdx.x * a.n_items / gridDim.x);
+    const int c1 = static_cast<int>((long long)(blockIdx.x + 1) * a.n_items / gridDim.x);
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < IBUF; ++i) {
+            mbar_init(&sb.it_full[i], 1);
+            mbar_init(&sb.it_empty[i], 2 + 256);      // the S and dP issuers + every math thread
+        }
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(&sb.kv_full[i], 1);
+            mbar_init(&sb.kv_empty[i], 1);
+        }
+        for (int i = 0; i < NX; ++i) {
+            mbar_init(&sb.x_full[i], 2);              // the S and the dP products
+            mbar_init(&sb.x_empty[i], 1);
+        }
+        for (int i = 0; i < NY; ++i) mbar_init(&sb.y_empty[i], 128);
+        for (int i = 0; i < 4; ++i) mbar_init(&sb.p_full[i], 128);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sb.q_full[i], 1);
-            mbar_init(&sb.q_empty[i], 1);
-            mbar_init(&sb.s_full[i], 1);
-            mbar_init(&sb.s_empty[i], 128);
-            mbar_init(&sb.ds_full[i], 128);
-            mbar_init(&sb.ds_empty[i], 1);
             mbar_init(&sb.o_full[i], 1);
             mbar_init(&sb.o_empty[i], 128);
-            mbar_init(&sb.epi_full[i], 128);
-            mbar_init(&sb.epi_free[i], 1);
-        }
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&sb.k_full[i], 1);
-            mbar_init(&sb.k_empty[i], 1);
-            mbar_init(&sb.v_full[i], 1);
-            mbar_init(&sb.v_empty[i], 1);
         }
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
+        mbar_init(&sb.done3, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tq);
         prefetch_tmap(&tdo);
+        prefetch_tmap(&to);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
-        prefetch_tmap(&tdq);
     }
     if (warp == 1) {
         tmem_alloc(&sb.tmem, TMEM_COLS);
@@ -210,245 +237,274 @@ swa_bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // lane 0: Q / dO tiles and the K ring; lane 1: the V ring
-        if (lane < 2) {
-            const bool kl = lane == 0;
-            Ring rg{0, 0};
-            int kq[2] = {0, 0};
-            bool out[STAGES] = {}, q_out[2] = {false, false};
-            uint32_t ph[STAGES] = {}, q_ph[2] = {0, 0};
-            uint64_t* full = kl ? sb.k_full : sb.v_full;
-            uint64_t* empty = kl ? sb.k_empty : sb.v_empty;
-            const CUtensorMap* map = kl ? &tk : &tv;
-            uint8_t* ring = sm + (kl ? OFF_K : OFF_V);
-            bool ok = true;
-            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-                Item it[2];
-                int n[2];
-                for (int w = 0; w < 2; ++w) {
-                    const int e = e0 + w * stride;
-                    n[w] = 0;
-                    if (e < a.n_items) { it[w] = decode(a, e); n[w] = it[w].nt; }
-                }
-                if (kl)
-                    for (int w = 0; w < 2 && ok; ++w) {
-                        if (n[w] == 0) continue;
-                        if (!wait(&sb.q_empty[w], empty_par(kq[w]))) { ok = false; break; }
-                        uint8_t* qb = sm + OFF_QD + w * 2 * TILE128;
-                        mbar_arrive_expect_tx(&sb.q_full[w], 2 * TILE128);
-                        tma_load_3d(qb, &tq, &sb.q_full[w], it[w].h * 64, it[w].qt * BM, it[w].b);
-                        tma_load_3d(qb + TILE128, &tdo, &sb.q_full[w], it[w].h * 64, it[w].qt * BM, it[w].b);
-                        q_out[w] = true;
-                        q_ph[w] = full_par(kq[w]);
-                        ++kq[w];
-                    }
-                const int nmax = n[0] > n[1] ? n[0] : n[1];
-                for (int j = 0; j < nmax && ok; ++j)
-                    for (int w = 0; w < 2; ++w) {
-                        if (j >= n[w]) continue;
-                        if (!wait(&empty[rg.i], rg.ph ^ 1u)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&full[rg.i], TILE64);
-                        tma_load_3d(ring + rg.i * TILE64, map, &full[rg.i], it[w].h * 64,
-                                    (it[w].k0 + j) * BT, it[w].b);
-                        out[rg.i] = true;
-                        ph[rg.i] = rg.ph;
-                        rg.next(STAGES);
-                    }
-            }
-            for (int i = 0; i < STAGES; ++i)
-                if (out[i]) mbar_wait(&full[i], ph[i], nullptr, 100000000ull);
-            for (int i = 0; i < 2; ++i)
-                if (q_out[i]) mbar_wait(&sb.q_full[i], q_ph[i], nullptr, 100000000ull);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ S / dP issuer
         if (lane == 0) {
-            Ring rg{0, 0};
-            int kq[2] = {0, 0}, ts[2] = {0, 0};
+            Ring it{0, 0};
+            Slide sl{-1, -1, 0};
+            bool kept = false;
+            bool kv_out[NSLOT] = {}, it_out[IBUF] = {};
+            uint32_t kv_ph[NSLOT] = {}, it_ph[IBUF] = {};
+            bool ok = true;
+            // Q, dO and O of an item: issued one item ahead, before the item's new K/V
+            // tiles (whose slots the item's own first units free)
+            auto load_item = [&](int item) {
+                const Item J = decode(a, item);
+                if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) return false;
+                uint8_t* ib = sm + OFF_IT + it.i * ITEM;
+                mbar_arrive_expect_tx(&sb.it_full[it.i], 3 * TILE128);
+                tma_load_3d(ib, &tq, &sb.it_full[it.i], J.h * 64, J.qt * BM, J.b);
+                tma_load_3d(ib + TILE128, &tdo, &sb.it_full[it.i], J.h * 64, J.qt * BM, J.b);
+                tma_load_3d(ib + 2 * TILE128, &to, &sb.it_full[it.i], J.h * 64, J.qt * BM, J.b);
+                it_out[it.i] = true;
+                it_ph[it.i] = it.ph;
+                it.next(IBUF);
+                return true;
+            };
+            if (c0 < c1) ok = load_item(c0);
+            for (int item = c0; item < c1 && ok; ++item) {
+                const Item I = decode(a, item);
+                Item nx;
+                const bool keep = keeps(a, I, item, c1, nx);
+                if (item + 1 < c1 && !load_item(item + 1)) break;
+                const int from = sl.begin(kept, I.strip, I.k0, I.k1);
+                for (int k = from; k <= I.k1; ++k) {
+                    const int p = sl.pos(I.k1, k), slot = p % NSLOT;
+                    const uint32_t ph = static_cast<uint32_t>(p / NSLOT) & 1u;
+                    if (!wait(&sb.kv_empty[slot], ph ^ 1u)) { ok = false; break; }
+                    uint8_t* kv = sm + OFF_KV + slot * SLOT;
+                    mbar_arrive_expect_tx(&sb.kv_full[slot], 2 * TILE64);
+                    tma_load_3d(kv, &tk, &sb.kv_full[slot], I.h * 64, k * BT, I.b);
+                    tma_load_3d(kv + TILE64, &tv, &sb.kv_full[slot], I.h * 64, k * BT, I.b);
+                    kv_out[slot] = true;
+                    kv_ph[slot] = ph;
+                }
+                kept = keep;
+            }
+            for (int i = 0; i < NSLOT; ++i)
+                if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < IBUF; ++i)
+                if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
+        }
+    } else if (warp == 1 || warp == 11) {
+        // ------------------------------------------------------------ warp 1: S = Q K^T, warp 11: dP = dO V^T
+        // (two issuing threads: one thread issues at most one MMA per ~46 cycles)
+        const bool dpi = warp == 11;
+        if (lane == 0) {
+            Ring it{0, 0};
+            Slide sl{-1, -1, 0};
+            bool kept = false;
+            int u = 0;
             bool issued = false, ok = true;
             const uint32_t id_s = idesc_bf16(BM, BT, false, false);
-            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-                int n[2];
-                for (int w = 0; w < 2; ++w) {
-                    const int e = e0 + w * stride;
-                    n[w] = e < a.n_items ? decode(a, e).nt : 0;
-                }
-                const int nmax = n[0] > n[1] ? n[0] : n[1];
-                for (int j = 0; j < nmax && ok; ++j)
-                    for (int w = 0; w < 2; ++w) {
-                        if (j >= n[w]) continue;
-                        if ((j == 0 && !wait(&sb.q_full[w], full_par(kq[w]))) ||
-                            !wait(&sb.k_full[rg.i], rg.ph) || !wait(&sb.v_full[rg.i], rg.ph) ||
-                            !wait(&sb.s_empty[w], empty_par(ts[w]))) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t qaddr = smem_u32(sm + OFF_QD + w * 2 * TILE128);
-                        const uint32_t kaddr = smem_u32(sm + OFF_K + rg.i * TILE64);
-                        const uint32_t vaddr = smem_u32(sm + OFF_V + rg.i * TILE64);
-                        tcx::mma_kmajor_k64(tmem + COL_S + w * 128, qaddr, kaddr, id_s, 0);
-                        tcx::mma_kmajor_k64(tmem + COL_S + w * 128 + BT, qaddr + TILE128, vaddr, id_s, 0);
-                        mma_commit(&sb.s_full[w]);
-                        mma_commit(&sb.v_empty[rg.i]);        // V is read only by dP
-                        issued = true;
-                        ++ts[w];
-                        if (j == n[w] - 1) {
-                            mma_commit(&sb.q_empty[w]);       // Q and dO are read only here
-                            ++kq[w];
-                        }
-                        rg.next(STAGES);
+            for (int item = c0; item < c1 && ok; ++item) {
+                const Item I = decode(a, item);
+                Item nx;
+                const bool keep = keeps(a, I, item, c1, nx);
+                sl.begin(kept, I.strip, I.k0, I.k1);
+                kept = keep;
+                if (!wait(&sb.it_full[it.i], it.ph)) break;
+                // A = Q (S) or dO (dP); B = the K or V tile
+                const uint32_t aaddr = smem_u32(sm + OFF_IT + it.i * ITEM) + (dpi ? TILE128 : 0);
+                for (int k = I.k0; k <= I.k1; ++k, ++u) {
+                    const int p = sl.pos(I.k1, k), slot = p % NSLOT;
+                    const int xs = u % NX, ys = u % NY;
+                    if (!wait(&sb.kv_full[slot], static_cast<uint32_t>(p / NSLOT) & 1u) ||
+                        !(dpi ? wait(&sb.y_empty[ys], empty_par(u / NY)) : wait(&sb.x_empty[xs], empty_par(u / NX)))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t baddr = smem_u32(sm + OFF_KV + slot * SLOT) + (dpi ? TILE64 : 0);
+                    tcx::mma_kmajor_k64(dpi ? tmem + COL_Y + ys * 64 : tmem + COL_X + xs * 64, aaddr, baddr, id_s, 0);
+                    mma_commit(&sb.x_full[xs]);
+                    issued = true;
+                }
+                if (!ok) break;
+                mma_commit(&sb.it_empty[it.i]);       // Q (dO) is read only by these products
+                it.next(IBUF);
             }
             if (issued) {
-                mma_commit(&sb.done);
-                mbar_wait(&sb.done, 0, nullptr, 100000000ull);
+                uint64_t* dn = dpi ? &sb.done3 : &sb.done;
+                mma_commit(dn);
+                mbar_wait(dn, 0, nullptr, 100000000ull);
             }
         }
     } else if (warp == 2) {
-        // ------------------------------------------------------------ dQ issuer
+        // ------------------------------------------------------------ dQ += dS K (A from TMEM)
         if (lane == 0) {
-            Ring rg{0, 0};
-            int ko[2] = {0, 0}, td[2] = {0, 0};
+            Slide sl{-1, -1, 0};
+            bool kept = false;
+            int u = 0, e = 0;
             bool issued = false, ok = true;
-            const uint32_t id_dq = idesc_bf16(BM, 64, false, true);
-            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-                int n[2];
-                for (int w = 0; w < 2; ++w) {
-                    const int e = e0 + w * stride;
-                    n[w] = e < a.n_items ? decode(a, e).nt : 0;
+            const uint32_t id_acc = idesc_bf16(BM, 64, false, true);
+            for (int item = c0; item < c1 && ok; ++item, ++e) {
+                const Item I = decode(a, item);
+                Item nx;
+                const bool keep = keeps(a, I, item, c1, nx);
+                sl.begin(kept, I.strip, I.k0, I.k1);
+                kept = keep;
+                const int ob = e & 1;
+                if (!wait(&sb.o_empty[ob], empty_par(e >> 1))) break;
+                tc_fence_after();
+                for (int k = I.k0; k <= I.k1; ++k, ++u) {
+                    const int slot = sl.pos(I.k1, k) % NSLOT;
+                    const int xs = u % NX;
+                    if (!wait(&sb.p_full[u & 3], full_par(u >> 2))) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sm + OFF_KV + slot * SLOT);
+                    tcx::mma_ts_mn_dh<64, 4>(tmem + COL_ACC + ob * 64, tmem + COL_X + xs * 64, kaddr, BT, id_acc,
+                                             k > I.k0 ? 1u : 0u);
+                    mma_commit(&sb.x_empty[xs]);
+                    // the tile's last product (S, dP complete before ds exists): release
+                    // it unless the next item of the run uses it too
+                    if (!keep || k < nx.k0) mma_commit(&sb.kv_empty[slot]);
+                    issued = true;
                 }
-                const int nmax = n[0] > n[1] ? n[0] : n[1];
-                for (int j = 0; j < nmax && ok; ++j)
-                    for (int w = 0; w < 2; ++w) {
-                        if (j >= n[w]) continue;
-                        if ((j == 0 && !wait(&sb.o_empty[w], empty_par(ko[w]))) ||
-                            !wait(&sb.ds_full[w], full_par(td[w]))) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t dsaddr = smem_u32(sm + OFF_DS + w * OPB);
-                        const uint32_t kaddr = smem_u32(sm + OFF_K + rg.i * TILE64);
-                        tcx::mma_kmajor_mnmajor<4>(tmem + COL_DQ + w * 64, dsaddr, OPB, kaddr, id_dq, j > 0);
-                        mma_commit(&sb.k_empty[rg.i]);
-                        mma_commit(&sb.ds_empty[w]);
-                        issued = true;
-                        ++td[w];
-                        if (j == n[w] - 1) {
-                            mma_commit(&sb.o_full[w]);
-                            ++ko[w];
-                        }
-                        rg.next(STAGES);
-                    }
+                if (!ok) break;
+                mma_commit(&sb.o_full[ob]);
             }
             if (issued) {
                 mma_commit(&sb.done2);
                 mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
             }
         }
-    } else {
+    } else if (warp < 11) {
         // ------------------------------------------------------------ math warpgroups
         const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
-        const int row = 32 * qd + lane;
+        const int row = 32 * qd + lane;               // token row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-        const uint32_t ts_addr = tmem + lane_base + COL_S + wg * 128;
-        const uint32_t tq_addr = tmem + lane_base + COL_DQ + wg * 64;
-        uint8_t* dsbuf = sm + OFF_DS + wg * OPB;
-        int ts = 0, ko = 0;
+        const uint32_t span = static_cast<uint32_t>(a.W - 1);
+        const uint64_t sl2 = tcx::f2_pack(a.scale_log2, a.scale_log2);
+        const uint64_t sc2 = tcx::f2_pack(a.scale, a.scale);
+        // lse of this thread's row of an item (rows past L read row L - 1; unused)
+        auto lse_of = [&](int item) {
+            const Item J = decode(a, item);
+            const int t = min(J.qt * BM + row, a.L - 1);
+            return ld_early(a.lse + ((size_t)J.b * a.L + t) * a.H + J.h);
+        };
+        Ring it{0, 0};
+        int u = 0, e = 0;
         bool ok = true;
-        for (int item = blockIdx.x + wg * stride; item < a.n_items && ok; item += 2 * stride) {
-            const Item it = decode(a, item);
-            const int t0 = it.qt * BM;
+        float lse_next = c0 < c1 ? lse_of(c0) : 0.f;
+        // the dQ epilogue of an item this warpgroup stores runs after its first unit
+        // of the next item, so the wait for the item's last product overlaps work
+        int pend_e = -1;
+        __nv_bfloat16* pend_dst = nullptr;
+        bool pend_live = false;
+        auto epilogue = [&]() {
+            if (!wait(&sb.o_full[wg], full_par(pend_e >> 1))) return false;
+            tc_fence_after();
+            uint32_t pk[32];
+            load_row64(tmem + lane_base + COL_ACC + wg * 64, pk);
+            tc_fence_before();
+            mbar_arrive(&sb.o_empty[wg]);
+            if (pend_live) store_row64(pend_dst, pk);
+            pend_e = -1;
+            return true;
+        };
+        for (int item = c0; item < c1 && ok; ++item, ++e) {
+            const Item I = decode(a, item);
+            const int t0 = I.qt * BM;
             const int t = t0 + row;
-            const size_t vrow = ((size_t)it.b * a.H + it.h) * a.Lp + t;   // t < Lp
-            const float lse2 = a.lse2T[vrow];
-            const float dlt = a.deltaT[vrow];
-            const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2), l2 = tcx::f2_pack(lse2, lse2);
-            const uint64_t sc2 = tcx::f2_pack(a.scale, a.scale);
-            const uint64_t ndsc2 = tcx::f2_pack(-dlt * a.scale, -dlt * a.scale);
-            const uint32_t span = static_cast<uint32_t>(a.W - 1);
-            for (int j = 0; j < it.nt; ++j) {
-                if (!wait(&sb.s_full[wg], full_par(ts))) { ok = false; break; }
+            const bool live = t < a.L;
+            // this row's lse was loaded one item ahead; start the next one's load
+            const float nl2 = live ? -lse_next * kLog2e : 0.f;
+            if (item + 1 < c1) lse_next = lse_of(item + 1);
+            if (!wait(&sb.it_full[it.i], it.ph)) break;
+            // delta_t = dO_t . O_t from this row of the two tiles (128-byte swizzled rows)
+            float dlt;
+            {
+                const uint8_t* ib = sm + OFF_IT + it.i * ITEM;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t off = tcx::sw128_off(row, c);
+                    const uint4 g4 = *reinterpret_cast<const uint4*>(ib + TILE128 + off);
+                    const uint4 o4 = *reinterpret_cast<const uint4*>(ib + 2 * TILE128 + off);
+                    const __nv_bfloat162* hg = reinterpret_cast<const __nv_bfloat162*>(&g4);
+                    const __nv_bfloat162* ho = reinterpret_cast<const __nv_bfloat162*>(&o4);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const float2 fg = __bfloat1622float2(hg[v]), fo = __bfloat1622float2(ho[v]);
+                        acc[2 * v] = fmaf(fg.x, fo.x, acc[2 * v]);
+                        acc[2 * v + 1] = fmaf(fg.y, fo.y, acc[2 * v + 1]);
+                    }
+                }
+                dlt = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            }
+            mbar_arrive(&sb.it_empty[it.i]);
+            it.next(IBUF);
+            const float ndsc = -dlt * a.scale;
+            const bool mine = (e & 1) == wg;
+            if (mine) {
+                const size_t vrow = ((size_t)I.b * a.H + I.h) * a.Lp + t;    // t < Lp
+                a.nlse2T[vrow] = nl2;
+                a.ndscT[vrow] = live ? ndsc : 0.f;
+            }
+            const uint64_t nl22 = tcx::f2_pack(nl2, nl2), ndsc2 = tcx::f2_pack(ndsc, ndsc);
+            const int lo = t - a.W + 1;
+            for (int k = I.k0; k <= I.k1; ++k, ++u) {
+                if ((u & 1) != wg) continue;
+                const int xs = u % NX, ys = u % NY;
+                if (!wait(&sb.x_full[xs], full_par(u / NX))) { ok = false; break; }
                 tc_fence_after();
-                const int kbase = (it.k0 + j) * BT;
+                const int kbase = k * BT;
+                // warpgroup-uniform: does the window edge or the diagonal cross this tile?
                 const bool edge = kbase + BT - 1 > t0 || kbase < t0 + BM - a.W;
-                const int lo = t - a.W + 1;
-                // the previous dQ product has read the dS buffer (for a first tile: the
-                // previous item's dQ store has read it too)
-                if (!wait(&sb.ds_empty[wg], empty_par(ts)) ||
-                    (j == 0 && ko > 0 && !wait(&sb.epi_free[wg], full_par(ko - 1)))) { ok = false; break; }
-                // 32 columns at a time: S and dP from TMEM, dS out 8 columns (16 bytes) at a time
-                for (int hf = 0; hf < 2; ++hf) {
-                    float x[32], g[32];
+                const uint32_t xb = tmem + lane_base + COL_X + xs * 64;
+                const uint32_t yb = tmem + lane_base + COL_Y + ys * 64;
 #pragma unroll
-                    for (int ci = 0; ci < 2; ++ci) {
-                        uint32_t r[16], q[16];
-                        tmem_ld_32x32b_x16(ts_addr + 32 * hf + 16 * ci, r);
-                        tmem_ld_32x32b_x16(ts_addr + BT + 32 * hf + 16 * ci, q);
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            x[16 * ci + u] = __uint_as_float(r[u]);
-                            g[16 * ci + u] = __uint_as_float(q[u]);
-                        }
-                    }
+                for (int pc = 0; pc < 2; ++pc) {
+                    // keys kbase + 32 pc .. + 31: S (X columns 32 pc ..) and dP (Y columns 32 pc ..)
+                    uint32_t r0[16], r1[16], r2[16], r3[16];
+                    tmem_ld_32x32b_x16(xb + 32 * pc, r0);
+                    tmem_ld_32x32b_x16(xb + 32 * pc + 16, r1);
+                    tmem_ld_32x32b_x16(yb + 32 * pc, r2);
+                    tmem_ld_32x32b_x16(yb + 32 * pc + 16, r3);
                     tmem_wait_ld();
-                    if (hf == 1) {                      // S and dP fully read
+                    if (pc == 1) {                                // dP fully read: free its slot
                         tc_fence_before();
-                        mbar_arrive(&sb.s_empty[wg]);
+                        mbar_arrive(&sb.y_empty[ys]);
                     }
-                    // column pairs in packed f32x2 arithmetic: p = exp2(-(lse2 - s sl)),
-                    // dS = p (dP - delta) scale; on a tile that the window edge or the
-                    // diagonal crosses, key t0 + c outside [lo, t] gets p = 0 (a select)
+                    const int cb = kbase + 32 * pc - lo;          // column 0 relative to lo
                     uint32_t pk[16];
-                    const int cb = kbase + 32 * hf - lo;          // column 0 relative to lo
                     auto body = [&](bool msk) {
 #pragma unroll
-                        for (int pi = 0; pi < 16; ++pi) {
+                        for (int p2 = 0; p2 < 16; ++p2) {
+                            const uint32_t* rs = p2 < 8 ? r0 : r1;
+                            const uint32_t* rg = p2 < 8 ? r2 : r3;
+                            const int tt = 2 * (p2 & 7);
                             float y0, y1;
-                            tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(x[2 * pi], x[2 * pi + 1]), nsl2, l2), y0, y1);
-                            float p0 = fast_exp2(-y0), p1 = fast_exp2(-y1);
+                            tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(__uint_as_float(rs[tt]), __uint_as_float(rs[tt + 1])),
+                                                      sl2, nl22), y0, y1);
+                            float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
                             if (msk) {
-                                p0 = static_cast<uint32_t>(cb + 2 * pi) > span ? 0.f : p0;
-                                p1 = static_cast<uint32_t>(cb + 2 * pi + 1) > span ? 0.f : p1;
+                                p0 = static_cast<uint32_t>(cb + 2 * p2) > span ? 0.f : p0;
+                                p1 = static_cast<uint32_t>(cb + 2 * p2 + 1) > span ? 0.f : p1;
                             }
-                            const uint64_t gd = tcx::ffma2(tcx::f2_pack(g[2 * pi], g[2 * pi + 1]), sc2, ndsc2);
-                            pk[pi] = tcx::pack_bf16x2(tcx::fmul2(tcx::f2_pack(p0, p1), gd));
+                            const uint64_t gd = tcx::ffma2(
+                                tcx::f2_pack(__uint_as_float(rg[tt]), __uint_as_float(rg[tt + 1])), sc2, ndsc2);
+                            pk[p2] = tcx::pack_bf16x2(tcx::fmul2(tcx::f2_pack(p0, p1), gd));
                         }
                     };
                     if (edge) body(true);
                     else body(false);
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const int chunk = 4 * hf + ch;
-                        *reinterpret_cast<uint4*>(dsbuf + row * 128 + ((chunk ^ (row & 7)) << 4)) =
-                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                    }
+                    // dS over S columns 16 pc .. 16 pc + 15 (already read)
+                    tmem_st_32x32b_x16(xb + 16 * pc, pk);
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(&sb.ds_full[wg]);
-                ++ts;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sb.p_full[u & 3]);
+                if (pend_e >= 0 && !epilogue()) { ok = false; break; }
             }
             if (!ok) break;
-            // epilogue: dQ (TMEM) -> bf16 rows in the idle dS buffer -> one tensor store
-            if (!wait(&sb.o_full[wg], full_par(ko))) break;
-            tc_fence_after();
-            float x[64];
-            load64(tq_addr, x);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&sb.o_empty[wg]);
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = tcx::pack_bf16(x[2 * i], x[2 * i + 1]);
-            put_row64(dsbuf, row, pk);
-            fence_proxy_async_smem();
-            mbar_arrive(&sb.epi_full[wg]);
-            if (qd == 0 && lane == 0) {
-                if (!wait(&sb.epi_full[wg], full_par(ko))) break;
-                tma_store_3d(&tdq, dsbuf, it.h * 64, t0, it.b);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-                mbar_arrive(&sb.epi_free[wg]);
+            if (mine) {
+                pend_e = e;
+                pend_dst = a.dq + (((size_t)I.b * a.L + t) * a.H + I.h) * 64;
+                pend_live = live;
             }
-            ++ko;
         }
-        if (qd == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (ok && pend_e >= 0) epilogue();
     }
 
     tc_fence_before();
@@ -462,48 +518,53 @@ swa_bwd_q_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
 // ============================================================================ pass B (dK, dV)
 namespace pb {
-constexpr int OFF_KV = 0;                        // per warpgroup: K tile, V tile
-constexpr int VEC = TILE64;                      // 64 fp32 after each Q / dO tile (lse2 / delta)
-constexpr int STAGE = TILE64 + 1024;
-constexpr int OFF_Q = 2 * 2 * TILE128;
-constexpr int OFF_DO = OFF_Q + STAGES * STAGE;
-constexpr int OFF_OP = OFF_DO + STAGES * STAGE;  // per warpgroup: P^T operand, dS^T operand
-constexpr int SMEM = OFF_OP + 2 * 2 * OPB + 1024;
-constexpr uint32_t COL_S = 0;                    // warpgroup w: S^T at w*128, dP^T at w*128 + 64
-constexpr uint32_t COL_ACC = 256;                // warpgroup w: dK at 256 + w*128, dV at +64
+constexpr int kThreads = 384;                    // + warp 11: the dV issuer
+constexpr int IBUF = 2;
+constexpr int ITEM = 2 * TILE128;                // K, V
+constexpr int VEC_OFF = 2 * TILE128;             // after the Q and dO tiles: nlse2[128], ndsc[128]
+constexpr int SLOT = VEC_OFF + 1024;             // one 128-query stage
+constexpr int NSLOT = 4;
+constexpr int OFF_IT = 0;
+constexpr int OFF_ST = IBUF * ITEM;
+constexpr int SMEM = OFF_ST + NSLOT * SLOT + 1024;
 
 struct Item {
-    int b, kt, h, q0, nt;    // query tiles of 64: q0 .. q0 + nt - 1
+    int b, kt, h, strip, g0, g1;     // 128-query stages g0 .. g1
 };
+// item = (b * H + h) * nKT + kt
 __device__ __forceinline__ Item decode(const SwaBwdArgs& a, int item) {
     Item it;
-    it.h = item % a.H;
-    const int bk = item / a.H;
-    it.kt = bk % a.nKT;
-    it.b = bk / a.nKT;
-    it.q0 = it.kt * BM / BT;
-    int hi = (it.kt * BM + BM - 1 + a.W - 1) / BT;
-    if (hi > a.nQ64 - 1) hi = a.nQ64 - 1;
-    it.nt = hi - it.q0 + 1;
+    it.kt = item % a.nKT;
+    it.strip = item / a.nKT;
+    it.h = it.strip % a.H;
+    it.b = it.strip / a.H;
+    it.g0 = it.kt;
+    int last = it.kt * BM + BM - 1 + a.W - 1;            // last query that sees a key of the tile
+    if (last > a.L - 1) last = a.L - 1;
+    it.g1 = last / BM;
     return it;
+}
+__device__ __forceinline__ bool keeps(const SwaBwdArgs& a, const Item& I, int item, int c1, Item& nx) {
+    if (!a.slide || item + 1 >= c1) return false;
+    nx = decode(a, item + 1);
+    return nx.strip == I.strip;
 }
 
 struct __align__(8) Bars {
-    uint64_t kv_full[2], kv_empty[2];
-    uint64_t q_full[STAGES], q_empty[STAGES], d_full[STAGES], d_empty[STAGES];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full[2], p_empty[2];
-    uint64_t o_full[2], o_empty[2];
-    uint64_t epi_full[2], epi_free[2];
-    uint64_t done, done2;
+    uint64_t it_full[IBUF], it_empty[IBUF];
+    uint64_t st_full[NSLOT], st_empty[NSLOT];
+    uint64_t x_full[NX], x_empty[NX], y_empty[NY];
+    uint64_t p_full[4];
+    uint64_t o_full[2], o_empty;         // o_full per storing warpgroup
+    uint64_t done, done2, done3;
     uint32_t tmem;
     int abort;
 };
+static_assert(SMEM + sizeof(Bars) <= kSmemMax, "shared memory (pass B)");
 
 __global__ void __launch_bounds__(kThreads, 1)
 swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                  const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                   const SwaBwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -511,29 +572,30 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     __shared__ Bars sb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, a.status); };
-    const int stride = gridDim.x;
+    const int c0 = static_cast<int>((long long)blockIdx.x * a.n_items / gridDim.x);
+    const int c1 = static_cast<int>((long long)(blockIdx.x + 1) * a.n_items / gridDim.x);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&sb.kv_full[i], 1);
-            mbar_init(&sb.kv_empty[i], 1);
-            mbar_init(&sb.s_full[i], 1);
-            mbar_init(&sb.s_empty[i], 128);
-            mbar_init(&sb.p_full[i], 128);
-            mbar_init(&sb.p_empty[i], 1);
-            mbar_init(&sb.o_full[i], 1);
-            mbar_init(&sb.o_empty[i], 128);
-            mbar_init(&sb.epi_full[i], 128);
-            mbar_init(&sb.epi_free[i], 1);
+        for (int i = 0; i < IBUF; ++i) {
+            mbar_init(&sb.it_full[i], 1);
+            mbar_init(&sb.it_empty[i], 1);
         }
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&sb.q_full[i], 1);
-            mbar_init(&sb.q_empty[i], 1);
-            mbar_init(&sb.d_full[i], 1);
-            mbar_init(&sb.d_empty[i], 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(&sb.st_full[i], 1);
+            mbar_init(&sb.st_empty[i], 2);            // the dK and the dV issuer
         }
+        for (int i = 0; i < NX; ++i) {
+            mbar_init(&sb.x_full[i], 1);
+            mbar_init(&sb.x_empty[i], 2);            // the dK and the dV issuer
+        }
+        for (int i = 0; i < NY; ++i) mbar_init(&sb.y_empty[i], 128);
+        for (int i = 0; i < 4; ++i) mbar_init(&sb.p_full[i], 128);
+        mbar_init(&sb.o_full[0], 2);
+        mbar_init(&sb.o_full[1], 2);
+        mbar_init(&sb.o_empty, 128);
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
+        mbar_init(&sb.done3, 1);
         sb.abort = 0;
         fence_barrier_init();
     }
@@ -542,8 +604,6 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         prefetch_tmap(&tdo);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
-        prefetch_tmap(&tdk);
-        prefetch_tmap(&tdv);
     }
     if (warp == 1) {
         tmem_alloc(&sb.tmem, TMEM_COLS);
@@ -556,290 +616,258 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // lane 0: K / V tiles and the Q ring (+ lse2 rows); lane 1: the dO ring (+ delta rows)
-        if (lane < 2) {
-            const bool ql = lane == 0;
-            Ring rg{0, 0};
-            int kk[2] = {0, 0};
-            bool out[STAGES] = {}, kv_out[2] = {false, false};
-            uint32_t ph[STAGES] = {}, kv_ph[2] = {0, 0};
-            uint64_t* full = ql ? sb.q_full : sb.d_full;
-            uint64_t* empty = ql ? sb.q_empty : sb.d_empty;
-            const CUtensorMap* map = ql ? &tq : &tdo;
-            const float* vec = ql ? a.lse2T : a.deltaT;
-            uint8_t* ring = sm + (ql ? OFF_Q : OFF_DO);
+        if (lane == 0) {
+            Ring it{0, 0};
+            Slide sl{-1, -1, 0};
+            bool kept = false;
+            bool st_out[NSLOT] = {}, it_out[IBUF] = {};
+            uint32_t st_ph[NSLOT] = {}, it_ph[IBUF] = {};
             bool ok = true;
-            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-                Item it[2];
-                int n[2];
-                for (int w = 0; w < 2; ++w) {
-                    const int e = e0 + w * stride;
-                    n[w] = 0;
-                    if (e < a.n_items) { it[w] = decode(a, e); n[w] = it[w].nt; }
+            // K and V of an item: issued one item ahead, before the item's new stages
+            // (whose slots the item's own first units free)
+            auto load_item = [&](int item) {
+                const Item J = decode(a, item);
+                if (!wait(&sb.it_empty[it.i], it.ph ^ 1u)) return false;
+                uint8_t* ib = sm + OFF_IT + it.i * ITEM;
+                mbar_arrive_expect_tx(&sb.it_full[it.i], 2 * TILE128);
+                tma_load_3d(ib, &tk, &sb.it_full[it.i], J.h * 64, J.kt * BM, J.b);
+                tma_load_3d(ib + TILE128, &tv, &sb.it_full[it.i], J.h * 64, J.kt * BM, J.b);
+                it_out[it.i] = true;
+                it_ph[it.i] = it.ph;
+                it.next(IBUF);
+                return true;
+            };
+            if (c0 < c1) ok = load_item(c0);
+            for (int item = c0; item < c1 && ok; ++item) {
+                const Item I = decode(a, item);
+                Item nx;
+                const bool keep = keeps(a, I, item, c1, nx);
+                if (item + 1 < c1 && !load_item(item + 1)) break;
+                const size_t vbase = ((size_t)I.b * a.H + I.h) * a.Lp;
+                const int from = sl.begin(kept, I.strip, I.g0, I.g1);
+                for (int g = from; g <= I.g1; ++g) {
+                    const int p = sl.pos(I.g1, g), slot = p % NSLOT;
+                    const uint32_t ph = static_cast<uint32_t>(p / NSLOT) & 1u;
+                    if (!wait(&sb.st_empty[slot], ph ^ 1u)) { ok = false; break; }
+                    uint8_t* stg = sm + OFF_ST + slot * SLOT;
+                    const int qb = g * BM;
+                    mbar_arrive_expect_tx(&sb.st_full[slot], 2 * TILE128 + 2 * BM * 4);
+                    tma_load_3d(stg, &tq, &sb.st_full[slot], I.h * 64, qb, I.b);
+                    tma_load_3d(stg + TILE128, &tdo, &sb.st_full[slot], I.h * 64, qb, I.b);
+                    tcx::bulk_load(stg + VEC_OFF, a.nlse2T + vbase + qb, BM * 4, &sb.st_full[slot]);
+                    tcx::bulk_load(stg + VEC_OFF + BM * 4, a.ndscT + vbase + qb, BM * 4, &sb.st_full[slot]);
+                    st_out[slot] = true;
+                    st_ph[slot] = ph;
                 }
-                if (ql)
-                    for (int w = 0; w < 2 && ok; ++w) {
-                        if (n[w] == 0) continue;
-                        if (!wait(&sb.kv_empty[w], empty_par(kk[w]))) { ok = false; break; }
-                        uint8_t* kb = sm + OFF_KV + w * 2 * TILE128;
-                        mbar_arrive_expect_tx(&sb.kv_full[w], 2 * TILE128);
-                        tma_load_3d(kb, &tk, &sb.kv_full[w], it[w].h * 64, it[w].kt * BM, it[w].b);
-                        tma_load_3d(kb + TILE128, &tv, &sb.kv_full[w], it[w].h * 64, it[w].kt * BM, it[w].b);
-                        kv_out[w] = true;
-                        kv_ph[w] = full_par(kk[w]);
-                        ++kk[w];
-                    }
-                const int nmax = n[0] > n[1] ? n[0] : n[1];
-                for (int j = 0; j < nmax && ok; ++j)
-                    for (int w = 0; w < 2; ++w) {
-                        if (j >= n[w]) continue;
-                        if (!wait(&empty[rg.i], rg.ph ^ 1u)) { ok = false; break; }
-                        uint8_t* stg = ring + rg.i * STAGE;
-                        const int qb = (it[w].q0 + j) * BT;
-                        mbar_arrive_expect_tx(&full[rg.i], TILE64 + BT * 4);
-                        tma_load_3d(stg, map, &full[rg.i], it[w].h * 64, qb, it[w].b);
-                        tcx::bulk_load(stg + VEC, vec + ((size_t)it[w].b * a.H + it[w].h) * a.Lp + qb,
-                                       BT * 4, &full[rg.i]);
-                        out[rg.i] = true;
-                        ph[rg.i] = rg.ph;
-                        rg.next(STAGES);
-                    }
+                kept = keep;
             }
-            for (int i = 0; i < STAGES; ++i)
-                if (out[i]) mbar_wait(&full[i], ph[i], nullptr, 100000000ull);
-            for (int i = 0; i < 2; ++i)
-                if (kv_out[i]) mbar_wait(&sb.kv_full[i], kv_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < NSLOT; ++i)
+                if (st_out[i]) mbar_wait(&sb.st_full[i], st_ph[i], nullptr, 100000000ull);
+            for (int i = 0; i < IBUF; ++i)
+                if (it_out[i]) mbar_wait(&sb.it_full[i], it_ph[i], nullptr, 100000000ull);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ S^T / dP^T issuer
+        // ------------------------------------------------------------ S^T = K Q^T, dP^T = V dO^T
         if (lane == 0) {
-            Ring rg{0, 0};
-            int kk[2] = {0, 0}, ts[2] = {0, 0};
+            Ring it{0, 0};
+            Slide sl{-1, -1, 0};
+            bool kept = false;
+            int u = 0;
             bool issued = false, ok = true;
             const uint32_t id_s = idesc_bf16(BM, BT, false, false);
-            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-                int n[2];
-                for (int w = 0; w < 2; ++w) {
-                    const int e = e0 + w * stride;
-                    n[w] = e < a.n_items ? decode(a, e).nt : 0;
-                }
-                const int nmax = n[0] > n[1] ? n[0] : n[1];
-                for (int j = 0; j < nmax && ok; ++j)
-                    for (int w = 0; w < 2; ++w) {
-                        if (j >= n[w]) continue;
-                        if ((j == 0 && !wait(&sb.kv_full[w], full_par(kk[w]))) ||
-                            !wait(&sb.q_full[rg.i], rg.ph) || !wait(&sb.d_full[rg.i], rg.ph) ||
-                            !wait(&sb.s_empty[w], empty_par(ts[w]))) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t kaddr = smem_u32(sm + OFF_KV + w * 2 * TILE128);
-                        const uint32_t qaddr = smem_u32(sm + OFF_Q + rg.i * STAGE);
-                        const uint32_t daddr = smem_u32(sm + OFF_DO + rg.i * STAGE);
-                        tcx::mma_kmajor_k64(tmem + COL_S + w * 128, kaddr, qaddr, id_s, 0);
-                        tcx::mma_kmajor_k64(tmem + COL_S + w * 128 + BT, kaddr + TILE128, daddr, id_s, 0);
-                        mma_commit(&sb.s_full[w]);
-                        issued = true;
-                        ++ts[w];
-                        if (j == n[w] - 1) {
-                            mma_commit(&sb.kv_empty[w]);      // K and V are read only here
-                            ++kk[w];
+            for (int item = c0; item < c1 && ok; ++item) {
+                const Item I = decode(a, item);
+                Item nx;
+                const bool keep = keeps(a, I, item, c1, nx);
+                sl.begin(kept, I.strip, I.g0, I.g1);
+                kept = keep;
+                if (!wait(&sb.it_full[it.i], it.ph)) break;
+                const uint32_t kaddr = smem_u32(sm + OFF_IT + it.i * ITEM);
+                const uint32_t vaddr = kaddr + TILE128;
+                for (int g = I.g0; g <= I.g1 && ok; ++g) {
+                    const int p = sl.pos(I.g1, g), slot = p % NSLOT;
+                    if (!wait(&sb.st_full[slot], static_cast<uint32_t>(p / NSLOT) & 1u)) { ok = false; break; }
+                    const uint32_t qaddr = smem_u32(sm + OFF_ST + slot * SLOT);
+                    for (int hf = 0; hf < 2; ++hf, ++u) {
+                        const int xs = u % NX, ys = u % NY;
+                        if (!wait(&sb.x_empty[xs], empty_par(u / NX)) || !wait(&sb.y_empty[ys], empty_par(u / NY))) {
+                            ok = false;
+                            break;
                         }
-                        rg.next(STAGES);
+                        tc_fence_after();
+                        tcx::mma_kmajor_k64(tmem + COL_X + xs * 64, kaddr, qaddr + hf * TILE64, id_s, 0);
+                        tcx::mma_kmajor_k64(tmem + COL_Y + ys * 64, vaddr, qaddr + TILE128 + hf * TILE64, id_s, 0);
+                        mma_commit(&sb.x_full[xs]);
+                        issued = true;
                     }
+                }
+                if (!ok) break;
+                mma_commit(&sb.it_empty[it.i]);       // K and V are read only by these products
+                it.next(IBUF);
             }
             if (issued) {
                 mma_commit(&sb.done);
                 mbar_wait(&sb.done, 0, nullptr, 100000000ull);
             }
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ dK / dV issuer
+    } else if (warp == 2 || warp == 11) {
+        // warp 2: dK += dS^T Q, warp 11: dV += P^T dO (A from TMEM, K = 64 queries)
+        const bool dvi = warp == 11;
         if (lane == 0) {
-            Ring rg{0, 0};
-            int ko[2] = {0, 0}, tp[2] = {0, 0};
+            Slide sl{-1, -1, 0};
+            bool kept = false;
+            int u = 0, e = 0;
             bool issued = false, ok = true;
             const uint32_t id_acc = idesc_bf16(BM, 64, false, true);
-            for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-                int n[2];
-                for (int w = 0; w < 2; ++w) {
-                    const int e = e0 + w * stride;
-                    n[w] = e < a.n_items ? decode(a, e).nt : 0;
-                }
-                const int nmax = n[0] > n[1] ? n[0] : n[1];
-                for (int j = 0; j < nmax && ok; ++j)
-                    for (int w = 0; w < 2; ++w) {
-                        if (j >= n[w]) continue;
-                        if ((j == 0 && !wait(&sb.o_empty[w], empty_par(ko[w]))) ||
-                            !wait(&sb.p_full[w], full_par(tp[w]))) { ok = false; break; }
+            const uint32_t d_acc = tmem + COL_ACC + (dvi ? 64 : 0);
+            for (int item = c0; item < c1 && ok; ++item, ++e) {
+                const Item I = decode(a, item);
+                Item nx;
+                const bool keep = keeps(a, I, item, c1, nx);
+                sl.begin(kept, I.strip, I.g0, I.g1);
+                kept = keep;
+                if (!wait(&sb.o_empty, empty_par(e))) break;
+                tc_fence_after();
+                for (int g = I.g0; g <= I.g1 && ok; ++g) {
+                    const int slot = sl.pos(I.g1, g) % NSLOT;
+                    const uint32_t xaddr = smem_u32(sm + OFF_ST + slot * SLOT) + (dvi ? TILE128 : 0);
+                    for (int hf = 0; hf < 2; ++hf, ++u) {
+                        const int xs = u % NX;
+                        if (!wait(&sb.p_full[u & 3], full_par(u >> 2))) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t ptaddr = smem_u32(sm + OFF_OP + w * 2 * OPB);
-                        const uint32_t qaddr = smem_u32(sm + OFF_Q + rg.i * STAGE);
-                        const uint32_t daddr = smem_u32(sm + OFF_DO + rg.i * STAGE);
-                        const uint32_t acc = tmem + COL_ACC + w * 128;
-                        tcx::mma_kmajor_mnmajor<4>(acc + 64, ptaddr, OPB, daddr, id_acc, j > 0);        // dV
-                        tcx::mma_kmajor_mnmajor<4>(acc, ptaddr + OPB, OPB, qaddr, id_acc, j > 0);       // dK
-                        mma_commit(&sb.q_empty[rg.i]);
-                        mma_commit(&sb.d_empty[rg.i]);
-                        mma_commit(&sb.p_empty[w]);
+                        // A = dS^T (dK) or P^T (dV): K = 16 query steps at X columns
+                        // 0, 8, 32, 40 (dS^T) and 16, 24, 48, 56 (P^T), as the math wrote them
+                        const uint64_t xd = tcx::desc_head<64>(xaddr + hf * TILE64);
+                        const uint32_t xa = tmem + COL_X + xs * 64 + (dvi ? 16 : 0);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc::mma_bf16_ts(d_acc, xa + (ks >> 1) * 32 + (ks & 1) * 8, xd + (uint64_t)(ks * 128), id_acc,
+                                            (ks > 0 || g > I.g0 || hf > 0) ? 1u : 0u);
+                        mma_commit(&sb.x_empty[xs]);
                         issued = true;
-                        ++tp[w];
-                        if (j == n[w] - 1) {
-                            mma_commit(&sb.o_full[w]);
-                            ++ko[w];
-                        }
-                        rg.next(STAGES);
                     }
+                    if (!ok) break;
+                    // the stage's last products: release it unless the next item of the run uses it
+                    if (!keep || g < nx.g0) mma_commit(&sb.st_empty[slot]);
+                }
+                if (!ok) break;
+                mma_commit(&sb.o_full[e & 1]);
             }
             if (issued) {
-                mma_commit(&sb.done2);
-                mbar_wait(&sb.done2, 0, nullptr, 100000000ull);
+                uint64_t* dn = dvi ? &sb.done3 : &sb.done2;
+                mma_commit(dn);
+                mbar_wait(dn, 0, nullptr, 100000000ull);
             }
         }
     } else {
         // ------------------------------------------------------------ math warpgroups
         const int wg = (warp - 3) >> 2;
         const int qd = warp & 3;
-        const int row = 32 * qd + lane;               // key row of the item's tile
+        const int row = 32 * qd + lane;               // key row = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-        const uint32_t ts_addr = tmem + lane_base + COL_S + wg * 128;
-        const uint32_t ta_addr = tmem + lane_base + COL_ACC + wg * 128;
-        uint8_t* ptbuf = sm + OFF_OP + wg * 2 * OPB;
-        uint8_t* dsbuf = ptbuf + OPB;
-        Ring rg{0, 0};
-        int ts = 0, ko = 0;
+        const uint64_t sl2 = tcx::f2_pack(a.scale_log2, a.scale_log2);
+        const uint64_t sc2 = tcx::f2_pack(a.scale, a.scale);
+        Slide sl{-1, -1, 0};
+        bool kept = false;
+        int u = 0, e = 0;
         bool ok = true;
-        for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
-            int n[2];
-            Item mine;
-            for (int w = 0; w < 2; ++w) {
-                const int e = e0 + w * stride;
-                n[w] = 0;
-                if (e < a.n_items) {
-                    const Item it = decode(a, e);
-                    n[w] = it.nt;
-                    if (w == wg) mine = it;
-                }
-            }
-            if (n[wg] == 0) break;                    // no more items for this warpgroup
-            const int s = mine.kt * BM + row;         // this thread's key
-            const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
-            const uint64_t sc2 = tcx::f2_pack(a.scale, a.scale);
-            // queries s .. min(s + W - 1, L - 1) see this key (rows past L are never stored)
-            const uint32_t span = static_cast<uint32_t>(min(a.W - 1, a.L - 1 - s));
-            const int nmax = n[0] > n[1] ? n[0] : n[1];
-            for (int j = 0; j < nmax && ok; ++j)
-                for (int w = 0; w < 2; ++w) {
-                    if (j >= n[w]) continue;
-                    const int stg = rg.i;
-                    const uint32_t stph = rg.ph;
-                    rg.next(STAGES);
-                    if (w != wg) continue;
-                    if (!wait(&sb.s_full[wg], full_par(ts)) || !wait(&sb.q_full[stg], stph) ||
-                        !wait(&sb.d_full[stg], stph)) { ok = false; break; }
+        for (int item = c0; item < c1 && ok; ++item, ++e) {
+            const Item I = decode(a, item);
+            Item nx;
+            const bool keep = keeps(a, I, item, c1, nx);
+            sl.begin(kept, I.strip, I.g0, I.g1);
+            kept = keep;
+            const int s0 = I.kt * BM;
+            const int s = s0 + row;                   // this thread's key
+            // queries s .. min(s + W - 1, L - 1) see key s (key rows past L are never stored)
+            const int spn = min(a.W - 1, a.L - 1 - s);
+            const uint32_t span = spn < 0 ? 0u : static_cast<uint32_t>(spn);
+            for (int g = I.g0; g <= I.g1 && ok; ++g) {
+                const int p = sl.pos(I.g1, g), slot = p % NSLOT;
+                const uint32_t stph = static_cast<uint32_t>(p / NSLOT) & 1u;
+                for (int hf = 0; hf < 2; ++hf, ++u) {
+                    if ((u & 1) != wg) continue;
+                    const int xs = u % NX, ys = u % NY;
+                    // own x_full first: its completion implies this stage has landed, so
+                    // the stage barrier's phase below is unambiguous
+                    if (!wait(&sb.x_full[xs], full_par(u / NX)) || !wait(&sb.st_full[slot], stph)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    const float4* l4 = reinterpret_cast<const float4*>(sm + OFF_Q + stg * STAGE + VEC);
-                    const float4* d4 = reinterpret_cast<const float4*>(sm + OFF_DO + stg * STAGE + VEC);
-                    const int qb = (mine.q0 + j) * BT;
-                    // warp-uniform: the selects below are exact per lane
-                    const bool edge = __any_sync(0xffffffffu, qb < s || qb + BT - 1 > s + a.W - 1 || qb + BT > a.L);
-                    // the previous accumulation products have read the operand buffers
-                    // (for a first tile: the previous item's stores have read them too)
-                    if (!wait(&sb.p_empty[wg], empty_par(ts)) ||
-                        (j == 0 && ko > 0 && !wait(&sb.epi_free[wg], full_par(ko - 1)))) { ok = false; break; }
-                    // 32 columns at a time: S^T and dP^T from TMEM, P^T and dS^T out to the
-                    // operand buffers 8 columns (16 bytes) at a time
-                    for (int hf = 0; hf < 2; ++hf) {
-                        float x[32], g[32];
+                    const int qb = g * BM + hf * BT;
+                    // warpgroup-uniform: do the window edge, the diagonal or the sequence end cross the unit?
+                    const bool edge = qb < s0 + BM - 1 || qb + BT - 1 > s0 + a.W - 1 || qb + BT > a.L;
+                    const uint8_t* vec = sm + OFF_ST + slot * SLOT + VEC_OFF + hf * BT * 4;
+                    const uint64_t* nl = reinterpret_cast<const uint64_t*>(vec);              // pairs
+                    const uint64_t* nd = reinterpret_cast<const uint64_t*>(vec + BM * 4);
+                    const uint32_t xb = tmem + lane_base + COL_X + xs * 64;
+                    const uint32_t yb = tmem + lane_base + COL_Y + ys * 64;
 #pragma unroll
-                        for (int ci = 0; ci < 2; ++ci) {
-                            uint32_t r[16], q[16];
-                            tmem_ld_32x32b_x16(ts_addr + 32 * hf + 16 * ci, r);
-                            tmem_ld_32x32b_x16(ts_addr + BT + 32 * hf + 16 * ci, q);
-#pragma unroll
-                            for (int u = 0; u < 16; ++u) {
-                                x[16 * ci + u] = __uint_as_float(r[u]);
-                                g[16 * ci + u] = __uint_as_float(q[u]);
-                            }
-                        }
+                    for (int pc = 0; pc < 2; ++pc) {
+                        // queries qb + 32 pc .. + 31 of this key row
+                        uint32_t r0[16], r1[16], r2[16], r3[16];
+                        tmem_ld_32x32b_x16(xb + 32 * pc, r0);
+                        tmem_ld_32x32b_x16(xb + 32 * pc + 16, r1);
+                        tmem_ld_32x32b_x16(yb + 32 * pc, r2);
+                        tmem_ld_32x32b_x16(yb + 32 * pc + 16, r3);
                         tmem_wait_ld();
-                        if (hf == 1) {                  // S^T and dP^T fully read
+                        if (pc == 1) {                               // dP^T fully read: free its slot
                             tc_fence_before();
-                            mbar_arrive(&sb.s_empty[wg]);
+                            mbar_arrive(&sb.y_empty[ys]);
                         }
-                        // query pairs in packed f32x2 arithmetic: P^T = exp2(-(lse2 - s sl)),
-                        // dS^T = p (dP - delta) scale; on a tile that the window edges cross,
-                        // query tq outside [s, min(s + W - 1, L - 1)] gets p = 0 (a select)
-                        const ulonglong2* l2v = reinterpret_cast<const ulonglong2*>(l4) + 8 * hf;
-                        const ulonglong2* d2v = reinterpret_cast<const ulonglong2*>(d4) + 8 * hf;
-                        const int cb = qb + 32 * hf - s;            // column 0 relative to s
-                        uint32_t pp[16], pd[16];
+                        const int cb = qb + 32 * pc - s;             // column 0 relative to s
+                        uint32_t pd[16], pp[16];
                         auto body = [&](bool msk) {
 #pragma unroll
-                            for (int pi = 0; pi < 16; ++pi) {
-                                const ulonglong2 lv = l2v[pi >> 1], dv = d2v[pi >> 1];
+                            for (int p2 = 0; p2 < 16; ++p2) {
+                                const uint32_t* rs = p2 < 8 ? r0 : r1;
+                                const uint32_t* rg = p2 < 8 ? r2 : r3;
+                                const int tt = 2 * (p2 & 7);
                                 float y0, y1;
-                                tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(x[2 * pi], x[2 * pi + 1]), nsl2,
-                                                          (pi & 1) ? lv.y : lv.x), y0, y1);
-                                float p0 = fast_exp2(-y0), p1 = fast_exp2(-y1);
+                                tcx::f2_unpack(
+                                    tcx::ffma2(tcx::f2_pack(__uint_as_float(rs[tt]), __uint_as_float(rs[tt + 1])),
+                                               sl2, nl[16 * pc + p2]), y0, y1);
+                                float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
                                 if (msk) {
-                                    p0 = static_cast<uint32_t>(cb + 2 * pi) > span ? 0.f : p0;
-                                    p1 = static_cast<uint32_t>(cb + 2 * pi + 1) > span ? 0.f : p1;
+                                    p0 = static_cast<uint32_t>(cb + 2 * p2) > span ? 0.f : p0;
+                                    p1 = static_cast<uint32_t>(cb + 2 * p2 + 1) > span ? 0.f : p1;
                                 }
-                                const uint64_t p2 = tcx::f2_pack(p0, p1);
-                                const uint64_t g2 = tcx::f2_pack(g[2 * pi], g[2 * pi + 1]);
-                                pp[pi] = tcx::pack_bf16x2(p2);
-                                pd[pi] = tcx::pack_bf16x2(
-                                    tcx::fmul2(tcx::fmul2(p2, sc2), tcx::fsub2(g2, (pi & 1) ? dv.y : dv.x)));
+                                const uint64_t p2v = tcx::f2_pack(p0, p1);
+                                const uint64_t gd = tcx::ffma2(
+                                    tcx::f2_pack(__uint_as_float(rg[tt]), __uint_as_float(rg[tt + 1])), sc2,
+                                    nd[16 * pc + p2]);
+                                pd[p2] = tcx::pack_bf16x2(tcx::fmul2(p2v, gd));
+                                pp[p2] = tcx::pack_bf16x2(p2v);
                             }
                         };
                         if (edge) body(true);
                         else body(false);
-#pragma unroll
-                        for (int ch = 0; ch < 4; ++ch) {
-                            const int chunk = 4 * hf + ch;
-                            const int off = row * 128 + ((chunk ^ (row & 7)) << 4);
-                            *reinterpret_cast<uint4*>(ptbuf + off) =
-                                make_uint4(pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2], pp[4 * ch + 3]);
-                            *reinterpret_cast<uint4*>(dsbuf + off) =
-                                make_uint4(pd[4 * ch], pd[4 * ch + 1], pd[4 * ch + 2], pd[4 * ch + 3]);
-                        }
+                        // dS^T, then P^T, over the 32 S^T columns just read
+                        tmem_st_32x32b_x16(xb + 32 * pc, pd);
+                        tmem_st_32x32b_x16(xb + 32 * pc + 16, pp);
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&sb.p_full[wg]);
-                    ++ts;
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&sb.p_full[u & 3]);
                 }
+            }
             if (!ok) break;
-            // epilogue: dK, dV (TMEM) -> bf16 rows in the idle operand buffers -> tensor stores
-            if (!wait(&sb.o_full[wg], full_par(ko))) break;
+            if ((e & 1) != wg) continue;
+            // epilogue: dK and dV rows of key s
+            if (!wait(&sb.o_full[wg], full_par(e >> 1))) break;
             tc_fence_after();
-            {
-                float x[64];
-                uint32_t pk[32];
-                load64(ta_addr, x);                   // dK
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = tcx::pack_bf16(x[2 * i], x[2 * i + 1]);
-                put_row64(dsbuf, row, pk);
-                load64(ta_addr + 64, x);              // dV
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) pk[i] = tcx::pack_bf16(x[2 * i], x[2 * i + 1]);
-                put_row64(ptbuf, row, pk);
-            }
+            const size_t orow = (((size_t)I.b * a.L + s) * a.H + I.h) * 64;
+            uint32_t pkk[32], pkv[32];
+            load_row64(tmem + lane_base + COL_ACC, pkk);
+            load_row64(tmem + lane_base + COL_ACC + 64, pkv);
             tc_fence_before();
-            mbar_arrive(&sb.o_empty[wg]);
-            fence_proxy_async_smem();
-            mbar_arrive(&sb.epi_full[wg]);
-            if (qd == 0 && lane == 0) {
-                if (!wait(&sb.epi_full[wg], full_par(ko))) break;
-                tma_store_3d(&tdk, dsbuf, mine.h * 64, mine.kt * BM, mine.b);
-                tma_store_3d(&tdv, ptbuf, mine.h * 64, mine.kt * BM, mine.b);
-                bulk_commit_group();
-                bulk_wait_group_read0();
-                mbar_arrive(&sb.epi_free[wg]);
+            mbar_arrive(&sb.o_empty);                 // the next item may accumulate now
+            if (s < a.L) {
+                store_row64(a.dk + orow, pkk);
+                store_row64(a.dv + orow, pkv);
             }
-            ++ko;
         }
-        if (qd == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
 
     tc_fence_before();
@@ -852,6 +880,31 @@ swa_bwd_kv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 }  // namespace pb
 
 }  // namespace
+
+// Can consecutive items of a strip keep their shared tiles in a ring of
+// `nslot` slots filled and released in load order?  Items i = 0 .. n-1 use tiles
+// k0(i) .. k1(i) (both non-decreasing, no gaps between items).
+// A new tile k takes the slot of tile k - nslot, which is free once the last
+// item that uses k - nslot has passed it; that item must not come after the
+// first item that needs k, or the ring would wait on itself.
+template <typename Range>
+bool slide_safe(int n, int nslot, Range range) {
+    int pk0 = 0, pk1 = -1;
+    std::vector<int> first, last;
+    for (int i = 0; i < n; ++i) {
+        int k0, k1;
+        range(i, k0, k1);
+        if (k1 < k0 || (i > 0 && (k0 < pk0 || k1 < pk1 || k0 > pk1 + 1))) return false;
+        for (int k = pk1 + 1; k <= k1; ++k) first.push_back(i);    // first[k]: first item needing k
+        last.resize(k1 + 1, i);
+        for (int k = k0; k <= k1; ++k) last[k] = i;                // last[k]: last item needing k
+        pk0 = k0;
+        pk1 = k1;
+    }
+    for (int k = nslot; k <= pk1; ++k)
+        if (last[k - nslot] > first[k]) return false;
+    return true;
+}
 
 size_t swa_bwd_workspace_bytes(int B, int L, int H) {
     const size_t Lp = ((size_t)L + BM - 1) / BM * BM;
@@ -867,52 +920,57 @@ cudaError_t launch_swa_bwd_tc(int B, int L, int H, int W, float attn_scale, cons
     a.Lp = (L + BM - 1) / BM * BM;
     a.nQT = (L + BM - 1) / BM;
     a.nKT = a.nQT;
-    a.nQ64 = (L + BT - 1) / BT;
     a.scale = attn_scale;
     a.scale_log2 = attn_scale * kLog2e;
     a.status = status;
-    float* lse2T = static_cast<float*>(ws);
-    float* deltaT = lse2T + (size_t)B * H * a.Lp;
-    a.lse2T = lse2T;
-    a.deltaT = deltaT;
+    a.lse = lse;
+    a.nlse2T = static_cast<float*>(ws);
+    a.ndscT = a.nlse2T + (size_t)B * H * a.Lp;
+    a.dq = static_cast<__nv_bfloat16*>(dq);
+    a.dk = static_cast<__nv_bfloat16*>(dk);
+    a.dv = static_cast<__nv_bfloat16*>(dv);
     const uint64_t cols = (uint64_t)H * 64;
-    CUtensorMap q128, do128, k64, v64, dq128, k128, v128, q64, do64, dk128, dv128;
+    CUtensorMap q128, do128, o128, k64, v64, k128, v128;
     if (!encode_bf16_seq(&q128, q, B, L, cols, BM) || !encode_bf16_seq(&do128, dout, B, L, cols, BM) ||
-        !encode_bf16_seq(&k64, k, B, L, cols, BT) || !encode_bf16_seq(&v64, v, B, L, cols, BT) ||
-        !encode_bf16_seq(&dq128, dq, B, L, cols, BM) || !encode_bf16_seq(&k128, k, B, L, cols, BM) ||
-        !encode_bf16_seq(&v128, v, B, L, cols, BM) || !encode_bf16_seq(&q64, q, B, L, cols, BT) ||
-        !encode_bf16_seq(&do64, dout, B, L, cols, BT) || !encode_bf16_seq(&dk128, dk, B, L, cols, BM) ||
-        !encode_bf16_seq(&dv128, dv, B, L, cols, BM))
+        !encode_bf16_seq(&o128, o, B, L, cols, BM) || !encode_bf16_seq(&k64, k, B, L, cols, BT) ||
+        !encode_bf16_seq(&v64, v, B, L, cols, BT) || !encode_bf16_seq(&k128, k, B, L, cols, BM) ||
+        !encode_bf16_seq(&v128, v, B, L, cols, BM))
         return cudaErrorInvalidValue;
-    const size_t nvec = (size_t)B * H * a.Lp;
-    GCA_LAUNCH("swa_delta", st,
-               swa_delta_kernel<<<(unsigned)((nvec + 255) / 256), 256, 0, st>>>(
-                   static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse,
-                   B, L, H, a.Lp, lse2T, deltaT));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e;
 
-    a.n_items = B * a.nQT * H;
+    // pass A: items (b, h, query tile), 64-key tiles k0 .. k1 each
+    a.n_items = B * H * a.nQT;
+    a.slide = slide_safe(a.nQT, pa::NSLOT, [&](int qt, int& k0, int& k1) {
+        const int lo = qt * BM - W + 1;
+        k0 = (lo < 0 ? 0 : lo) / BT;
+        k1 = (qt * BM + BM - 1) / BT;
+    }) ? 1 : 0;
     int grid = a.n_items < sms ? a.n_items : sms;
     if ((e = cudaFuncSetAttribute(pa::swa_bwd_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   pa::SMEM)) != cudaSuccess)
         return e;
     GCA_LAUNCH("swa_bwd_q_tc", st,
-               pa::swa_bwd_q_kernel<<<grid, kThreads, pa::SMEM, st>>>(q128, do128, k64, v64, dq128, a));
+               pa::swa_bwd_q_kernel<<<grid, pa::kThreads, pa::SMEM, st>>>(q128, do128, o128, k64, v64, a));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    a.n_items = B * a.nKT * H;
+    // pass B: items (b, h, key tile), 128-query stages g0 .. g1 each
+    a.n_items = B * H * a.nKT;
+    a.slide = slide_safe(a.nKT, pb::NSLOT, [&](int kt, int& g0, int& g1) {
+        int last = kt * BM + BM - 1 + W - 1;
+        if (last > L - 1) last = L - 1;
+        g0 = kt;
+        g1 = last / BM;
+    }) ? 1 : 0;
     grid = a.n_items < sms ? a.n_items : sms;
     if ((e = cudaFuncSetAttribute(pb::swa_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   pb::SMEM)) != cudaSuccess)
         return e;
     GCA_LAUNCH("swa_bwd_kv_tc", st,
-               pb::swa_bwd_kv_kernel<<<grid, kThreads, pb::SMEM, st>>>(q64, do64, k128, v128, dk128,
-                                                                       dv128, a));
-    if ((e = cudaGetLastError()) == cudaSuccess) *launches += 3;
+               pb::swa_bwd_kv_kernel<<<grid, pb::kThreads, pb::SMEM, st>>>(q128, do128, k128, v128, a));
+    if ((e = cudaGetLastError()) == cudaSuccess) *launches += 2;
     return e;
 }
 

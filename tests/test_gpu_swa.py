@@ -114,9 +114,12 @@ def dout_like(q, seed):
     return torch.randn(q.shape, generator=g).to(torch.bfloat16)
 
 
+# (1, 3000, 1, 1000): a window so wide that consecutive query tiles cannot keep
+# their shared key tiles resident, so every tile loads its whole window
 @pytest.mark.parametrize("B,L,H,W", [(2, 384, 2, 512), (1, 1000, 3, 200), (2, 640, 2, 64),
                                      (1, 256, 1, 1), (1, 517, 2, 128), (1, 700, 2, 129),
-                                     (1, 1536, 4, 512), (3, 100, 1, 5000)])
+                                     (1, 1536, 4, 512), (3, 100, 1, 5000), (1, 3000, 1, 1000),
+                                     (2, 2304, 3, 512)])
 def test_bwd_every_element(B, L, H, W):
     q, k, v = qkv(B, L, H, 64, seed=B * 1000 + L + W)
     check_bwd(q, k, v, dout_like(q, 99), W)
