@@ -5,19 +5,24 @@
 // s = l_{c-1} . l_kappa (rebuttal "Cmt 1": Eq. 1 with one group; README "Model
 // Architecture": the landmark of chunk c-1 selects the chunks chunk c attends
 // to), i.e. one entry of the Gram matrix L L^T of a batch row's landmarks.
-// One CTA owns 128 consecutive landmark rows t (query chunks c = t + 1) and
-// computes their rows of the Gram matrix tile by tile: TMA stages 64-column
-// blocks of the row tile and of a 128-row candidate tile (128-byte swizzle),
-// one thread issues tcgen05.mma (M = 128, N = 128, bf16 products, fp32
-// accumulation: exact for integer landmarks with |s| < 2^24) into up to four
-// TMEM accumulators, and each of 128 epilogue threads owns one row t: it reads
-// the row's scores from TMEM and keeps a running top-k of them in registers
-// (four threads per row, each over a quarter of the columns; their lists are
-// merged at the end),
-// offered in ascending candidate order, so ties keep the lower chunk index
-// (score descending, then chunk ascending).  The softmax (vanilla or off by
-// one, rebuttal Q4) of the selected scores is computed by the same thread.
-// Nothing is written but idx / score / weight, so no workspace is needed.
+// A cluster of kCL CTAs owns 128 consecutive landmark rows t (query chunks
+// c = t + 1); CTA rank r of the cluster computes their Gram-matrix entries
+// against the r-th of kCL equal slices (a multiple of 16 candidates) of the
+// tile's candidate range, in candidate tiles of up to 128: TMA stages 64-column
+// blocks of the row tile and of the candidate tile (128-byte swizzle), one
+// thread issues tcgen05.mma (M = 128, N = the tile width, bf16 products, fp32
+// accumulation over the K blocks in order: exact for integer landmarks with
+// |s| < 2^24, and every entry is summed whole inside one CTA) into up to four
+// TMEM accumulators, and four epilogue threads per row t read the row's scores
+// from TMEM and keep running top-k lists in registers, offered in ascending
+// candidate order, so ties keep the lower chunk index (score descending, then
+// chunk ascending).  The four lists of a row are merged through shared memory;
+// then, after a cluster barrier, each CTA merges 128 / kCL rows' lists from all
+// kCL CTAs of the cluster (distributed shared memory: the slices are disjoint
+// and ordered) and computes the softmax (vanilla or off by one, rebuttal Q4)
+// of the selected scores.  A second cluster barrier keeps every CTA's lists in
+// place until all have been read.  Nothing is written but idx / score /
+// weight, so no workspace is needed.
 //
 // With a noise tensor (section 3.2: Gumbel noise added to the relevance
 // scores before the top-k selection) the selection key is
@@ -47,8 +52,33 @@ constexpr int kTile = kRows * kBlk * 2;          // one 128 x 64 bf16 tile, 16 K
 constexpr int kStageBytes = 2 * kTile;           // row tile block, then candidate tile block
 constexpr int kAcc = 4;                          // candidate tiles accumulated at once (4 x 128 TMEM columns)
 constexpr int kSmem = kStages * kStageBytes + 1024;
-// the epilogue's four lists per row (key, clean score, chunk) reuse the stages
-static_assert(3 * kRows * 4 * 16 * 4 <= kStages * kStageBytes, "list merge area");
+constexpr int kCL = 4;                           // CTAs per cluster = candidate slices per row tile (8 ran in two waves)
+// the epilogue's four lists per row (key, clean score, chunk) reuse the stages,
+// followed by the row's merged list that the cluster reads
+static_assert(3 * kRows * 5 * 16 * 4 + 3 * (kRows / kCL) * kCL * 16 * 4 <= kStages * kStageBytes,
+              "list merge area");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives, then waits: release/acquire
+// order the shared-memory lists written before it with the reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of this CTA's shared-memory word `p` in the shared memory of CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 struct __align__(8) GramBars {
     uint64_t full[kStages], empty[kStages];
@@ -115,10 +145,17 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                                              ~static_cast<uintptr_t>(1023));
     __shared__ GramBars sb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int R = blockIdx.x, b = blockIdx.y;
+    const int crank = static_cast<int>(cluster_rank());
+    const int R = blockIdx.x / kCL, b = blockIdx.y;
     const int row0 = R * kRows;
-    // candidate tiles 0 .. R hold every chunk below this tile's last row
-    const int ntile = R + 1;
+    // the tile's candidates are the chunks below its last row; this CTA takes the
+    // slice [c_lo, c_hi) in tiles of up to 128 candidates (tile j starts at c_lo + 128 j)
+    const int range = min((R + 1) * kRows, nC);
+    const int span = 16 * ((range + 16 * kCL - 1) / (16 * kCL));
+    const int c_lo = min(crank * span, range), c_hi = min(c_lo + span, range);
+    const int ntile = (c_hi - c_lo + kRows - 1) / kRows;
+    // MMA width of tile j: its candidates rounded up to 16 (columns past c_hi are ignored)
+    auto tile_n = [&](int j) { return min(kRows, (c_hi - c_lo - j * kRows + 15) & ~15); };
     const int nkb = D / kBlk;
     auto wait = [&](uint64_t* bar, uint32_t par) { return tcx::wait_bar(&sb.abort, bar, par, status); };
 
@@ -157,7 +194,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                         uint8_t* stg = sm + st.i * kStageBytes;
                         mbar_arrive_expect_tx(&sb.full[st.i], kStageBytes);
                         tma_load_3d(stg, &tl, &sb.full[st.i], kb * kBlk, row0, b);
-                        tma_load_3d(stg + kTile, &tl, &sb.full[st.i], kb * kBlk, (c0 + j) * kRows, b);
+                        tma_load_3d(stg + kTile, &tl, &sb.full[st.i], kb * kBlk, c_lo + (c0 + j) * kRows, b);
                         out[st.i] = true;
                         oph[st.i] = st.ph;
                         st.next(kStages);
@@ -170,7 +207,6 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
     } else if (warp == 1) {
         if (lane == 0) {
             tcx::Ring st{0, 0};
-            const uint32_t id = idesc_bf16(128, 128, false, false);
             bool ok = true, issued = false;
             int chunk = 0;
             for (int c0 = 0; c0 < ntile && ok; c0 += kAcc, ++chunk) {
@@ -183,6 +219,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                         if (!wait(&sb.full[st.i], st.ph)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t a = smem_u32(sm + st.i * kStageBytes);
+                        const uint32_t id = idesc_bf16(128, tile_n(c0 + j), false, false);
                         tcx::mma_kmajor_k64(tmem + j * 128, a, a + kTile, id, kb > 0 ? 1u : 0u);
                         mma_commit(&sb.empty[st.i]);
                         issued = true;
@@ -215,9 +252,10 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
             if (!wait(&sb.acc_full, full_par(chunk))) { ok = false; break; }
             tc_fence_after();
             for (int j = 0; j < nj; ++j) {
-                const int kap0 = (c0 + j) * kRows + 32 * cq;
+                const int kap0 = c_lo + (c0 + j) * kRows + 32 * cq;
 #pragma unroll 1
                 for (int q = 0; q < 2; ++q) {
+                    if (32 * cq + 16 * q >= tile_n(c0 + j)) break;     // warp-uniform: no such columns
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(tmem + lane_base + j * 128 + 32 * cq + 16 * q, v);
                     tmem_wait_ld();
@@ -230,8 +268,9 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                     for (int u = 0; u < 16; ++u) {
                         const int kap = k16 + u;
                         const float sc = __uint_as_float(v[u]);
-                        kvs[u] = (NOISY && kap < lim) ? __fadd_rn(__fmul_rn(sc, sscale), __ldg(nrow + kap)) : sc;
-                        if (kap < lim && (!tk.full || kvs[u] > tk.thr)) pend |= 1u << u;
+                        const bool in = kap < lim && kap < c_hi;
+                        kvs[u] = (NOISY && in) ? __fadd_rn(__fmul_rn(sc, sscale), __ldg(nrow + kap)) : sc;
+                        if (in && (!tk.full || kvs[u] > tk.thr)) pend |= 1u << u;
                     }
                     while (__any_sync(0xffffffffu, pend != 0u)) {
                         float ck = -INFINITY, cs = 0.f;     // a lane with nothing pending inserts a no-op
@@ -252,73 +291,149 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
             mbar_arrive(&sb.acc_empty);
         }
         // merge the four lists of each row through the stage memory (every product
-        // that read it has completed: the last accumulators were full)
+        // that read it has completed: the last accumulators were full), into the
+        // row's list that the other CTAs of the cluster read
         float* lk = reinterpret_cast<float*>(sm);                 // [128 rows][4][KCAP] keys
         float* ls = lk + kRows * 4 * KCAP;                         // clean scores
         int* li = reinterpret_cast<int*>(ls + kRows * 4 * KCAP);   // chunks
+        float* mk = reinterpret_cast<float*>(li + kRows * 4 * KCAP);   // [128 rows][KCAP] merged
+        float* ms = mk + kRows * KCAP;
+        int* mi = reinterpret_cast<int*>(ms + kRows * KCAP);
         const int base = (r * 4 + cq) * KCAP;
 #pragma unroll
         for (int p = 0; p < KCAP; ++p) { lk[base + p] = tk.key[p]; ls[base + p] = tk.s[p]; li[base + p] = tk.i[p]; }
         asm volatile("bar.sync 1, %0;" ::"r"(kEpi) : "memory");
-        if (cq == 0 && ok && t + 1 <= nC - 1) {
+        if (cq == 0) {
             // four sorted lists of disjoint candidates (entries past a list's end are
-            // -inf / no chunk): take the best head k times
+            // -inf / no chunk): take the best head KCAP times
             int h[4] = {0, 0, 0, 0};
             const int rb = r * 4 * KCAP;
-            RowTopk<KCAP> mg;
-            mg.init();
 #pragma unroll
             for (int j = 0; j < KCAP; ++j) {
-                if (j < topk) {
-                    int best = -1, bi = 0x7fffffff;
-                    float bk = -INFINITY, bs = 0.f;
+                int best = -1, bi = 0x7fffffff;
+                float bk = -INFINITY, bs = 0.f;
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const bool in = h[qq] < KCAP;
-                        const int at = rb + qq * KCAP + (in ? h[qq] : 0);
-                        const float kq = in ? lk[at] : -INFINITY;
-                        const int iq = in ? li[at] : 0x7fffffff;
-                        if (iq != 0x7fffffff && (best < 0 || kq > bk || (kq == bk && iq < bi))) {
-                            best = qq; bk = kq; bi = iq; bs = ls[at];
-                        }
+                for (int qq = 0; qq < 4; ++qq) {
+                    const bool in = h[qq] < KCAP;
+                    const int at = rb + qq * KCAP + (in ? h[qq] : 0);
+                    const float kq = in ? lk[at] : -INFINITY;
+                    const int iq = in ? li[at] : 0x7fffffff;
+                    if (iq != 0x7fffffff && (best < 0 || kq > bk || (kq == bk && iq < bi))) {
+                        best = qq; bk = kq; bi = iq; bs = ls[at];
                     }
-                    mg.key[j] = bk;
-                    mg.s[j] = bs;
-                    mg.i[j] = bi;
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) h[qq] += (best == qq) ? 1 : 0;
                 }
-            }
-            const size_t o = ((size_t)b * nC + t + 1) * topk;
-            const int m = lim < topk ? lim : topk;
-            float rr[KCAP];
-            float mx = -INFINITY;
+                mk[r * KCAP + j] = bk;
+                ms[r * KCAP + j] = bs;
+                mi[r * KCAP + j] = bi;
 #pragma unroll
-            for (int j = 0; j < KCAP; ++j) {
-                rr[j] = (j < m) ? mg.s[j] * sscale : -INFINITY;
-                mx = fmaxf(mx, rr[j]);
+                for (int qq = 0; qq < 4; ++qq) h[qq] += (best == qq) ? 1 : 0;
             }
-            if (off_by_one) mx = fmaxf(mx, 0.f);
-            float den = off_by_one ? expf(-mx) : 0.f;
-#pragma unroll
-            for (int j = 0; j < KCAP; ++j)
-                if (j < m) den += expf(rr[j] - mx);
-#pragma unroll
-            for (int j = 0; j < KCAP; ++j) {
-                if (j < topk) {
-                    const bool v = j < m;
-                    idx[o + j] = v ? mg.i[j] : -1;
-                    score[o + j] = v ? rr[j] : 0.f;
-                    weight[o + j] = v ? expf(rr[j] - mx) / den : 0.f;
-                }
-            }
-        }
-        if (R == 0 && r == 0 && cq == 0) {
-            // query chunk 0 has no earlier chunk to retrieve
-            const size_t o = (size_t)b * nC * topk;
-            for (int j = 0; j < topk; ++j) { idx[o + j] = -1; score[o + j] = 0.f; weight[o + j] = 0.f; }
         }
     }
+
+    // every thread of the cluster: the merged lists are complete
+    cluster_sync();
+    // rows kRowsPer crank .. of the tile (128 / kCL of them): warps 4-7 first copy
+    // the lists of the kCL CTAs into this CTA's shared memory (128 threads, one
+    // (row, CTA) list each, independent loads), then one thread per row merges them
+    constexpr int kRowsPer = kRows / kCL;
+    {
+        float* mk = reinterpret_cast<float*>(sm) + 3 * kRows * 4 * KCAP;
+        float* ms = mk + kRows * KCAP;
+        int* mi = reinterpret_cast<int*>(ms + kRows * KCAP);
+        // local copies [kRowsPer rows][kCL][KCAP] after this CTA's own lists (which the
+        // other CTAs may still be reading)
+        float* ck = reinterpret_cast<float*>(mi + kRows * KCAP);
+        float* cs = ck + kRowsPer * kCL * KCAP;
+        int* ci = reinterpret_cast<int*>(cs + kRowsPer * kCL * KCAP);
+        if (warp >= 4 && warp < 8) {
+            const int tid = threadIdx.x - 128;
+            const int rl = tid / kCL, q = tid % kCL;
+            const int at = (kRowsPer * crank + rl) * KCAP;
+            const uint32_t rk = map_rank(mk + at, q), rs = map_rank(ms + at, q), ri = map_rank(mi + at, q);
+            uint32_t vk[KCAP], vs[KCAP], vi[KCAP];
+#pragma unroll
+            for (int p = 0; p < KCAP; ++p) {
+                vk[p] = ld_cluster_u32(rk + 4 * p);
+                vs[p] = ld_cluster_u32(rs + 4 * p);
+                vi[p] = ld_cluster_u32(ri + 4 * p);
+            }
+            const int lb = (rl * kCL + q) * KCAP;
+#pragma unroll
+            for (int p = 0; p < KCAP; ++p) {
+                ck[lb + p] = __uint_as_float(vk[p]);
+                cs[lb + p] = __uint_as_float(vs[p]);
+                ci[lb + p] = static_cast<int>(vi[p]);
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+        }
+        if (warp == 4 && lane < kRowsPer) {
+            const int r = kRowsPer * crank + lane;
+            const int t = row0 + r;
+            if (t + 1 <= nC - 1) {
+                const int lim = include_self ? t + 1 : t;
+                int h[kCL];
+#pragma unroll
+                for (int q = 0; q < kCL; ++q) h[q] = 0;
+                RowTopk<KCAP> mg;
+                mg.init();
+                const int rb = lane * kCL * KCAP;
+#pragma unroll
+                for (int j = 0; j < KCAP; ++j) {
+                    if (j < topk) {
+                        // the CTAs' candidate slices are in rank order: equal keys keep the lower chunk
+                        int best = -1, bi = 0x7fffffff;
+                        float bk = -INFINITY, bs = 0.f;
+#pragma unroll
+                        for (int q = 0; q < kCL; ++q) {
+                            const bool in = h[q] < KCAP;
+                            const int at = rb + q * KCAP + (in ? h[q] : 0);
+                            const int iq = in ? ci[at] : 0x7fffffff;
+                            const float kq = in ? ck[at] : -INFINITY;
+                            if (iq != 0x7fffffff && (best < 0 || kq > bk || (kq == bk && iq < bi))) {
+                                best = q; bk = kq; bi = iq; bs = cs[at];
+                            }
+                        }
+                        mg.key[j] = bk;
+                        mg.s[j] = bs;
+                        mg.i[j] = bi;
+#pragma unroll
+                        for (int q = 0; q < kCL; ++q) h[q] += (best == q) ? 1 : 0;
+                    }
+                }
+                const size_t o = ((size_t)b * nC + t + 1) * topk;
+                const int m = lim < topk ? lim : topk;
+                float rr[KCAP];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < KCAP; ++j) {
+                    rr[j] = (j < m) ? mg.s[j] * sscale : -INFINITY;
+                    mx = fmaxf(mx, rr[j]);
+                }
+                if (off_by_one) mx = fmaxf(mx, 0.f);
+                float den = off_by_one ? expf(-mx) : 0.f;
+#pragma unroll
+                for (int j = 0; j < KCAP; ++j)
+                    if (j < m) den += expf(rr[j] - mx);
+#pragma unroll
+                for (int j = 0; j < KCAP; ++j) {
+                    if (j < topk) {
+                        const bool v = j < m;
+                        idx[o + j] = v ? mg.i[j] : -1;
+                        score[o + j] = v ? rr[j] : 0.f;
+                        weight[o + j] = v ? expf(rr[j] - mx) / den : 0.f;
+                    }
+                }
+            }
+            if (R == 0 && crank == 0 && lane == 0) {
+                // query chunk 0 has no earlier chunk to retrieve
+                const size_t o = (size_t)b * nC * topk;
+                for (int j = 0; j < topk; ++j) { idx[o + j] = -1; score[o + j] = 0.f; weight[o + j] = 0.f; }
+            }
+        }
+    }
+    // no CTA leaves while another may still read its lists
+    cluster_sync();
 
     tc_fence_before();
     __syncthreads();
@@ -334,25 +449,31 @@ cudaError_t launch_k(const Shape& sp, const CUtensorMap& tl, const float* noise,
     auto kern = score_topk_tc_kernel<KCAP, NOISY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((sp.nQ + kRows - 1) / kRows, sp.B);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCL * ((sp.nQ + kRows - 1) / kRows), sp.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     GCA_LAUNCH(NOISY ? "score_topk_noisy" : "score_topk", st,
-               kern<<<grid, kThreads, kSmem, st>>>(tl, noise, sp.nQ, sp.D, sp.topk, sp.include_self,
-                                                  sp.off_by_one, sp.score_scale, idx, score, weight,
-                                                  status));
+               e = cudaLaunchKernelEx(&cfg, kern, tl, noise, sp.nQ, sp.D, sp.topk, sp.include_self,
+                                      sp.off_by_one, sp.score_scale, idx, score, weight, status));
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// k <= 16 (the four lists per row live in registers; larger k runs the SIMT
-// scorer).  One CTA per 128-row tile takes about the same time however many
-// tiles there are (the per-row selection paces it), while the SIMT scorer's
-// time grows with the rows, so this path is taken from 16 tiles on (where it
-// measured faster: 0.064 against 0.077 ms at 8 x 256 chunks x 768).
+// bf16 landmarks with D a multiple of 64 and k <= 16 (the lists per row live in
+// registers; larger k runs the SIMT scorer).
 bool score_topk_tc_supported(const Shape& sp) {
-    const int tiles = sp.B * ((sp.nQ + kRows - 1) / kRows);
-    return sp.dtype == GCA_BF16 && sp.D % kBlk == 0 && sp.D <= 8192 && sp.nQ >= 2 && sp.topk <= 16 &&
-           tiles >= 16;
+    return sp.dtype == GCA_BF16 && sp.D % kBlk == 0 && sp.D <= 8192 && sp.nQ >= 2 && sp.topk <= 16;
 }
 
 cudaError_t launch_score_topk_tc(const Shape& sp, const void* lm, const float* noise, int32_t* idx,
