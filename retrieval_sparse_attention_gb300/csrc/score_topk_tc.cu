@@ -91,46 +91,83 @@ struct __align__(8) GramBars {
 __device__ __forceinline__ uint32_t full_par(int k) { return static_cast<uint32_t>(k) & 1u; }
 __device__ __forceinline__ uint32_t empty_par(int k) { return (static_cast<uint32_t>(k) & 1u) ^ 1u; }
 
-// Running top-k of one thread, sorted by (key descending, chunk ascending);
-// candidates arrive in ascending chunk order, so a candidate whose key equals
-// the k-th key ranks after it and is rejected.
-template <int KCAP>
+// Element of a candidate list: selection key, clean score (differs from the key
+// only with noise), chunk.  Lists are sorted by (key descending, chunk
+// ascending); an empty entry is (-inf, 0, 0x7fffffff) and ranks last.
+struct Cand {
+    float k, s;
+    int i;
+};
+__device__ __forceinline__ bool ranks_first(const Cand& a, const Cand& b) {
+    return a.k > b.k || (a.k == b.k && a.i < b.i);
+}
+// Compare-exchange: afterwards a ranks first.  Branch-free selects, so every
+// lane runs the same instructions and the networks below have no data-dependent
+// control flow.
+template <bool WITH_S>
+__device__ __forceinline__ void cex(Cand& a, Cand& b) {
+    const bool sw = ranks_first(b, a);
+    const Cand t = a;
+    a.k = sw ? b.k : a.k;
+    a.i = sw ? b.i : a.i;
+    b.k = sw ? t.k : b.k;
+    b.i = sw ? t.i : b.i;
+    if (WITH_S) {
+        a.s = sw ? b.s : a.s;
+        b.s = sw ? t.s : b.s;
+    }
+}
+// Bitonic sort of N (a power of two) elements into rank order.
+template <int N, bool WITH_S>
+__device__ __forceinline__ void bitonic_sort(Cand (&c)[N]) {
+#pragma unroll
+    for (int k = 2; k <= N; k *= 2)
+#pragma unroll
+        for (int j = k / 2; j > 0; j /= 2)
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    if ((i & k) == 0) cex<WITH_S>(c[i], c[l]);
+                    else cex<WITH_S>(c[l], c[i]);
+                }
+            }
+}
+// Bitonic sequence of N elements -> rank order.
+template <int N, bool WITH_S>
+__device__ __forceinline__ void bitonic_clean(Cand (&c)[N]) {
+#pragma unroll
+    for (int j = N / 2; j > 0; j /= 2)
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int l = i ^ j;
+            if (l > i) cex<WITH_S>(c[i], c[l]);
+        }
+}
+
+// Running top-KCAP of one thread (KCAP >= the call's k, so the first k entries
+// are its top-k).  A chunk of 16 (or 8) candidates is sorted by a bitonic
+// network and merged: the better of list[i] and chunk[KCAP - 1 - i] for every i is exactly
+// the top KCAP of the union, as a bitonic sequence, which a half-cleaner cascade
+// puts in order.  No insertion chain, no run-time index into the list (which
+// would move it out of registers).
+template <int KCAP, bool WITH_S>
 struct RowTopk {
-    float key[KCAP];       // selection key (the score, or the noisy key)
-    float s[KCAP];         // clean score
-    int i[KCAP];
-    float thr;             // key of rank topk - 1
-    bool full;             // topk entries held
+    Cand e[KCAP];
     __device__ __forceinline__ void init() {
 #pragma unroll
-        for (int p = 0; p < KCAP; ++p) { key[p] = -INFINITY; s[p] = 0.f; i[p] = 0x7fffffff; }
-        thr = -INFINITY;
-        full = false;
+        for (int p = 0; p < KCAP; ++p) e[p] = Cand{-INFINITY, 0.f, 0x7fffffff};
     }
-    // Insert (kv, sc, ix); kv = -inf with ix = 0x7fffffff is a no-op.  Branch-free,
-    // so the lanes of a warp insert in lock step.
-    __device__ __forceinline__ void insert(int topk, float kv, float sc, int ix) {
-        // one insertion pass: the carried entry swaps with every entry it ranks before
-        float ck = kv, cs = sc;
-        int ci = ix;
+    // merge N (8 or 16) candidates; with N < KCAP the chunk is padded with empty
+    // entries, which never win, so only its N real entries are compared
+    template <int N>
+    __device__ __forceinline__ void merge(Cand (&c)[N]) {
+        bitonic_sort<N, WITH_S>(c);
 #pragma unroll
-        for (int p = 0; p < KCAP; ++p) {
-            if (p < topk) {
-                const bool before = ck > key[p] || (ck == key[p] && ci < i[p]);
-                const float tk = key[p], ts = s[p];
-                const int ti = i[p];
-                key[p] = before ? ck : tk;
-                s[p] = before ? cs : ts;
-                i[p] = before ? ci : ti;
-                ck = before ? tk : ck;
-                cs = before ? ts : cs;
-                ci = before ? ti : ci;
-            }
-            if (p == topk - 1) {
-                thr = key[p];
-                full = i[p] != 0x7fffffff;
-            }
-        }
+        for (int p = 0; p < KCAP; ++p)
+            if (KCAP - 1 - p < N && ranks_first(c[KCAP - 1 - p < N ? KCAP - 1 - p : 0], e[p]))
+                e[p] = c[KCAP - 1 - p < N ? KCAP - 1 - p : 0];
+        bitonic_clean<KCAP, WITH_S>(e);
     }
 };
 
@@ -243,7 +280,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
         // candidates kappa < t (kappa <= t with include_self) for c = t + 1 <= nC - 1
         const int lim = (t + 1 <= nC - 1) ? (include_self ? t + 1 : t) : 0;
         const float* nrow = NOISY ? noise + ((size_t)b * nC + (t + 1 < nC ? t + 1 : 0)) * nC : nullptr;
-        RowTopk<KCAP> tk;
+        RowTopk<KCAP, NOISY> tk;
         tk.init();
         bool ok = true;
         int chunk = 0;
@@ -260,30 +297,25 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                     tmem_ld_32x32b_x16(tmem + lane_base + j * 128 + 32 * cq + 16 * q, v);
                     tmem_wait_ld();
                     const int k16 = kap0 + 16 * q;
-                    // the candidates of these 16 columns that beat this thread's current
-                    // k-th key, then one insertion per warp iteration in lock step
-                    float kvs[16];
-                    unsigned pend = 0;
+                    // the candidates of these columns in chunks of CW (invalid ones rank
+                    // last); skip a chunk when no lane has one that beats its list's last
+                    // entry.  k <= 16 with noise merges halves of 8: 16 + 16 entries of
+                    // three fields would not fit the registers.
+                    constexpr int CW = (KCAP == 16 && NOISY) ? 8 : 16;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int kap = k16 + u;
-                        const float sc = __uint_as_float(v[u]);
-                        const bool in = kap < lim && kap < c_hi;
-                        kvs[u] = (NOISY && in) ? __fadd_rn(__fmul_rn(sc, sscale), __ldg(nrow + kap)) : sc;
-                        if (in && (!tk.full || kvs[u] > tk.thr)) pend |= 1u << u;
-                    }
-                    while (__any_sync(0xffffffffu, pend != 0u)) {
-                        float ck = -INFINITY, cs = 0.f;     // a lane with nothing pending inserts a no-op
-                        int ci = 0x7fffffff;
-                        if (pend) {
-                            const int u0 = __ffs(pend) - 1;
-                            pend &= pend - 1u;
+                    for (int h0 = 0; h0 < 16; h0 += CW) {
+                        Cand c[CW];
+                        bool any = false;
 #pragma unroll
-                            for (int u = 0; u < 16; ++u)
-                                if (u == u0) { ck = kvs[u]; cs = __uint_as_float(v[u]); }
-                            ci = k16 + u0;
+                        for (int u = 0; u < CW; ++u) {
+                            const int kap = k16 + h0 + u;
+                            const float sc = __uint_as_float(v[h0 + u]);
+                            const bool in = kap < lim && kap < c_hi;
+                            const float kv = (NOISY && in) ? __fadd_rn(__fmul_rn(sc, sscale), __ldg(nrow + kap)) : sc;
+                            c[u] = in ? Cand{kv, sc, kap} : Cand{-INFINITY, 0.f, 0x7fffffff};
+                            any = any || (in && ranks_first(c[u], tk.e[KCAP - 1]));
                         }
-                        tk.insert(topk, ck, cs, ci);
+                        if (__any_sync(0xffffffffu, any)) tk.template merge<CW>(c);
                     }
                 }
             }
@@ -301,7 +333,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
         int* mi = reinterpret_cast<int*>(ms + kRows * KCAP);
         const int base = (r * 4 + cq) * KCAP;
 #pragma unroll
-        for (int p = 0; p < KCAP; ++p) { lk[base + p] = tk.key[p]; ls[base + p] = tk.s[p]; li[base + p] = tk.i[p]; }
+        for (int p = 0; p < KCAP; ++p) { lk[base + p] = tk.e[p].k; ls[base + p] = NOISY ? tk.e[p].s : tk.e[p].k; li[base + p] = tk.e[p].i; }
         asm volatile("bar.sync 1, %0;" ::"r"(kEpi) : "memory");
         if (cq == 0) {
             // four sorted lists of disjoint candidates (entries past a list's end are
@@ -375,8 +407,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                 int h[kCL];
 #pragma unroll
                 for (int q = 0; q < kCL; ++q) h[q] = 0;
-                RowTopk<KCAP> mg;
-                mg.init();
+                Cand mg[KCAP];
                 const int rb = lane * kCL * KCAP;
 #pragma unroll
                 for (int j = 0; j < KCAP; ++j) {
@@ -394,9 +425,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                                 best = q; bk = kq; bi = iq; bs = cs[at];
                             }
                         }
-                        mg.key[j] = bk;
-                        mg.s[j] = bs;
-                        mg.i[j] = bi;
+                        mg[j] = Cand{bk, bs, bi};
 #pragma unroll
                         for (int q = 0; q < kCL; ++q) h[q] += (best == q) ? 1 : 0;
                     }
@@ -407,7 +436,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                 float mx = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < KCAP; ++j) {
-                    rr[j] = (j < m) ? mg.s[j] * sscale : -INFINITY;
+                    rr[j] = (j < m) ? mg[j].s * sscale : -INFINITY;
                     mx = fmaxf(mx, rr[j]);
                 }
                 if (off_by_one) mx = fmaxf(mx, 0.f);
@@ -419,7 +448,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
                 for (int j = 0; j < KCAP; ++j) {
                     if (j < topk) {
                         const bool v = j < m;
-                        idx[o + j] = v ? mg.i[j] : -1;
+                        idx[o + j] = v ? mg[j].i : -1;
                         score[o + j] = v ? rr[j] : 0.f;
                         weight[o + j] = v ? expf(rr[j] - mx) / den : 0.f;
                     }
