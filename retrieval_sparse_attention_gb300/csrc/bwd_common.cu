@@ -248,11 +248,14 @@ cudaError_t launch_inverse_index_to(const Shape& s, const int32_t* idx, int* cou
                                     int* entry, const float* w, float* entry_w, cudaStream_t st,
                                     int* launches) {
     const int nE = s.nQ * s.topk;
-    // one CTA per row while its staging fits shared memory: 32 warps' count rows for
-    // up to 512 chunks, 8 for more
+    // one CTA per row while its staging fits shared memory (a CTA may use 227 KB):
+    // 32 warps' count rows for up to 512 chunks, 8 for more (16 measured slower at
+    // 1024 chunks: the per-chunk prefix over the warps grows with them).  The
+    // three-pass fallback scans the whole row once per chunk, so it is only for
+    // rows that do not fit.
     const int nw = s.nP <= 512 ? 32 : 8;
     const size_t smem = sizeof(int) * (2 * (size_t)nE + (size_t)s.nP + 1 + (size_t)nw * s.nP);
-    if (smem <= 160 * 1024) {
+    if (smem <= 220 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(inv_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;

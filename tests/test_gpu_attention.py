@@ -170,3 +170,58 @@ def test_out_of_range_index_sets_status():
     api.fwd(q, k, v, idx, w, S=64)
     assert api.gca_get_status() == 6      # GCA_ERR_DEVICE_INDEX
     assert api.gca_get_status() == 0      # reading clears it
+
+
+def test_long_row_inverse_index_fallback():
+    # 4096 chunks x k = 8 in one batch row: the row's inverse index (count, offset
+    # and entry arrays, ~400 KB) does not fit one CTA's shared memory, so the
+    # backward builds it in three passes.  Caller-supplied retrieval: each query
+    # chunk c >= 1 takes k distinct random earlier chunks, weights a softmax.
+    S, nC, H, d, k = 64, 4096, 1, 64, 8
+    L = nC * S
+    g = torch.Generator().manual_seed(21)
+    q, kk, v, dout = [(torch.randn(1, L, H, d, generator=g) * s).to(torch.bfloat16)
+                      for s in (0.125, 0.125, 0.125, 1.0)]
+    rng = np.random.default_rng(22)
+    idx = np.full((1, nC, k), -1, np.int32)
+    for c in range(1, nC):
+        m = min(k, c)
+        idx[0, c, :m] = np.sort(rng.choice(c, m, replace=False))
+    raw = rng.standard_normal((1, nC, k))
+    w = np.where(idx >= 0, np.exp(raw), 0.0)
+    w = (w / np.maximum(w.sum(-1, keepdims=True), 1e-30)).astype(np.float32)
+    dev = "cuda"
+    ti, tw = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
+    qc, kc, vc, gc = (x.to(dev) for x in (q, kk, v, dout))
+    o, lse = api.fwd(qc, kc, vc, ti, tw, S=S)
+    dq, dk, dv, ds = api.bwd(qc, kc, vc, ti, tw, lse, gc, S=S)
+    torch.cuda.synchronize()
+    assert api.gca_get_status() == 0
+    atol, rtol = tol_for(torch.bfloat16)
+    w64 = w.astype(np.float64)
+    # key side: the most retrieved chunk, the last (never retrieved) and random ones
+    counts = np.bincount(idx[0][idx[0] >= 0].ravel(), minlength=nC)
+    for kap in [int(np.argmax(counts)), nC - 1] + [int(x) for x in rng.integers(0, nC - 1, 3)]:
+        users = [c for c in range(nC) if (idx[0, c] == kap).any()]
+        k_ = take_chunks(kk, 0, [kap], S)
+        v_ = take_chunks(v, 0, [kap], S)
+        if not users:
+            want_k, want_v = np.zeros_like(k_), np.zeros_like(v_)
+        else:
+            rows_k = np.where(idx[0, users] == kap, 0, -1).astype(np.int32)
+            _, want_k, want_v, _ = oracle.bwd(take_chunks(q, 0, users, S), k_, v_, rows_k[None],
+                                              w64[0, users][None], take_chunks(dout, 0, users, S), S,
+                                              qmask=np.zeros((1, len(users)), bool))
+        assert_close("dk[chunk=%d]" % kap, f64(dk[0, kap * S:(kap + 1) * S])[None], want_k, atol, rtol)
+        assert_close("dv[chunk=%d]" % kap, f64(dv[0, kap * S:(kap + 1) * S])[None], want_v, atol, rtol)
+    # query side: a few chunks
+    cs = sorted(set([1, 2, nC - 1] + [int(x) for x in rng.integers(1, nC, 3)]))
+    pool, rows = mini_problem(idx[0], cs, S)
+    q_ = take_chunks(q, 0, cs, S)
+    k_ = take_chunks(kk, 0, pool, S)
+    v_ = take_chunks(v, 0, pool, S)
+    g_ = take_chunks(dout, 0, cs, S)
+    want_dq, _, _, want_ds = oracle.bwd(q_, k_, v_, rows[None], w64[0, cs][None], g_, S,
+                                        kmask=np.zeros((1, len(pool)), bool))
+    assert_close("dq", take_chunks(dq, 0, cs, S), want_dq, atol, rtol)
+    assert_close("dscore", f64(ds[0, cs])[None], want_ds, atol, rtol)
