@@ -52,11 +52,9 @@ constexpr int kTile = kRows * kBlk * 2;          // one 128 x 64 bf16 tile, 16 K
 constexpr int kStageBytes = 2 * kTile;           // row tile block, then candidate tile block
 constexpr int kAcc = 4;                          // candidate tiles accumulated at once (4 x 128 TMEM columns)
 constexpr int kSmem = kStages * kStageBytes + 1024;
-constexpr int kCL = 4;                           // CTAs per cluster = candidate slices per row tile (8 ran in two waves)
 // the epilogue's four lists per row (key, clean score, chunk) reuse the stages,
 // followed by the row's merged list that the cluster reads
-static_assert(3 * kRows * 5 * 16 * 4 + 3 * (kRows / kCL) * kCL * 16 * 4 <= kStages * kStageBytes,
-              "list merge area");
+static_assert(3 * kRows * 5 * 16 * 4 + 3 * kRows * 16 * 4 <= kStages * kStageBytes, "list merge area");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -171,7 +169,8 @@ struct RowTopk {
     }
 };
 
-template <int KCAP, bool NOISY>
+// kCL = CTAs per cluster = candidate slices per row tile (4 or 8)
+template <int KCAP, bool NOISY, int kCL>
 __global__ void __launch_bounds__(kThreads, 1)
 score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __restrict__ noise, int nC,
                      int D, int topk, int include_self, int off_by_one, float sscale,
@@ -472,20 +471,20 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap tl, const float* __rest
     }
 }
 
-template <int KCAP, bool NOISY>
-cudaError_t launch_k(const Shape& sp, const CUtensorMap& tl, const float* noise, int32_t* idx,
-                     float* score, float* weight, int* status, cudaStream_t st) {
-    auto kern = score_topk_tc_kernel<KCAP, NOISY>;
+template <int KCAP, bool NOISY, int CL>
+cudaError_t launch_cl(const Shape& sp, const CUtensorMap& tl, const float* noise, int32_t* idx,
+                      float* score, float* weight, int* status, cudaStream_t st) {
+    auto kern = score_topk_tc_kernel<KCAP, NOISY, CL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCL * ((sp.nQ + kRows - 1) / kRows), sp.B);
+    cfg.gridDim = dim3(CL * ((sp.nQ + kRows - 1) / kRows), sp.B);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCL;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -495,6 +494,16 @@ cudaError_t launch_k(const Shape& sp, const CUtensorMap& tl, const float* noise,
                                       sp.off_by_one, sp.score_scale, idx, score, weight, status));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Clusters of 8 while the whole grid stays within 64 CTAs (measured: 128 CTAs in
+// clusters of 8 ran in two waves, slower than 64 in clusters of 4), else 4.
+template <int KCAP, bool NOISY>
+cudaError_t launch_k(const Shape& sp, const CUtensorMap& tl, const float* noise, int32_t* idx,
+                     float* score, float* weight, int* status, cudaStream_t st) {
+    const int tiles = sp.B * ((sp.nQ + kRows - 1) / kRows);
+    if (tiles * 8 <= 64) return launch_cl<KCAP, NOISY, 8>(sp, tl, noise, idx, score, weight, status, st);
+    return launch_cl<KCAP, NOISY, 4>(sp, tl, noise, idx, score, weight, status, st);
 }
 
 }  // namespace
