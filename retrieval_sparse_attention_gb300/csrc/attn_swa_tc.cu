@@ -360,31 +360,38 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             if (have) {
                 if (!wwait(&sb.s_full[wg], full_par(ts))) break;
                 tc_fence_after();
+                float mt;                               // the tile's row max of s
                 {
+                    // the loads return each 16-column chunk's max as well
                     uint32_t r[8][16];
+                    float mc[8];
 #pragma unroll
-                    for (int ci = 0; ci < 8; ++ci) tmem_ld_32x32b_x16(ts_addr + 16 * ci, r[ci]);
+                    for (int ci = 0; ci < 8; ++ci) mc[ci] = tmem_ld_max_32x32b_x16(ts_addr + 16 * ci, r[ci]);
                     tmem_wait_ld();
 #pragma unroll
                     for (int ci = 0; ci < 8; ++ci)
 #pragma unroll
                         for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[ci][u]);
+                    mt = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
+                               fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
                 }
                 tc_fence_before();
                 mbar_arrive(&sb.s_empty[wg]);           // S is in registers: the buffer is free
                 if (tile_masked(a, it, j)) {
                     // row t sees the keys t - W + 1 .. t: columns c_lo .. c_lo + W - 1
-                    // (a select per column; a conditional store here becomes a branch)
+                    // (a select per column; a conditional store here becomes a branch);
+                    // the max is then taken again over the visible columns
                     const int c_lo = it.qt * BM + row - a.W + 1 - (it.k0 + j) * BN;
                     const uint32_t span = static_cast<uint32_t>(a.W - 1);
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
                         x[i] = static_cast<uint32_t>(i - c_lo) > span ? -INFINITY : x[i];
-                }
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
-                const float mts = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl;
+                    for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                }
+                const float mts = mt * sl;
                 if (mts > m + kRescaleLog2) {
                     if (m != -INFINITY) {
                         resc = true;

@@ -207,6 +207,21 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
+// tmem_ld_32x32b_x16 that also returns the maximum of the 16 loaded fp32 values of
+// the thread's lane (tcgen05.ld.red, an sm_103a instruction); -inf columns take
+// part like any other value.  Complete with tmem_wait_ld before using either result.
+__device__ __forceinline__ float tmem_ld_max_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    float m;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(m)
+        : "r"(taddr));
+    return m;
+}
+
 // Store counterpart of tmem_ld_32x32b_x16: thread i writes lane (taddr.lane + i),
 // columns taddr.col .. +15.  Complete with tmem_wait_st before the data is used.
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
