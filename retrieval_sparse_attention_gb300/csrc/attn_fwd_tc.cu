@@ -412,14 +412,38 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_after();
                 float x[C::VALS];
                 const uint32_t taddr = tmem + lane_base + C::COL_S + sbuf * 128;
-                if (S == 64) {
+                float mx, l;
+                if constexpr (S == 64) {
+                    // the loads return each 16-column chunk's max as well
+                    float mc[4];
 #pragma unroll
-                    for (int ci = 0; ci < C::VALS / 16; ++ci) {
+                    for (int ci = 0; ci < 4; ++ci) {
                         uint32_t r[16];
-                        tmem_ld_16x32bx2_x16<64>(taddr + 16 * ci, r);
+                        mc[ci] = tmem_ld_max_16x32bx2_x16<64>(taddr + 16 * ci, r);
 #pragma unroll
                         for (int t = 0; t < 16; ++t) x[16 * ci + t] = __uint_as_float(r[t]);
                     }
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&sb.s_empty[sbuf]);
+                    // exponentials and the row sum on column pairs (packed f32x2 FMA and
+                    // add), four sum chains combined in a fixed order
+                    mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+                    const float mb = mx * a.scale_log2;
+                    const uint64_t sl2 = tcx::f2_pack(a.scale_log2, a.scale_log2), nmb2 = tcx::f2_pack(-mb, -mb);
+                    uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        float y0, y1;
+                        tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(x[2 * c], x[2 * c + 1]), sl2, nmb2), y0, y1);
+                        x[2 * c] = fast_exp2(y0);
+                        x[2 * c + 1] = fast_exp2(y1);
+                        acc2[c & 3] = tcx::fadd2(acc2[c & 3], tcx::f2_pack(x[2 * c], x[2 * c + 1]));
+                    }
+                    float l8[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) tcx::f2_unpack(acc2[u], l8[2 * u], l8[2 * u + 1]);
+                    l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
                 } else {
 #pragma unroll
                     for (int ci = 0; ci < C::VALS / 16; ++ci) {
@@ -428,15 +452,8 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                         for (int t = 0; t < 16; ++t) x[16 * ci + t] = __uint_as_float(r[t]);
                     }
-                }
-                tmem_wait_ld();
-                if constexpr (!C::TP) {
-                    tc_fence_before();
-                    mbar_arrive(&sb.s_empty[sbuf]);
-                }
-                // row max and row sum (S = 128: eight independent chains, combined in a fixed order)
-                float mx, l;
-                if constexpr (S == 128) {
+                    tmem_wait_ld();
+                    // row max and row sum: eight independent chains, combined in a fixed order
                     float m8[8], l8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) m8[i] = x[i];
@@ -453,20 +470,10 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         l8[i & 7] += x[i];
                     }
                     l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-                } else {
-                    mx = -INFINITY;
-#pragma unroll
-                    for (int i = 0; i < C::VALS; ++i) mx = fmaxf(mx, x[i]);
-                    const float mb = mx * a.scale_log2;
-                    l = 0.f;
-#pragma unroll
-                    for (int i = 0; i < C::VALS; ++i) {
-                        x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -mb));
-                        l += x[i];
-                    }
                 }
                 const float mb = mx * a.scale_log2;
                 const float coef = active ? wj / l : 0.f;
+                const uint64_t coef2 = tcx::f2_pack(coef, coef);
                 if (active && lrow) lrow[j] = (mb + log2f(l)) * kLn2;
                 if constexpr (C::TP) {
                     // P over the first 64 columns of this row's S buffer, two keys per column
@@ -489,7 +496,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             const int blk = (S == 64) ? u : (ch >> 3);
                             const int cc = ch & 7;
                             *reinterpret_cast<uint4*>(pbase + blk * C::P_BLOCK + ((cc ^ (row & 7)) << 4)) =
-                                tcx::pack8(x + 8 * ch, coef);
+                                tcx::pack8x2(x + 8 * ch, coef2);
                         }
                     }
                     fence_proxy_async_smem();

@@ -77,6 +77,12 @@ __device__ __forceinline__ uint4 pack8(const float* x, float s) {
                       pack_bf16(x[4] * s, x[5] * s), pack_bf16(x[6] * s, x[7] * s));
 }
 
+// pack8 with the scaling on column pairs (packed f32x2 multiply; the same roundings)
+__device__ __forceinline__ uint4 pack8x2(const float* x, uint64_t s2) {
+    return make_uint4(pack_bf16x2(fmul2(f2_pack(x[0], x[1]), s2)), pack_bf16x2(fmul2(f2_pack(x[2], x[3]), s2)),
+                      pack_bf16x2(fmul2(f2_pack(x[4], x[5]), s2)), pack_bf16x2(fmul2(f2_pack(x[6], x[7]), s2)));
+}
+
 __device__ __forceinline__ uint4 pack8u(const uint32_t* r) {
     return make_uint4(pack_bf16(__uint_as_float(r[0]), __uint_as_float(r[1])),
                       pack_bf16(__uint_as_float(r[2]), __uint_as_float(r[3])),

@@ -248,6 +248,21 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&
         : "r"(taddr), "n"(HALF_OFF));
 }
 
+// tmem_ld_16x32bx2_x16 that also returns the maximum of the thread's 16 loaded
+// fp32 values (tcgen05.ld.red, an sm_103a instruction).  Complete with tmem_wait_ld.
+template <int HALF_OFF>
+__device__ __forceinline__ float tmem_ld_max_16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    float m;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x16.max.f32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17], %18;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(m)
+        : "r"(taddr), "n"(HALF_OFF));
+    return m;
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (sm_100 format): start address, leading and
 // stride byte offsets (16-byte units), fixed version field 1 at bit 46, and
