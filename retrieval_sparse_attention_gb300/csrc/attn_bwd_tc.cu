@@ -37,7 +37,7 @@
 // d = 32 one 32-column tile (64-byte swizzle); products contract over every
 // sub-tile and products with N = d issue one product per sub-tile.  Stage
 // counts, item buffers and the number of dK/dV accumulators are chosen per
-// (S, d) to fit shared memory and the 512 TMEM columns; at d = 128 the S = 64
+// (S, d) to fit shared memory and the 512 TMEM columns; at d = 64 and 128 the S = 64
 // key-major pass shares one operand pair between its math warpgroups.
 #include <math.h>
 
@@ -1005,17 +1005,20 @@ gca_bwd_kv128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 // the accumulation products read as MN-major A operands:
 // dK += dA^T [Q_1; Q_2] and dV += (w P)^T [dO_1; dO_2] over K = 128 queries
 // (64 for a single entry).
-template <int DH>
+template <int DH, bool SHARE>
 struct CfgP {
     using G = tcx::HeadGeom<DH>;
     static constexpr int S = 64;
     static constexpr int TILE = G::tile_bytes(64);        // 64 rows x DH bf16
     static constexpr int ITEM_BYTES = 2 * TILE;           // K then V
     // what fits: d = 128 keeps one K/V item buffer and one operand pair shared
-    // by both math warpgroups, and a single dK/dV accumulator in TMEM
+    // by both math warpgroups, and a single dK/dV accumulator in TMEM; at d = 64
+    // (SHARE) a shared operand pair buys a second K/V item buffer, which hides
+    // the K/V load at item boundaries: worth more than private pairs when items
+    // hold few entries
     static constexpr int STAGES = DH == 32 ? 4 : (DH == 64 ? 4 : 2);
-    static constexpr int IBUF = DH == 32 ? 2 : 1;
-    static constexpr bool SHARED_P = DH == 128;
+    static constexpr int IBUF = DH == 32 || (DH == 64 && SHARE) ? 2 : 1;
+    static constexpr bool SHARED_P = DH == 128 || (DH == 64 && SHARE);
     static constexpr int NACC = DH == 128 ? 1 : 2;
     // Q of entries 0 and 1: sub-tile s holds rows 0-63 (entry 0) then 64-127
     // (entry 1), so [Q_1; Q_2] is one 128-row operand per sub-tile
@@ -1037,12 +1040,12 @@ struct CfgP {
     static_assert(STAGES <= 6, "barrier arrays");
 };
 
-template <int DH>
+template <int DH, bool SHARE>
 __global__ void __launch_bounds__(kThreadsA, 1)
 gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const BwdArgs a) {
-    using C = CfgP<DH>;
+    using C = CfgP<DH, SHARE>;
     using HG = tcx::HeadGeom<DH>;
     constexpr int S = C::S;
     extern __shared__ uint8_t smem_raw[];
@@ -1438,7 +1441,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, CfgP<DH>::TMEM_COLS);
+        tmem_dealloc(tmem, CfgP<DH, SHARE>::TMEM_COLS);
     }
 }
 
@@ -1450,7 +1453,10 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
                          const int32_t* idx, const float* w, const float* lse, const void* dout,
                          void* dq, void* dk, void* dv, void* ws, int* status, cudaStream_t st) {
     static_assert(CfgA<S, DH>::SMEM + sizeof(BarsA) <= kSmemMax, "shared memory (query-major pass)");
-    if constexpr (S == 64) static_assert(CfgP<DH>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
+    if constexpr (S == 64) {
+        static_assert(CfgP<DH, false>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
+        static_assert(CfgP<DH, true>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
+    }
     else static_assert(CfgK<DH>::SMEM + sizeof(BarsK) <= kSmemMax, "shared memory (key-major pass)");
     CUtensorMap tq, tdo, tk, tv;
     const uint64_t cols = (uint64_t)sp.H * DH;
@@ -1500,10 +1506,19 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     a.n_items = sp.B * sp.nP * sp.H;
     grid = a.n_items < sms ? a.n_items : sms;
     if constexpr (S == 64) {
-        auto kb = gca_bwd_kv_pair_kernel<DH>;
-        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgP<DH>::SMEM);
+        // d = 64: the shared operand pair with two K/V item buffers while an item
+        // holds on average at most 12 entries (boundaries frequent), else private pairs
+        auto kb = gca_bwd_kv_pair_kernel<DH, false>;
+        int smem = CfgP<DH, false>::SMEM;
+        if constexpr (DH == 64) {
+            if ((long long)sp.nQ * sp.topk <= 12LL * sp.nP) {
+                kb = gca_bwd_kv_pair_kernel<DH, true>;
+                smem = CfgP<DH, true>::SMEM;
+            }
+        }
+        e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, CfgP<DH>::SMEM, st>>>(tq, tdo, tk, tv, a));
+        GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, smem, st>>>(tq, tdo, tk, tv, a));
     } else {
         auto kb = gca_bwd_kv128_kernel<DH>;
         e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgK<DH>::SMEM);
