@@ -35,7 +35,7 @@ def test_noisy_topk(name, include_self):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(1, 16, 128, 2), (2, 64, 768, 8), (1, 300, 96, 16)])
+@pytest.mark.parametrize("shape", [(1, 16, 128, 2), (2, 64, 768, 8), (1, 300, 96, 16), (1, 40, 100, 4)])
 def test_landmark_grad_seeded_dscore(dtype, shape):
     B, nC, D, k = shape
     gen = torch.Generator().manual_seed(nC)
@@ -49,6 +49,22 @@ def test_landmark_grad_seeded_dscore(dtype, shape):
         assert_close("dlandmarks", f64(got), want, 1e-4, 1e-5)
     else:
         assert_close("dlandmarks", f64(got), want, 2e-2, 2e-2)
+
+
+def test_landmark_grad_long_inverse_list():
+    # chunk 0 outscores every other landmark, so every query chunk that may retrieve it
+    # does: its list of terms is longer than one staging pass of the kernel (1024 terms)
+    B, nC, D, k = 1, 1100, 64, 4
+    gen = torch.Generator().manual_seed(5)
+    lm = torch.randint(0, 3, (B, nC, D), generator=gen).to(torch.float32)
+    lm[:, 0, :] = 8
+    idx, _, _ = oracle.score_topk(f64(lm), k)
+    assert (idx == 0).sum() > 1024
+    dr = torch.randn(B, nC, k, generator=gen, dtype=torch.float64) * torch.from_numpy(idx >= 0)
+    got = api.landmark_bwd(lm.cuda(), torch.from_numpy(idx).cuda(), dr.float().cuda(), S=64, H=1, d=D)
+    torch.cuda.synchronize()
+    want = oracle.landmark_bwd(f64(lm), idx, dr.float().double().numpy())
+    assert_close("dlandmarks", f64(got), want, 1e-4, 1e-5)
 
 
 def test_landmark_grad_after_backward_pipeline():
