@@ -943,12 +943,14 @@ gca_bwd_kv128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 #pragma unroll
                     for (int pc = 0; pc < 2; ++pc) {
                         // tokens 64 hf + 32 pc .. + 31 of this key row
-                        uint32_t r0[16], r1[16], r2[16], r3[16];
-                        tmem_ld_32x32b_x16(tb + 32 * pc, r0);
-                        tmem_ld_32x32b_x16(tb + 32 * pc + 16, r1);
-                        tmem_ld_32x32b_x16(tb + 64 + 32 * pc, r2);
-                        tmem_ld_32x32b_x16(tb + 64 + 32 * pc + 16, r3);
+                        uint32_t rx[32], ry[32];
+                        tmem_ld_32x32b_x32(tb + 32 * pc, rx);
+                        tmem_ld_32x32b_x32(tb + 64 + 32 * pc, ry);
                         tmem_wait_ld();
+                        const uint32_t* r0 = rx;
+                        const uint32_t* r1 = rx + 16;
+                        const uint32_t* r2 = ry;
+                        const uint32_t* r3 = ry + 16;
                         uint32_t pa[16], pp[16];
 #pragma unroll
                         for (int p2 = 0; p2 < 16; ++p2) {
@@ -1369,13 +1371,15 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 const uint32_t tg0 = ts0 + 64;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    // keys 32 hf .. 32 hf + 31 of this query row
-                    uint32_t r0[16], r1[16], r2[16], r3[16];
-                    tmem_ld_32x32b_x16(ts0 + 32 * hf, r0);
-                    tmem_ld_32x32b_x16(ts0 + 32 * hf + 16, r1);
-                    tmem_ld_32x32b_x16(tg0 + 32 * hf, r2);
-                    tmem_ld_32x32b_x16(tg0 + 32 * hf + 16, r3);
+                    // keys 32 hf .. 32 hf + 31 of this query row: S and G columns, one load each
+                    uint32_t rx[32], ry[32];
+                    tmem_ld_32x32b_x32(ts0 + 32 * hf, rx);
+                    tmem_ld_32x32b_x32(tg0 + 32 * hf, ry);
                     tmem_wait_ld();
+                    const uint32_t* r0 = rx;
+                    const uint32_t* r1 = rx + 16;
+                    const uint32_t* r2 = ry;
+                    const uint32_t* r3 = ry + 16;
                     if (hf == 1) {
                         tc_fence_before();
                         mbar_arrive(&sb.s_empty[sbuf]);

@@ -362,18 +362,17 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 tc_fence_after();
                 float mt;                               // the tile's row max of s
                 {
-                    // the loads return each 16-column chunk's max as well
-                    uint32_t r[8][16];
-                    float mc[8];
+                    // two 64-column loads, each returning its columns' max as well
+                    uint32_t r[2][64];
+                    float mc[2];
 #pragma unroll
-                    for (int ci = 0; ci < 8; ++ci) mc[ci] = tmem_ld_max_32x32b_x16(ts_addr + 16 * ci, r[ci]);
+                    for (int ci = 0; ci < 2; ++ci) mc[ci] = tmem_ld_max_32x32b_x64(ts_addr + 64 * ci, r[ci]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int ci = 0; ci < 8; ++ci)
+                    for (int ci = 0; ci < 2; ++ci)
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) x[16 * ci + u] = __uint_as_float(r[ci][u]);
-                    mt = fmaxf(fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])),
-                               fmaxf(fmaxf(mc[4], mc[5]), fmaxf(mc[6], mc[7])));
+                        for (int u = 0; u < 64; ++u) x[64 * ci + u] = __uint_as_float(r[ci][u]);
+                    mt = fmaxf(mc[0], mc[1]);
                 }
                 tc_fence_before();
                 mbar_arrive(&sb.s_empty[wg]);           // S is in registers: the buffer is free
