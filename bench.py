@@ -580,7 +580,7 @@ def next_rows(api, inputs, dev, hbm):
                             "roofline": {"bound": "hbm", "achieved": round((lm.numel() * 2 + cand * 4) / noisy_us / 1e3, 1),
                                          "peak": hbm, "unit": "GB/s",
                                          "frac": round((lm.numel() * 2 + cand * 4) / noisy_us / 1e3 / hbm, 4),
-                                         "note": "latency-bound: 2048 CTAs of one landmark row each"}}
+                                         "note": "latency-bound: the tensor-core scorer with the noisy selection key; per-row top-k selection and the cross-CTA merge dominate"}}
     idx, r, w = api.score_topk(lm, **kw)
     dr = (torch.randn(B, nC, wl.topk, generator=g) * 0.1).float().to(dev) * (idx >= 0)
     U = int((idx >= 0).sum().item())
