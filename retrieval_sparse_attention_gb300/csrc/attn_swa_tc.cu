@@ -14,12 +14,13 @@
 //              first (window edge) and the last (causal diagonal) are masked.
 //   warp 0     producer: TMA (3-D maps over [B, L, H*d]: rows outside a
 //              sequence read as zeros) of the Q tile (lane 0), each key
-//              tile's K (lane 0) and V (lane 1) into separate 3-stage rings:
+//              tile's K (lane 0) and V (lane 1) into separate 5-stage rings:
 //              a K stage is free once its S product completes, long before
 //              the V stage, which waits for P V.
 //   warp 1     S issuer and TMEM owner: S = Q K^T into the item's warpgroup's
 //              S buffer (128 columns).
-//   warp 2     P V issuer: O += P V into the warpgroup's O accumulator.
+//   warp 2     P V issuer: O += P V into the warpgroup's O accumulator, A = P
+//              read from tensor memory.
 //   warp 3     idle (completes the first warpgroup, which gives registers
 //              to the softmax warpgroups with setmaxnreg).
 //   warps 4-11 two softmax warpgroups owning alternate items (the online
@@ -29,9 +30,18 @@
 // Masking: only the tiles that the window edge or the diagonal crosses are
 // masked, in registers, by straight-line selects (no per-chunk branches: the
 // unrolled exponential loop relies on interleaving across the whole row).
+// Tensor memory: S buffers (2 x 128 columns), O accumulators (2 x 64) and P
+// buffers (2 x 64: bf16 pairs in the A operand layout) fill the 512 columns.
+// With P out of shared memory the P V products read only V there, the P
+// stores leave shared memory alone, and the freed 64 KB deepen the K and V
+// rings.  (The P V products stay on one issuing thread: a second issuer,
+// spinning on its barriers, costs its SM sub-partition's softmax warps more
+// issue slots than it saves.)
 // Softmax of one tile: the thread reads its row of S (128 columns) from TMEM
 // once and frees the buffer at once, so the next S product overlaps this
-// tile's arithmetic; the scaling and the row sum use packed f32x2 arithmetic.
+// tile's arithmetic; the scaling and the row sum use packed f32x2 arithmetic;
+// P goes to its TMEM buffer 32 keys per store once the previous P V has read
+// it.
 // Online softmax with a stale running max: P = exp2(s' - m) is written
 // unnormalised; O (TMEM) and the running sum are rescaled only when a tile's
 // max exceeds m by more than 2^8, which keeps every P below 256 and the result
@@ -67,19 +77,17 @@ static_assert(128 * kRegsCtrl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 constexpr int BM = 128;                // query rows per item (MMA M)
 constexpr int BN = 128;                // keys per tile (MMA N of S)
-constexpr int STAGES = 3;              // depth of the K ring and of the V ring
+constexpr int STAGES = 5;              // depth of the K ring and of the V ring
 constexpr int TILE = 128 * 128;        // 128 rows x 64 bf16: a Q, K, V or O tile
-constexpr int P_BLOCK = BM * 128;      // 64 keys of P for the 128 rows
-constexpr int P_BYTES = 2 * P_BLOCK;   // 128 keys
 constexpr int OFF_Q = 0;               // one Q tile per warpgroup
 constexpr int OFF_K = 2 * TILE;
 constexpr int OFF_V = OFF_K + STAGES * TILE;
-constexpr int OFF_P = OFF_V + STAGES * TILE;            // one P buffer per warpgroup
-constexpr int OFF_O = OFF_P + 2 * P_BYTES;              // one O staging tile per warpgroup
+constexpr int OFF_O = OFF_V + STAGES * TILE;            // one O staging tile per warpgroup
 constexpr int SMEM = OFF_O + 2 * TILE + 1024;           // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;          // S buffer of warpgroup w at w * 128
 constexpr uint32_t COL_O = 256;        // O accumulator of warpgroup w at 256 + w * 64
+constexpr uint32_t COL_P = 384;        // P of warpgroup w (bf16 pairs, 128 keys) at 384 + w * 64
 constexpr float kRescaleLog2 = 8.f;
 
 struct SwaArgs {
@@ -304,10 +312,9 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                             !wait(&sb.p_full[w], full_par(tp[w])) ||
                             !wait(&sb.v_full[kv.i], kv.ph)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t paddr = smem_u32(sm + OFF_P + w * P_BYTES);
                         const uint32_t vaddr = smem_u32(sm + OFF_V + kv.i * TILE);
-                        tcx::mma_kmajor_mnmajor<8>(tmem + COL_O + w * 64, paddr, P_BLOCK, vaddr, id_o,
-                                                   j > 0);
+                        tcx::mma_ts_mn_dh<64, 8>(tmem + COL_O + w * 64, tmem + COL_P + w * 64, vaddr, BN, id_o,
+                                                 j > 0);
                         mma_commit(&sb.v_empty[kv.i]);
                         mma_commit(&sb.p_empty[w]);
                         issued = true;
@@ -334,7 +341,7 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
         const uint32_t ts_addr = tmem + lane_base + COL_S + wg * 128;
         const uint32_t to_addr = tmem + lane_base + COL_O + wg * 64;
-        uint8_t* const pbuf = sm + OFF_P + wg * P_BYTES + row * 128;
+        const uint32_t tp_addr = tmem + lane_base + COL_P + wg * 64;
         uint8_t* const obuf = sm + OFF_O + wg * TILE;
         const bool leader = qd == 0 && lane == 0;       // issues this warpgroup's O stores
         const float sl = a.scale_log2;
@@ -463,6 +470,7 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             // column pairs (packed f32x2 FMA and add: one instruction for two columns)
             const uint64_t sl2 = tcx::f2_pack(sl, sl), nmu2 = tcx::f2_pack(-mu, -mu);
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t pk2[16];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t pk[8];
@@ -476,17 +484,20 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                     acc2[u & 3] = tcx::fadd2(acc2[u & 3], tcx::f2_pack(e0, e1));
                     pk[u] = tcx::pack_bf16(e0, e1);
                 }
-                uint8_t* dst = pbuf + (c >> 2) * P_BLOCK;
-                const int p0 = 2 * (c & 3);             // 16-byte pieces of the 128-byte row
-                *reinterpret_cast<uint4*>(dst + ((p0 ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4*>(dst + (((p0 + 1) ^ (row & 7)) << 4)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                if (c & 1) {                            // 16 keys a column pair: store 32 keys
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) pk2[8 + u] = pk[u];
+                    tmem_st_32x32b_x16(tp_addr + 16 * (c >> 1), pk2);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) pk2[u] = pk[u];
+                }
             }
+            tmem_wait_st();
             float l4[8];
 #pragma unroll
             for (int u = 0; u < 4; ++u) tcx::f2_unpack(acc2[u], l4[2 * u], l4[2 * u + 1]);
             l += ((l4[0] + l4[1]) + (l4[2] + l4[3])) + ((l4[4] + l4[5]) + (l4[6] + l4[7]));
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&sb.p_full[wg]);
             ++ts;
