@@ -14,7 +14,7 @@
 //              first (window edge) and the last (causal diagonal) are masked.
 //   warp 0     producer: TMA (3-D maps over [B, L, H*d]: rows outside a
 //              sequence read as zeros) of the Q tile (lane 0), each key
-//              tile's K (lane 0) and V (lane 1) into separate 5-stage rings:
+//              tile's K (lane 0) and V (lane 1) into a 3-stage and a 7-stage ring:
 //              a K stage is free once its S product completes, long before
 //              the V stage, which waits for P V.
 //   warp 1     S issuer and TMEM owner: S = Q K^T into the item's warpgroup's
@@ -40,8 +40,8 @@
 // Softmax of one tile: the thread reads its row of S (128 columns) from TMEM
 // once and frees the buffer at once, so the next S product overlaps this
 // tile's arithmetic; the scaling and the row sum use packed f32x2 arithmetic;
-// P goes to its TMEM buffer 32 keys per store once the previous P V has read
-// it.
+// the first 64 keys' P is formed in registers before the wait for the
+// previous P V, then P goes to its TMEM buffer 32 keys per store.
 // Online softmax with a stale running max: P = exp2(s' - m) is written
 // unnormalised; O (TMEM) and the running sum are rescaled only when a tile's
 // max exceeds m by more than 2^8, which keeps every P below 256 and the result
@@ -77,12 +77,14 @@ static_assert(128 * kRegsCtrl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
               "register split exceeds the launch allocation");
 constexpr int BM = 128;                // query rows per item (MMA M)
 constexpr int BN = 128;                // keys per tile (MMA N of S)
-constexpr int STAGES = 5;              // depth of the K ring and of the V ring
+constexpr int KST = 3;                 // depth of the K ring (a K stage frees when its S product completes)
+constexpr int VST = 7;                 // depth of the V ring (a V stage is held until P V completes)
+constexpr int STAGES = KST > VST ? KST : VST;
 constexpr int TILE = 128 * 128;        // 128 rows x 64 bf16: a Q, K, V or O tile
 constexpr int OFF_Q = 0;               // one Q tile per warpgroup
 constexpr int OFF_K = 2 * TILE;
-constexpr int OFF_V = OFF_K + STAGES * TILE;
-constexpr int OFF_O = OFF_V + STAGES * TILE;            // one O staging tile per warpgroup
+constexpr int OFF_V = OFF_K + KST * TILE;
+constexpr int OFF_O = OFF_V + VST * TILE;            // one O staging tile per warpgroup
 constexpr int SMEM = OFF_O + 2 * TILE + 1024;           // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;          // S buffer of warpgroup w at w * 128
@@ -212,6 +214,7 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             uint64_t* empty = kl ? sb.k_empty : sb.v_empty;
             const CUtensorMap* map = kl ? &tk : &tv;
             uint8_t* ring = sm + (kl ? OFF_K : OFF_V);
+            const int nst = kl ? KST : VST;
             bool ok = true;
             for (int e0 = blockIdx.x; e0 < a.n_items && ok; e0 += 2 * stride) {
                 Item it[2];
@@ -242,11 +245,11 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                                     (it[w].k0 + j) * BN, it[w].b);
                         out[rg.i] = true;
                         ph[rg.i] = rg.ph;
-                        rg.next(STAGES);
+                        rg.next(nst);
                     }
             }
             // no copy may still be writing shared memory when the CTA exits
-            for (int i = 0; i < STAGES; ++i)
+            for (int i = 0; i < nst; ++i)
                 if (out[i]) mbar_wait(&full[i], ph[i], nullptr, 100000000ull);
             for (int i = 0; i < 2; ++i)
                 if (q_out[i]) mbar_wait(&sb.q_full[i], q_ph[i], nullptr, 100000000ull);
@@ -283,7 +286,7 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                             mma_commit(&sb.q_empty[w]);    // Q is read only by these products
                             ++kq[w];
                         }
-                        kv.next(STAGES);
+                        kv.next(KST);
                     }
             }
             if (issued) {
@@ -323,7 +326,7 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                             mma_commit(&sb.o_full[w]);
                             ++ko[w];
                         }
-                        kv.next(STAGES);
+                        kv.next(VST);
                     }
             }
             if (issued) {
@@ -451,6 +454,19 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
             }
             if (!have) break;
             const float mu = (m == -INFINITY) ? 0.f : m;
+            const uint64_t sl2 = tcx::f2_pack(sl, sl), nmu2 = tcx::f2_pack(-mu, -mu);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            // the first 64 keys' P is formed before the wait for the P buffer
+            uint32_t pka[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float y0, y1;
+                tcx::f2_unpack(tcx::ffma2(tcx::f2_pack(x[2 * c], x[2 * c + 1]), sl2, nmu2), y0, y1);
+                const float e0 = fast_exp2(y0);
+                const float e1 = fast_exp2(y1);
+                acc2[c & 3] = tcx::fadd2(acc2[c & 3], tcx::f2_pack(e0, e1));
+                pka[c] = tcx::pack_bf16(e0, e1);
+            }
             // the previous tile's P V has completed: O is stable, P buffer free
             if (!wwait(&sb.p_empty[wg], empty_par(ts))) break;
             if (__any_sync(0xffffffffu, resc)) {
@@ -466,13 +482,18 @@ gca_swa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
                 }
                 tmem_wait_st();
             }
-            // p = exp2(s * scale * log2(e) - m); the scaling and the row sum run on
-            // column pairs (packed f32x2 FMA and add: one instruction for two columns)
-            const uint64_t sl2 = tcx::f2_pack(sl, sl), nmu2 = tcx::f2_pack(-mu, -mu);
-            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            {                                           // the first 64 keys' P into the buffer
+                uint32_t h0[16], h1[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) { h0[u] = pka[u]; h1[u] = pka[16 + u]; }
+                tmem_st_32x32b_x16(tp_addr, h0);
+                tmem_st_32x32b_x16(tp_addr + 16, h1);
+            }
+            // p = exp2(s * scale * log2(e) - m) for the other 64 keys; the scaling and the
+            // row sum run on column pairs (packed f32x2 FMA and add: one instruction for two)
             uint32_t pk2[16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 4; c < 8; ++c) {
                 uint32_t pk[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
