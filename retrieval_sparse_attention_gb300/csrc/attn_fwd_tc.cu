@@ -15,16 +15,17 @@
 //              128-byte swizzle) straight from the [tokens, H*d] tensors into
 //              a ring of stages.
 //   warp 1     S issuer (one thread) and TMEM owner: S_g = Q K_g^T for a
-//              group of retrieved chunks (N = 128 keys) into one of two TMEM
-//              buffers.
-//   warp 2     P V issuer (one thread): O += P_g V_g in a TMEM accumulator.
-//              Two issuers keep either kind of product from waiting behind
-//              the other's issue (a tcgen05.mma blocks while the queue drains).
+//              group of retrieved chunks (N = 128 keys) into one of three
+//              TMEM buffers.
+//   warp 2     P V issuer (one thread): O += P_g V_g in a TMEM accumulator,
+//              A = P_g read from tensor memory.  Two issuers keep either kind
+//              of product from waiting behind the other's issue (a
+//              tcgen05.mma blocks while the queue drains).
 //   warps 3-10 two softmax warpgroups taking alternate groups: read S_g from
 //              TMEM, per-slot max / sum / exp2, write P_g = exp(S - m) *
-//              (w_j / l_j) as bf16 into shared memory (the A operand of the
-//              PV MMA), write the lse; each warpgroup also stores O (read
-//              from TMEM) for alternate items.
+//              (w_j / l_j) as bf16 over the S columns already read (the A
+//              operand of the PV MMA), write the lse; each warpgroup also
+//              stores O (read from TMEM) for alternate items.
 // Because each slot's softmax is normalised before PV and carries its fusion
 // weight, the per-slot outputs O_t^j are summed by the tensor core in TMEM
 // and never exist in memory.  A work item is (batch row, query chunk, head).
@@ -66,12 +67,13 @@ struct Cfg {
     static constexpr int M = S;                         // tokens per item = MMA M
     static constexpr int GS = 128 / S;                  // slots per group
     static constexpr int NG = 128;                      // keys per full group
-    // S = 128 keeps P in tensor memory over its own S row (the softmax thread
-    // owns TMEM lane = row, which is the A operand layout of P V), so it needs
-    // no shared-memory P buffers; an S buffer is then held until its P V
-    // products complete.  Three S buffers rotate (two at d = 128, where the O
-    // buffers take 256 columns).
-    static constexpr bool TP = (S == 128);
+    // P stays in tensor memory over its own S row (the softmax thread owns the
+    // TMEM lane of its row, which is the A operand layout of P V for M = 128 and,
+    // row r at lane r % 16 + 32 (r / 16), for M = 64 too), so there are no
+    // shared-memory P buffers; an S buffer is then held until its P V products
+    // complete.  Three S buffers rotate (two at d = 128, where the O buffers
+    // take 256 columns).
+    static constexpr bool TP = true;
     static constexpr int NSB = DH == 128 ? 2 : 3;
     // K/V ring depth: what fits beside Q (and the P buffers when S = 64)
     static constexpr int STAGES = TP ? (DH == 32 ? 6 : (DH == 64 ? 5 : 2)) : (DH == 128 ? 2 : 4);
@@ -339,9 +341,13 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     tc_fence_after();
                     const uint32_t vaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES + C::HALF_BYTES);
                     if constexpr (C::TP) {
-                        // P_g sits in its S buffer's first 64 columns (bf16 pairs)
+                        // P_g sits in its S buffer's first 64 columns (bf16 pairs); a group of
+                        // one 64-key slot contracts over its 64 keys only
                         const int sbuf = qq % C::NSB;
-                        tcx::mma_ts_mn_dh<DH, 8>(d_o, tmem + C::COL_S + sbuf * 128, vaddr, C::NG, id_o, g > 0);
+                        if (ns * S == 128)
+                            tcx::mma_ts_mn_dh<DH, 8>(d_o, tmem + C::COL_S + sbuf * 128, vaddr, C::NG, id_o, g > 0);
+                        else
+                            tcx::mma_ts_mn_dh<DH, 4>(d_o, tmem + C::COL_S + sbuf * 128, vaddr, C::NG, id_o, g > 0);
                         mma_commit(&sb.kv_empty[kv.i]);
                         mma_commit(&sb.s_empty[sbuf]);
                     } else {
@@ -424,8 +430,10 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         for (int t = 0; t < 16; ++t) x[16 * ci + t] = __uint_as_float(r[t]);
                     }
                     tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&sb.s_empty[sbuf]);
+                    if constexpr (!C::TP) {
+                        tc_fence_before();
+                        mbar_arrive(&sb.s_empty[sbuf]);
+                    }
                     // exponentials and the row sum on column pairs (packed f32x2 FMA and
                     // add), four sum chains combined in a fixed order
                     mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
@@ -475,7 +483,7 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const float coef = active ? wj / l : 0.f;
                 const uint64_t coef2 = tcx::f2_pack(coef, coef);
                 if (active && lrow) lrow[j] = (mb + log2f(l)) * kLn2;
-                if constexpr (C::TP) {
+                if constexpr (C::TP && S == 128) {
                     // P over the first 64 columns of this row's S buffer, two keys per column
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
@@ -484,6 +492,24 @@ gca_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         for (int t = 0; t < 16; ++t)
                             pk[t] = tcx::pack_bf16(x[32 * ch + 2 * t] * coef, x[32 * ch + 2 * t + 1] * coef);
                         tmem_st_32x32b_x16(taddr + 16 * ch, pk);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                } else if constexpr (C::TP) {
+                    // S = 64: P of the group's two slots as one M = 64 A operand over the first
+                    // 64 columns of the S buffer (row r at lane r % 16 + 32 (r / 16), as the
+                    // score rows): slot u's 64 keys at columns 32 u .. 32 u + 31, written by
+                    // the thread that read them (the warp's loads have completed, so the
+                    // other slot's scores there are already in registers)
+#pragma unroll
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            pk[t] = active ? tcx::pack_bf16x2(tcx::fmul2(tcx::f2_pack(x[32 * ch + 2 * t],
+                                                                                  x[32 * ch + 2 * t + 1]), coef2))
+                                           : 0u;
+                        tmem_st_16x32bx2_x16<32>(taddr + 16 * ch, pk);
                     }
                     tmem_wait_st();
                     tc_fence_before();

@@ -255,6 +255,17 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         : "memory");
 }
 
+// Store counterpart of tmem_ld_16x32bx2_x16: threads 0-15 write lanes taddr.lane+0..15
+// at columns taddr.col .. +15, threads 16-31 the same lanes at columns
+// taddr.col + half_off .. +15.  Complete with tmem_wait_st.
+template <int HALF_OFF>
+__device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::"r"(taddr), "n"(HALF_OFF),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 // 16 lanes x 32 bits, taken twice: threads 0-15 read lanes taddr.lane+0..15 at
 // columns taddr.col .. +15, threads 16-31 the same lanes at columns
 // taddr.col + half_off .. +15.
