@@ -120,6 +120,10 @@ struct CfgA {
     static constexpr int M = S;
     static constexpr int NG = S;                           // keys per group
     static constexpr int NSB = (S == 64) ? (DH == 128 ? 2 : 3) : 1;   // S/G TMEM buffers
+    // S = 64: dA goes over the S columns of its S/G buffer as the M = 64 A operand of
+    // dQ += dA K (row r at lane r % 16 + 32 (r / 16), the layout of the score rows), so
+    // the buffer is released by the dQ product, not by the math warps' loads
+    static constexpr bool TA = (S == 64);
     // K/V ring depth and Q/dO buffers: what fits beside the P and lse buffers
     static constexpr int STAGES = (S == 64) ? (DH == 128 ? 3 : 8) : (DH == 32 ? 4 : (DH == 64 ? 2 : 1));
     static constexpr int IBUF = (S == 128 && DH == 128) ? 1 : 2;
@@ -157,7 +161,7 @@ struct __align__(8) BarsA {
     uint64_t it_full[2], it_empty[2];
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[3], s_empty[3];    // per S/G buffer (per warpgroup when one buffer)
-    uint64_t p_full[2], p_empty[2];
+    uint64_t p_full[4], p_empty[2];      // p_full: [wg] (S = 128), [group & 3] (S = 64)
     uint64_t o_full[2], o_empty[2];
     uint64_t done, done2, done3;
     uint32_t tmem;
@@ -187,17 +191,17 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sb.it_full[i], 1);
             mbar_init(&sb.it_empty[i], 2);            // Q read by the S products, dO by the G products
-            mbar_init(&sb.p_full[i], 128);
             mbar_init(&sb.p_empty[i], 1);
             mbar_init(&sb.o_full[i], 1);
             mbar_init(&sb.o_empty[i], 128);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(&sb.p_full[i], 128);
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&sb.kv_full[i], 1);
             mbar_init(&sb.kv_empty[i], 1);
         }
         for (int i = 0; i < 3; ++i) mbar_init(&sb.s_full[i], 2);   // S issuer + G issuer
-        for (int i = 0; i < C::NSB; ++i) mbar_init(&sb.s_empty[i], 128);
+        for (int i = 0; i < C::NSB; ++i) mbar_init(&sb.s_empty[i], C::TA ? 1 : 128);
         mbar_init(&sb.done, 1);
         mbar_init(&sb.done2, 1);
         mbar_init(&sb.done3, 1);
@@ -381,14 +385,26 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 bool ok = true;
                 for (int g = 0; g < n; ++g) {
                     const int qq = q + g, pb = qq & 1;
-                    if (!wait(&sb.p_full[pb], full_par(qq >> 1))) { ok = false; break; }
+                    // S = 64: a warpgroup alternates two full barriers (no operand-buffer wait
+                    // holds a fast warp back, so its arrival for the next group must not
+                    // count toward this one)
+                    const bool pf = C::TA ? wait(&sb.p_full[qq & 3], full_par(qq >> 2))
+                                          : wait(&sb.p_full[pb], full_par(qq >> 1));
+                    if (!pf) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
                     const uint32_t kaddr = smem_u32(sm + C::OFF_KV + kv.i * C::STAGE_BYTES);
-                    tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dq, paddr, C::P_BLOCK, kaddr, S, id_dq, g > 0);
-                    // the S / G products of this group are complete (their P exists)
-                    mma_commit(&sb.kv_empty[kv.i]);
-                    mma_commit(&sb.p_empty[pb]);
+                    if constexpr (C::TA) {
+                        const int sbuf = qq % C::NSB;
+                        tcx::mma_ts_mn_dh<DH, S / 16>(d_dq, tmem + sbuf * C::SGW, kaddr, S, id_dq, g > 0);
+                        mma_commit(&sb.kv_empty[kv.i]);
+                        mma_commit(&sb.s_empty[sbuf]);   // dA (over S) read: the S/G buffer is free
+                    } else {
+                        const uint32_t paddr = smem_u32(sm + C::OFF_P + pb * C::P_BYTES);
+                        tcx::mma_kmajor_mn_dh<DH, S / 16>(d_dq, paddr, C::P_BLOCK, kaddr, S, id_dq, g > 0);
+                        // the S / G products of this group are complete (their P exists)
+                        mma_commit(&sb.kv_empty[kv.i]);
+                        mma_commit(&sb.p_empty[pb]);
+                    }
                     issued = true;
                     kv.next(C::STAGES);
                 }
@@ -468,8 +484,6 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                     tmem_ld_16x32bx2_x16<32>(tg0, r2);
                     tmem_ld_16x32bx2_x16<32>(tg0 + 16, r3);
                     tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(&sb.s_empty[sbuf]);
                     // column pairs in packed f32x2 arithmetic: p = exp2(s sl - L2) as
                     // exp2(-(L2 - s sl)), delta = sum p g, dA = p (g - delta) w scale
                     const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
@@ -499,11 +513,10 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
 #pragma unroll
                     for (int p = 0; p < 16; ++p)
                         pk[p] = tcx::pack_bf16x2(tcx::fmul2(pr2[p], tcx::ffma2(gv2[p], wsc2, ndl2)));
-                    if (!wait(&sb.p_empty[wg], empty_par(kg))) { ok = false; break; }
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-                        *reinterpret_cast<uint4*>(pb + sw128_off(row, 4 * u + c4)) =
-                            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+                    // dA over the S columns 16 u .. 16 u + 15 of this row (keys 32 u ..): the
+                    // warp's loads have completed, so the scores there are in registers
+                    tmem_st_16x32bx2_x16<16>(ts0, pk);
+                    tmem_wait_st();
                 } else {
                     // this thread: one token row, all 128 keys in two 64-key chunks
                     float x[64];
@@ -556,8 +569,13 @@ gca_bwd_q_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                         }
                     }
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(&sb.p_full[wg]);
+                if constexpr (C::TA) {
+                    tc_fence_before();
+                    mbar_arrive(&sb.p_full[qq & 3]);
+                } else {
+                    fence_proxy_async_smem();
+                    mbar_arrive(&sb.p_full[wg]);
+                }
                 ++kg;
                 if constexpr (S != 64) emit_rows(dl);     // (S = 64 emitted them before the P wait)
             }
@@ -1459,7 +1477,8 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     static_assert(CfgA<S, DH>::SMEM + sizeof(BarsA) <= kSmemMax, "shared memory (query-major pass)");
     if constexpr (S == 64) {
         static_assert(CfgP<DH, false>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
-        static_assert(CfgP<DH, true>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
+        if constexpr (DH == 64)
+            static_assert(CfgP<DH, true>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
     }
     else static_assert(CfgK<DH>::SMEM + sizeof(BarsK) <= kSmemMax, "shared memory (key-major pass)");
     CUtensorMap tq, tdo, tk, tv;
