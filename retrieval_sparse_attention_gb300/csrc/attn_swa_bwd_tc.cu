@@ -140,6 +140,9 @@ namespace pa {
 constexpr int kThreads = 384;                    // producer, S, dQ and dP issuers, 8 math warps
 constexpr int IBUF = 2;
 constexpr int ITEM = 3 * TILE128;                // Q, dO, O
+// the producer issues the next item's buffer (and its lse load) an item ahead, so a
+// single item buffer would wait on its own item: the protocol needs two
+static_assert(IBUF == 2, "pass A needs two item buffers");
 constexpr int NSLOT = 8;                         // K/V tile slots
 constexpr int SLOT = 2 * TILE64;                 // K, V
 constexpr int OFF_IT = 0;
@@ -521,6 +524,7 @@ namespace pb {
 constexpr int kThreads = 384;                    // + warp 11: the dV issuer
 constexpr int IBUF = 2;
 constexpr int ITEM = 2 * TILE128;                // K, V
+static_assert(IBUF == 2, "pass B needs two item buffers (one item of lead)");
 constexpr int VEC_OFF = 2 * TILE128;             // after the Q and dO tiles: nlse2[128], ndsc[128]
 constexpr int SLOT = VEC_OFF + 1024;             // one 128-query stage
 constexpr int NSLOT = 4;
