@@ -72,6 +72,8 @@ struct BwdArgs {
     const int* offset;         // [B, nP + 1]
     const int* entry;          // [B, nQ * topk]
     const float* entry_w;      // [B, nQ * topk]: the weight of each entry
+    const int* order;          // [B, nP]: each row's chunks by descending retrieval count
+    int ordered;               // S = 64 key-major pass: deal the items by `order` (else by stride)
     __nv_bfloat16* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -1025,6 +1027,67 @@ gca_bwd_kv128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 // the accumulation products read as MN-major A operands:
 // dK += dA^T [Q_1; Q_2] and dV += (w P)^T [dO_1; dO_2] over K = 128 queries
 // (64 for a single entry).
+// The order in which the S = 64 key-major pass deals its items.  An item's cost is
+// the number of entry pairs of its chunk, and a fixed stride over items in index
+// order leaves the busiest CTA ~5% above the mean.  One CTA per batch row ranks the
+// row's chunks by retrieval count (descending, counts above 255 taken as 255; ties by
+// chunk index) with a stable counting sort: a histogram of the counts, its scan from
+// the top, and each chunk's place among equal counts from warp matches plus the
+// per-warp counts of the warps before it.  Position p of the dealt sequence is then
+// rank k = p / (B H) of row (p / H) % B, head p % H, and round r of the CTAs takes
+// positions r G .. r G + G - 1 boustrophedon (CTA c takes c in even rounds, G - 1 - c
+// in odd ones).
+__global__ void __launch_bounds__(1024) pair_order_kernel(const int* __restrict__ count, int nP,
+                                                          int* __restrict__ order) {
+    __shared__ int hist[256];
+    __shared__ int start[256];
+    __shared__ int per_warp[32][256];      // chunks of each count in each warp
+    const int b = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const bool real = t < nP;
+    const int key = real ? min(count[(size_t)b * nP + t], 255) : -1;
+    if (t < 256) hist[t] = 0;
+    for (int i = t; i < 32 * 256; i += 1024) (&per_warp[0][0])[i] = 0;
+    __syncthreads();
+    // equal keys in this warp: the lowest such lane records the warp's count of the key
+    const unsigned same = __match_any_sync(0xffffffffu, key);
+    const int in_warp = __popc(same & ((1u << lane) - 1u));
+    if (real) {
+        atomicAdd(&hist[key], 1);
+        if (in_warp == 0) per_warp[warp][key] = __popc(same);
+    }
+    __syncthreads();
+    if (warp == 0) {                       // start[k] = chunks with a larger count
+        int v[8], run = 0;
+        for (int i = 0; i < 8; ++i) { v[i] = hist[255 - (8 * lane + i)]; run += v[i]; }
+        int incl = run;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int acc = incl - run;
+        for (int i = 0; i < 8; ++i) { start[255 - (8 * lane + i)] = acc; acc += v[i]; }
+    }
+    __syncthreads();
+    if (real) {
+        int pos = start[key] + in_warp;
+        for (int w = 0; w < warp; ++w) pos += per_warp[w][key];
+        order[(size_t)b * nP + pos] = t;
+    }
+}
+
+// Position of round r for CTA c (boustrophedon when the items are dealt by rank).
+__device__ __forceinline__ int pair_pos(const BwdArgs& a, int r) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((a.ordered && (r & 1)) ? G - 1 - c : c);
+}
+// Item at position p: (b, chunk of rank k in row b, h), or p itself when not ordered.
+__device__ __forceinline__ int pair_item(const BwdArgs& a, int p) {
+    if (!a.ordered) return p;
+    const int BH = a.B * a.H;
+    const int k = p / BH, rem = p - k * BH, b = rem / a.H, h = rem - b * a.H;
+    return (b * a.nP + a.order[(size_t)b * a.nP + k]) * a.H + h;
+}
+
 template <int DH, bool SHARE>
 struct CfgP {
     using G = tcx::HeadGeom<DH>;
@@ -1131,12 +1194,14 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             if (lane == 0) r = wait(bar, par) ? 1 : 0;
             return __shfl_sync(kAll, r, 0) != 0;
         };
-        int my_e0 = 0, my_ne = 0;           // lane l: offsets of the batch's l-th item
-        auto load_offsets = [&](int item0) {
-            const int it_l = item0 + lane * gridDim.x;
+        int my_item = a.n_items, my_e0 = 0, my_ne = 0;   // lane l: item and offsets of round r0 + l
+        auto load_offsets = [&](int r0) {
+            const int p_l = pair_pos(a, r0 + lane);
+            my_item = a.n_items;
             my_e0 = my_ne = 0;
-            if (it_l < a.n_items) {
-                const int bk_l = it_l / a.H, kap_l = bk_l % a.nP, b_l = bk_l / a.nP;
+            if (p_l < a.n_items) {
+                my_item = pair_item(a, p_l);
+                const int bk_l = my_item / a.H, kap_l = bk_l % a.nP, b_l = bk_l / a.nP;
                 const int* off = a.offset + (size_t)b_l * (a.nP + 1) + kap_l;
                 my_e0 = off[0];
                 my_ne = off[1] - my_e0;
@@ -1151,20 +1216,23 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
                 w_out = a.entry_w[at];
             }
         };
-        int item = blockIdx.x, n_item = 0;
-        if (item < a.n_items) load_offsets(item);
+        int n_item = 0;
+        load_offsets(0);
+        int item = __shfl_sync(kAll, my_item, 0);
         int nx_e0 = __shfl_sync(kAll, my_e0, 0), nx_ne = __shfl_sync(kAll, my_ne, 0);
         int nx_e = 0;
         float nx_w = 0.f;
         if (item < a.n_items) fetch(item / a.H / a.nP, nx_e0, nx_ne, 0, nx_e, nx_w);
-        for (; item < a.n_items; item += gridDim.x, ++n_item) {
+        int nitem = a.n_items;
+        for (; item < a.n_items; ++n_item, item = nitem) {
             const int h = item % a.H, bk = item / a.H, kap = bk % a.nP, b = bk / a.nP;
             const int e0 = nx_e0, ne = nx_ne;
             int bat_e = nx_e;
             float bat_w = nx_w;
             {
-                const int nn = n_item + 1, nitem = item + gridDim.x;
-                if ((nn & 31) == 0 && nitem < a.n_items) load_offsets(nitem);
+                const int nn = n_item + 1;
+                if ((nn & 31) == 0) load_offsets(nn);
+                nitem = __shfl_sync(kAll, my_item, nn & 31);
                 nx_e0 = __shfl_sync(kAll, my_e0, nn & 31);
                 nx_ne = __shfl_sync(kAll, my_ne, nn & 31);
                 if (nitem < a.n_items) fetch(nitem / a.H / a.nP, nx_e0, nx_ne, 0, nx_e, nx_w);
@@ -1247,7 +1315,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             int q = 0;
             bool issued = false;
             const uint32_t id_s = idesc_bf16(128, S, false, false);
-            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+            for (int r = 0; pair_pos(a, r) < a.n_items; ++r) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
                 mbar_arrive(&sb.info_empty[inf.i]);
@@ -1292,7 +1360,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
             int q = 0, e = 0;
             bool issued = false;
             const uint32_t id_acc = idesc_bf16(64, HG::SUB_COLS, true, true);
-            for (int item = blockIdx.x; item < a.n_items; item += gridDim.x) {
+            for (int r = 0; pair_pos(a, r) < a.n_items; ++r) {
                 if (!wait(&sb.info_full[inf.i], inf.ph)) break;
                 const int ne = sb.info[inf.i].ne;
                 mbar_arrive(&sb.info_empty[inf.i]);
@@ -1347,7 +1415,7 @@ gca_bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_cons
         Ring inf{0, 0}, st{0, 0};
         int q = 0, e = 0, n_all = 0, kg = 0;
         const uint64_t nsl2 = tcx::f2_pack(-a.scale_log2, -a.scale_log2);
-        for (int item = blockIdx.x; item < a.n_items; item += gridDim.x, ++n_all) {
+        for (int r = 0; pair_pos(a, r) < a.n_items; ++r, ++n_all) {
             if (!wait(&sb.info_full[inf.i], inf.ph)) break;
             const ItemInfoB I = sb.info[inf.i];
             mbar_arrive(&sb.info_empty[inf.i]);
@@ -1473,7 +1541,7 @@ constexpr int kSmemMax = 232448;
 template <int S, int DH>
 cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const void* v,
                          const int32_t* idx, const float* w, const float* lse, const void* dout,
-                         void* dq, void* dk, void* dv, void* ws, int* status, cudaStream_t st) {
+                         void* dq, void* dk, void* dv, void* ws, int* status, cudaStream_t st, int* launches) {
     static_assert(CfgA<S, DH>::SMEM + sizeof(BarsA) <= kSmemMax, "shared memory (query-major pass)");
     if constexpr (S == 64) {
         static_assert(CfgP<DH, false>::SMEM + sizeof(BarsB) <= kSmemMax, "shared memory (pair pass)");
@@ -1499,6 +1567,8 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
     a.offset = reinterpret_cast<const int*>(base + L.offset_off);
     a.entry = reinterpret_cast<const int*>(base + L.entry_off);
     a.entry_w = reinterpret_cast<const float*>(base + L.entry_w_off);
+    a.order = reinterpret_cast<const int*>(base + L.order_off);
+    a.ordered = 0;
     a.dq = static_cast<__nv_bfloat16*>(dq);
     a.dk = static_cast<__nv_bfloat16*>(dk);
     a.dv = static_cast<__nv_bfloat16*>(dv);
@@ -1541,6 +1611,14 @@ cudaError_t launch_bwd_s(const Shape& sp, const void* q, const void* k, const vo
         }
         e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
+        if (sp.nP <= 1024) {
+            const int* count = reinterpret_cast<const int*>(base + L.count_off);
+            GCA_LAUNCH("pair_order", st, pair_order_kernel<<<sp.B, 1024, 0, st>>>(count, sp.nP,
+                                                                                    const_cast<int*>(a.order)));
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            *launches += 1;
+            a.ordered = 1;
+        }
         GCA_LAUNCH("bwd_kv_tc", st, kb<<<grid, kThreadsA, smem, st>>>(tq, tdo, tk, tv, a));
     } else {
         auto kb = gca_bwd_kv128_kernel<DH>;
@@ -1559,7 +1637,7 @@ cudaError_t launch_bwd_tc(const Shape& sp, const void* q, const void* k, const v
                           cudaStream_t st, int* launches) {
     cudaError_t e = launch_inverse_index(sp, idx, w, ws, st, launches);
     if (e != cudaSuccess) return e;
-#define GCA_BWD_S(S_, DH_) launch_bwd_s<S_, DH_>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st)
+#define GCA_BWD_S(S_, DH_) launch_bwd_s<S_, DH_>(sp, q, k, v, idx, w, lse, dout, dq, dk, dv, ws, status, st, launches)
     if (sp.S == 64) e = sp.d == 32 ? GCA_BWD_S(64, 32) : (sp.d == 128 ? GCA_BWD_S(64, 128) : GCA_BWD_S(64, 64));
     else e = sp.d == 32 ? GCA_BWD_S(128, 32) : (sp.d == 128 ? GCA_BWD_S(128, 128) : GCA_BWD_S(128, 64));
 #undef GCA_BWD_S

@@ -23,6 +23,7 @@ BwdWorkspace bwd_workspace_layout(const Shape& s) {
     w.offset_off = off; off += align256(sizeof(int) * (size_t)s.B * (s.nP + 1));
     w.entry_off = off;  off += align256(sizeof(int) * (size_t)s.B * s.nQ * s.topk);
     w.entry_w_off = off; off += align256(sizeof(float) * (size_t)s.B * s.nQ * s.topk);
+    w.order_off = off;  off += align256(sizeof(int) * (size_t)s.B * s.nP);
     w.total = off;
     return w;
 }

@@ -56,6 +56,7 @@ struct BwdWorkspace {
     size_t offset_off;    // int32 [B, nP + 1]: CSR offsets of the inverse index
     size_t entry_off;     // int32 [B, nQ * topk]: entries c * topk + j, ascending
     size_t entry_w_off;   // fp32 [B, nQ * topk]: the fusion weight w[b][c][j] of each entry
+    size_t order_off;     // int32 [B, nP]: each row's chunks by descending retrieval count
     size_t total;
 };
 BwdWorkspace bwd_workspace_layout(const Shape& s);
