@@ -1033,10 +1033,13 @@ gca_bwd_kv128_kernel(const __grid_constant__ CUtensorMap tq, const __grid_consta
 // row's chunks by retrieval count (descending, counts above 255 taken as 255; ties by
 // chunk index) with a stable counting sort: a histogram of the counts, its scan from
 // the top, and each chunk's place among equal counts from warp matches plus the
-// per-warp counts of the warps before it.  Position p of the dealt sequence is then
-// rank k = p / (B H) of row (p / H) % B, head p % H, and round r of the CTAs takes
-// positions r G .. r G + G - 1 boustrophedon (CTA c takes c in even rounds, G - 1 - c
-// in odd ones).
+// per-warp counts of the warps before it.  The dealt sequence takes the rows one after
+// another (so the Q / dO in flight is one batch row's, not every row's) and
+// snakes: position p is head p % H of rank k = (p / H) % nP of row b = p / (nP H),
+// ranks descending in the last row and in every second row before it, ascending in
+// the others, so the cost of consecutive positions never jumps at a row boundary.
+// Round r of the CTAs takes positions r G .. r G + G - 1 boustrophedon (CTA c takes
+// c in even rounds, G - 1 - c in odd ones).
 __global__ void __launch_bounds__(1024) pair_order_kernel(const int* __restrict__ count, int nP,
                                                           int* __restrict__ order) {
     __shared__ int hist[256];
@@ -1080,11 +1083,12 @@ __device__ __forceinline__ int pair_pos(const BwdArgs& a, int r) {
     const int G = gridDim.x, c = blockIdx.x;
     return r * G + ((a.ordered && (r & 1)) ? G - 1 - c : c);
 }
-// Item at position p: (b, chunk of rank k in row b, h), or p itself when not ordered.
+// Item at position p: (row b, chunk of rank k in row b, head h), or p itself when not ordered.
 __device__ __forceinline__ int pair_item(const BwdArgs& a, int p) {
     if (!a.ordered) return p;
-    const int BH = a.B * a.H;
-    const int k = p / BH, rem = p - k * BH, b = rem / a.H, h = rem - b * a.H;
+    const int bk = p / a.H, h = p - bk * a.H, b = bk / a.nP;
+    int k = bk - b * a.nP;
+    if ((a.B - 1 - b) & 1) k = a.nP - 1 - k;     // snake: rows alternate, the last one descends
     return (b * a.nP + a.order[(size_t)b * a.nP + k]) * a.H + h;
 }
 
