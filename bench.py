@@ -64,16 +64,26 @@ def peaks():
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+    """nvidia-smi clocks / throttle reasons, sampled every 100 ms.
+
+    Sampling starts before the timed region (the first sample is awaited, up to
+    3 s, so the sampler is live when the region starts) and stops 150 ms after
+    it.  Each sample is stamped on arrival; ``mark_start`` / ``mark_end`` bracket
+    the timed region.  The median SM clock is taken over the samples that arrived
+    inside the region when there are any, else over all of them; the throttle
+    reasons are those active in any sample.
+    """
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, first_wait_s: float = 3.0):
         self.idx = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (arrival time, line)
+        self.first_wait_s = first_wait_s
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -84,11 +94,21 @@ class ClockSampler:
             self.t.start()
         except OSError:
             self.proc = None
+        deadline = time.monotonic() + self.first_wait_s
+        while (self.proc is not None and not self.lines and self.proc.poll() is None
+               and time.monotonic() < deadline):
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -100,23 +120,26 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        samples, reasons = [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in list(self.lines):
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 8:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                samples.append((ts, float(f[1]), float(f[2])))
             except ValueError:
                 continue
             for n, v in zip(names, f[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [x for x in samples
+                  if self.t0 is not None and self.t1 is not None and self.t0 <= x[0] <= self.t1]
+        use = inside or samples
+        return {"sm_mhz": statistics.median(x[1] for x in use) if use else None,
+                "sm_max_mhz": max(x[2] for x in samples) if samples else None,
+                "reasons": sorted(reasons), "samples": len(samples),
+                "samples_in_region": len(inside)}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -245,11 +268,13 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        clk.mark_start()
         e0.record()
         for _ in range(args.steps):
             step(g)
         e1.record()
         barrier()
+        clk.mark_end()
     lib.gca_prof_enable(0)
     ms = e0.elapsed_time(e1)
     prof = read_prof(lib)

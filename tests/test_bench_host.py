@@ -1,7 +1,11 @@
-"""Host-side arithmetic of bench.py's roofline: the algorithmic bytes of each
-GCA kernel (gathered tiles plus the resident tensors it reads and writes once)
-worked out by hand for a small case, and the committed DRAM-traffic table it
-reads per kernel and workload."""
+"""Host-side parts of bench.py: the roofline's algorithmic bytes of each GCA
+kernel (gathered tiles plus the resident tensors it reads and writes once)
+worked out by hand for a small case, the committed DRAM-traffic table it reads
+per kernel and workload, and the clock sampler (driven by a stand-in
+nvidia-smi that prints fixed samples)."""
+import os
+import stat
+import time
 import types
 
 import bench
@@ -28,3 +32,39 @@ def test_traffic_table_reads_only_data_lines():
         assert nbytes > 0 and nbytes == int(nbytes)
     assert ("fwd_tc", "gpt2s_fwdbwd_b8") in t
     assert ("decode_retrieve", "decode_262144x768") in t
+
+
+def _fake_smi(tmp_path, lines):
+    """An executable named nvidia-smi that prints `lines` in a loop, 20 ms apart."""
+    body = "".join("echo '%s'; sleep 0.02; " % ln for ln in lines)
+    p = tmp_path / "nvidia-smi"
+    p.write_text("#!/bin/sh\nwhile true; do %sdone\n" % body)
+    p.chmod(p.stat().st_mode | stat.S_IXUSR | stat.S_IXGRP | stat.S_IXOTH)
+    return str(tmp_path)
+
+
+def test_clock_sampler_counts_samples_inside_the_region(tmp_path, monkeypatch):
+    d = _fake_smi(tmp_path, ["0, 2070, 2070, 900.5, Not Active, Not Active, Not Active, Active",
+                             "0, 2055, 2070, 910.0, Not Active, Not Active, Not Active, Not Active",
+                             "garbage line"])
+    monkeypatch.setenv("PATH", d + os.pathsep + os.environ.get("PATH", ""))
+    with bench.ClockSampler(0) as clk:
+        assert clk.lines, "the first sample is awaited before the region starts"
+        clk.mark_start()
+        time.sleep(0.3)
+        clk.mark_end()
+    s = clk.summary()
+    assert s["samples_in_region"] >= 3
+    assert s["samples"] >= s["samples_in_region"]
+    assert 2055.0 <= s["sm_mhz"] <= 2070.0
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))          # nothing executable there
+    with bench.ClockSampler(0, first_wait_s=0.2) as clk:
+        clk.mark_start()
+        clk.mark_end()
+    assert clk.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                             "samples": 0, "samples_in_region": 0}
